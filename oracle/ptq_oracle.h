@@ -1,0 +1,110 @@
+/*
+ * ptq_oracle.h -- CPU oracle for the PTQ1_0 ternary matmul and the signed
+ * 1024-wide Walsh-Hadamard rotation.
+ *
+ * TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only the test-suite, the smoke
+ * check and the CPU-baseline leg of the benchmark may load this library.
+ * It shares no code, header, table or helper with the CUDA library: it is
+ * written from the definitions on the source pages, in plain C, in fp64.
+ *
+ * Sources (page title, section):
+ *   [P1] "A 27B model in 5.5 GB: Bonsai ternary on Ferrox, locally"
+ *        - "What Bonsai is": weights in {-1,0,+1}, one 16-bit scale per 128
+ *          weights, five trits per byte in base 3 (1.75 bits/weight); every
+ *          weight matrix is multiplied by a 1024-wide Walsh-Hadamard
+ *          butterfly with a sign pattern, so the same rotation must be
+ *          applied to the activation before every matmul.
+ *        - "What Ferrox does with it": trit n of a byte is
+ *          floor(3^(n+1) u) - 3 floor(3^n u) with u = byte/256.
+ *        - "Speed, and where it goes": the feed-forward block is rotate,
+ *          gate (+ up), SwiGLU, rotate, down.
+ *   The encode rule (digit = trit + 1, v = sum d_i 3^(4-i),
+ *   byte = ceil(256 v / 243), last byte of a block holds 3 trits padded with
+ *   digit 1) is the workload definition of the tiny PTQ1_0 matvec case.
+ *
+ * Readings where the pages are silent (each is stated again in the design doc):
+ *   - trit order inside a block is contiguous: byte j, digit n <-> weight
+ *     5j+n, n = 0 is the most significant base-3 digit;
+ *   - the rotation flips signs first, then applies the Sylvester-ordered
+ *     Hadamard matrix H[i][j] = (-1)^popcount(i & j), then scales by 1/32;
+ *     the sign vector has one entry per element (block b uses its own 1024);
+ *   - the gate/up weight of the fused feed-forward block stacks the gate rows
+ *     (0..I-1) above the up rows (I..2I-1); h = silu(gate) * up.
+ *
+ * Storage (the same on both sides of the parity tests):
+ *   wq     : N x (K/128) x 26 bytes, row-major (row n is (K/128)*26 bytes)
+ *   scales : N x (K/128) IEEE binary16 bit patterns
+ *   signs  : K int8 values, each +1 or -1
+ */
+#ifndef PTQ_ORACLE_H
+#define PTQ_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Threads used by the parallel loops (over independent output rows). */
+void orc_set_threads(int n);
+int orc_get_threads(void);
+
+/* Exact decodes of the storage formats into double. */
+double orc_half_to_double(uint16_t h);
+double orc_bf16_to_double(uint16_t b);
+void orc_decode_f16(const uint16_t* in, double* out, int64_t n);
+void orc_decode_bf16(const uint16_t* in, double* out, int64_t n);
+void orc_decode_f32(const float* in, double* out, int64_t n);
+
+/* The peel of [P1] "What Ferrox does with it", evaluated in double.
+   Returns the base-3 digit n (0..4, 0 = most significant) of `byte`. */
+int orc_peel_digit(uint8_t byte, int n);
+
+/* Encode N x K trits (int8 in {-1,0,1}) into PTQ1_0 bytes.
+   Returns 0, or -1 if a trit is outside {-1,0,1} or K % 128 != 0. */
+int orc_pack(const int8_t* trits, uint8_t* wq, int64_t N, int64_t K);
+
+/* Decode PTQ1_0 bytes back into trits with orc_peel_digit.
+   Returns 0, or -1 if K % 128 != 0. */
+int orc_unpack(const uint8_t* wq, int8_t* trits, int64_t N, int64_t K);
+
+/* Signed rotation, the definition: for every row m and 1024-block b,
+   y_j = (1/32) sum_i (-1)^popcount(i&j) s_i x_i.  O(1024^2) per block.
+   x and y are M x K row-major; y may not alias x. */
+void orc_fwht_def(const double* x, const int8_t* signs, double* y,
+                  int64_t M, int64_t K);
+
+/* The same transform by the radix-2 butterfly (10 stages), for speed.
+   y may alias x. */
+void orc_fwht_fast(const double* x, const int8_t* signs, double* y,
+                   int64_t M, int64_t K);
+
+/* y[m,n] = sum_b s[n,b] * sum_{i<128} t[n,128b+i] * x[m,128b+i], where the
+   trits are peeled from wq.  x is M x K, y is M x N, both row-major. */
+void orc_matmul(const uint8_t* wq, const uint16_t* scales, const double* x,
+                double* y, int64_t M, int64_t N, int64_t K);
+
+/* The same, for the listed output rows only: y is M x nrows, column r holds
+   output row rows[r]. */
+void orc_matmul_rows(const uint8_t* wq, const uint16_t* scales,
+                     const double* x, double* y, int64_t M, int64_t N,
+                     int64_t K, const int64_t* rows, int64_t nrows);
+
+/* h = silu(g) * u, silu(a) = a / (1 + exp(-a)). */
+void orc_swiglu(const double* g, const double* u, double* h, int64_t n);
+
+/* Feed-forward block of [P1] "Speed, and where it goes":
+   xr = R_in x; [g;u] = W_gu xr; h = silu(g) * u; hr = R_mid h; y = W_d hr.
+   x: M x H, y: M x H, W_gu: 2I x H (gate rows then up rows), W_d: H x I.
+   Everything in double, no intermediate rounding.  Returns 0 or -1 (shape or
+   allocation failure). */
+int orc_ffn(const uint8_t* wgu_q, const uint16_t* wgu_s, const uint8_t* wd_q,
+            const uint16_t* wd_s, const int8_t* signs_in,
+            const int8_t* signs_mid, const double* x, double* y, int64_t M,
+            int64_t H, int64_t I);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PTQ_ORACLE_H */

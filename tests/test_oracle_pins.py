@@ -1,0 +1,295 @@
+"""Pins of the CPU oracle against what the pages and mathematics fix.
+
+Every test here checks the oracle against something other than itself: the
+hand-worked codec examples and geometry printed on the pages (tests/golden),
+an independent characterisation of the base-3 decode, the textbook Sylvester
+Hadamard matrix (scipy.linalg.hadamard), closed forms, invariants
+(orthogonality, Parseval, the weight fold) and brute force on tiny inputs.
+
+Source pages: "A 27B model in 5.5 GB: Bonsai ternary on Ferrox, locally",
+sections "What Bonsai is", "What Ferrox does with it" and "Speed, and where
+it goes".
+"""
+import itertools
+
+import numpy as np
+import pytest
+import scipy.linalg
+import scipy.special
+
+from conftest import read_golden
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+def _f16(bits):
+    return np.asarray(bits, np.uint16).view(np.float16).astype(np.float64)
+
+
+# ---- codec ---------------------------------------------------------------
+
+def test_codec_golden_examples(orc):
+    rows = read_golden("ptq1_codec_examples.txt")
+    for kind, *rest in rows:
+        byte = int(rest[-1])
+        trits = [int(v) for v in rest[:-1]]
+        t = np.zeros((1, 128), np.int8)
+        if kind == "full":
+            t[0, 0:5] = trits            # byte 0 holds weights 0..4
+            wq = orc.pack(t)
+            assert wq[0, 0] == byte, (trits, wq[0, 0], byte)
+        else:
+            t[0, 125:128] = trits        # byte 25 holds weights 125..127
+            wq = orc.pack(t)
+            assert wq[0, 25] == byte, (trits, wq[0, 25], byte)
+        back = orc.unpack(wq, 128)
+        np.testing.assert_array_equal(back, t)
+
+
+def test_codec_roundtrip_all_243_tuples(orc):
+    tuples = list(itertools.product((-1, 0, 1), repeat=5))
+    assert len(tuples) == 243
+    # one row per tuple: byte 0 carries the tuple, the rest of the block is 0
+    t = np.zeros((243, 128), np.int8)
+    t[:, :5] = np.array(tuples, np.int8)
+    wq = orc.pack(t)
+    np.testing.assert_array_equal(orc.unpack(wq, 128), t)
+    assert len(set(wq[:, 0].tolist())) == 243
+
+
+def test_decode_of_every_byte_is_base3_of_floor(orc):
+    # Independent characterisation: the five peeled digits of any byte are the
+    # base-3 digits (most significant first) of floor(243 * byte / 256).
+    for byte in range(256):
+        digits = [orc.peel_digit(byte, n) for n in range(5)]
+        assert all(d in (0, 1, 2) for d in digits)
+        v = (243 * byte) // 256
+        expect = [(v // 3 ** (4 - n)) % 3 for n in range(5)]
+        assert digits == expect, byte
+
+
+def test_peel_is_exact_in_fp32(orc):
+    # The pages state the peel is exact in fp32: every product 3^k * byte / 256
+    # has at most 16 significant bits.  Evaluate it in float32 and compare.
+    for byte in range(256):
+        u = np.float32(byte) / np.float32(256)
+        for n in range(5):
+            a = np.floor(np.float32(3 ** (n + 1)) * u)
+            b = np.floor(np.float32(3 ** n) * u)
+            assert int(a - np.float32(3) * b) == orc.peel_digit(byte, n)
+
+
+def test_pack_refuses_invalid(orc):
+    t = np.zeros((2, 128), np.int8)
+    t[1, 7] = 2
+    with pytest.raises(ValueError):
+        orc.pack(t)
+    with pytest.raises(ValueError):
+        orc.pack(np.zeros((1, 100), np.int8))
+
+
+def test_geometry_matches_pages(orc):
+    g = {k: v for k, v in read_golden("ptq1_geometry.txt")}
+    block = int(g["weights_per_block"])
+    K = 4 * block
+    wq = orc.pack(np.zeros((3, K), np.int8))
+    bytes_per_block = wq.shape[1] // (K // block)
+    assert bytes_per_block * int(g["trits_per_byte"]) >= block
+    bits = (bytes_per_block * 8 + int(g["scale_bits"])) / block
+    assert bits == float(g["bits_per_weight"])
+    # 27e9 weights at 1.75 bits: 5.9e9 bytes = 5.5 GiB, the size on disk
+    gib = float(g["model_params"]) * bits / 8 / 2 ** 30
+    assert abs(gib - float(g["model_gb_on_disk"])) < 0.05
+
+
+# ---- storage decodes -------------------------------------------------------
+
+def test_half_decode_all_patterns(orc):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ours = orc.decode_f16(bits)
+    ref = bits.view(np.float16).astype(np.float64)
+    finite = np.isfinite(ref)
+    np.testing.assert_array_equal(ours[finite], ref[finite])
+    np.testing.assert_array_equal(np.isnan(ours), np.isnan(ref))
+    assert orc.half_to_double(0x0001) == 2.0 ** -24
+
+
+def test_bf16_decode_all_patterns(orc):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ours = orc.decode_bf16(bits)
+    ref = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    finite = np.isfinite(ref)
+    np.testing.assert_array_equal(ours[finite], ref[finite])
+
+
+# ---- rotation --------------------------------------------------------------
+
+def test_fwht_unsigned_is_sylvester_hadamard(orc):
+    rng = np.random.default_rng(1)
+    x = rng.standard_normal((3, 1024))
+    ones = np.ones(1024, np.int8)
+    H = scipy.linalg.hadamard(1024).astype(np.float64)
+    np.testing.assert_allclose(orc.fwht_def(x, ones), x @ H.T / 32, rtol=0, atol=1e-12)
+
+
+def test_fwht_signed_flips_then_rotates(orc):
+    rng = np.random.default_rng(2)
+    x = rng.standard_normal((2, 2048))
+    s = np.where(rng.random(2048) < 0.5, -1, 1).astype(np.int8)
+    H = scipy.linalg.hadamard(1024).astype(np.float64)
+    y = orc.fwht_def(x, s)
+    for b in range(2):
+        sl = slice(1024 * b, 1024 * (b + 1))
+        expect = (x[:, sl] * s[sl]) @ H.T / 32
+        np.testing.assert_allclose(y[:, sl], expect, rtol=0, atol=1e-12)
+
+
+def test_fwht_butterfly_equals_definition(orc):
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((4, 3072))
+    s = np.where(rng.random(3072) < 0.5, -1, 1).astype(np.int8)
+    np.testing.assert_allclose(orc.fwht(x, s), orc.fwht_def(x, s), rtol=0, atol=1e-12)
+
+
+def test_fwht_unsigned_is_involution(orc):
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((2, 1024))
+    ones = np.ones(1024, np.int8)
+    np.testing.assert_allclose(orc.fwht(orc.fwht(x, ones), ones), x, atol=1e-12)
+
+
+def test_fwht_signed_roundtrip_and_parseval(orc):
+    # R = H D_s / 32 is orthogonal: R^T (R x) = D_s H (R x) / 32 = x.
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((3, 2048))
+    s = np.where(rng.random(2048) < 0.5, -1, 1).astype(np.int8)
+    y = orc.fwht(x, s)
+    np.testing.assert_allclose(np.linalg.norm(y, axis=1), np.linalg.norm(x, axis=1), rtol=1e-13)
+    back = orc.fwht(y, np.ones(2048, np.int8)) * s
+    np.testing.assert_allclose(back, x, atol=1e-12)
+
+
+def test_fwht_unit_vector(orc):
+    s = np.where(np.arange(1024) % 3 == 0, -1, 1).astype(np.int8)
+    e0 = np.zeros((1, 1024))
+    e0[0, 0] = 1.0
+    np.testing.assert_array_equal(orc.fwht_def(e0, s), np.full((1, 1024), s[0] / 32.0))
+
+
+def test_weight_fold_identity(orc):
+    # The fold of "What Bonsai is": a weight multiplied by the rotation,
+    # applied to a rotated activation, gives the plain product:
+    # (W R^T)(R x) = W x, with row n of W R^T equal to R w_n.
+    rng = np.random.default_rng(6)
+    for K in (1024, 2048):
+        W = rng.standard_normal((3, K))
+        x = rng.standard_normal((1, K))
+        s = np.where(rng.random(K) < 0.5, -1, 1).astype(np.int8)
+        folded = orc.fwht(W, s)
+        xr = orc.fwht(x, s)
+        np.testing.assert_allclose(folded @ xr[0], W @ x[0], rtol=1e-12, atol=1e-12)
+
+
+# ---- ternary matmul --------------------------------------------------------
+
+def test_ternary_dot_brute_force(orc):
+    rng = np.random.default_rng(7)
+    N, K, M = 5, 384, 2
+    t = rng.integers(-1, 2, size=(N, K)).astype(np.int8)
+    sbits = (np.abs(rng.standard_normal((N, K // 128))) * 0.02).astype(np.float16).view(np.uint16)
+    x = rng.standard_normal((M, K))
+    y = orc.matmul(orc.pack(t), sbits, x)
+    s = _f16(sbits)
+    for m in range(M):
+        for n in range(N):
+            total = 0.0
+            for b in range(K // 128):
+                plus = minus = 0.0
+                for i in range(128 * b, 128 * (b + 1)):
+                    if t[n, i] == 1:
+                        plus += x[m, i]
+                    elif t[n, i] == -1:
+                        minus += x[m, i]
+                total += s[n, b] * (plus - minus)
+            assert abs(y[m, n] - total) <= 1e-12 * (1 + abs(total))
+
+
+def test_matmul_one_hot_is_exact(orc):
+    rng = np.random.default_rng(8)
+    N, K = 6, 512
+    t = rng.integers(-1, 2, size=(N, K)).astype(np.int8)
+    sbits = (np.abs(rng.standard_normal((N, K // 128))) + 0.5).astype(np.float16).view(np.uint16)
+    wq = orc.pack(t)
+    s = _f16(sbits)
+    for k in (0, 4, 5, 127, 128, 300, 511):
+        x = np.zeros((1, K))
+        x[0, k] = 1.0
+        y = orc.matmul(wq, sbits, x)
+        np.testing.assert_array_equal(y[0], s[:, k // 128] * t[:, k])
+
+
+def test_matmul_special_scales(orc):
+    K = 256
+    ones = np.ones((2, K), np.int8)
+    x = np.arange(K, dtype=np.float64)[None, :]
+    one = np.full((2, 2), 0x3C00, np.uint16)                   # 1.0
+    y = orc.matmul(orc.pack(ones), one, x)
+    assert y[0, 0] == x.sum() and y[0, 1] == x.sum()
+    zero = np.zeros((2, 2), np.uint16)
+    assert not orc.matmul(orc.pack(ones), zero, x).any()
+    sub = np.full((2, 2), 0x0001, np.uint16)                   # 2^-24
+    e = np.zeros((1, K))
+    e[0, 200] = 1.0
+    assert orc.matmul(orc.pack(ones), sub, e)[0, 0] == 2.0 ** -24
+    assert not orc.matmul(orc.pack(np.zeros((2, K), np.int8)), one, x).any()
+
+
+def test_matmul_rows_equals_full(orc, syn):
+    mv = syn.gaussian_matvec(11, 3, 40, 1024)
+    wq = orc.pack(mv.trits)
+    x = orc.decode_f32(mv.x)
+    full = orc.matmul(wq, mv.scales, x)
+    rows = [0, 7, 39, 13]
+    np.testing.assert_array_equal(orc.matmul_rows(wq, mv.scales, x, rows), full[:, rows])
+
+
+# ---- SwiGLU and the feed-forward block ------------------------------------
+
+def test_swiglu_closed_forms(orc):
+    g = np.array([0.0, 40.0, -40.0, 1.5, -1.5, 3.0])
+    one = np.ones_like(g)
+    h = orc.swiglu(g, one)
+    assert h[0] == 0.0
+    assert abs(h[1] - 40.0) < 1e-12 and abs(h[2]) < 1e-12
+    assert abs((h[3] - h[4]) - 1.5) < 1e-15          # silu(a) - silu(-a) = a
+    u = np.array([2.0, 1.0, 1.0, -3.0, 0.5, 0.25])
+    np.testing.assert_allclose(orc.swiglu(g, u), g * scipy.special.expit(g) * u, rtol=1e-14)
+
+
+def test_ffn_against_dense_numpy(orc, syn):
+    # Independent route: dense real-valued weights from the trits and the
+    # numpy fp16 decode, the rotation as the scipy Sylvester matrix.
+    H_, I_, M = 1024, 2048, 2
+    t_gu, s_gu = syn.weights(21, 2 * I_, H_)
+    t_d, s_d = syn.weights(22, H_, I_)
+    s_in = syn.signs(23, 3, H_)
+    s_mid = syn.signs(23, 4, I_)
+    x = syn.normal_f64(23, 2, (M, H_))
+    y = orc.ffn(orc.pack(t_gu), s_gu, orc.pack(t_d), s_d, s_in, s_mid, x)
+
+    Had = scipy.linalg.hadamard(1024).astype(np.float64) / 32
+
+    def rot(v, s):
+        out = np.empty_like(v)
+        for b in range(v.shape[1] // 1024):
+            sl = slice(1024 * b, 1024 * (b + 1))
+            out[:, sl] = (v[:, sl] * s[sl]) @ Had.T
+        return out
+
+    def dense(t, sbits):
+        return t.astype(np.float64) * np.repeat(_f16(sbits), 128, axis=1)
+
+    gu = rot(x, s_in) @ dense(t_gu, s_gu).T
+    h = gu[:, :I_] * scipy.special.expit(gu[:, :I_]) * gu[:, I_:]
+    ref = rot(h, s_mid) @ dense(t_d, s_d).T
+    np.testing.assert_allclose(y, ref, rtol=1e-10, atol=1e-10 * np.abs(ref).max())

@@ -1,0 +1,44 @@
+"""The seeded input generator: determinism, storage rounding, distributions."""
+import numpy as np
+import torch
+
+
+def test_half_rounding_matches_numpy(syn):
+    rng = np.random.default_rng(0)
+    v = np.concatenate([np.abs(rng.standard_normal(20000)) * 0.02,
+                        np.logspace(-9, 4.8, 5000),
+                        [0.0, 6.103515625e-05, 5.96e-8, 2.98e-8, 65504.0, 65519.0]])
+    ours = np.array([syn.half_bits(x) for x in v], np.uint16)
+    np.testing.assert_array_equal(ours, v.astype(np.float16).view(np.uint16))
+
+
+def test_bf16_rounding_matches_torch(syn):
+    f = np.random.default_rng(1).standard_normal(20000).astype(np.float32)
+    ours = np.array([syn.bf16_bits(x) for x in f], np.uint16)
+    ref = torch.from_numpy(f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(ours, ref)
+
+
+def test_deterministic_and_stream_separated(syn):
+    a = syn.trits_uniform(5, 0, (1000,))
+    b = syn.trits_uniform(5, 0, (1000,))
+    c = syn.trits_uniform(5, 1, (1000,))
+    np.testing.assert_array_equal(a, b)
+    assert (a != c).any()
+    # counter-based: a prefix of a longer draw is the shorter draw
+    np.testing.assert_array_equal(syn.normal_f32(3, 2, (4096,))[:100], syn.normal_f32(3, 2, (100,)))
+
+
+def test_distributions(syn):
+    t = syn.trits_uniform(0, 0, (300000,))
+    freq = np.bincount(t + 1, minlength=3) / t.size
+    assert np.all(np.abs(freq - 1 / 3) < 0.005)
+    t = syn.trits_sparse(2, 0, (300000,), 0.4)
+    freq = np.bincount(t + 1, minlength=3) / t.size
+    assert abs(freq[1] - 0.4) < 0.005 and abs(freq[0] - 0.3) < 0.005
+    z = syn.normal_f64(0, 2, (200000,))
+    assert abs(z.mean()) < 0.01 and abs(z.std() - 1) < 0.01
+    s = syn.scales_f16(0, 1, (200000,)).view(np.float16).astype(np.float64)
+    assert abs(s.mean() - 0.02 * np.sqrt(2 / np.pi)) < 2e-4 and (s >= 0).all()
+    # about 0.24% of 0.02|z| fall below the smallest normal fp16 (2^-14)
+    assert 0.001 < (s < 2.0 ** -14).mean() < 0.005
