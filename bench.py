@@ -1,0 +1,398 @@
+"""Benchmark of the PTQ1_0 hot path on one GB300 (or N independent replicas).
+
+Headline workload (decode gate/up): M=1, K=5120, N=17408 PTQ1_0 weights
+(19,496,960 bytes).  One step = rotate the activation (5 signed 1024-blocks)
++ decode GEMV.  Metric: weight bytes per second.  A second line item times
+the prefill GEMM (M=512, K=5120, N=17408, bf16) in TFLOP/s.
+
+Inputs are resident in HBM before the timed region.  Every step uses the next
+of R distinct weight sets (R * 19.5 MB > the 129 MB L2), so no step finds its
+weights in L2.  Steps are captured in CUDA graphs and timed with CUDA events
+on the launching stream; the dominant kernel is also timed on its own.
+
+--impl reference times the CPU oracle (fp64 C, all host cores) on a bounded
+sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+N_ROWS, K_COLS = 17408, 5120
+WEIGHT_BYTES = N_ROWS * (K_COLS // 128) * 28          # 19,496,960
+PREFILL_M = 512
+METRIC = "PTQ1_0 GEMV weight GB/s (% HBM peak) at M=1; prefill GEMM TFLOP/s"
+L2_BYTES = 129 * 2 ** 20
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm": float(p["hbm_gbs"]), "bf16": float(p["bf16_tflops"]),
+                "bf16_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = max(mx, float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx or None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---- our arm -------------------------------------------------------------------
+
+def make_ring(P, torch, syn, R, M, N, K, dtype):
+    """R distinct weight sets (packed once on the host, copied to HBM)."""
+    import ternary_weight_ptq1_gb300  # noqa: F401
+
+    ring = []
+    for r in range(R):
+        t, s = syn.weights(1000 + r, N, K)
+        wq = torch.from_numpy(P.pack(t)).cuda()
+        sc = torch.from_numpy(s.view(np.int16)).cuda()
+        if dtype == "f32":
+            x = torch.from_numpy(syn.normal_f32(1000 + r, 2, (M, K))).cuda()
+        else:
+            x = torch.from_numpy(syn.normal_bf16(1000 + r, 2, (M, K)).view(np.int16)).cuda().view(
+                torch.bfloat16)
+        ring.append((wq, sc, x))
+    return ring
+
+
+def capture(torch, fn, n_steps, start):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(n_steps):
+            fn(start + i)
+    return g
+
+
+def timed_steps(torch, fn, K, W, chunk=500):
+    """W warm-up steps, then exactly K steps in CUDA graphs of <= chunk steps.
+    Returns (elapsed ms, graphs)."""
+    for i in range(W):
+        fn(i)
+    torch.cuda.synchronize()
+    full, rem = divmod(K, chunk)
+    g_full = capture(torch, fn, min(chunk, K), 0) if full else None
+    g_rem = capture(torch, fn, rem, full * chunk) if rem else None
+    # one untimed replay so the graphs are uploaded
+    if g_full:
+        g_full.replay()
+    if g_rem:
+        g_rem.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(full):
+        g_full.replay()
+    if g_rem:
+        g_rem.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    return e0.elapsed_time(e1)
+
+
+_dist = None
+
+
+def barrier():
+    if _dist is not None:
+        _dist.barrier()
+
+
+def max_over_ranks(v: float) -> float:
+    if _dist is None:
+        return v
+    import torch
+
+    t = torch.tensor([v], dtype=torch.float64)
+    _dist.all_reduce(t, op=_dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_ours(args, world, rank):
+    import torch
+
+    import synth as syn
+    import ternary_weight_ptq1_gb300 as P
+
+    P.load()
+    pk = peaks()
+    dev_index = torch.cuda.current_device()
+    R = max(8, int(np.ceil(4 * L2_BYTES / WEIGHT_BYTES)))       # 27 sets, 526 MB
+    ring = make_ring(P, torch, syn, R, 1, N_ROWS, K_COLS, "f32")
+    signs = torch.from_numpy(syn.signs(1, 3, K_COLS)).cuda()
+    xr = [torch.empty((1, K_COLS), device="cuda") for _ in range(R)]
+    ys = [torch.empty((1, N_ROWS), device="cuda") for _ in range(R)]
+
+    def step(i):
+        wq, sc, x = ring[i % R]
+        P.fwht(x, signs, out=xr[i % R])
+        P.matmul(wq, sc, xr[i % R], out=ys[i % R])
+
+    def gemv_only(i):
+        wq, sc, _ = ring[i % R]
+        P.matmul(wq, sc, xr[i % R], out=ys[i % R])
+
+    def fwht_only(i):
+        P.fwht(ring[i % R][2], signs, out=xr[i % R])
+
+    K, W = args.steps, args.warmup
+    with ClockSampler(dev_index) as clk:
+        ms = max_over_ranks(timed_steps(torch, step, K, W))
+        ms_gemv = timed_steps(torch, gemv_only, K, W)
+        ms_fwht = timed_steps(torch, fwht_only, K, W)
+    P.device_check()
+    ms_per_step = ms / K
+    value = world * WEIGHT_BYTES / (ms_per_step * 1e-3) / 1e9       # GB/s, all ranks
+    gemv_bytes = WEIGHT_BYTES + K_COLS * 4 + N_ROWS * 4
+    gemv_us = ms_gemv / K * 1e3
+    achieved = gemv_bytes / (gemv_us * 1e-6) / 1e9
+
+    # e2e through the public API: pinned host x -> device, rotate, GEMV, y -> host
+    xh = torch.from_numpy(syn.normal_f32(77, 2, (1, K_COLS))).pin_memory()
+    yh = torch.empty((1, N_ROWS)).pin_memory()
+    xd = torch.empty((1, K_COLS), device="cuda")
+    E = max(50, min(K, 2000))
+    for i in range(5):
+        xd.copy_(xh, non_blocking=True)
+        P.fwht(xd, signs, out=xr[0])
+        P.matmul(ring[0][0], ring[0][1], xr[0], out=ys[0])
+        yh.copy_(ys[0], non_blocking=True)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for i in range(E):
+        wq, sc, _ = ring[i % R]
+        xd.copy_(xh, non_blocking=True)
+        P.fwht(xd, signs, out=xr[i % R])
+        P.matmul(wq, sc, xr[i % R], out=ys[i % R])
+        yh.copy_(ys[i % R], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1)) / E
+    e2e = world * WEIGHT_BYTES / (ms_e2e * 1e-3) / 1e9
+
+    # prefill GEMM line item (M=512, bf16)
+    pre = None
+    if not args.skip_prefill:
+        pre_R = 8
+        pring = make_ring(P, torch, syn, pre_R, PREFILL_M, N_ROWS, K_COLS, "bf16")
+        pys = [torch.empty((PREFILL_M, N_ROWS), device="cuda", dtype=torch.bfloat16)
+               for _ in range(pre_R)]
+
+        def pstep(i):
+            wq, sc, x = pring[i % pre_R]
+            P.matmul(wq, sc, x, out=pys[i % pre_R])
+
+        pK = max(3, min(K, 200))
+        pms = timed_steps(torch, pstep, pK, max(3, min(W, 10)), chunk=50) / pK
+        flops = 2.0 * PREFILL_M * N_ROWS * K_COLS
+        tf = flops / (pms * 1e-3) / 1e12
+        pre = {"value": round(world * tf, 2), "unit": "TFLOP/s", "ms_per_step": round(pms, 4),
+               "config": {"workload": "prefill GEMM", "M": PREFILL_M, "K": K_COLS, "N": N_ROWS,
+                          "dtype": "bf16 in, fp32 accumulate, bf16 out",
+                          "l2": f"ring of {pre_R} weight/activation sets"},
+               "kernel": P.route(PREFILL_M, P.PTQ_BF16),
+               "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": pk["bf16"],
+                            "unit": "TFLOP/s", "frac": round(tf / pk["bf16"], 4),
+                            "traffic": None, "peak_source": pk["source"] + " burst bf16"}}
+
+    cpu = cpu_baseline(args) if rank == 0 and not args.skip_cpu else None
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": round(ms_per_step, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "decode gate/up: rotate (5 signed 1024-blocks) + PTQ1_0 GEMV",
+                   "M": 1, "K": K_COLS, "N": N_ROWS, "weight_bytes_per_step": WEIGHT_BYTES,
+                   "l2": f"inputs larger than L2: ring of {R} distinct weight sets "
+                         f"({R * WEIGHT_BYTES / 1e6:.0f} MB)",
+                   "parallelism": f"{world} independent replicas" if world > 1 else "single GPU",
+                   "timing": "CUDA graphs of <=500 steps, CUDA events on the launching stream"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm"],
+                     "unit": "GB/s", "frac": round(achieved / pk["hbm"], 4), "traffic": None,
+                     "kernel": P.route(1, P.PTQ_F32), "kernel_us": round(gemv_us, 3),
+                     "bytes_per_launch": gemv_bytes, "peak_source": pk["source"] + " copy bandwidth"},
+        "stage_us": {"fwht": round(ms_fwht / K * 1e3, 3), "gemv": round(gemv_us, 3),
+                     "step": round(ms_per_step * 1e3, 3)},
+        "tokens_per_s_equiv": round(value * 1e9 / 5.906e9, 1),
+        "e2e": {"value": round(e2e, 2), "unit": "GB/s", "h2d_bytes_per_step": K_COLS * 4,
+                "d2h_bytes_per_step": N_ROWS * 4, "ms_per_step": round(ms_e2e, 5),
+                "path": "python ctypes binding, eager launches, pinned host buffers"},
+        "gpu_launches": 2 * K,
+        "clocks": clocks,
+        "prefill": pre,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+
+
+# ---- the oracle arm -------------------------------------------------------------
+
+def _oracle_step(orc, syn, reps):
+    """Rotation + GEMV of the headline workload on the oracle, `reps` times on
+    distinct seeds.  Returns (seconds, weight bytes processed)."""
+    t0 = 0.0
+    done = 0
+    for r in range(reps):
+        t, s = syn.weights(2000 + r, N_ROWS, K_COLS)
+        wq = orc.pack(t)
+        x = orc.decode_f32(syn.normal_f32(2000 + r, 2, (1, K_COLS)))
+        sg = syn.signs(2000 + r, 3, K_COLS)
+        a = time.perf_counter()
+        xr = orc.fwht(x, sg)
+        orc.matmul(wq, s, xr)
+        t0 += time.perf_counter() - a
+        done += WEIGHT_BYTES
+    return t0, done
+
+
+def cpu_baseline(args):
+    import oracle as orc
+    import synth as syn
+
+    reps = max(1, args.cpu_reps)
+    secs, nbytes = _oracle_step(orc, syn, reps)
+    return {"value": round(nbytes / secs / 1e9, 3), "unit": "GB/s", "cores": orc.get_threads(),
+            "kind": "oracle",
+            "sample": f"{reps} full decode gate/up steps (rotation + 17408x5120 GEMV, fp64 C, "
+                      f"OpenMP over output rows), {secs:.2f} s"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import oracle as orc
+    import synth as syn
+
+    K, W = args.steps, args.warmup
+    per = 1  # one full rotation + GEMV per step
+    # warm-up steps are bounded too
+    _oracle_step(orc, syn, min(W, 3))
+    steps = min(K, args.reference_max_steps)
+    secs, nbytes = _oracle_step(orc, syn, steps * per)
+    ms_per_step = secs * 1e3 / steps
+    value = nbytes / secs / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
+        "n_gpus": world, "steps": steps, "warmup": min(W, 3), "ms_per_step": round(ms_per_step, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "decode gate/up: rotate (5 signed 1024-blocks) + PTQ1_0 GEMV",
+                   "M": 1, "K": K_COLS, "N": N_ROWS, "weight_bytes_per_step": WEIGHT_BYTES},
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": orc.get_threads(),
+                         "kind": "oracle",
+                         "sample": f"{steps} full steps (of {K} requested), {secs:.2f} s"},
+        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=100)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-reps", type=int, default=20)
+    ap.add_argument("--reference-max-steps", type=int, default=40)
+    ap.add_argument("--skip-prefill", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    global _dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("gloo")
+        _dist = dist
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        import torch
+
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        run_ours(args, world, rank)
+    if _dist is not None:
+        _dist.barrier()
+        _dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,168 @@
+/*
+ * ptq.h -- C ABI of the GB300 (sm_103a) PTQ1_0 ternary matmul library.
+ *
+ * PTQ1_0 ("A 27B model in 5.5 GB: Bonsai ternary on Ferrox, locally",
+ * section "What Bonsai is"): every weight is -1, 0 or +1; five weights are
+ * packed base-3 into one byte; each run of 128 weights along K (a "block")
+ * has one 16-bit scale.  A block is 26 bytes of trits plus a 2-byte scale,
+ * 1.75 bits per weight.  The stored weights have a 1024-wide signed
+ * Walsh-Hadamard rotation folded in, so activations must be rotated the same
+ * way before every matmul (same section; section "What Ferrox does with
+ * it").
+ *
+ * Layouts (all row-major, all caller-owned):
+ *   trits  int8   N x K, values in {-1, 0, +1}
+ *   wq     uint8  N x (K/128) x 26: row n is (K/128)*26 bytes; inside a block
+ *                 byte j holds weights 5j..5j+4 as base-3 digits (weight 5j
+ *                 most significant, digit = trit + 1); byte 25 holds weights
+ *                 125..127 and two pad digits equal to 1.
+ *   scales uint16 N x (K/128) IEEE binary16 bit patterns (one per block);
+ *                 subnormal scales are honoured exactly.
+ *   signs  int8   K values, each +1 or -1; rotation block b uses
+ *                 signs[1024 b .. 1024 b + 1023].
+ *   x, y   activations: PTQ_F32 -> float, PTQ_BF16 -> bfloat16 bit patterns.
+ *
+ * Conventions:
+ *   - Every call returns a ptq_status and never aborts.  A call that returns
+ *     anything but PTQ_OK has launched nothing.  ptq_last_error() returns a
+ *     message for the calling thread's most recent failure.
+ *   - Device pointers must be 16-byte aligned (signs: 4-byte aligned).
+ *   - Device calls are asynchronous on `stream` (NULL = the legacy default
+ *     stream); the library never synchronises inside a call and allocates no
+ *     device memory.  Scratch memory, where a call needs it, is passed in.
+ *   - Sizes are checked with overflow-safe arithmetic; unsupported
+ *     combinations are refused by name (PTQ_ERR_UNSUPPORTED), never guessed.
+ */
+#ifndef PTQ_H
+#define PTQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define PTQ_API __attribute__((visibility("default")))
+#define PTQ_NODISCARD __attribute__((warn_unused_result))
+#else
+#define PTQ_API
+#define PTQ_NODISCARD
+#endif
+
+/* Same type as cudaStream_t, declared without the CUDA headers. */
+struct CUstream_st;
+typedef struct CUstream_st* ptq_stream_t;
+
+typedef enum ptq_status {
+  PTQ_OK = 0,
+  PTQ_ERR_NULL = 1,        /* a required pointer is NULL */
+  PTQ_ERR_SHAPE = 2,       /* a size is negative, overflows, or breaks a
+                              divisibility rule (K % 128, K % 1024) */
+  PTQ_ERR_ALIGN = 3,       /* a pointer is not aligned as required */
+  PTQ_ERR_VALUE = 4,       /* an input value is invalid (a trit not in
+                              {-1,0,1}, an unknown dtype) */
+  PTQ_ERR_UNSUPPORTED = 5, /* a valid but unsupported (M, dtype) combination */
+  PTQ_ERR_WORKSPACE = 6,   /* workspace missing or too small */
+  PTQ_ERR_CUDA = 7,        /* a CUDA runtime call or launch failed */
+  PTQ_ERR_TIMEOUT = 8      /* a bounded device-side wait ran out */
+} ptq_status;
+
+typedef enum ptq_dtype { PTQ_F32 = 0, PTQ_BF16 = 1 } ptq_dtype;
+
+/* ptq1_pack -- host-side PTQ1_0 encoder (used to build test weights).
+ * Encodes N x K trits into wq (host memory, (K/128)*26 bytes per row) with
+ * digit = trit + 1, v = sum_i d_i 3^(4-i), byte = ceil(256 v / 243).  The
+ * decode it must invert is the peel of "What Ferrox does with it": digit n
+ * of byte is floor(3^(n+1) u) - 3 floor(3^n u), u = byte / 256.
+ * Errors: PTQ_ERR_NULL, PTQ_ERR_SHAPE (N < 0, K <= 0, K % 128 != 0, size
+ * overflow), PTQ_ERR_VALUE (a trit outside {-1,0,1}; wq is then untouched).
+ * Synchronous; touches no GPU. */
+PTQ_API PTQ_NODISCARD ptq_status ptq1_pack(const int8_t* trits, uint8_t* wq,
+                                           int64_t N, int64_t K);
+
+/* ptq1_unpack -- device-side decode of PTQ1_0 bytes into N x K int8 trits,
+ * with the fp32 peel of "What Ferrox does with it".  Bit-exact; exists so
+ * the codec of the matmul kernels can be tested on its own.
+ * wq and trits are device pointers. */
+PTQ_API PTQ_NODISCARD ptq_status ptq1_unpack(const uint8_t* wq, int8_t* trits,
+                                             int64_t N, int64_t K,
+                                             ptq_stream_t stream);
+
+/* ptq_fwht -- signed Walsh-Hadamard rotation of activations
+ * ("What Bonsai is": a 1024-wide butterfly with a sign pattern).  For every
+ * row m and every 1024-block b:
+ *     y[m, 1024b + j] = (1/32) sum_i (-1)^popcount(i & j) s[1024b + i] x[m, 1024b + i]
+ * i.e. flip signs, apply the Sylvester-ordered Hadamard matrix, scale by
+ * 1/32 (which makes the rotation orthogonal).  x, y: M x K of `dtype`
+ * (device); y may equal x (in place); signs: K int8 (device).  Arithmetic is
+ * fp32; a bf16 output is rounded to nearest-even once, at the end.
+ * Errors: PTQ_ERR_NULL, PTQ_ERR_SHAPE (K % 1024 != 0), PTQ_ERR_ALIGN,
+ * PTQ_ERR_VALUE (dtype), PTQ_ERR_CUDA. */
+PTQ_API PTQ_NODISCARD ptq_status ptq_fwht(const void* x, void* y,
+                                          const int8_t* signs, int64_t M,
+                                          int64_t K, ptq_dtype dtype,
+                                          ptq_stream_t stream);
+
+/* ptq_matmul -- y = x W^T for a PTQ1_0 weight W (N x K):
+ *     y[m, n] = sum_b scale[n, b] * sum_{i<128} trit[n, 128b + i] * x[m, 128b + i]
+ * x is M x K and must already be rotated (ptq_fwht) when W carries the fold.
+ * Routing (one table, queryable with ptq_route):
+ *   PTQ_F32,  1 <= M <= 8 : decode GEMV, fp32 in / fp32 accumulate / fp32 out
+ *   PTQ_BF16, M >= 1      : prefill GEMM, bf16 in / fp32 accumulate / bf16 out
+ *   PTQ_F32,  M > 8       : refused with PTQ_ERR_UNSUPPORTED
+ * M == 0 or N == 0 is a no-op.  Requires K % 128 == 0 (fastest at
+ * K % 1024 == 0).  All pointers are device pointers. */
+PTQ_API PTQ_NODISCARD ptq_status ptq_matmul(const uint8_t* wq,
+                                            const uint16_t* scales,
+                                            const void* x, void* y, int64_t M,
+                                            int64_t N, int64_t K,
+                                            ptq_dtype dtype,
+                                            ptq_stream_t stream);
+
+/* ptq_ffn_workspace_bytes -- scratch size ptq_ffn needs for (M, H, I, dtype);
+ * 0 when the arguments are invalid. */
+PTQ_API size_t ptq_ffn_workspace_bytes(int64_t M, int64_t H, int64_t I,
+                                       ptq_dtype dtype);
+
+/* ptq_ffn -- the feed-forward block of "Speed, and where it goes":
+ *     xr = R_in x;  [g; u] = W_gu xr;  h = silu(g) * u;  hr = R_mid h;  y = W_d hr
+ * with silu(a) = a / (1 + e^-a), R_* the signed rotations of ptq_fwht.
+ * wgu_q/wgu_s: the fused gate+up weight, 2I x H, gate rows 0..I-1 then up
+ * rows I..2I-1.  wd_q/wd_s: the down weight, H x I.  signs_in: H values,
+ * signs_mid: I values.  x, y: M x H (x is not modified).  Requires
+ * H % 1024 == 0 and I % 1024 == 0; dtype routing as in ptq_matmul.
+ * workspace: device scratch of at least ptq_ffn_workspace_bytes(...) bytes,
+ * 16-byte aligned, owned by the caller; its contents on return are
+ * unspecified.  Errors as ptq_matmul, plus PTQ_ERR_WORKSPACE. */
+PTQ_API PTQ_NODISCARD ptq_status ptq_ffn(
+    const uint8_t* wgu_q, const uint16_t* wgu_s, const uint8_t* wd_q,
+    const uint16_t* wd_s, const int8_t* signs_in, const int8_t* signs_mid,
+    const void* x, void* y, int64_t M, int64_t H, int64_t I, ptq_dtype dtype,
+    void* workspace, size_t workspace_bytes, ptq_stream_t stream);
+
+/* ptq_route -- the kernel ptq_matmul would run for (M, dtype): writes its
+ * name to *kernel_name (static storage) and returns PTQ_OK, or returns
+ * PTQ_ERR_UNSUPPORTED / PTQ_ERR_VALUE.  Host only. */
+PTQ_API PTQ_NODISCARD ptq_status ptq_route(int64_t M, ptq_dtype dtype,
+                                           const char** kernel_name);
+
+/* ptq_device_check -- synchronises `stream`, then reads and clears the
+ * library's device status word.  Returns PTQ_ERR_TIMEOUT if a bounded
+ * device-side wait in an earlier kernel ran out (that kernel's outputs are
+ * then invalid), PTQ_ERR_CUDA if the stream reports an error, else PTQ_OK. */
+PTQ_API PTQ_NODISCARD ptq_status ptq_device_check(ptq_stream_t stream);
+
+/* ptq_status_str -- static name of a status code. */
+PTQ_API const char* ptq_status_str(ptq_status status);
+
+/* ptq_last_error -- message describing the calling thread's last failure
+ * ("" if none).  Valid until the thread's next library call. */
+PTQ_API const char* ptq_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PTQ_H */

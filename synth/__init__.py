@@ -158,3 +158,26 @@ def gaussian_matvec(seed: int, M: int, N: int, K: int, dtype: str = "f32",
 def gated_pair(seed: int, M: int, K: int):
     """The two N(0,1) factors (a, b) of the decode-down activations."""
     return normal_f64(seed, 2, (M, K)), normal_f64(seed, 5, (M, K))
+
+
+@dataclass
+class FfnLayer:
+    wgu_trits: np.ndarray   # 2I x H
+    wgu_scales: np.ndarray  # 2I x H/128
+    wd_trits: np.ndarray    # H x I
+    wd_scales: np.ndarray   # H x I/128
+    signs_in: np.ndarray    # H
+    signs_mid: np.ndarray   # I
+
+
+def ffn_layer(seed: int, layer: int, H: int, I: int) -> FfnLayer:
+    """Weights and signs of one feed-forward layer (streams offset by 16 * layer)."""
+    base = 16 * layer
+    t_gu, s_gu = weights(seed, 2 * I, H, stream_base=base + 0)
+    t_d, s_d = weights(seed, H, I, stream_base=base + 8)
+    return FfnLayer(t_gu, s_gu, t_d, s_d, signs(seed, base + 4, H), signs(seed, base + 5, I))
+
+
+def ffn_input(seed: int, layer: int, M: int, H: int, dtype: str = "f32") -> np.ndarray:
+    base = 16 * layer
+    return normal_f32(seed, base + 6, (M, H)) if dtype == "f32" else normal_bf16(seed, base + 6, (M, H))

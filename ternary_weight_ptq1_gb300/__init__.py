@@ -1,0 +1,192 @@
+"""Python binding of libptq.so, the GB300 (sm_103a) PTQ1_0 ternary matmul
+library (C ABI in include/ptq.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI.  PyTorch supplies device memory and the current
+stream.  There is no fallback: if the library is missing or a call fails,
+these functions raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import _build
+
+LIB_PATH = _build.LIB
+
+PTQ_F32 = 0
+PTQ_BF16 = 1
+
+STATUS = {
+    0: "PTQ_OK", 1: "PTQ_ERR_NULL", 2: "PTQ_ERR_SHAPE", 3: "PTQ_ERR_ALIGN", 4: "PTQ_ERR_VALUE",
+    5: "PTQ_ERR_UNSUPPORTED", 6: "PTQ_ERR_WORKSPACE", 7: "PTQ_ERR_CUDA", 8: "PTQ_ERR_TIMEOUT",
+}
+
+# Every symbol include/ptq.h declares.
+EXPORTS = ("ptq1_pack", "ptq1_unpack", "ptq_fwht", "ptq_matmul", "ptq_ffn_workspace_bytes",
+           "ptq_ffn", "ptq_route", "ptq_device_check", "ptq_status_str", "ptq_last_error")
+
+
+class PTQError(RuntimeError):
+    def __init__(self, status: int, call: str, message: str):
+        self.status = status
+        self.name = STATUS.get(status, f"status {status}")
+        super().__init__(f"{call}: {self.name}: {message}")
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I32 = ctypes.c_int
+
+
+def load(path: str | None = None):
+    """Load libptq.so (building it first if it is absent)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        _build.build()
+    L = ctypes.CDLL(path)
+    L.ptq1_pack.argtypes = [_P, _P, _I64, _I64]
+    L.ptq1_unpack.argtypes = [_P, _P, _I64, _I64, _P]
+    L.ptq_fwht.argtypes = [_P, _P, _P, _I64, _I64, _I32, _P]
+    L.ptq_matmul.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _P]
+    L.ptq_ffn_workspace_bytes.argtypes = [_I64, _I64, _I64, _I32]
+    L.ptq_ffn_workspace_bytes.restype = ctypes.c_size_t
+    L.ptq_ffn.argtypes = [_P] * 8 + [_I64, _I64, _I64, _I32, _P, ctypes.c_size_t, _P]
+    L.ptq_route.argtypes = [_I64, _I32, ctypes.POINTER(ctypes.c_char_p)]
+    L.ptq_device_check.argtypes = [_P]
+    L.ptq_status_str.argtypes = [_I32]
+    L.ptq_status_str.restype = ctypes.c_char_p
+    L.ptq_last_error.argtypes = []
+    L.ptq_last_error.restype = ctypes.c_char_p
+    for name in ("ptq1_pack", "ptq1_unpack", "ptq_fwht", "ptq_matmul", "ptq_ffn", "ptq_route",
+                 "ptq_device_check"):
+        getattr(L, name).restype = _I32
+    _lib = L
+    return L
+
+
+def _check(status: int, call: str) -> None:
+    if status != 0:
+        msg = load().ptq_last_error().decode(errors="replace")
+        raise PTQError(status, call, msg)
+
+
+def _stream(stream=None) -> ctypes.c_void_p:
+    import torch
+
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t, dtype=None, name="tensor"):
+    import torch
+
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _act_dtype(t):
+    import torch
+
+    if t.dtype == torch.float32:
+        return PTQ_F32
+    if t.dtype == torch.bfloat16:
+        return PTQ_BF16
+    raise TypeError(f"activations must be float32 or bfloat16, got {t.dtype}")
+
+
+# ---- host encoder ------------------------------------------------------------
+
+def pack(trits: np.ndarray) -> np.ndarray:
+    """ptq1_pack: N x K int8 trits -> N x (K/128*26) uint8 (host)."""
+    trits = np.ascontiguousarray(trits, dtype=np.int8)
+    if trits.ndim != 2:
+        raise ValueError("trits must be 2-D")
+    N, K = trits.shape
+    out = np.empty((N, (K // 128) * 26 if K % 128 == 0 else 0), np.uint8)
+    _check(load().ptq1_pack(ctypes.c_void_p(trits.ctypes.data), ctypes.c_void_p(out.ctypes.data),
+                            N, K), "ptq1_pack")
+    return out
+
+
+# ---- device calls --------------------------------------------------------------
+
+def unpack(wq, K: int, stream=None):
+    import torch
+
+    N = wq.shape[0]
+    out = torch.empty((N, K), dtype=torch.int8, device=wq.device)
+    _check(load().ptq1_unpack(_dev(wq, torch.uint8, "wq"), _dev(out), N, K, _stream(stream)),
+           "ptq1_unpack")
+    return out
+
+
+def fwht(x, signs, out=None, stream=None):
+    """Signed 1024-wide rotation of the rows of x (in place when out is x)."""
+    import torch
+
+    y = torch.empty_like(x) if out is None else out
+    M, K = x.shape
+    _check(load().ptq_fwht(_dev(x, None, "x"), _dev(y, x.dtype, "out"), _dev(signs, torch.int8, "signs"),
+                           M, K, _act_dtype(x), _stream(stream)), "ptq_fwht")
+    return y
+
+
+def matmul(wq, scales, x, out=None, stream=None):
+    """y = x W^T, W the PTQ1_0 weight (N x K); x M x K (float32 or bfloat16)."""
+    import torch
+
+    M, K = x.shape
+    N = wq.shape[0]
+    y = torch.empty((M, N), dtype=x.dtype, device=x.device) if out is None else out
+    _check(load().ptq_matmul(_dev(wq, torch.uint8, "wq"), _dev(scales, torch.int16, "scales"),
+                             _dev(x, None, "x"), _dev(y, x.dtype, "out"), M, N, K, _act_dtype(x),
+                             _stream(stream)), "ptq_matmul")
+    return y
+
+
+def ffn_workspace_bytes(M: int, H: int, I: int, dtype: int) -> int:
+    return int(load().ptq_ffn_workspace_bytes(M, H, I, dtype))
+
+
+def ffn(wgu_q, wgu_s, wd_q, wd_s, signs_in, signs_mid, x, out=None, workspace=None, stream=None):
+    """The feed-forward block: rotate, gate+up, SwiGLU, rotate, down."""
+    import torch
+
+    M, H = x.shape
+    I = signs_mid.shape[0]
+    dt = _act_dtype(x)
+    need = ffn_workspace_bytes(M, H, I, dt)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
+    y = torch.empty_like(x) if out is None else out
+    _check(load().ptq_ffn(_dev(wgu_q, torch.uint8, "wgu_q"), _dev(wgu_s, torch.int16, "wgu_s"),
+                          _dev(wd_q, torch.uint8, "wd_q"), _dev(wd_s, torch.int16, "wd_s"),
+                          _dev(signs_in, torch.int8, "signs_in"),
+                          _dev(signs_mid, torch.int8, "signs_mid"), _dev(x, None, "x"),
+                          _dev(y, x.dtype, "out"), M, H, I, dt, _dev(workspace, None, "workspace"),
+                          workspace.numel() * workspace.element_size(), _stream(stream)),
+           "ptq_ffn")
+    return y
+
+
+def route(M: int, dtype: int) -> str:
+    name = ctypes.c_char_p()
+    _check(load().ptq_route(M, dtype, ctypes.byref(name)), "ptq_route")
+    return name.value.decode()
+
+
+def device_check(stream=None) -> None:
+    _check(load().ptq_device_check(_stream(stream)), "ptq_device_check")

@@ -1,0 +1,330 @@
+// api.cu -- the C ABI: argument validation, the (M, dtype) routing table,
+// the host-side PTQ1_0 encoder and error reporting.  Every public entry point
+// validates everything before it launches anything.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "ptq_internal.cuh"
+
+namespace ptq {
+
+static thread_local char t_msg[512];
+
+ptq_status fail(ptq_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_msg, sizeof t_msg, fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+ptq_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(PTQ_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e),
+              cudaGetErrorString(e));
+}
+
+// ---- device status word ----------------------------------------------------
+static __device__ int g_device_status;
+static constexpr int kMaxDevices = 64;
+static int* g_status_ptr[kMaxDevices];
+static std::once_flag g_status_once[kMaxDevices];
+
+int* device_status_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return nullptr;
+  std::call_once(g_status_once[dev], [dev] {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) == cudaSuccess)
+      g_status_ptr[dev] = static_cast<int*>(p);
+  });
+  return g_status_ptr[dev];
+}
+
+cudaError_t read_and_clear_device_status(int* out, cudaStream_t st) {
+  int* p = device_status_ptr();
+  if (!p) return cudaErrorInvalidDevice;
+  cudaError_t e = cudaMemcpyAsync(out, p, sizeof(int), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(p, 0, sizeof(int), st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  return e;
+}
+
+// ---- routing table ---------------------------------------------------------
+// The single source of truth for which kernel serves which (dtype, M); both
+// ptq_matmul and ptq_ffn dispatch through it and ptq_route reports it.
+enum class Kernel { GemvF32, GemmBf16 };
+struct Route {
+  ptq_dtype dtype;
+  int64_t m_min, m_max;
+  Kernel kernel;
+  const char* name;
+};
+static const Route kRoutes[] = {
+    {PTQ_F32, 1, 8, Kernel::GemvF32, "gemv_ptq1_f32"},
+    {PTQ_BF16, 1, INT64_MAX, Kernel::GemmBf16, "gemm_ptq1_bf16"},
+};
+
+static const Route* find_route(int64_t M, ptq_dtype dt) {
+  for (const Route& r : kRoutes)
+    if (r.dtype == dt && M >= r.m_min && M <= r.m_max) return &r;
+  return nullptr;
+}
+
+// ---- validation helpers ----------------------------------------------------
+static bool mul_ok(int64_t a, int64_t b, int64_t* out) {
+  if (a < 0 || b < 0) return false;
+  if (a != 0 && b > INT64_MAX / a) return false;
+  *out = a * b;
+  return true;
+}
+
+static bool aligned(const void* p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+static bool dtype_ok(ptq_dtype dt) { return dt == PTQ_F32 || dt == PTQ_BF16; }
+
+static size_t dsize(ptq_dtype dt) { return dt == PTQ_F32 ? 4 : 2; }
+
+}  // namespace ptq
+
+using namespace ptq;
+
+// ---- public ABI ------------------------------------------------------------
+extern "C" {
+
+PTQ_API const char* ptq_status_str(ptq_status s) {
+  switch (s) {
+    case PTQ_OK: return "PTQ_OK";
+    case PTQ_ERR_NULL: return "PTQ_ERR_NULL";
+    case PTQ_ERR_SHAPE: return "PTQ_ERR_SHAPE";
+    case PTQ_ERR_ALIGN: return "PTQ_ERR_ALIGN";
+    case PTQ_ERR_VALUE: return "PTQ_ERR_VALUE";
+    case PTQ_ERR_UNSUPPORTED: return "PTQ_ERR_UNSUPPORTED";
+    case PTQ_ERR_WORKSPACE: return "PTQ_ERR_WORKSPACE";
+    case PTQ_ERR_CUDA: return "PTQ_ERR_CUDA";
+    case PTQ_ERR_TIMEOUT: return "PTQ_ERR_TIMEOUT";
+  }
+  return "PTQ_ERR_UNKNOWN";
+}
+
+PTQ_API const char* ptq_last_error(void) { return t_msg; }
+
+PTQ_API ptq_status ptq_route(int64_t M, ptq_dtype dtype, const char** name) {
+  t_msg[0] = 0;
+  if (!name) return fail(PTQ_ERR_NULL, "ptq_route: kernel_name is NULL");
+  if (!dtype_ok(dtype)) return fail(PTQ_ERR_VALUE, "ptq_route: unknown dtype %d", (int)dtype);
+  const Route* r = find_route(M, dtype);
+  if (!r)
+    return fail(PTQ_ERR_UNSUPPORTED, "no kernel for M=%lld dtype=%s", (long long)M,
+                dtype == PTQ_F32 ? "f32" : "bf16");
+  *name = r->name;
+  return PTQ_OK;
+}
+
+PTQ_API ptq_status ptq1_pack(const int8_t* trits, uint8_t* wq, int64_t N, int64_t K) {
+  t_msg[0] = 0;
+  if (N < 0 || K <= 0 || K % kBlockWeights != 0)
+    return fail(PTQ_ERR_SHAPE, "ptq1_pack: need N >= 0, K > 0, K %% 128 == 0 (N=%lld K=%lld)",
+                (long long)N, (long long)K);
+  int64_t total;
+  if (!mul_ok(N, K, &total)) return fail(PTQ_ERR_SHAPE, "ptq1_pack: N*K overflows");
+  if (total == 0) return PTQ_OK;
+  if (!trits || !wq) return fail(PTQ_ERR_NULL, "ptq1_pack: NULL pointer");
+  for (int64_t i = 0; i < total; ++i)
+    if (trits[i] < -1 || trits[i] > 1)
+      return fail(PTQ_ERR_VALUE, "ptq1_pack: trit %d at index %lld is not in {-1,0,1}",
+                  (int)trits[i], (long long)i);
+  const int64_t nb = K / kBlockWeights;
+  for (int64_t n = 0; n < N; ++n) {
+    for (int64_t b = 0; b < nb; ++b) {
+      const int8_t* t = trits + n * K + b * kBlockWeights;
+      uint8_t* out = wq + (n * nb + b) * kBlockBytes;
+      for (int j = 0; j < kBlockBytes; ++j) {
+        int v = 0;  // sum_i (t_i + 1) 3^(4-i), pads carry digit 1
+        for (int i = 0; i < 5; ++i) {
+          const int pos = 5 * j + i;
+          v = v * 3 + (pos < kBlockWeights ? t[pos] + 1 : 1);
+        }
+        out[j] = static_cast<uint8_t>((v * 256 + 242) / 243);
+      }
+    }
+  }
+  return PTQ_OK;
+}
+
+PTQ_API ptq_status ptq1_unpack(const uint8_t* wq, int8_t* trits, int64_t N, int64_t K,
+                               ptq_stream_t stream) {
+  t_msg[0] = 0;
+  int64_t total;
+  if (N < 0 || K <= 0 || K % kBlockWeights != 0 || !mul_ok(N, K, &total))
+    return fail(PTQ_ERR_SHAPE, "ptq1_unpack: bad shape N=%lld K=%lld", (long long)N,
+                (long long)K);
+  if (total == 0) return PTQ_OK;
+  if (!wq || !trits) return fail(PTQ_ERR_NULL, "ptq1_unpack: NULL pointer");
+  cudaError_t e = launch_unpack(wq, trits, N, K, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq1_unpack launch");
+}
+
+static ptq_status check_fwht(const void* x, const void* y, const int8_t* signs, int64_t M,
+                             int64_t K, ptq_dtype dt, const char* who) {
+  if (!dtype_ok(dt)) return fail(PTQ_ERR_VALUE, "%s: unknown dtype %d", who, (int)dt);
+  int64_t total;
+  if (M < 0 || K <= 0 || K % kRot != 0 || !mul_ok(M, K, &total) ||
+      !mul_ok(total, (int64_t)dsize(dt), &total))
+    return fail(PTQ_ERR_SHAPE, "%s: need M >= 0, K > 0, K %% 1024 == 0 (M=%lld K=%lld)", who,
+                (long long)M, (long long)K);
+  if (M == 0) return PTQ_OK;
+  if (!x || !y || !signs) return fail(PTQ_ERR_NULL, "%s: NULL pointer", who);
+  if (!aligned(x, 16) || !aligned(y, 16) || !aligned(signs, 4))
+    return fail(PTQ_ERR_ALIGN, "%s: x and y need 16-byte, signs 4-byte alignment", who);
+  return PTQ_OK;
+}
+
+PTQ_API ptq_status ptq_fwht(const void* x, void* y, const int8_t* signs, int64_t M, int64_t K,
+                            ptq_dtype dtype, ptq_stream_t stream) {
+  t_msg[0] = 0;
+  ptq_status s = check_fwht(x, y, signs, M, K, dtype, "ptq_fwht");
+  if (s != PTQ_OK || M == 0) return s;
+  cudaError_t e =
+      launch_fwht(x, act_of(dtype), y, act_of(dtype), signs, M, K,
+                  reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq_fwht launch");
+}
+
+static ptq_status check_matmul(const uint8_t* wq, const uint16_t* scales, const void* x,
+                               const void* y, int64_t M, int64_t N, int64_t K, ptq_dtype dt,
+                               const char* who, const Route** route) {
+  if (!dtype_ok(dt)) return fail(PTQ_ERR_VALUE, "%s: unknown dtype %d", who, (int)dt);
+  int64_t t;
+  if (M < 0 || N < 0 || K <= 0 || K % kBlockWeights != 0 || !mul_ok(N, K, &t) ||
+      !mul_ok(M, K, &t) || !mul_ok(M, N, &t) || !mul_ok(t, 4, &t))
+    return fail(PTQ_ERR_SHAPE, "%s: need M, N >= 0, K > 0, K %% 128 == 0 (M=%lld N=%lld K=%lld)",
+                who, (long long)M, (long long)N, (long long)K);
+  if (M == 0 || N == 0) return PTQ_OK;
+  *route = find_route(M, dt);
+  if (!*route)
+    return fail(PTQ_ERR_UNSUPPORTED, "%s: no kernel for M=%lld dtype=%s (fp32 serves M <= 8)",
+                who, (long long)M, dt == PTQ_F32 ? "f32" : "bf16");
+  if (!wq || !scales || !x || !y) return fail(PTQ_ERR_NULL, "%s: NULL pointer", who);
+  if (!aligned(wq, 16) || !aligned(scales, 16) || !aligned(x, 16) || !aligned(y, 16))
+    return fail(PTQ_ERR_ALIGN, "%s: wq, scales, x and y need 16-byte alignment", who);
+  return PTQ_OK;
+}
+
+// x_t / y_t: the GEMV is fp32 in and out; the GEMM reads bf16 (public call)
+// or fp16 (inside the feed-forward block) and writes bf16 (public call) or
+// fp32 (the feed-forward block keeps gate/up in fp32).
+static cudaError_t run_matmul(const Route* r, const uint8_t* wq, const uint16_t* scales,
+                              const void* x, Act x_t, void* y, Act y_t, int64_t M, int64_t N,
+                              int64_t K, cudaStream_t st) {
+  switch (r->kernel) {
+    case Kernel::GemvF32:
+      return launch_gemv(wq, scales, static_cast<const float*>(x), static_cast<float*>(y), M, N,
+                         K, st);
+    case Kernel::GemmBf16:
+      return launch_gemm(wq, scales, x, x_t, y, y_t, M, N, K, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+PTQ_API ptq_status ptq_matmul(const uint8_t* wq, const uint16_t* scales, const void* x, void* y,
+                              int64_t M, int64_t N, int64_t K, ptq_dtype dtype,
+                              ptq_stream_t stream) {
+  t_msg[0] = 0;
+  const Route* r = nullptr;
+  ptq_status s = check_matmul(wq, scales, x, y, M, N, K, dtype, "ptq_matmul", &r);
+  if (s != PTQ_OK || M == 0 || N == 0) return s;
+  cudaError_t e =
+      run_matmul(r, wq, scales, x, act_of(dtype), y, act_of(dtype), M, N, K,
+                 reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq_matmul launch");
+}
+
+// Workspace of ptq_ffn, each region rounded up to 256 bytes:
+//   xr (M x H) | gu (M x 2I, fp32) | h (M x I, fp32) [| hr (M x I, fp16)]
+// fp32 path: xr fp32, h rotated in place.  bf16 path: xr and hr are fp16
+// (the tensor-core operands; 11 significant bits against bf16's 8, and the
+// block scale times a trit is exact in fp16), gate/up and SwiGLU stay fp32,
+// so the only bf16 rounding is the output.
+static bool ffn_layout(int64_t M, int64_t H, int64_t I, ptq_dtype dt, size_t off[4],
+                       size_t* total) {
+  int64_t a, b, c, d = 0;
+  const int64_t ds = (int64_t)dsize(dt);
+  if (!mul_ok(M, H, &a) || !mul_ok(a, ds, &a) || !mul_ok(M, 2 * I, &b) || !mul_ok(b, 4, &b) ||
+      !mul_ok(M, I, &c) || !mul_ok(c, 4, &c))
+    return false;
+  if (dt == PTQ_BF16 && (!mul_ok(M, I, &d) || !mul_ok(d, 2, &d))) return false;
+  auto up = [](int64_t v) { return (v + 255) / 256 * 256; };
+  off[0] = 0;
+  off[1] = (size_t)up(a);
+  off[2] = off[1] + (size_t)up(b);
+  off[3] = off[2] + (size_t)up(c);
+  *total = off[3] + (size_t)up(d);
+  return true;
+}
+
+PTQ_API size_t ptq_ffn_workspace_bytes(int64_t M, int64_t H, int64_t I, ptq_dtype dtype) {
+  size_t off[4], total;
+  if (!dtype_ok(dtype) || M < 0 || H <= 0 || I <= 0 || H % kRot || I % kRot ||
+      I > INT64_MAX / 2 || !ffn_layout(M, H, I, dtype, off, &total))
+    return 0;
+  return total;
+}
+
+PTQ_API ptq_status ptq_ffn(const uint8_t* wgu_q, const uint16_t* wgu_s, const uint8_t* wd_q,
+                           const uint16_t* wd_s, const int8_t* signs_in, const int8_t* signs_mid,
+                           const void* x, void* y, int64_t M, int64_t H, int64_t I,
+                           ptq_dtype dtype, void* ws, size_t ws_bytes, ptq_stream_t stream) {
+  t_msg[0] = 0;
+  const char* who = "ptq_ffn";
+  if (!dtype_ok(dtype)) return fail(PTQ_ERR_VALUE, "%s: unknown dtype %d", who, (int)dtype);
+  if (M < 0 || H <= 0 || I <= 0 || H % kRot || I % kRot || I > INT64_MAX / 4)
+    return fail(PTQ_ERR_SHAPE, "%s: need M >= 0, H and I positive multiples of 1024", who);
+  size_t off[4], need;
+  if (!ffn_layout(M, H, I, dtype, off, &need)) return fail(PTQ_ERR_SHAPE, "%s: size overflow", who);
+  if (M == 0) return PTQ_OK;
+  const Route *r_gu = nullptr, *r_d = nullptr;
+  ptq_status s = check_matmul(wgu_q, wgu_s, x, y, M, 2 * I, H, dtype, who, &r_gu);
+  if (s != PTQ_OK) return s;
+  s = check_matmul(wd_q, wd_s, x, y, M, H, I, dtype, who, &r_d);
+  if (s != PTQ_OK) return s;
+  if (!signs_in || !signs_mid) return fail(PTQ_ERR_NULL, "%s: NULL signs", who);
+  if (!aligned(signs_in, 4) || !aligned(signs_mid, 4))
+    return fail(PTQ_ERR_ALIGN, "%s: signs need 4-byte alignment", who);
+  if (!ws) return fail(PTQ_ERR_WORKSPACE, "%s: workspace is NULL (%zu bytes needed)", who, need);
+  if (ws_bytes < need)
+    return fail(PTQ_ERR_WORKSPACE, "%s: workspace has %zu bytes, %zu needed", who, ws_bytes, need);
+  if (!aligned(ws, 16)) return fail(PTQ_ERR_ALIGN, "%s: workspace needs 16-byte alignment", who);
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char* base = static_cast<char*>(ws);
+  void* xr = base + off[0];
+  float* gu = reinterpret_cast<float*>(base + off[1]);
+  float* h = reinterpret_cast<float*>(base + off[2]);
+  const bool bf = dtype == PTQ_BF16;
+  void* hr = bf ? static_cast<void*>(base + off[3]) : static_cast<void*>(h);
+  const Act op = bf ? Act::F16 : Act::F32;  // tensor-core operand type
+  cudaError_t e = launch_fwht(x, act_of(dtype), xr, op, signs_in, M, H, st);
+  if (e == cudaSuccess) e = run_matmul(r_gu, wgu_q, wgu_s, xr, op, gu, Act::F32, M, 2 * I, H, st);
+  if (e == cudaSuccess) e = launch_swiglu(gu, h, M, I, st);
+  if (e == cudaSuccess) e = launch_fwht(h, Act::F32, hr, op, signs_mid, M, I, st);
+  if (e == cudaSuccess) e = run_matmul(r_d, wd_q, wd_s, hr, op, y, act_of(dtype), M, H, I, st);
+  return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq_ffn launch");
+}
+
+PTQ_API ptq_status ptq_device_check(ptq_stream_t stream) {
+  t_msg[0] = 0;
+  int v = 0;
+  cudaError_t e = read_and_clear_device_status(&v, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "ptq_device_check");
+  if (v & kDevTimeout)
+    return fail(PTQ_ERR_TIMEOUT, "a bounded device-side wait ran out (status word 0x%x)", v);
+  return PTQ_OK;
+}
+
+}  // extern "C"

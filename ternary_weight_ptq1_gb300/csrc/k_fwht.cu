@@ -1,0 +1,146 @@
+// k_fwht.cu -- signed 1024-wide Walsh-Hadamard rotation of activations.
+//
+// "A 27B model in 5.5 GB: Bonsai ternary on Ferrox, locally", section "What
+// Bonsai is": the stored weights carry a 1024-wide butterfly with a sign
+// pattern, so every activation is flipped by the signs, pushed through the
+// Sylvester-ordered Hadamard butterfly and scaled by 1/32 (orthonormal).
+//
+// One warp owns one 1024-element block.  Lane l holds elements
+// 128 j + 4 l + c (j = 0..7, c = 0..3): index bits 0-1 (c) and 7-9 (j) live
+// in registers, bits 2-6 are the lane id.  The ten butterfly stages are the
+// five in-register ones plus five xor-shuffles; H is a tensor product over
+// the index bits, so the stage order is free.  Loads and stores are 16-byte
+// (fp32) or 8-byte (16-bit types) vectors, 512 (256) contiguous bytes per warp
+// instruction.  Arithmetic is fp32 (16-bit outputs are rounded
+// to nearest-even once, at the end); y may alias x because a warp reads its
+// whole block before it writes any of it (in-place needs equal element
+// sizes, which the callers guarantee).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ptq_internal.cuh"
+
+namespace ptq {
+namespace {
+
+// 16-bit storage: decode to fp32 exactly, encode with round-to-nearest-even.
+template <Act T>
+__device__ __forceinline__ float from16(uint32_t bits) {
+  if constexpr (T == Act::BF16) return __uint_as_float(bits << 16);
+  else return __half2float(__ushort_as_half(static_cast<unsigned short>(bits)));
+}
+
+template <Act T>
+__device__ __forceinline__ uint32_t to16(float f) {
+  if constexpr (T == Act::BF16) return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+  else return __half_as_ushort(__float2half_rn(f));
+}
+
+template <Act kIn, Act kOut>
+__global__ void __launch_bounds__(256) fwht1024_kernel(const void* x, void* y,
+                                                       const int8_t* __restrict__ signs,
+                                                       int64_t total_blocks, int64_t blocks_per_row) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t wb = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); wb < total_blocks;
+       wb += nwarps) {
+    const int64_t b = wb % blocks_per_row;
+    const int64_t base = wb * kRot;  // rows are contiguous: row m, block b -> wb * 1024
+    float v[8][4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int64_t e = base + 128 * j + 4 * lane;
+      const uint32_t sg = *reinterpret_cast<const uint32_t*>(signs + b * kRot + 128 * j + 4 * lane);
+      float a[4];
+      if constexpr (kIn != Act::F32) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(x) + e);
+        a[0] = from16<kIn>(raw.x & 0xffffu);
+        a[1] = from16<kIn>(raw.x >> 16);
+        a[2] = from16<kIn>(raw.y & 0xffffu);
+        a[3] = from16<kIn>(raw.y >> 16);
+      } else {
+        const float4 raw = *reinterpret_cast<const float4*>(static_cast<const float*>(x) + e);
+        a[0] = raw.x; a[1] = raw.y; a[2] = raw.z; a[3] = raw.w;
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int s = static_cast<int8_t>((sg >> (8 * c)) & 0xffu);
+        v[j][c] = s < 0 ? -a[c] : a[c];
+      }
+    }
+    // index bits 0 and 1 (c)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float a0 = v[j][0] + v[j][1], a1 = v[j][0] - v[j][1];
+      float a2 = v[j][2] + v[j][3], a3 = v[j][2] - v[j][3];
+      v[j][0] = a0 + a2; v[j][2] = a0 - a2;
+      v[j][1] = a1 + a3; v[j][3] = a1 - a3;
+    }
+    // index bits 7, 8, 9 (j)
+#pragma unroll
+    for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (j & h) continue;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float a = v[j][c], d = v[j + h][c];
+          v[j][c] = a + d;
+          v[j + h][c] = a - d;
+        }
+      }
+    }
+    // index bits 2..6 (lane): partner holds the other element of the pair
+#pragma unroll
+    for (int mask = 1; mask < 32; mask <<= 1) {
+      const float sgn = (lane & mask) ? -1.0f : 1.0f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float p = __shfl_xor_sync(0xffffffffu, v[j][c], mask);
+          v[j][c] = fmaf(sgn, v[j][c], p);  // low: v + p, high: p - v
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int64_t e = base + 128 * j + 4 * lane;
+      const float s = 1.0f / 32.0f;
+      if constexpr (kOut != Act::F32) {
+        uint2 out;
+        out.x = to16<kOut>(v[j][0] * s) | (to16<kOut>(v[j][1] * s) << 16);
+        out.y = to16<kOut>(v[j][2] * s) | (to16<kOut>(v[j][3] * s) << 16);
+        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(y) + e) = out;
+      } else {
+        *reinterpret_cast<float4*>(static_cast<float*>(y) + e) =
+            make_float4(v[j][0] * s, v[j][1] * s, v[j][2] * s, v[j][3] * s);
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_fwht(const void* x, Act in, void* y, Act out, const int8_t* signs,
+                        int64_t M, int64_t K, cudaStream_t st) {
+  const int64_t bpr = K / kRot;
+  const int64_t total = M * bpr;
+  const int warps = 8;
+  int64_t grid = (total + warps - 1) / warps;
+  if (grid > 152 * 64) grid = 152 * 64;
+  const dim3 g((unsigned)grid), b(32 * warps);
+  if (in == Act::F32 && out == Act::F32)
+    fwht1024_kernel<Act::F32, Act::F32><<<g, b, 0, st>>>(x, y, signs, total, bpr);
+  else if (in == Act::BF16 && out == Act::BF16)
+    fwht1024_kernel<Act::BF16, Act::BF16><<<g, b, 0, st>>>(x, y, signs, total, bpr);
+  else if (in == Act::BF16 && out == Act::F16)
+    fwht1024_kernel<Act::BF16, Act::F16><<<g, b, 0, st>>>(x, y, signs, total, bpr);
+  else if (in == Act::F32 && out == Act::F16)
+    fwht1024_kernel<Act::F32, Act::F16><<<g, b, 0, st>>>(x, y, signs, total, bpr);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+}  // namespace ptq

@@ -1,0 +1,54 @@
+// ptq_internal.cuh -- declarations shared by the translation units of the
+// CUDA library (launchers, geometry constants, the device status word).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ptq.h"
+
+namespace ptq {
+
+// PTQ1_0 geometry ("What Bonsai is": 128 weights per 16-bit scale, five
+// trits per byte).
+constexpr int kBlockWeights = 128;
+constexpr int kBlockBytes = 26;   // ceil(128 / 5)
+constexpr int kRot = 1024;        // rotation width
+constexpr int kGroupBlocks = kRot / kBlockWeights;     // 8 blocks per 1024
+constexpr int kGroupBytes = kGroupBlocks * kBlockBytes;  // 208 = 13 * 16
+
+// Activation storage types used inside the library.  F16 never crosses the
+// C ABI: the feed-forward block keeps its rotated tensor-core operands in
+// fp16 (11 significant bits; the block scale times a trit is exact in fp16).
+enum class Act { F32, BF16, F16 };
+inline Act act_of(ptq_dtype d) { return d == PTQ_BF16 ? Act::BF16 : Act::F32; }
+
+// Device status word: bounded waits that run out OR in a code here.
+constexpr int kDevTimeout = 1;
+
+// Records a failure message for ptq_last_error() and returns `s`.
+ptq_status fail(ptq_status s, const char* fmt, ...);
+// Maps a CUDA error to PTQ_ERR_CUDA with a message naming `what`.
+ptq_status cuda_fail(cudaError_t e, const char* what);
+
+// ---- launchers (arguments already validated) -------------------------------
+cudaError_t launch_unpack(const uint8_t* wq, int8_t* trits, int64_t N,
+                          int64_t K, cudaStream_t st);
+// Supported (in, out): (F32, F32), (BF16, BF16), (BF16, F16), (F32, F16).
+cudaError_t launch_fwht(const void* x, Act in, void* y, Act out,
+                        const int8_t* signs, int64_t M, int64_t K, cudaStream_t st);
+cudaError_t launch_gemv(const uint8_t* wq, const uint16_t* scales,
+                        const float* x, float* y, int64_t M, int64_t N,
+                        int64_t K, cudaStream_t st);
+// x is BF16 or F16; y is BF16 or F32.
+cudaError_t launch_gemm(const uint8_t* wq, const uint16_t* scales, const void* x, Act x_t,
+                        void* y, Act y_t, int64_t M, int64_t N, int64_t K, cudaStream_t st);
+// gu: M x 2I fp32 (gate half first) -> h: M x I fp32.
+cudaError_t launch_swiglu(const float* gu, float* h, int64_t M, int64_t I,
+                          cudaStream_t st);
+
+// Device status word access (defined in api.cu).
+cudaError_t read_and_clear_device_status(int* out, cudaStream_t st);
+int* device_status_ptr();
+
+}  // namespace ptq

@@ -1,0 +1,124 @@
+"""The C ABI on the host: the library loads and exports everything the
+header declares, the host encoder matches the oracle's encoder byte for byte,
+arguments are refused by name before anything is launched, and the routing
+table is consistent.  No call here touches a GPU."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def P():
+    import ternary_weight_ptq1_gb300 as P
+
+    P._build.build()
+    P.load()
+    return P
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "ptq.h")).read()
+    return sorted(set(re.findall(r"PTQ_API(?:\s+PTQ_NODISCARD)?\s+[\w\s\*]+?\b(ptq\w+)\s*\(", text)))
+
+
+def test_header_declares_the_exports(P):
+    syms = declared_symbols()
+    assert set(syms) == set(P.EXPORTS), syms
+    lib = ctypes.CDLL(P.LIB_PATH)
+    for s in syms:
+        assert hasattr(lib, s), s
+
+
+def test_no_oracle_in_the_product():
+    pkg = os.path.join(ROOT, "ternary_weight_ptq1_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in text.replace("the oracle", ""), f
+                assert "import synth" not in text, f
+
+
+def test_pack_matches_oracle_pack(P, orc, syn):
+    for seed, N, K, p0 in ((0, 7, 1024, None), (1, 64, 5120, None), (2, 16, 17408, 0.4), (3, 3, 128, None)):
+        t, _ = syn.weights(seed, N, K, p0)
+        np.testing.assert_array_equal(P.pack(t), orc.pack(t))
+    every = np.array(np.meshgrid(*[[-1, 0, 1]] * 5)).reshape(5, -1).T  # 243 tuples
+    t = np.zeros((243, 128), np.int8)
+    t[:, :5] = every
+    t[:, 125:128] = every[:, :3]
+    np.testing.assert_array_equal(P.pack(t), orc.pack(t))
+
+
+def test_pack_refusals(P):
+    with pytest.raises(P.PTQError, match="PTQ_ERR_VALUE"):
+        t = np.zeros((2, 128), np.int8)
+        t[1, 3] = -2
+        P.pack(t)
+    with pytest.raises(P.PTQError, match="PTQ_ERR_SHAPE"):
+        P.pack(np.zeros((2, 100), np.int8))
+    L = P.load()
+    assert L.ptq1_pack(None, None, 4, 128) == 1  # PTQ_ERR_NULL
+    assert L.ptq1_pack(None, None, 0, 128) == 0  # empty is a no-op
+    assert L.ptq1_pack(None, None, 2 ** 62, 2 ** 10) == 2  # N*K overflows
+
+
+def test_refusals_before_launch(P):
+    L = P.load()
+    p16 = ctypes.c_void_p(16 * 1024)   # never dereferenced: every call below is refused
+    odd = ctypes.c_void_p(16 * 1024 + 4)
+    # matmul
+    assert L.ptq_matmul(p16, p16, p16, p16, 1, 8, 100, P.PTQ_F32, None) == 2
+    assert L.ptq_matmul(p16, p16, p16, p16, -1, 8, 128, P.PTQ_F32, None) == 2
+    assert L.ptq_matmul(p16, p16, p16, p16, 9, 8, 128, P.PTQ_F32, None) == 5
+    assert b"M=9" in L.ptq_last_error()
+    assert L.ptq_matmul(p16, p16, p16, p16, 1, 8, 128, 7, None) == 4
+    assert L.ptq_matmul(None, p16, p16, p16, 1, 8, 128, P.PTQ_F32, None) == 1
+    assert L.ptq_matmul(p16, odd, p16, p16, 1, 8, 128, P.PTQ_F32, None) == 3
+    assert L.ptq_matmul(None, None, None, None, 0, 8, 128, P.PTQ_F32, None) == 0
+    assert L.ptq_matmul(None, None, None, None, 4, 0, 128, P.PTQ_BF16, None) == 0
+    assert L.ptq_matmul(p16, p16, p16, p16, 2 ** 40, 2 ** 40, 128, P.PTQ_BF16, None) == 2
+    # rotation
+    assert L.ptq_fwht(p16, p16, p16, 1, 1000, P.PTQ_F32, None) == 2
+    assert L.ptq_fwht(p16, odd, p16, 1, 1024, P.PTQ_F32, None) == 3
+    assert L.ptq_fwht(p16, p16, None, 1, 1024, P.PTQ_F32, None) == 1
+    assert L.ptq_fwht(None, None, None, 0, 1024, P.PTQ_BF16, None) == 0
+    # feed-forward block
+    need = P.ffn_workspace_bytes(1, 1024, 2048, P.PTQ_F32)
+    assert need > 0
+    args = [p16] * 8 + [1, 1024, 2048, P.PTQ_F32]
+    assert L.ptq_ffn(*args, None, need, None) == 6
+    assert L.ptq_ffn(*args, p16, need - 1, None) == 6
+    assert L.ptq_ffn(*([p16] * 8 + [1, 1000, 2048, P.PTQ_F32]), p16, need, None) == 2
+    assert L.ptq_ffn(*([p16] * 8 + [9, 1024, 2048, P.PTQ_F32]), p16, 10 ** 9, None) == 5
+    assert P.ffn_workspace_bytes(1, 1000, 2048, P.PTQ_F32) == 0
+
+
+def test_routing_table(P):
+    for M in range(1, 9):
+        assert P.route(M, P.PTQ_F32) == "gemv_ptq1_f32"
+    for M in (1, 8, 64, 128, 512, 2048, 10 ** 6):
+        assert P.route(M, P.PTQ_BF16).startswith("gemm_ptq1_bf16")
+    with pytest.raises(P.PTQError, match="UNSUPPORTED"):
+        P.route(9, P.PTQ_F32)
+    with pytest.raises(P.PTQError, match="UNSUPPORTED"):
+        P.route(0, P.PTQ_F32)
+
+
+def test_status_strings(P):
+    L = P.load()
+    for code, name in P.STATUS.items():
+        assert L.ptq_status_str(code).decode() == name
+
+
+def test_workspace_sizes(P):
+    M, H, I = 256, 5120, 17408
+    bf = P.ffn_workspace_bytes(M, H, I, P.PTQ_BF16)
+    f = P.ffn_workspace_bytes(1, H, I, P.PTQ_F32)
+    assert bf >= M * H * 2 + M * 2 * I * 4 + M * I * 4 + M * I * 2
+    assert f >= H * 4 + 2 * I * 4 + I * 4

@@ -1,0 +1,157 @@
+"""GPU parity of ptq_matmul against the oracle on the same seeded inputs:
+the decode GEMV (fp32, M <= 8) and the prefill GEMM (bf16), at the workload
+sizes and on small, ragged and degenerate shapes."""
+import numpy as np
+import pytest
+
+import parity as Q
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def P():
+    import torch
+
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import ternary_weight_ptq1_gb300 as P
+
+    P.load()
+    return P
+
+
+def run(P, t, s, x):
+    wq = P.pack(t)
+    xd = Q.dev(x) if x.dtype == np.float32 else Q.dev_bf16(x)
+    return P.matmul(Q.dev(wq), Q.dev(s), xd), wq
+
+
+# ---- decode GEMV (fp32) ------------------------------------------------------
+
+@pytest.mark.parametrize("M", [1])
+def test_tiny_matvec(P, orc, syn, M):
+    mv = syn.gaussian_matvec(0, M, 1024, 1024)
+    y, wq = run(P, mv.trits, mv.scales, mv.x)
+    Q.check_f32(Q.host_f64(y), orc.matmul(orc.pack(mv.trits), mv.scales, Q.x_f64(mv.x)), "tiny")
+
+
+@pytest.mark.parametrize("M", [1, 4])
+def test_decode_gate_up(P, orc, syn, M):
+    mv = syn.gaussian_matvec(1, M, 17408, 5120)
+    y, _ = run(P, mv.trits, mv.scales, mv.x)
+    Q.check_f32(Q.host_f64(y), orc.matmul(orc.pack(mv.trits), mv.scales, Q.x_f64(mv.x)),
+                f"gate/up M={M}")
+
+
+@pytest.mark.parametrize("M", [1, 8])
+def test_decode_down(P, orc, syn, M):
+    t, s = syn.weights(2, 5120, 17408, p_zero=0.4)
+    x = Q.swiglu_like(2, M, 17408)
+    y, _ = run(P, t, s, x)
+    Q.check_f32(Q.host_f64(y), orc.matmul(orc.pack(t), s, Q.x_f64(x)), f"down M={M}")
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 5, 6, 7, 8])
+@pytest.mark.parametrize("N,K", [(1, 1024), (33, 2048), (1000, 3072), (5, 128), (70, 384)])
+def test_gemv_small_shapes(P, orc, syn, M, N, K):
+    mv = syn.gaussian_matvec(100 + M, M, N, K)
+    y, _ = run(P, mv.trits, mv.scales, mv.x)
+    Q.check_f32(Q.host_f64(y), orc.matmul(orc.pack(mv.trits), mv.scales, Q.x_f64(mv.x)),
+                f"gemv M={M} N={N} K={K}")
+
+
+def test_gemv_special_values(P, orc, syn):
+    N, K = 96, 2048
+    x = syn.normal_f32(5, 2, (2, K))
+    # all-zero and all-plus trits, extreme and subnormal scales
+    t = np.zeros((N, K), np.int8)
+    t[32:64] = 1
+    t[64:] = syn.trits_uniform(5, 0, (N - 64, K))
+    s = syn.scales_f16(5, 1, (N, K // 128))
+    s[64:72] = np.arange(1, 1 + 8 * 16, dtype=np.uint16).reshape(8, 16)     # subnormals
+    s[72:74] = 0x7BFF                                                         # 65504
+    s[74] = 0x0000
+    y, _ = run(P, t, s, x)
+    ref = orc.matmul(orc.pack(t), s, Q.x_f64(x))
+    # rows of zero trits: the oracle gives exactly 0; the kernel's telescoped
+    # sum minus the block sum of x leaves fp32 rounding, inside the tolerance
+    Q.check_f32(Q.host_f64(y), ref, "special")
+
+
+def test_gemv_one_hot_is_exact(P, orc, syn):
+    N, K = 64, 1024
+    t, s = syn.weights(6, N, K)
+    s[:] = 0x3C00  # 1.0
+    x = np.zeros((4, K), np.float32)
+    x[0, 0] = 1.0
+    x[1, 127] = 1.0
+    x[2, 128 + 64] = 1.0
+    x[3, 1023] = 1.0
+    y = Q.host_f64(run(P, t, s, x)[0])
+    np.testing.assert_array_equal(y, t[:, [0, 127, 192, 1023]].T.astype(np.float64))
+
+
+def test_gemv_deterministic_and_in_bounds(P, syn):
+    import torch
+
+    mv = syn.gaussian_matvec(8, 4, 3000, 5120)
+    wq = Q.dev(P.pack(mv.trits))
+    s = Q.dev(mv.scales)
+    x = Q.dev(mv.x)
+    guard = 4096
+    buf = torch.full((4 * 3000 + 2 * guard,), float("nan"), device="cuda")
+    out = buf[guard:guard + 4 * 3000].view(4, 3000)
+    P.matmul(wq, s, x, out=out)
+    first = out.clone()
+    for _ in range(3):
+        P.matmul(wq, s, x, out=out)
+        assert torch.equal(out, first)
+    assert torch.isnan(buf[:guard]).all() and torch.isnan(buf[-guard:]).all()
+    assert torch.isfinite(out).all()
+
+
+def test_f32_above_eight_rows_is_refused(P, syn):
+    mv = syn.gaussian_matvec(9, 9, 16, 128)
+    with pytest.raises(P.PTQError, match="UNSUPPORTED"):
+        run(P, mv.trits, mv.scales, mv.x)
+
+
+# ---- prefill GEMM (bf16) -----------------------------------------------------
+
+def _sampled(P, orc, mv, rows, what):
+    y, wq = run(P, mv.trits, mv.scales, mv.x)
+    ref = orc.matmul_rows(wq, mv.scales, Q.x_f64(mv.x), rows)
+    got = Q.host_f64(y)[:, rows]
+    Q.check_bf16(got, ref, what)
+    return y
+
+
+@pytest.mark.parametrize("M", [128, 512, 2048])
+def test_prefill_sampled_rows(P, orc, syn, M):
+    mv = syn.gaussian_matvec(3, M, 17408, 5120, dtype="bf16")
+    rng = np.random.default_rng(M)
+    rows = np.unique(np.concatenate([rng.integers(0, 17408, 192), [0, 1, 127, 128, 17407]]))
+    if M == 2048:
+        rows = rows[:96]
+    _sampled(P, orc, mv, rows, f"prefill M={M}")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 33, 128), (5, 200, 1024), (64, 256, 2048), (130, 300, 1024),
+                                   (128, 128, 5120), (257, 17, 384), (8, 4096, 1024)])
+def test_prefill_small_shapes(P, orc, syn, M, N, K):
+    mv = syn.gaussian_matvec(30 + M, M, N, K, dtype="bf16")
+    y, wq = run(P, mv.trits, mv.scales, mv.x)
+    Q.check_bf16(Q.host_f64(y), orc.matmul(wq, mv.scales, Q.x_f64(mv.x)), f"bf16 {M}x{N}x{K}")
+
+
+def test_prefill_in_bounds(P, syn):
+    import torch
+
+    M, N, K = 130, 300, 1024
+    mv = syn.gaussian_matvec(40, M, N, K, dtype="bf16")
+    guard = 8192
+    buf = torch.full((M * N + 2 * guard,), float("nan"), device="cuda", dtype=torch.bfloat16)
+    out = buf[guard:guard + M * N].view(M, N)
+    P.matmul(Q.dev(P.pack(mv.trits)), Q.dev(mv.scales), Q.dev_bf16(mv.x), out=out)
+    assert torch.isnan(buf[:guard].float()).all() and torch.isnan(buf[-guard:].float()).all()
+    assert torch.isfinite(out.float()).all()
