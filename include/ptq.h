@@ -142,6 +142,32 @@ PTQ_API PTQ_NODISCARD ptq_status ptq_ffn(
     const void* x, void* y, int64_t M, int64_t H, int64_t I, ptq_dtype dtype,
     void* workspace, size_t workspace_bytes, ptq_stream_t stream);
 
+/* ptq_ffn_noalloc -- ptq_ffn without a workspace argument; it allocates
+ * nothing.  (The source pages have no counterpart: this exists for callers,
+ * not for the method.)
+ * Some callers cannot allocate device memory: code running while its stream
+ * is captured into a CUDA graph, real-time decode loops that may not take the
+ * synchronisation and latency of cudaMalloc, and hosts whose device memory is
+ * held by another allocator that a C caller cannot reach.  This entry point
+ * takes the block's scratch from one file-scope device array of
+ * PTQ_FFN_NOALLOC_SCRATCH_BYTES bytes that every device loading the library
+ * holds until the process exits; inputs and output are still the caller's.
+ * Arguments, layouts and errors are those of ptq_ffn; a shape whose scratch
+ * (ptq_ffn_workspace_bytes) exceeds the array is refused with
+ * PTQ_ERR_WORKSPACE.  At the default shapes (H = 5120, I = 17408) that admits
+ * the fp32 decode path up to M = 8 and the bf16 path up to M = 16.
+ * The first call on a device looks the array's device address up
+ * (cudaGetSymbolAddress) and caches it; make that first call before any
+ * stream capture.  All calls share the one array and it keeps the last
+ * call's contents (none of which has to start at zero): calls whose kernels
+ * overlap on the GPU race on it, so order them on one stream. */
+#define PTQ_FFN_NOALLOC_SCRATCH_BYTES (4 * 1024 * 1024)
+PTQ_API PTQ_NODISCARD ptq_status ptq_ffn_noalloc(
+    const uint8_t* wgu_q, const uint16_t* wgu_s, const uint8_t* wd_q,
+    const uint16_t* wd_s, const int8_t* signs_in, const int8_t* signs_mid,
+    const void* x, void* y, int64_t M, int64_t H, int64_t I, ptq_dtype dtype,
+    ptq_stream_t stream);
+
 /* ptq_route -- the kernel ptq_matmul would run for (M, dtype): writes its
  * name to *kernel_name (static storage) and returns PTQ_OK, or returns
  * PTQ_ERR_UNSUPPORTED / PTQ_ERR_VALUE.  Host only. */

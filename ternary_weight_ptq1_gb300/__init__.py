@@ -27,7 +27,11 @@ STATUS = {
 
 # Every symbol include/ptq.h declares.
 EXPORTS = ("ptq1_pack", "ptq1_unpack", "ptq_fwht", "ptq_matmul", "ptq_ffn_workspace_bytes",
-           "ptq_ffn", "ptq_route", "ptq_device_check", "ptq_status_str", "ptq_last_error")
+           "ptq_ffn", "ptq_ffn_noalloc", "ptq_route", "ptq_device_check", "ptq_status_str",
+           "ptq_last_error")
+
+# Size of the built-in scratch array behind ptq_ffn_noalloc (include/ptq.h).
+FFN_NOALLOC_SCRATCH_BYTES = 4 * 1024 * 1024
 
 
 class PTQError(RuntimeError):
@@ -59,14 +63,15 @@ def load(path: str | None = None):
     L.ptq_ffn_workspace_bytes.argtypes = [_I64, _I64, _I64, _I32]
     L.ptq_ffn_workspace_bytes.restype = ctypes.c_size_t
     L.ptq_ffn.argtypes = [_P] * 8 + [_I64, _I64, _I64, _I32, _P, ctypes.c_size_t, _P]
+    L.ptq_ffn_noalloc.argtypes = [_P] * 8 + [_I64, _I64, _I64, _I32, _P]
     L.ptq_route.argtypes = [_I64, _I32, ctypes.POINTER(ctypes.c_char_p)]
     L.ptq_device_check.argtypes = [_P]
     L.ptq_status_str.argtypes = [_I32]
     L.ptq_status_str.restype = ctypes.c_char_p
     L.ptq_last_error.argtypes = []
     L.ptq_last_error.restype = ctypes.c_char_p
-    for name in ("ptq1_pack", "ptq1_unpack", "ptq_fwht", "ptq_matmul", "ptq_ffn", "ptq_route",
-                 "ptq_device_check"):
+    for name in ("ptq1_pack", "ptq1_unpack", "ptq_fwht", "ptq_matmul", "ptq_ffn", "ptq_ffn_noalloc",
+                 "ptq_route", "ptq_device_check"):
         getattr(L, name).restype = _I32
     _lib = L
     return L
@@ -179,6 +184,27 @@ def ffn(wgu_q, wgu_s, wd_q, wd_s, signs_in, signs_mid, x, out=None, workspace=No
                           _dev(y, x.dtype, "out"), M, H, I, dt, _dev(workspace, None, "workspace"),
                           workspace.numel() * workspace.element_size(), _stream(stream)),
            "ptq_ffn")
+    return y
+
+
+def ffn_noalloc(wgu_q, wgu_s, wd_q, wd_s, signs_in, signs_mid, x, out=None, stream=None):
+    """The feed-forward block without a workspace: for callers that cannot
+    allocate device memory (graph capture, real-time loops, memory owned by
+    another allocator).  Its scratch is one built-in device array of
+    FFN_NOALLOC_SCRATCH_BYTES shared by all calls, so calls that overlap on
+    the GPU race; larger shapes raise PTQ_ERR_WORKSPACE.  Only `out` (if not
+    given) is allocated here, by PyTorch, before the call."""
+    import torch
+
+    M, H = x.shape
+    I = signs_mid.shape[0]
+    y = torch.empty_like(x) if out is None else out
+    _check(load().ptq_ffn_noalloc(_dev(wgu_q, torch.uint8, "wgu_q"), _dev(wgu_s, torch.int16, "wgu_s"),
+                                  _dev(wd_q, torch.uint8, "wd_q"), _dev(wd_s, torch.int16, "wd_s"),
+                                  _dev(signs_in, torch.int8, "signs_in"),
+                                  _dev(signs_mid, torch.int8, "signs_mid"), _dev(x, None, "x"),
+                                  _dev(y, x.dtype, "out"), M, H, I, _act_dtype(x), _stream(stream)),
+           "ptq_ffn_noalloc")
     return y
 
 
