@@ -64,7 +64,8 @@ struct Route {
   const char* name;
 };
 static const Route kRoutes[] = {
-    {PTQ_F32, 1, 8, Kernel::GemvF32, "gemv_ptq1_f32"},
+    {PTQ_F32, 1, 1, Kernel::GemvF32, "gemv_ptq1_f32_m1_tc"},
+    {PTQ_F32, 2, 8, Kernel::GemvF32, "gemv_ptq1_f32"},
     {PTQ_BF16, 1, INT64_MAX, Kernel::GemmBf16, "gemm_ptq1_bf16"},
 };
 

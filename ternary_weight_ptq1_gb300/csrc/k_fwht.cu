@@ -14,7 +14,9 @@
 // instruction.  Arithmetic is fp32 (16-bit outputs are rounded
 // to nearest-even once, at the end); y may alias x because a warp reads its
 // whole block before it writes any of it (in-place needs equal element
-// sizes, which the callers guarantee).
+// sizes, which the callers guarantee).  Launched with programmatic
+// dependent launch: it lets its consumer start at once and waits for its
+// own producer before reading x.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -42,6 +44,8 @@ __global__ void __launch_bounds__(256) fwht1024_kernel(const void* x, void* y,
                                                        int64_t total_blocks, int64_t blocks_per_row) {
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  pdl_release();  // the consumer's prologue (its weight prefetch) may start now
+  pdl_wait();     // x may come from the previous kernel
   for (int64_t wb = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); wb < total_blocks;
        wb += nwarps) {
     const int64_t b = wb % blocks_per_row;
@@ -131,16 +135,14 @@ cudaError_t launch_fwht(const void* x, Act in, void* y, Act out, const int8_t* s
   if (grid > 152 * 64) grid = 152 * 64;
   const dim3 g((unsigned)grid), b(32 * warps);
   if (in == Act::F32 && out == Act::F32)
-    fwht1024_kernel<Act::F32, Act::F32><<<g, b, 0, st>>>(x, y, signs, total, bpr);
-  else if (in == Act::BF16 && out == Act::BF16)
-    fwht1024_kernel<Act::BF16, Act::BF16><<<g, b, 0, st>>>(x, y, signs, total, bpr);
-  else if (in == Act::BF16 && out == Act::F16)
-    fwht1024_kernel<Act::BF16, Act::F16><<<g, b, 0, st>>>(x, y, signs, total, bpr);
-  else if (in == Act::F32 && out == Act::F16)
-    fwht1024_kernel<Act::F32, Act::F16><<<g, b, 0, st>>>(x, y, signs, total, bpr);
-  else
-    return cudaErrorInvalidValue;
-  return cudaGetLastError();
+    return launch_pdl(fwht1024_kernel<Act::F32, Act::F32>, g, b, 0, st, x, y, signs, total, bpr);
+  if (in == Act::BF16 && out == Act::BF16)
+    return launch_pdl(fwht1024_kernel<Act::BF16, Act::BF16>, g, b, 0, st, x, y, signs, total, bpr);
+  if (in == Act::BF16 && out == Act::F16)
+    return launch_pdl(fwht1024_kernel<Act::BF16, Act::F16>, g, b, 0, st, x, y, signs, total, bpr);
+  if (in == Act::F32 && out == Act::F16)
+    return launch_pdl(fwht1024_kernel<Act::F32, Act::F16>, g, b, 0, st, x, y, signs, total, bpr);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace ptq

@@ -21,10 +21,12 @@
 //
 // Work split: a CTA owns 32 rows (lane = row) and its warps split the row's
 // 1024-wide groups (8 blocks = 208 bytes = 13 x 16 B, loaded with 16-byte
-// vector loads; each block of each row is read exactly once).  Coefficients
-// live in shared memory; all lanes of a warp read the same coefficient
-// (broadcast).  Partial sums are reduced across warps in a fixed order, so
-// results are bitwise reproducible.
+// vector loads; each block of each row is read exactly once).  Each warp
+// issues the loads of its first group before the CTA builds the coefficient
+// table, so the weight stream overlaps the table build.  Coefficients live in
+// shared memory; all lanes of a warp read the same coefficient (broadcast).
+// Partial sums are reduced across warps in a fixed order, so results are
+// bitwise reproducible.
 #include <cuda_fp16.h>
 
 #include "ptq_internal.cuh"
@@ -34,7 +36,7 @@ namespace {
 
 constexpr int kCoef = kGroupBytes * 5;       // 1040 coefficients per group
 constexpr int kGroupStride = kCoef + 8;      // + E_b for the 8 blocks
-constexpr int kTableBudget = 160 * 1024;     // bytes of shared memory for tables
+constexpr int kSmemBudget = 200 * 1024;      // bytes: x staging + tables
 
 __device__ __forceinline__ float floor_pow3(float tb, int j) {
   // tb = 2^23 + byte; returns floor(3^j byte / 256) (exact)
@@ -45,53 +47,67 @@ __device__ __forceinline__ float floor_pow3(float tb, int j) {
   return __fmaf_rd(tb, mul, add) - 8388608.0f;
 }
 
-// Builds the coefficient table of groups [g0, g0 + gp) for all M tokens.
-// Layout per (m, group slot): quad q = p / 4 of byte positions, coefficient
-// index jf (0..4 for f_1..f_5), lane e = p % 4:  [q * 20 + jf * 4 + e], then
-// E_b at [1040 + b].
+// Builds the coefficient tables of groups [g0, g0 + gp) for all M tokens.
+// x is first staged in shared memory (xs: M x gp x 1024) with 16-byte loads.
+// Table layout per (m, group slot): quad q = p / 4 of byte positions,
+// coefficient jf (0..4 for f_1..f_5), lane e = p % 4: [q * 20 + jf * 4 + e];
+// then E_b, the block sums of x, at [1040 + b], reduced with warp shuffles.
 template <int M>
-__device__ void build_table(float* tab, const float* __restrict__ x, int K, int g0, int gp) {
-  const int per = gp * kGroupStride;
-  for (int i = threadIdx.x; i < M * per; i += blockDim.x) {
-    const int m = i / per;
-    const int r = i - m * per;
-    const int gs = r / kGroupStride;
-    const int slot = r - gs * kGroupStride;
-    const float* xg = x + (size_t)m * K + (size_t)(g0 + gs) * kRot;
-    float v;
-    if (slot < kCoef) {
-      const int q = slot / 20, jf = (slot % 20) / 4, e = slot % 4;
-      const int p = 4 * q + e;
-      const int bl = p / kBlockBytes, jj = p % kBlockBytes;
-      const float* xb = xg + bl * kBlockWeights;
-      auto xv = [&](int n) { return 5 * jj + n < kBlockWeights ? xb[5 * jj + n] : 0.0f; };
-      v = jf < 4 ? fmaf(-3.0f, xv(jf + 1), xv(jf)) : xv(4);
-    } else {
-      const float* xb = xg + (slot - kCoef) * kBlockWeights;
-      float s = 0.0f;
-      for (int t = 0; t < kBlockWeights; ++t) s += xb[t];
-      v = s;
-    }
-    tab[i] = v;
+__device__ void build_table(float* tab, float* xs, const float* __restrict__ x, int K, int g0,
+                            int gp) {
+  const int per_x = gp * kRot;
+  for (int i = threadIdx.x; i < M * per_x / 4; i += blockDim.x) {
+    const int m = (4 * i) / per_x, r = 4 * i - m * per_x;
+    reinterpret_cast<float4*>(xs)[i] =
+        __ldg(reinterpret_cast<const float4*>(x + (size_t)m * K + (size_t)g0 * kRot + r));
   }
+  __syncthreads();
+  const int per = gp * kGroupStride;
+  for (int i = threadIdx.x; i < M * gp * kCoef; i += blockDim.x) {
+    const int mg = i / kCoef, slot = i - mg * kCoef;  // mg = m * gp + gs
+    const int q = slot / 20, jf = (slot % 20) / 4, e = slot % 4;
+    const int p = 4 * q + e;
+    const int bl = p / kBlockBytes, jj = p % kBlockBytes;
+    const float* xb = xs + mg * kRot + bl * kBlockWeights;
+    auto xv = [&](int n) { return 5 * jj + n < kBlockWeights ? xb[5 * jj + n] : 0.0f; };
+    tab[mg * kGroupStride + slot] = jf < 4 ? fmaf(-3.0f, xv(jf + 1), xv(jf)) : xv(4);
+  }
+  const int lane = threadIdx.x & 31;
+  for (int wb = threadIdx.x >> 5; wb < M * gp * kGroupBlocks; wb += blockDim.x >> 5) {
+    const int mg = wb / kGroupBlocks, b = wb % kGroupBlocks;
+    const float4 v = reinterpret_cast<const float4*>(xs + mg * kRot + b * kBlockWeights)[lane];
+    float sum = (v.x + v.y) + (v.z + v.w);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane == 0) tab[mg * kGroupStride + kCoef + b] = sum;
+  }
+  (void)per;
+}
+
+// 16-byte read-only load issued where it is written: a volatile asm keeps
+// the compiler from sinking it to its first use, so all loads of a group are
+// in flight together instead of paying one memory latency each.
+__device__ __forceinline__ void ld16(const void* p, uint32_t& a, uint32_t& b, uint32_t& c,
+                                     uint32_t& d) {
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+               : "l"(p));
+}
+
+// One lane = one row: the 208 bytes of group g (13 x 16 B) and its 8 scales.
+__device__ __forceinline__ void load_group(const uint8_t* __restrict__ wq,
+                                           const uint16_t* __restrict__ scales, int row, int g,
+                                           int row_bytes, int nblk, uint32_t w[52],
+                                           uint32_t sw[4]) {
+  const uint8_t* src = wq + (size_t)row * row_bytes + (size_t)g * kGroupBytes;
+#pragma unroll
+  for (int i = 0; i < 13; ++i) ld16(src + 16 * i, w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+  ld16(scales + (size_t)row * nblk + 8 * g, sw[0], sw[1], sw[2], sw[3]);
 }
 
 template <int M>
-__device__ __forceinline__ void process_group(const uint8_t* __restrict__ wq,
-                                              const uint16_t* __restrict__ scales,
-                                              const float* tab, int per, int row, int g,
-                                              int row_bytes, int nblk, float acc[M]) {
-  const uint4* src = reinterpret_cast<const uint4*>(wq + (size_t)row * row_bytes +
-                                                    (size_t)g * kGroupBytes);
-  uint32_t w[52];
-#pragma unroll
-  for (int i = 0; i < 13; ++i) {
-    const uint4 v = __ldg(src + i);
-    w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
-  }
-  const uint4 sraw = __ldg(reinterpret_cast<const uint4*>(scales + (size_t)row * nblk + 8 * g));
-  const uint32_t sw[4] = {sraw.x, sraw.y, sraw.z, sraw.w};
-
+__device__ __forceinline__ void compute_group(const uint32_t w[52], const uint32_t sw[4],
+                                              const float* tab, int per, float acc[M]) {
   float blk[M][2];
 #pragma unroll
   for (int m = 0; m < M; ++m) blk[m][0] = blk[m][1] = 0.0f;
@@ -152,19 +168,27 @@ __global__ void __launch_bounds__(256) gemv_ptq1_f32_kernel(const uint8_t* __res
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const int row = blockIdx.x * 32 + lane;
   const int G = K / kRot, nblk = K / kBlockWeights, row_bytes = nblk * kBlockBytes;
+  float* tab = smem;                                          // M x gp x 1048
+  float* xs = smem + M * groups_per_pass * kGroupStride;      // M x gp x 1024
   float acc[M];
 #pragma unroll
   for (int m = 0; m < M; ++m) acc[m] = 0.0f;
+  uint32_t w[52], sw[4];
 
   for (int g0 = 0; g0 < G; g0 += groups_per_pass) {
     const int gp = min(groups_per_pass, G - g0);
     const int per = gp * kGroupStride;
-    build_table<M>(smem, x, K, g0, gp);
+    int gs = warp;
+    bool have = row < N && gs < gp;
+    if (have) load_group(wq, scales, row, g0 + gs, row_bytes, nblk, w, sw);  // in flight
+    build_table<M>(tab, xs, x, K, g0, gp);                                   // meanwhile
     __syncthreads();
-    if (row < N)
-      for (int gs = warp; gs < gp; gs += nwarps)
-        process_group<M>(wq, scales, smem + gs * kGroupStride, per, row, g0 + gs, row_bytes, nblk,
-                         acc);
+    while (have) {
+      compute_group<M>(w, sw, tab + gs * kGroupStride, per, acc);
+      gs += nwarps;
+      have = gs < gp;
+      if (have) load_group(wq, scales, row, g0 + gs, row_bytes, nblk, w, sw);
+    }
     __syncthreads();
   }
   // fixed-order reduction across warps
@@ -176,7 +200,7 @@ __global__ void __launch_bounds__(256) gemv_ptq1_f32_kernel(const uint8_t* __res
 #pragma unroll
     for (int m = 0; m < M; ++m) {
       float s = 0.0f;
-      for (int w = 0; w < nwarps; ++w) s += red[(w * M + m) * 32 + lane];
+      for (int w2 = 0; w2 < nwarps; ++w2) s += red[(w2 * M + m) * 32 + lane];
       y[(size_t)m * N + row] = s;
     }
   }
@@ -228,11 +252,11 @@ cudaError_t launch_m(const uint8_t* wq, const uint16_t* scales, const float* x, 
     return cudaGetLastError();
   }
   const int G = K / kRot;
-  int gp = kTableBudget / (M * kGroupStride * 4);
+  int gp = kSmemBudget / (M * (kGroupStride + kRot) * 4);
   if (gp > G) gp = G;
   if (gp < 1) gp = 1;
   const int warps = gp < 8 ? gp : 8;
-  size_t smem = (size_t)M * gp * kGroupStride * 4;
+  size_t smem = (size_t)M * gp * (kGroupStride + kRot) * 4;
   const size_t red = (size_t)warps * M * 32 * 4;
   if (smem < red) smem = red;
   static bool attr_set[64] = {};  // per device; setting the attribute twice is harmless
@@ -241,7 +265,7 @@ cudaError_t launch_m(const uint8_t* wq, const uint16_t* scales, const float* x, 
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
     e = cudaFuncSetAttribute(gemv_ptq1_f32_kernel<M>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kTableBudget + 8 * 1024);
+                             kSmemBudget + 8 * 1024);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
@@ -254,6 +278,10 @@ cudaError_t launch_m(const uint8_t* wq, const uint16_t* scales, const float* x, 
 cudaError_t launch_gemv(const uint8_t* wq, const uint16_t* scales, const float* x, float* y,
                         int64_t M, int64_t N, int64_t K, cudaStream_t st) {
   if (N > INT32_MAX || K > INT32_MAX) return cudaErrorInvalidValue;
+  if (M == 1) {  // tensor-core decode when the shape fits it, else the SIMT kernel
+    const cudaError_t e = launch_gemv_m1_tc(wq, scales, x, y, N, K, st);
+    if (e != cudaErrorNotSupported) return e;
+  }
   const int n = (int)N, k = (int)K;
   switch (M) {
     case 1: return launch_m<1>(wq, scales, x, y, n, k, st);

@@ -26,6 +26,31 @@ inline Act act_of(ptq_dtype d) { return d == PTQ_BF16 ? Act::BF16 : Act::F32; }
 // Device status word: bounded waits that run out OR in a code here.
 constexpr int kDevTimeout = 1;
 
+// Launch with programmatic dependent launch allowed: the kernel may start
+// while the previous kernel in the stream is still running, and must run
+// `griddepcontrol.wait` before it touches anything that kernel writes.  Used
+// for kernels whose prologue (weight prefetch) does not depend on it.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Records a failure message for ptq_last_error() and returns `s`.
 ptq_status fail(ptq_status s, const char* fmt, ...);
 // Maps a CUDA error to PTQ_ERR_CUDA with a message naming `what`.
@@ -40,6 +65,10 @@ cudaError_t launch_fwht(const void* x, Act in, void* y, Act out,
 cudaError_t launch_gemv(const uint8_t* wq, const uint16_t* scales,
                         const float* x, float* y, int64_t M, int64_t N,
                         int64_t K, cudaStream_t st);
+// M = 1 decode on the tensor cores (k_gemv_tc.cu); cudaErrorNotSupported
+// when the shape does not fit it (K % 1024 != 0 or shared memory).
+cudaError_t launch_gemv_m1_tc(const uint8_t* wq, const uint16_t* scales, const float* x,
+                              float* y, int64_t N, int64_t K, cudaStream_t st);
 // x is BF16 or F16; y is BF16 or F32.
 cudaError_t launch_gemm(const uint8_t* wq, const uint16_t* scales, const void* x, Act x_t,
                         void* y, Act y_t, int64_t M, int64_t N, int64_t K, cudaStream_t st);

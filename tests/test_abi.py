@@ -100,7 +100,8 @@ def test_refusals_before_launch(P):
 
 
 def test_routing_table(P):
-    for M in range(1, 9):
+    assert P.route(1, P.PTQ_F32) == "gemv_ptq1_f32_m1_tc"
+    for M in range(2, 9):
         assert P.route(M, P.PTQ_F32) == "gemv_ptq1_f32"
     for M in (1, 8, 64, 128, 512, 2048, 10 ** 6):
         assert P.route(M, P.PTQ_BF16).startswith("gemm_ptq1_bf16")
