@@ -95,6 +95,8 @@ __global__ void __launch_bounds__(256) gemm_ptq1_bf16_simt(const uint8_t* __rest
 
 cudaError_t launch_gemm(const uint8_t* wq, const uint16_t* scales, const void* xv, Act x_t,
                         void* y, Act y_t, int64_t M, int64_t N, int64_t K, cudaStream_t st) {
+  const cudaError_t tc = launch_gemm_tc(wq, scales, xv, x_t, y, y_t, M, N, K, st);
+  if (tc != cudaErrorNotSupported) return tc;  // K % 1024 != 0 falls through to SIMT
   const uint16_t* x = static_cast<const uint16_t*>(xv);
   if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return cudaErrorInvalidValue;
   dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM));

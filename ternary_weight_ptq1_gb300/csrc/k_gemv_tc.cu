@@ -56,8 +56,6 @@
 // stops issuing work.
 #include <cuda.h>
 #include <cuda_fp16.h>
-#include <cudaTypedefs.h>
-
 #include <mutex>
 
 #include "ptq_internal.cuh"
@@ -428,35 +426,6 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
 }
 
 // ---- host side ---------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-std::once_flag g_encode_once;
-cudaError_t g_encode_err = cudaSuccess;
-
-cudaError_t get_encoder() {
-  std::call_once(g_encode_once, [] {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                    cudaEnableDefault, &q);
-    if (g_encode_err == cudaSuccess && q != cudaDriverEntryPointSuccess)
-      g_encode_err = cudaErrorNotSupported;
-    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  });
-  return g_encode_err;
-}
-
-cudaError_t encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
-                      uint64_t rows, uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows) {
-  const cuuint64_t dims[2] = {inner, rows};
-  const cuuint64_t strides[1] = {row_bytes};
-  const cuuint32_t box[2] = {box_inner, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 int g_sms[64];
 
 }  // namespace
@@ -500,14 +469,13 @@ cudaError_t launch_gemv_m1_tc(const uint8_t* wq, const uint16_t* scales, const f
     smem = gemv_m1_tc_smem(N, K, grid, warps);
   }
   if (smem > 227 * 1024) return cudaErrorNotSupported;
-  if ((e = get_encoder()) != cudaSuccess) return e;
   const int64_t nblk = K / kBlockWeights, row_bytes = nblk * kBlockBytes;
   CUtensorMap mq, ms;
-  if ((e = encode_2d(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, row_bytes, N, row_bytes, kGroupBytes,
-                     kSlabRows)) != cudaSuccess)
+  if ((e = encode_tma_2d(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, row_bytes, N, row_bytes,
+                         kGroupBytes, kSlabRows, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
     return e;
-  if ((e = encode_2d(&ms, CU_TENSOR_MAP_DATA_TYPE_UINT16, scales, nblk, N, nblk * 2, kGroupBlocks,
-                     kSlabRows)) != cudaSuccess)
+  if ((e = encode_tma_2d(&ms, CU_TENSOR_MAP_DATA_TYPE_UINT16, scales, nblk, N, nblk * 2,
+                         kGroupBlocks, kSlabRows, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
     return e;
   int* status = device_status_ptr();
   if (!status) return cudaErrorInvalidDevice;

@@ -2,6 +2,7 @@
 // CUDA library (launchers, geometry constants, the device status word).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -75,6 +76,17 @@ cudaError_t launch_gemm(const uint8_t* wq, const uint16_t* scales, const void* x
 // gu: M x 2I fp32 (gate half first) -> h: M x I fp32.
 cudaError_t launch_swiglu(const float* gu, float* h, int64_t M, int64_t I,
                           cudaStream_t st);
+
+// Tensor-core GEMM (k_gemm_tc.cu); cudaErrorNotSupported when the shape does
+// not fit it (the caller then uses the SIMT kernel).
+cudaError_t launch_gemm_tc(const uint8_t* wq, const uint16_t* scales, const void* x, Act x_t,
+                           void* y, Act y_t, int64_t M, int64_t N, int64_t K, cudaStream_t st);
+
+// 2-D TMA tensor map over a row-major array (tma_util.cu): `inner` elements
+// per row, `rows` rows `row_bytes` apart, boxes of box_inner x box_rows.
+cudaError_t encode_tma_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base,
+                          uint64_t inner, uint64_t rows, uint64_t row_bytes, uint32_t box_inner,
+                          uint32_t box_rows, CUtensorMapSwizzle swizzle);
 
 // Device status word access (defined in api.cu).
 cudaError_t read_and_clear_device_status(int* out, cudaStream_t st);
