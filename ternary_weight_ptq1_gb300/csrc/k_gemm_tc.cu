@@ -15,16 +15,22 @@
 // to fp16 in shared memory, in place (exact for |x| in fp16's normal range;
 // bf16 values beyond +-65504 are outside the supported domain).
 //
-// Tile: 128 (M) x 128 (N), K consumed in 64-wide slices (one 128-byte
-// swizzle atom of fp16), kStages slices in flight.  Warp roles:
-//   warp 0      TMA producer: A slices (box 64 x 128, 128B swizzle) and, per
+// Tile: 256 (M) x 128 (N): two 128-row accumulators in TMEM share every
+// expanded B slice, so each weight is peeled once per 256 activation rows.
+// K is consumed in 64-wide slices (one 128-byte swizzle atom of fp16),
+// kStages slices in flight.  Warp roles (14 warps):
+//   warp 0      TMA producer: A slices (box 64 x 256, 128B swizzle) and, per
 //               1024-wide group, the packed trits (box 208 B x 128 rows) and
-//               scales (box 8 x 128) into a 2-deep group ring.
-//   warp 1      TMEM allocation; lane 0 issues tcgen05.mma (4 per slice).
-//   warps 2-3   convert bf16 A slices to fp16 in place (idle for fp16 A).
-//   warps 4-7   one thread per weight row: peel the row's bytes and write the
-//               fp16 values t * s in the canonical K-major 128B-swizzled
-//               layout; afterwards, the epilogue (TMEM -> registers -> y).
+//               scales (box 8 x 128) into a 2-deep group ring, one group ahead.
+//   warp 1      TMEM allocation; lane 0 issues tcgen05.mma (8 per slice).
+//   warps 2-5   convert bf16 A slices to fp16 in place (idle for fp16 A).
+//   warps 6-13  expansion: thread (row r, half h) peels the 64 weights of half
+//               h of each 128-weight block of row r.  A table built per CTA
+//               maps each byte value to byte-permute selectors, so every pair
+//               of fp16 outputs is one permute of the per-block bytes
+//               {-s, 0, +s}.  Writes use the canonical K-major 128B-swizzled
+//               layout; afterwards these warps run the epilogue
+//               (TMEM -> registers -> y).
 // Every mbarrier wait is bounded; a wait that runs out raises the device
 // status word, the CTA drains what it has in flight (bounded) and exits.
 #include <cuda.h>
@@ -36,20 +42,24 @@
 namespace ptq {
 namespace {
 
-constexpr int BM = 128, BN = 128, BK = 64;
-constexpr int kStages = 4;
-constexpr int kSliceBytes = BM * BK * 2;                    // 16 KB (A) = BN * BK * 2 (B)
+constexpr int BM = 256, BN = 128, BK = 64, UM = 128;   // UM: rows per MMA
+constexpr int kStages = 3;
+constexpr int kASlice = BM * BK * 2;                        // 32 KB
+constexpr int kBSlice = BN * BK * 2;                        // 16 KB
 constexpr int kQsBytes = BN * kGroupBytes;                  // 26,624
 constexpr int kScBytes = BN * kGroupBlocks * 2;             // 2,048
 constexpr int kGroupBuf = kQsBytes + kScBytes;              // 28,672 = 28 * 1024
-constexpr int kThreads = 256;
+constexpr int kLutBytes = 2 * 256 * 16;                     // even / odd selector tables
+constexpr int kThreads = 14 * 32;
+constexpr int kConvThreads = 128, kExpThreads = 256;
 constexpr uint32_t kWaitLimit = 1u << 22;
 
 // shared memory layout (offsets from a 1024-aligned base)
 constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kStages * kSliceBytes;
-constexpr int kOffQ = kOffB + kStages * kSliceBytes;
-constexpr int kOffBar = kOffQ + 2 * kGroupBuf;
+constexpr int kOffB = kOffA + kStages * kASlice;
+constexpr int kOffQ = kOffB + kStages * kBSlice;
+constexpr int kOffLut = kOffQ + 2 * kGroupBuf;
+constexpr int kOffBar = kOffLut + kLutBytes;
 // barriers: a_full[S], a_ready[S], b_full[S], empty[S], q_full[2], q_empty[2], acc
 constexpr int kNumBars = 4 * kStages + 4 + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;            // tmem base, abort flag
@@ -114,7 +124,7 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
 
 // Instruction descriptor: fp32 accumulator, fp16 A and B, both K-major,
 // N = 128, M = 128.
-constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(UM >> 4) << 24);
 
 __device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
                                          uint32_t accumulate) {
@@ -138,43 +148,118 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int k) {
   return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + (((k >> 3) ^ (r & 7)) << 4) + (k & 7) * 2);
 }
 
-// fp16 bits of t * s for the digit d = t + 1 (s16: fp16 bits of the scale)
-__device__ __forceinline__ uint32_t trit_times(uint32_t d, uint32_t s16) {
-  return d == 1u ? 0u : (d == 2u ? s16 : (s16 ^ 0x8000u));
+// Selector tables.  PRMT picks each output byte from 8 source bytes; the
+// per-block sources are {-s, 0, +s} as fp16 (bytes 0-1, 2-3, 4-5), so digit
+// d = t + 1 of a weight selects bytes 2d and 2d + 1.  For a byte value v with
+// digits d0..d4 (weights 5j .. 5j+4): an even-positioned byte (5j even) is
+// emitted as pairs (d0,d1), (d2,d3) and a low half d4; an odd-positioned
+// byte as a high half d0 and pairs (d1,d2), (d3,d4).  Entry = 4 words:
+// {pair selector, pair selector, half selector, 0}; the straddling pair is
+// the OR of the two half selectors.
+__device__ __forceinline__ uint32_t sel_pair(uint32_t da, uint32_t db) {
+  return (2 * da) | ((2 * da + 1) << 4) | ((2 * db) << 8) | ((2 * db + 1) << 12);
 }
 
-// Peels 64 weights of one row (half `h` of block `bb` in the staged group)
-// into the B slice at `bslice`: the fp16 values t * s, 8 per 16-byte store.
-template <int h>
-__device__ __forceinline__ void expand_half(const unsigned char* qrow, uint32_t s16,
-                                            unsigned char* bslice, int r) {
-  // weights 64h .. 64h + 63 of the block; byte j holds weights 5j .. 5j + 4
-  uint32_t vals[32];  // 64 fp16, two per register, in k order
+__device__ void build_luts(uint4* lut) {
+  for (int i = threadIdx.x; i < 512; i += blockDim.x) {
+    const uint32_t v = i & 255;
+    uint32_t d[5], fprev = 0;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) vals[i] = 0u;
-  constexpr int w0 = 64 * h;
-  constexpr int j_first = w0 / 5, j_last = (w0 + 63) / 5;
-#pragma unroll
-  for (int j = j_first; j <= j_last && j < kBlockBytes; ++j) {
-    const uint32_t byte = qrow[j];
-    uint32_t fprev = 0;
-#pragma unroll
-    for (int n = 0; n < 5; ++n) {
-      const uint32_t pw = n == 0 ? 3u : n == 1 ? 9u : n == 2 ? 27u : n == 3 ? 81u : 243u;
-      const uint32_t fnext = (byte * pw) >> 8;  // floor(3^(n+1) byte / 256)
-      const uint32_t d = fnext - 3u * fprev;
+    for (int n = 0; n < 5; ++n) {  // digit n = floor(3^(n+1) v/256) - 3 floor(3^n v/256)
+      const uint32_t p = n == 0 ? 3u : n == 1 ? 9u : n == 2 ? 27u : n == 3 ? 81u : 243u;
+      const uint32_t fnext = (v * p) >> 8;
+      d[n] = fnext - 3u * fprev;
       fprev = fnext;
-      const int k = 5 * j + n;                    // weight index in the block
-      if (k < w0 || k >= w0 + 64 || k >= kBlockWeights) continue;
-      const int kk = k - w0;
-      vals[kk >> 1] |= trit_times(d, s16) << (16 * (kk & 1));
     }
+    lut[i] = i < 256 ? make_uint4(sel_pair(d[0], d[1]), sel_pair(d[2], d[3]),
+                                  (2 * d[4]) | ((2 * d[4] + 1) << 4), 0u)
+                     : make_uint4(sel_pair(d[1], d[2]), sel_pair(d[3], d[4]),
+                                  ((2 * d[0]) | ((2 * d[0] + 1) << 4)) << 8, 0u);
+  }
+}
+
+// Half h of one 128-weight block of one row: 64 fp16 values t * s written as
+// 8 swizzled 16-byte chunks.  `win` holds the 16-byte-aligned 48 bytes that
+// contain the block, which starts at byte `o` of the window.
+template <int h, int o>
+__device__ __forceinline__ void expand_half(const uint32_t win[12], uint32_t ta, uint32_t tb,
+                                            const unsigned char* lut, unsigned char* bslice,
+                                            int r) {
+  auto byte_of = [&](int j) -> uint32_t {
+    return __byte_perm(win[(o + j) >> 2], 0u, 0x4440u | ((o + j) & 3));
+  };
+  auto even = [&](int j) { return *reinterpret_cast<const uint4*>(lut + byte_of(j) * 16); };
+  auto odd = [&](int j) { return *reinterpret_cast<const uint4*>(lut + 4096 + byte_of(j) * 16); };
+  auto P = [&](uint32_t sel) { return __byte_perm(ta, tb, sel); };
+  uint32_t out[32];
+  int n = 0;
+  if constexpr (h == 0) {
+#pragma unroll
+    for (int j = 0; j < 12; j += 2) {  // bytes 0..11: weights 0..59
+      const uint4 e = even(j), q = odd(j + 1);
+      out[n++] = P(e.x);
+      out[n++] = P(e.y);
+      out[n++] = P(e.z | q.z);
+      out[n++] = P(q.x);
+      out[n++] = P(q.y);
+    }
+    const uint4 e = even(12);  // weights 60..63
+    out[n++] = P(e.x);
+    out[n++] = P(e.y);
+  } else {
+    {
+      const uint4 e = even(12), q = odd(13);  // weights 64..69
+      out[n++] = P(e.z | q.z);
+      out[n++] = P(q.x);
+      out[n++] = P(q.y);
+    }
+#pragma unroll
+    for (int j = 14; j < 24; j += 2) {  // bytes 14..23: weights 70..119
+      const uint4 e = even(j), q = odd(j + 1);
+      out[n++] = P(e.x);
+      out[n++] = P(e.y);
+      out[n++] = P(e.z | q.z);
+      out[n++] = P(q.x);
+      out[n++] = P(q.y);
+    }
+    const uint4 e = even(24), q = odd(25);  // weights 120..127 (byte 25 holds 3)
+    out[n++] = P(e.x);
+    out[n++] = P(e.y);
+    out[n++] = P(e.z | q.z);
+    out[n++] = P(q.x);
   }
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    const uint4 v = make_uint4(vals[4 * c], vals[4 * c + 1], vals[4 * c + 2], vals[4 * c + 3]);
-    *reinterpret_cast<uint4*>(bslice + sw128_off(r, 8 * c)) = v;
+  for (int c = 0; c < 8; ++c)
+    *reinterpret_cast<uint4*>(bslice + sw128_off(r, 8 * c)) =
+        make_uint4(out[4 * c], out[4 * c + 1], out[4 * c + 2], out[4 * c + 3]);
+}
+
+// The 8 blocks of one staged group for this thread's row and half.
+template <int h, int bb = 0>
+__device__ __forceinline__ bool expand_group(const unsigned char* qrow, const uint16_t* srow,
+                                             const unsigned char* lut, unsigned char* smem,
+                                             uint64_t* empty, uint64_t* b_full, int g, int r,
+                                             volatile int* abort_flag) {
+  if constexpr (bb < kGroupBlocks) {
+    constexpr int base16 = (kBlockBytes * bb) & ~15, o = (kBlockBytes * bb) & 15;
+    uint32_t win[12];
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+      const uint4 v = *reinterpret_cast<const uint4*>(qrow + base16 + 16 * i);
+      win[4 * i] = v.x; win[4 * i + 1] = v.y; win[4 * i + 2] = v.z; win[4 * i + 3] = v.w;
+    }
+    const uint32_t s16 = srow[bb];
+    // PRMT sources: bytes 0-1 = -s, 2-3 = 0, 4-5 = +s
+    const uint32_t ta = (s16 ^ 0x8000u), tb = s16;
+    const int kb = g * 16 + bb * 2 + h;
+    const int s = kb % kStages, round = kb / kStages;
+    if (round > 0 && !mbar_wait(&empty[s], (round - 1) & 1, abort_flag)) return false;
+    expand_half<h, o>(win, ta, tb, lut, smem + kOffB + s * kBSlice, r);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_arrive(&b_full[s]);
+    return expand_group<h, bb + 1>(qrow, srow, lut, smem, empty, b_full, g, r, abort_flag);
   }
+  return true;
 }
 
 template <bool kConvertA, bool kOutF32>
@@ -196,6 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_full = q_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 8);
+  const unsigned char* lut = smem + kOffLut;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
@@ -205,22 +291,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&a_full[s], 1);
-      mbar_init(&a_ready[s], 64);
-      mbar_init(&b_full[s], 128);
+      mbar_init(&a_ready[s], kConvThreads);
+      mbar_init(&b_full[s], kExpThreads / 2);
       mbar_init(&empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&q_full[i], 1);
-      mbar_init(&q_empty[i], 128);
+      mbar_init(&q_empty[i], kExpThreads);
     }
     mbar_init(acc_full, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 1) {  // TMEM: 128 fp32 columns x 128 lanes
+  build_luts(reinterpret_cast<uint4*>(smem + kOffLut));
+  if (warp == 1) {  // TMEM: two 128-column fp32 accumulators x 128 lanes
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
-                 "r"(BN)
+                 "r"(2 * BN)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -231,6 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_wait();  // A may come from the previous kernel
 
   bool ok = true;
+  int a_issued = 0;
   if (warp == 0) {
     // ---- TMA producer ----------------------------------------------------------
     if (lane == 0) {
@@ -251,8 +339,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         if (round > 0) ok = mbar_wait(&empty[s], (round - 1) & 1, abort_flag);
         if (!ok) break;
-        mbar_expect_tx(&a_full[s], kSliceBytes);
-        tma_2d(smem_u32(smem + kOffA + s * kSliceBytes), &map_a, kb * BK, m0, &a_full[s]);
+        mbar_expect_tx(&a_full[s], kASlice);
+        tma_2d(smem_u32(smem + kOffA + s * kASlice), &map_a, kb * BK, m0, &a_full[s]);
+        ++a_issued;
       }
     }
   } else if (warp == 1) {
@@ -264,35 +353,36 @@ __global__ void __launch_bounds__(kThreads, 1)
              mbar_wait(&b_full[s], round & 1, abort_flag);
         if (!ok) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint32_t a_addr = smem_u32(smem + kOffA + s * kSliceBytes);
-        const uint32_t b_addr = smem_u32(smem + kOffB + s * kSliceBytes);
+        const uint32_t a_addr = smem_u32(smem + kOffA + s * kASlice);
+        const uint32_t b_addr = smem_u32(smem + kOffB + s * kBSlice);
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)  // K = 16 per MMA: 32 bytes along the atom
-          umma_f16(tmem, sw128_desc(a_addr + 32 * kk), sw128_desc(b_addr + 32 * kk),
-                   (kb | kk) != 0);
+        for (int mh = 0; mh < 2; ++mh)
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)  // K = 16 per MMA: 32 bytes along the atom
+            umma_f16(tmem + mh * BN, sw128_desc(a_addr + mh * (UM * 128) + 32 * kk),
+                     sw128_desc(b_addr + 32 * kk), (kb | kk) != 0);
         umma_commit(&empty[s]);  // frees the slice once these MMAs have read it
       }
       umma_commit(acc_full);     // all MMAs issued by this thread
     }
-  } else if (warp < 4) {
+  } else if (warp < 6) {
     // ---- A conversion bf16 -> fp16, in place ---------------------------------------
     if (kConvertA) {
-      const int t = threadIdx.x - 64;  // 0..63
+      const int t = threadIdx.x - 64;  // 0..127
       for (int kb = 0; kb < nk && ok; ++kb) {
         const int s = kb % kStages, round = kb / kStages;
         ok = mbar_wait(&a_full[s], round & 1, abort_flag);
         if (!ok) break;
-        uint4* a = reinterpret_cast<uint4*>(smem + kOffA + s * kSliceBytes);
+        uint4* a = reinterpret_cast<uint4*>(smem + kOffA + s * kASlice);
 #pragma unroll 4
-        for (int c = t; c < kSliceBytes / 16; c += 64) {
+        for (int c = t; c < kASlice / 16; c += kConvThreads) {
           uint4 v = a[c];
-          uint32_t* w = reinterpret_cast<uint32_t*>(&v);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xFFFF0000u);
-            const __half2 hv = __floats2half2_rn(lo, hi);
-            w[i] = *reinterpret_cast<const uint32_t*>(&hv);
-          }
+          auto cv = [](uint32_t w) {
+            const __half2 h2 =
+                __floats2half2_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+            return (uint32_t)__half_as_ushort(h2.x) | ((uint32_t)__half_as_ushort(h2.y) << 16);
+          };
+          v.x = cv(v.x); v.y = cv(v.y); v.z = cv(v.z); v.w = cv(v.w);
           a[c] = v;
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -300,8 +390,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ---- B expansion: thread r = weight row n0 + r --------------------------------
-    const int r = threadIdx.x - 128;  // 0..127
+    // ---- B expansion: thread (row r, half h) ---------------------------------------
+    const int t = threadIdx.x - 192, r = t & (BN - 1), h = t >> 7;  // h is warp-uniform
     for (int g = 0; g < ng && ok; ++g) {
       const int qb = g & 1;
       ok = mbar_wait(&q_full[qb], (g >> 1) & 1, abort_flag);
@@ -309,24 +399,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const unsigned char* qrow = smem + kOffQ + qb * kGroupBuf + r * kGroupBytes;
       const uint16_t* srow =
           reinterpret_cast<const uint16_t*>(smem + kOffQ + qb * kGroupBuf + kQsBytes) + r * 8;
-#pragma unroll 1
-      for (int bb = 0; bb < kGroupBlocks && ok; ++bb) {
-        const uint32_t s16 = srow[bb];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int kb = g * 16 + bb * 2 + h;
-          const int s = kb % kStages, round = kb / kStages;
-          if (round > 0) ok = mbar_wait(&empty[s], (round - 1) & 1, abort_flag);
-          if (!ok) break;
-          unsigned char* bslice = smem + kOffB + s * kSliceBytes;
-          if (h == 0)
-            expand_half<0>(qrow + bb * kBlockBytes, s16, bslice, r);
-          else
-            expand_half<1>(qrow + bb * kBlockBytes, s16, bslice, r);
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          mbar_arrive(&b_full[s]);
-        }
-      }
+      ok = h == 0 ? expand_group<0>(qrow, srow, lut, smem, empty, b_full, g, r, abort_flag)
+                  : expand_group<1>(qrow, srow, lut, smem, empty, b_full, g, r, abort_flag);
       if (ok) mbar_arrive(&q_empty[qb]);
     }
   }
@@ -335,13 +409,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) atomicOr(status, kDevTimeout);
   }
 
-  // ---- epilogue: warps 4-7 read TMEM lanes 32 (warp % 4) .. + 31 -------------------
-  if (warp >= 4) {
+  // ---- epilogue: warps 6-13; warp w reads TMEM lanes 32 (w % 4) .. + 31 of
+  // accumulator (w - 6) / 4 -------------------------------------------------------------
+  if (warp >= 6) {
     const bool done = !*abort_flag && mbar_wait(acc_full, 0, abort_flag);
     if (done) {
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const int q = warp & 3;
-      const int row = m0 + 32 * q + lane;
+      const int q = warp & 3, mh = (warp - 6) >> 2;
+      const int row = m0 + mh * UM + 32 * q + lane;
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 32) {
         uint32_t v[32];
@@ -355,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
               "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]),
               "=r"(v[30]), "=r"(v[31])
-            : "r"(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0));
+            : "r"(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(mh * BN + c0)));
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
         if (row < M) {
           const int ncol = n0 + c0;
@@ -374,15 +449,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint16_t* out = static_cast<uint16_t*>(y) + (size_t)row * N + ncol;
             uint32_t pk[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const __nv_bfloat162 b2 =
-                  __floats2bfloat162_rn(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-              pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
-            }
+            for (int i = 0; i < 16; ++i)
+              pk[i] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[2 * i]))) |
+                      ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[2 * i + 1])))
+                       << 16);
             if (ncol + 32 <= N && (N & 7) == 0) {
 #pragma unroll
               for (int i = 0; i < 16; i += 4)
-                *reinterpret_cast<uint4*>(out + 2 * i) = make_uint4(pk[i], pk[i + 1], pk[i + 2], pk[i + 3]);
+                *reinterpret_cast<uint4*>(out + 2 * i) =
+                    make_uint4(pk[i], pk[i + 1], pk[i + 2], pk[i + 3]);
             } else {
               for (int i = 0; i < 32 && ncol + i < N; ++i)
                 out[i] = (uint16_t)(pk[i >> 1] >> (16 * (i & 1)));
@@ -399,14 +474,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (*abort_flag && warp == 0 && lane == 0) {
     // let this CTA's copies in flight land before its shared memory goes away
-    for (int s = 0; s < kStages; ++s) static_cast<void>(mbar_wait(&a_full[s], 0, nullptr));
+    for (int kb = (a_issued > kStages ? a_issued - kStages : 0); kb < a_issued; ++kb)
+      static_cast<void>(mbar_wait(&a_full[kb % kStages], (kb / kStages) & 1, nullptr));
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   pdl_release();
   if (warp == 1) {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(BN)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * BN)
                  : "memory");
   }
 }
@@ -436,7 +512,7 @@ cudaError_t launch_gemm_tc(const uint8_t* wq, const uint16_t* scales, const void
   const int64_t nblk = K / kBlockWeights, row_bytes = nblk * kBlockBytes;
   CUtensorMap ma, mq, ms;
   if ((e = encode_tma_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT16, x, K, M, K * 2, BK, BM,
-                         CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+                         CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)  // box 64 x 256
     return e;
   if ((e = encode_tma_2d(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, row_bytes, N, row_bytes,
                          kGroupBytes, BN, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
