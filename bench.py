@@ -360,6 +360,42 @@ def run_reference(args, world, rank):
     print(json.dumps(line))
 
 
+def run_profile_case(which: str):
+    """A few launches of one kernel on a small case sized for an ncu capture:
+    gemv -- decode GEMV, M=1, K=5120, N=8*17408 (156 MB of weights > L2);
+    gemm -- prefill GEMM, M=512, K=5120, N=17408, bf16.  Prints the event
+    time of the last launch (not a bench number)."""
+    import torch
+
+    import synth as syn
+    import ternary_weight_ptq1_gb300 as P
+
+    if which == "gemv":
+        M, N, dt = 1, 8 * N_ROWS, "f32"
+    else:
+        M, N, dt = PREFILL_M, N_ROWS, "bf16"
+    mv = syn.gaussian_matvec(7, M, N, K_COLS, dtype=dt)
+    wq = torch.from_numpy(P.pack(mv.trits)).cuda()
+    sc = torch.from_numpy(mv.scales.view(np.int16)).cuda()
+    if dt == "f32":
+        x = torch.from_numpy(mv.x).cuda()
+        y = torch.empty((M, N), device="cuda")
+    else:
+        x = torch.from_numpy(mv.x.view(np.int16)).cuda().view(torch.bfloat16)
+        y = torch.empty((M, N), device="cuda", dtype=torch.bfloat16)
+    for _ in range(3):
+        P.matmul(wq, sc, x, out=y)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    P.matmul(wq, sc, x, out=y)
+    e1.record()
+    torch.cuda.synchronize()
+    P.device_check()
+    print(json.dumps({"profile_case": which, "M": M, "N": N, "K": K_COLS,
+                      "last_launch_us": round(e0.elapsed_time(e1) * 1e3, 2)}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -370,7 +406,15 @@ def main():
     ap.add_argument("--reference-max-steps", type=int, default=40)
     ap.add_argument("--skip-prefill", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--profile", choices=["gemv", "gemm"],
+                    help="run a small case of one kernel for an ncu capture, then exit")
     args = ap.parse_args()
+    if args.profile:
+        import torch
+
+        torch.cuda.set_device(0)
+        run_profile_case(args.profile)
+        return
     if args.warmup < 3:
         args.warmup = 3
 

@@ -63,7 +63,7 @@ constexpr int kOffBar = kOffLut + kLutBytes;
 // barriers: a_full[S], a_ready[S], b_full[S], empty[S], q_full[2], q_empty[2], acc
 constexpr int kNumBars = 4 * kStages + 4 + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;            // tmem base, abort flag
-constexpr int kSmemBytes = kOffMisc + 16 + 1024;            // + alignment slack
+constexpr int kSmemBytes = kOffMisc + 16;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -268,9 +268,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap map_q,
                    const __grid_constant__ CUtensorMap map_s, void* __restrict__ y, int M, int N,
                    int K, int* status) {
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // No static shared variables: the dynamic window starts at offset 0, so the
+  // declared 1024-byte alignment holds, and every access below stays a
+  // shared-memory instruction (an address laundered through an integer
+  // would turn them into generic ones).
+  extern __shared__ __align__(1024) unsigned char smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint64_t* a_full = bars;
   uint64_t* a_ready = bars + kStages;
