@@ -105,20 +105,38 @@ PTQ_API PTQ_NODISCARD ptq_status ptq_fwht(const void* x, void* y,
                                           int64_t K, ptq_dtype dtype,
                                           ptq_stream_t stream);
 
+/* ptq_matmul_workspace_bytes -- scratch size ptq_matmul needs for
+ * (M, N, K, dtype); 0 when it needs none or the arguments are invalid.
+ * Only the M = 1 fp32 decode path with K/128 even needs scratch: one fp32
+ * partial row sum per (K-chunk of at most 640 weights, output row). */
+PTQ_API size_t ptq_matmul_workspace_bytes(int64_t M, int64_t N, int64_t K,
+                                          ptq_dtype dtype);
+
 /* ptq_matmul -- y = x W^T for a PTQ1_0 weight W (N x K):
  *     y[m, n] = sum_b scale[n, b] * sum_{i<128} trit[n, 128b + i] * x[m, 128b + i]
  * x is M x K and must already be rotated (ptq_fwht) when W carries the fold.
  * Routing (one table, queryable with ptq_route):
- *   PTQ_F32,  1 <= M <= 8 : decode GEMV, fp32 in / fp32 accumulate / fp32 out
+ *   PTQ_F32,  M == 1      : decode GEMV by per-position lookup tables of the
+ *                           five-trit sums (K/128 even; otherwise the
+ *                           general GEMV below), fp32 throughout
+ *   PTQ_F32,  2 <= M <= 8 : decode GEMV with the fp32 peel, fp32 throughout
  *   PTQ_BF16, M >= 1      : prefill GEMM, bf16 in / fp32 accumulate / bf16 out
  *   PTQ_F32,  M > 8       : refused with PTQ_ERR_UNSUPPORTED
  * M == 0 or N == 0 is a no-op.  Requires K % 128 == 0 (fastest at
- * K % 1024 == 0).  All pointers are device pointers. */
+ * K % 1024 == 0).  All pointers are device pointers.
+ * workspace: device scratch of at least ptq_matmul_workspace_bytes(...) bytes,
+ * 16-byte aligned, caller-owned, any initial contents, unspecified contents
+ * on return; may be NULL when that size is 0.  Calls whose kernels overlap
+ * on the GPU need separate workspaces.  Results are bitwise reproducible:
+ * the same inputs give the same bits on every run.
+ * Errors: PTQ_ERR_NULL, PTQ_ERR_SHAPE, PTQ_ERR_ALIGN, PTQ_ERR_VALUE (dtype),
+ * PTQ_ERR_UNSUPPORTED, PTQ_ERR_WORKSPACE, PTQ_ERR_CUDA. */
 PTQ_API PTQ_NODISCARD ptq_status ptq_matmul(const uint8_t* wq,
                                             const uint16_t* scales,
                                             const void* x, void* y, int64_t M,
                                             int64_t N, int64_t K,
-                                            ptq_dtype dtype,
+                                            ptq_dtype dtype, void* workspace,
+                                            size_t workspace_bytes,
                                             ptq_stream_t stream);
 
 /* ptq_ffn_workspace_bytes -- scratch size ptq_ffn needs for (M, H, I, dtype);
@@ -168,9 +186,9 @@ PTQ_API PTQ_NODISCARD ptq_status ptq_ffn_noalloc(
     const void* x, void* y, int64_t M, int64_t H, int64_t I, ptq_dtype dtype,
     ptq_stream_t stream);
 
-/* ptq_route -- the kernel ptq_matmul would run for (M, dtype): writes its
- * name to *kernel_name (static storage) and returns PTQ_OK, or returns
- * PTQ_ERR_UNSUPPORTED / PTQ_ERR_VALUE.  Host only. */
+/* ptq_route -- the kernel ptq_matmul would run for (M, dtype) when K/128 is
+ * even: writes its name to *kernel_name (static storage) and returns PTQ_OK,
+ * or returns PTQ_ERR_UNSUPPORTED / PTQ_ERR_VALUE.  Host only. */
 PTQ_API PTQ_NODISCARD ptq_status ptq_route(int64_t M, ptq_dtype dtype,
                                            const char** kernel_name);
 

@@ -26,7 +26,8 @@ STATUS = {
 }
 
 # Every symbol include/ptq.h declares.
-EXPORTS = ("ptq1_pack", "ptq1_unpack", "ptq_fwht", "ptq_matmul", "ptq_ffn_workspace_bytes",
+EXPORTS = ("ptq1_pack", "ptq1_unpack", "ptq_fwht", "ptq_matmul_workspace_bytes", "ptq_matmul",
+           "ptq_ffn_workspace_bytes",
            "ptq_ffn", "ptq_ffn_noalloc", "ptq_route", "ptq_device_check", "ptq_status_str",
            "ptq_last_error")
 
@@ -59,7 +60,9 @@ def load(path: str | None = None):
     L.ptq1_pack.argtypes = [_P, _P, _I64, _I64]
     L.ptq1_unpack.argtypes = [_P, _P, _I64, _I64, _P]
     L.ptq_fwht.argtypes = [_P, _P, _P, _I64, _I64, _I32, _P]
-    L.ptq_matmul.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _P]
+    L.ptq_matmul_workspace_bytes.argtypes = [_I64, _I64, _I64, _I32]
+    L.ptq_matmul_workspace_bytes.restype = ctypes.c_size_t
+    L.ptq_matmul.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, ctypes.c_size_t, _P]
     L.ptq_ffn_workspace_bytes.argtypes = [_I64, _I64, _I64, _I32]
     L.ptq_ffn_workspace_bytes.restype = ctypes.c_size_t
     L.ptq_ffn.argtypes = [_P] * 8 + [_I64, _I64, _I64, _I32, _P, ctypes.c_size_t, _P]
@@ -149,16 +152,28 @@ def fwht(x, signs, out=None, stream=None):
     return y
 
 
-def matmul(wq, scales, x, out=None, stream=None):
-    """y = x W^T, W the PTQ1_0 weight (N x K); x M x K (float32 or bfloat16)."""
+def matmul_workspace_bytes(M: int, N: int, K: int, dtype: int) -> int:
+    return int(load().ptq_matmul_workspace_bytes(M, N, K, dtype))
+
+
+def matmul(wq, scales, x, out=None, workspace=None, stream=None):
+    """y = x W^T, W the PTQ1_0 weight (N x K); x M x K (float32 or bfloat16).
+    The scratch the call needs (ptq_matmul_workspace_bytes) is allocated by
+    PyTorch here when `workspace` is not given."""
     import torch
 
     M, K = x.shape
     N = wq.shape[0]
+    dt = _act_dtype(x)
     y = torch.empty((M, N), dtype=x.dtype, device=x.device) if out is None else out
+    need = matmul_workspace_bytes(M, N, K, dt)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    ws = _dev(workspace, None, "workspace") if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(load().ptq_matmul(_dev(wq, torch.uint8, "wq"), _dev(scales, torch.int16, "scales"),
-                             _dev(x, None, "x"), _dev(y, x.dtype, "out"), M, N, K, _act_dtype(x),
-                             _stream(stream)), "ptq_matmul")
+                             _dev(x, None, "x"), _dev(y, x.dtype, "out"), M, N, K, dt, ws,
+                             ws_bytes, _stream(stream)), "ptq_matmul")
     return y
 
 

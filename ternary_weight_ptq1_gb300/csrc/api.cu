@@ -64,7 +64,7 @@ struct Route {
   const char* name;
 };
 static const Route kRoutes[] = {
-    {PTQ_F32, 1, 1, Kernel::GemvF32, "gemv_ptq1_f32_m1_tc"},
+    {PTQ_F32, 1, 1, Kernel::GemvF32, "gemv_ptq1_f32_m1_lut"},
     {PTQ_F32, 2, 8, Kernel::GemvF32, "gemv_ptq1_f32"},
     {PTQ_BF16, 1, INT64_MAX, Kernel::GemmBf16, "gemm_ptq1_bf16"},
 };
@@ -220,11 +220,18 @@ static ptq_status check_matmul(const uint8_t* wq, const uint16_t* scales, const 
 // x_t / y_t: the GEMV is fp32 in and out; the GEMM reads bf16 (public call)
 // or fp16 (inside the feed-forward block) and writes bf16 (public call) or
 // fp32 (the feed-forward block keeps gate/up in fp32).
+// ws: matmul_ws_bytes(M, N, K, dtype) bytes of scratch (NULL when that is 0).
 static cudaError_t run_matmul(const Route* r, const uint8_t* wq, const uint16_t* scales,
                               const void* x, Act x_t, void* y, Act y_t, int64_t M, int64_t N,
-                              int64_t K, cudaStream_t st) {
+                              int64_t K, void* ws, cudaStream_t st) {
   switch (r->kernel) {
     case Kernel::GemvF32:
+      if (M == 1) {  // table-lookup decode when the shape fits it
+        const cudaError_t e = launch_gemv_lut(wq, scales, static_cast<const float*>(x),
+                                              static_cast<float*>(y), static_cast<float*>(ws), N,
+                                              K, st);
+        if (e != cudaErrorNotSupported) return e;
+      }
       return launch_gemv(wq, scales, static_cast<const float*>(x), static_cast<float*>(y), M, N,
                          K, st);
     case Kernel::GemmBf16:
@@ -233,26 +240,49 @@ static cudaError_t run_matmul(const Route* r, const uint8_t* wq, const uint16_t*
   return cudaErrorInvalidValue;
 }
 
+// Scratch of ptq_matmul for valid arguments: the GEMV's per-chunk row sums.
+static size_t matmul_ws_bytes(int64_t M, int64_t N, int64_t K, ptq_dtype dt) {
+  return (dt == PTQ_F32 && M == 1) ? gemv_lut_workspace_bytes(N, K) : 0;
+}
+
+PTQ_API size_t ptq_matmul_workspace_bytes(int64_t M, int64_t N, int64_t K, ptq_dtype dtype) {
+  int64_t t;
+  if (!dtype_ok(dtype) || M < 0 || N < 0 || K <= 0 || K % kBlockWeights != 0 ||
+      !mul_ok(N, K, &t) || !mul_ok(M, N, &t) || !mul_ok(t, 4, &t))
+    return 0;
+  return matmul_ws_bytes(M, N, K, dtype);
+}
+
 PTQ_API ptq_status ptq_matmul(const uint8_t* wq, const uint16_t* scales, const void* x, void* y,
-                              int64_t M, int64_t N, int64_t K, ptq_dtype dtype,
-                              ptq_stream_t stream) {
+                              int64_t M, int64_t N, int64_t K, ptq_dtype dtype, void* ws,
+                              size_t ws_bytes, ptq_stream_t stream) {
   t_msg[0] = 0;
+  const char* who = "ptq_matmul";
   const Route* r = nullptr;
-  ptq_status s = check_matmul(wq, scales, x, y, M, N, K, dtype, "ptq_matmul", &r);
+  ptq_status s = check_matmul(wq, scales, x, y, M, N, K, dtype, who, &r);
   if (s != PTQ_OK || M == 0 || N == 0) return s;
-  cudaError_t e =
-      run_matmul(r, wq, scales, x, act_of(dtype), y, act_of(dtype), M, N, K,
-                 reinterpret_cast<cudaStream_t>(stream));
+  const size_t need = matmul_ws_bytes(M, N, K, dtype);
+  if (need > 0) {
+    if (!ws) return fail(PTQ_ERR_WORKSPACE, "%s: workspace is NULL (%zu bytes needed)", who, need);
+    if (ws_bytes < need)
+      return fail(PTQ_ERR_WORKSPACE, "%s: workspace has %zu bytes, %zu needed", who, ws_bytes,
+                  need);
+    if (!aligned(ws, 16)) return fail(PTQ_ERR_ALIGN, "%s: workspace needs 16-byte alignment", who);
+  }
+  cudaError_t e = run_matmul(r, wq, scales, x, act_of(dtype), y, act_of(dtype), M, N, K,
+                             need > 0 ? ws : nullptr, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq_matmul launch");
 }
 
 // Workspace of ptq_ffn, each region rounded up to 256 bytes:
 //   xr (M x H) | gu (M x 2I, fp32) | h (M x I, fp32) [| hr (M x I, fp16)]
+//   | part (the decode GEMV's row sums; shared by the two projections,
+//     which never hold it at the same time)
 // fp32 path: xr fp32, h rotated in place.  bf16 path: xr and hr are fp16
 // (the tensor-core operands; 11 significant bits against bf16's 8, and the
 // block scale times a trit is exact in fp16), gate/up and SwiGLU stay fp32,
 // so the only bf16 rounding is the output.
-static bool ffn_layout(int64_t M, int64_t H, int64_t I, ptq_dtype dt, size_t off[4],
+static bool ffn_layout(int64_t M, int64_t H, int64_t I, ptq_dtype dt, size_t off[5],
                        size_t* total) {
   int64_t a, b, c, d = 0;
   const int64_t ds = (int64_t)dsize(dt);
@@ -265,12 +295,14 @@ static bool ffn_layout(int64_t M, int64_t H, int64_t I, ptq_dtype dt, size_t off
   off[1] = (size_t)up(a);
   off[2] = off[1] + (size_t)up(b);
   off[3] = off[2] + (size_t)up(c);
-  *total = off[3] + (size_t)up(d);
+  off[4] = off[3] + (size_t)up(d);
+  const size_t p1 = matmul_ws_bytes(M, 2 * I, H, dt), p2 = matmul_ws_bytes(M, H, I, dt);
+  *total = off[4] + (p1 > p2 ? p1 : p2);
   return true;
 }
 
 PTQ_API size_t ptq_ffn_workspace_bytes(int64_t M, int64_t H, int64_t I, ptq_dtype dtype) {
-  size_t off[4], total;
+  size_t off[5], total;
   if (!dtype_ok(dtype) || M < 0 || H <= 0 || I <= 0 || H % kRot || I % kRot ||
       I > INT64_MAX / 2 || !ffn_layout(M, H, I, dtype, off, &total))
     return 0;
@@ -286,7 +318,7 @@ PTQ_API ptq_status ptq_ffn(const uint8_t* wgu_q, const uint16_t* wgu_s, const ui
   if (!dtype_ok(dtype)) return fail(PTQ_ERR_VALUE, "%s: unknown dtype %d", who, (int)dtype);
   if (M < 0 || H <= 0 || I <= 0 || H % kRot || I % kRot || I > INT64_MAX / 4)
     return fail(PTQ_ERR_SHAPE, "%s: need M >= 0, H and I positive multiples of 1024", who);
-  size_t off[4], need;
+  size_t off[5], need;
   if (!ffn_layout(M, H, I, dtype, off, &need)) return fail(PTQ_ERR_SHAPE, "%s: size overflow", who);
   if (M == 0) return PTQ_OK;
   const Route *r_gu = nullptr, *r_d = nullptr;
@@ -309,12 +341,15 @@ PTQ_API ptq_status ptq_ffn(const uint8_t* wgu_q, const uint16_t* wgu_s, const ui
   float* h = reinterpret_cast<float*>(base + off[2]);
   const bool bf = dtype == PTQ_BF16;
   void* hr = bf ? static_cast<void*>(base + off[3]) : static_cast<void*>(h);
+  void* part = base + off[4];
   const Act op = bf ? Act::F16 : Act::F32;  // tensor-core operand type
   cudaError_t e = launch_fwht(x, act_of(dtype), xr, op, signs_in, M, H, st);
-  if (e == cudaSuccess) e = run_matmul(r_gu, wgu_q, wgu_s, xr, op, gu, Act::F32, M, 2 * I, H, st);
+  if (e == cudaSuccess)
+    e = run_matmul(r_gu, wgu_q, wgu_s, xr, op, gu, Act::F32, M, 2 * I, H, part, st);
   if (e == cudaSuccess) e = launch_swiglu(gu, h, M, I, st);
   if (e == cudaSuccess) e = launch_fwht(h, Act::F32, hr, op, signs_mid, M, I, st);
-  if (e == cudaSuccess) e = run_matmul(r_d, wd_q, wd_s, hr, op, y, act_of(dtype), M, H, I, st);
+  if (e == cudaSuccess)
+    e = run_matmul(r_d, wd_q, wd_s, hr, op, y, act_of(dtype), M, H, I, part, st);
   return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq_ffn launch");
 }
 

@@ -278,10 +278,6 @@ cudaError_t launch_m(const uint8_t* wq, const uint16_t* scales, const float* x, 
 cudaError_t launch_gemv(const uint8_t* wq, const uint16_t* scales, const float* x, float* y,
                         int64_t M, int64_t N, int64_t K, cudaStream_t st) {
   if (N > INT32_MAX || K > INT32_MAX) return cudaErrorInvalidValue;
-  if (M == 1) {  // tensor-core decode when the shape fits it, else the SIMT kernel
-    const cudaError_t e = launch_gemv_m1_tc(wq, scales, x, y, N, K, st);
-    if (e != cudaErrorNotSupported) return e;
-  }
   const int n = (int)N, k = (int)K;
   switch (M) {
     case 1: return launch_m<1>(wq, scales, x, y, n, k, st);

@@ -1,0 +1,361 @@
+// k_gemv_lut.cu -- decode GEMV over PTQ1_0 weights at M = 1 by table lookup.
+//
+//   y[n] = sum_b s[n, b] * sum_{i<128} t[n, 128b + i] * x[128b + i]
+//
+// A PTQ1_0 byte carries five trits ("A 27B model in 5.5 GB: Bonsai ternary on
+// Ferrox, locally", section "What Bonsai is"), so its whole contribution
+// sum_{i<5} t_i x_{5q+i} depends only on the byte value and on the five
+// activations at its position.  For each byte position p of a K-chunk this
+// kernel tabulates
+//
+//   T_p[e] = sum_{i<5} (d_i(e) - 1) x_{5q+i},   e = 0..255,
+//
+// where d_i(e) is digit i of the page's peel (section "What Ferrox does with
+// it": digit n = floor(3^(n+1) u) - 3 floor(3^n u), u = e / 256).  Those are
+// the base-3 digits of V(e) = floor(243 e / 256), the identity that makes the
+// decode total over all 256 byte values.  A weight byte then costs one byte
+// permute (which forms the table address) and one shared-memory load, and
+// the per-block scale is applied in fp32 to the sum of the lookups that fall
+// into that block.  The peel itself runs once per table entry, as the two
+// partial sums A[V / 27] (digits 0, 1) + B[V % 27] (digits 2..4).
+//
+// Layout of the work.  A row of W has 13 * nblk / 2 32-bit words of trits.
+// They are cut into nch chunks of at most 32 words.  A CTA owns one chunk and
+// a range of rows, and lane L of every warp owns word L of the chunk, i.e.
+// byte positions 4L..4L+3.  The four tables of lane L live in shared-memory
+// bank L only (entry e of position j at 0x10000 * (1 + j/2) + 256 e +
+// 128 (j%2) + 4L), so the 32 lookups of a warp never conflict, whatever the
+// bytes are.  The table region starts at shared address 0x10000, so one
+// byte permute builds the whole address: byte 1 is the weight byte, byte 0
+// the lane's column, byte 2 the region.
+//
+// A warp streams its rows with 4-byte coalesced loads kept 16 rows ahead in
+// registers (the weights do not depend on the previous kernel, so the first
+// loads are issued before griddepcontrol.wait), turns every row into one
+// fp32 value per lane (the block scales of the lane's two half-words applied),
+// and sums the 32 lanes of 16 rows at a time through a padded shared-memory
+// transpose.  Each CTA writes its chunk's row sums to part[c][n]; a second
+// kernel adds the nch chunks of every row in a fixed order, so the result is
+// bitwise reproducible.  No kernel here waits on another CTA.
+#include <cuda_fp16.h>
+
+#include "ptq_internal.cuh"
+
+namespace ptq {
+namespace {
+
+constexpr int kWarps = 16;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kChunkWords = 32;            // one word per lane
+constexpr int kRows = 16;                  // rows per batch = prefetch distance
+constexpr int kRedPitch = 36;              // words per row of a reduction buffer
+constexpr int kRedBytes = kRows * kRedPitch * 4;             // 2304 per warp
+constexpr int kXBlocks = 6;                // blocks one chunk can touch
+constexpr int kLowBytes = kWarps * kRedBytes + kXBlocks * kBlockWeights * 4;
+constexpr uint32_t kTab = 0x10000u;        // shared address of the tables
+constexpr uint32_t kTabEnd = 0x30000u;     // 4 positions x 32 lanes x 256 x 4 B
+constexpr size_t kSmemBytes = kTabEnd;     // dynamic bytes requested (covers
+                                           // [base, kTabEnd) for any base)
+constexpr int kMinRowsPerCta = 256;        // below this the table build dominates
+
+struct LutArgs {
+  const uint8_t* wq;
+  const uint16_t* sc;
+  const float* x;
+  float* part;   // nch x N row sums (y itself when nch == 1)
+  int N, nblk, words, nch, cpc;  // cpc: CTAs per chunk
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ float lds_f32(uint32_t a) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float4 lds_f32x4(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(a));
+  return v;
+}
+__device__ __forceinline__ void sts_f32(uint32_t a, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
+}
+// v = *p when `ok`, else v keeps its value.  The predicate sits inside the
+// instruction: a conditional assignment in C++ would load into a temporary and
+// copy it, and the copy would wait for the load -- the prefetch would be lost.
+__device__ __forceinline__ void ldg_stream(uint32_t& v, const uint32_t* p, bool ok) {
+  asm volatile(
+      "{\n .reg .pred q;\n setp.ne.b32 q, %2, 0;\n"
+      " @q ld.global.nc.L1::no_allocate.u32 %0, [%1];\n}"
+      : "+r"(v)
+      : "l"(p), "r"((uint32_t)ok));
+}
+
+// Per-lane constants of the main loop.
+struct Lanes {
+  uint32_t lb0, lb1, lb2, lb3;  // table address bytes of positions 0..3
+  uint32_t ssel;                // byte selector that puts s[bA], s[bB] low/high
+  uint32_t red;                 // this warp's reduction buffer
+  uint32_t wrow, srow;          // words per row of trits and of scales
+};
+
+__device__ __forceinline__ void ldg_stream(uint32_t& v, const uint32_t* p) {
+  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "+r"(v) : "l"(p));
+}
+
+// One batch of up to 16 rows: slot r holds row r0 + r; it is consumed, then
+// refilled with row r0 + r + 16 from pb/qb + r rows (when r < nref).  Each
+// lane turns its word of the row into one fp32 value (the two half-words
+// with their block scales) and stores it in row r of the reduction buffer.
+template <bool kFull>
+__device__ __forceinline__ void rows_batch(uint32_t (&wr)[kRows], uint32_t (&sr)[kRows], int nrows,
+                                           int nref, const uint32_t* pb, const uint32_t* qb,
+                                           const Lanes& ln) {
+  const int L = threadIdx.x & 31;
+#pragma unroll
+  for (int r = 0; r < kRows; ++r) {
+    if (!kFull && r >= nrows) break;
+    const uint32_t a0 = __byte_perm(wr[r], ln.lb0, 0x7604), a1 = __byte_perm(wr[r], ln.lb1, 0x7614);
+    const uint32_t a2 = __byte_perm(wr[r], ln.lb2, 0x7624), a3 = __byte_perm(wr[r], ln.lb3, 0x7634);
+    const uint32_t s2 = __byte_perm(sr[r], 0u, ln.ssel);
+    const uint32_t* p = pb + (size_t)((uint32_t)r * ln.wrow);
+    const uint32_t* q = qb + (size_t)((uint32_t)r * ln.srow);
+    if (kFull) {
+      ldg_stream(wr[r], p);
+      ldg_stream(sr[r], q);
+    } else {
+      ldg_stream(wr[r], p, r < nref);
+      ldg_stream(sr[r], q, r < nref);
+    }
+    const float t0 = lds_f32(a0), t1 = lds_f32(a1), t2 = lds_f32(a2), t3 = lds_f32(a3);
+    const float sA = __half2float(__ushort_as_half((unsigned short)(s2 & 0xffffu)));
+    const float sB = __half2float(__ushort_as_half((unsigned short)(s2 >> 16)));
+    sts_f32(ln.red + 4u * (uint32_t)(r * kRedPitch + L), fmaf(t2 + t3, sB, (t0 + t1) * sA));
+  }
+}
+
+// Sum of the 32 lane values of each row of the batch, in a fixed order:
+// lanes L and L + 16 each add half of row L % 16.
+__device__ __forceinline__ void reduce_batch(uint32_t red, int L, float* out, int r0, int rb) {
+  __syncwarp();
+  const int rr = L & 15, h = L >> 4;
+  const uint32_t src = red + 4u * (uint32_t)(rr * kRedPitch + 16 * h);
+  float acc = 0.0f;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float4 v = lds_f32x4(src + 16u * q);
+    acc += (v.x + v.y) + (v.z + v.w);
+  }
+  acc += __shfl_xor_sync(0xffffffffu, acc, 16);
+  if (h == 0 && r0 + rr < rb) out[r0 + rr] = acc;
+  __syncwarp();
+}
+
+// Entries e = 64 R .. 64 R + 63 of one table: T[e] = A[V / 27] + B[V % 27].
+template <int R>
+__device__ __forceinline__ void build_entries(const float (&A)[9], const float (&B)[27],
+                                              uint32_t dst) {
+#pragma unroll
+  for (int i = 0; i < 64; ++i) {
+    constexpr int e0 = 64 * R;
+    const int e = e0 + i;
+    const int v = (243 * e) >> 8;  // the five digits the peel reads from byte e
+    sts_f32(dst + 256u * (uint32_t)e, A[v / 27] + B[v % 27]);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) gemv_lut_kernel(const LutArgs P) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int L = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t base = (smem_u32(smem) + 15u) & ~15u;
+  // The table addresses are absolute; the layout needs the dynamic window
+  // to start low enough.  (It starts after the 1 KB the driver reserves.)
+  if (base + (uint32_t)kLowBytes > kTab) return;
+  const uint32_t red = base + (uint32_t)(warp * kRedBytes);
+  const uint32_t xs = base + (uint32_t)(kWarps * kRedBytes);
+
+  // ---- this CTA's chunk and rows ------------------------------------------------
+  const int c = blockIdx.x / P.cpc, k = blockIdx.x % P.cpc;
+  const int R0 = (int)((long long)k * P.N / P.cpc);
+  const int R1 = (int)((long long)(k + 1) * P.N / P.cpc);
+  const int ws = (int)((long long)c * P.words / P.nch);
+  const int we = (int)((long long)(c + 1) * P.words / P.nch);
+  const int Wc = we - ws;                      // 1..32 words
+  const bool live = L < Wc;
+  const int wl = ws + (live ? L : Wc - 1);     // lanes past the chunk re-read its last word
+  const int P0 = 4 * wl;                       // first byte of the word within the row
+  const int bA = P0 / kBlockBytes, bB = (P0 + 2) / kBlockBytes;
+  // A block boundary can only fall in the middle of a word (26 is even), and
+  // then the first half's block is even, so the two scales are the two halves
+  // of one aligned 32-bit word.  The permute puts s[bA] low and s[bB] high.
+  const uint32_t ssel = (bB != bA) ? 0x3210u : ((bA & 1) ? 0x3232u : 0x1010u);
+  const int pw = bA >> 1;
+
+  const int nr = R1 - R0;
+  const int ra = R0 + (int)((long long)warp * nr / kWarps);
+  const int rb = R0 + (int)((long long)(warp + 1) * nr / kWarps);
+
+  // ---- weight prefetch (independent of the previous kernel) ---------------------
+  // Slot r of the ring holds the trits word and the scale pair of row r0 + r
+  // of the current batch.
+  const size_t wrow = (size_t)P.words, srow = (size_t)(P.nblk / 2);
+  uint32_t wr[kRows], sr[kRows];
+  {
+    const uint32_t* p = reinterpret_cast<const uint32_t*>(P.wq) + (size_t)ra * wrow + wl;
+    const uint32_t* q = reinterpret_cast<const uint32_t*>(P.sc) + (size_t)ra * srow + pw;
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+      wr[r] = 0u;
+      sr[r] = 0u;
+      const bool ok = ra + r < rb;
+      ldg_stream(wr[r], p + (size_t)r * wrow, ok);
+      ldg_stream(sr[r], q + (size_t)r * srow, ok);
+    }
+  }
+
+  // ---- activations of the chunk, then its tables ---------------------------------
+  pdl_wait();
+  const int bx0 = (4 * ws) / kBlockBytes, bx1 = (4 * we - 1) / kBlockBytes;
+  const int nx = (bx1 - bx0 + 1) * kBlockWeights;  // <= kXBlocks * 128
+  for (int i = threadIdx.x; i < nx; i += kThreads)
+    sts_f32(xs + 4u * (uint32_t)i, P.x[(size_t)bx0 * kBlockWeights + i]);
+  __syncthreads();
+  {
+    // warp -> (position j of every lane's word, quarter R of the entries)
+    const int j = warp & 3;
+    const int Pj = 4 * (ws + L) + j;
+    const int b = Pj / kBlockBytes, q = Pj % kBlockBytes;
+    float xv[5];
+#pragma unroll
+    for (int i = 0; i < 5; ++i) {
+      const bool in = live && 5 * q + i < kBlockWeights;  // byte 25 holds three trits
+      xv[i] = in ? lds_f32(xs + 4u * (uint32_t)((b - bx0) * kBlockWeights + 5 * q + i)) : 0.0f;
+    }
+    float A[9], B[27];
+#pragma unroll
+    for (int a = 0; a < 9; ++a) {
+      // digits d0 = a / 3, d1 = a % 3 contribute (d - 1) x
+      const int d0 = a / 3 - 1, d1 = a % 3 - 1;
+      const float t0 = d0 > 0 ? xv[0] : (d0 < 0 ? -xv[0] : 0.0f);
+      A[a] = d1 > 0 ? t0 + xv[1] : (d1 < 0 ? t0 - xv[1] : t0);
+    }
+#pragma unroll
+    for (int bb = 0; bb < 27; ++bb) {
+      const int d2 = bb / 9 - 1, d3 = (bb / 3) % 3 - 1, d4 = bb % 3 - 1;
+      float t = d2 > 0 ? xv[2] : (d2 < 0 ? -xv[2] : 0.0f);
+      t = d3 > 0 ? t + xv[3] : (d3 < 0 ? t - xv[3] : t);
+      B[bb] = d4 > 0 ? t + xv[4] : (d4 < 0 ? t - xv[4] : t);
+    }
+    const uint32_t dst = kTab + 0x10000u * (uint32_t)(j >> 1) + 128u * (uint32_t)(j & 1) + 4u * L;
+    switch (warp >> 2) {
+      case 0: build_entries<0>(A, B, dst); break;
+      case 1: build_entries<1>(A, B, dst); break;
+      case 2: build_entries<2>(A, B, dst); break;
+      default: build_entries<3>(A, B, dst); break;
+    }
+  }
+  __syncthreads();
+  pdl_release();  // the reduction kernel may start its prologue
+
+  // ---- main loop: 16 rows per batch ----------------------------------------------
+  // address of entry e of position j: byte 0 = lane column (+128 for odd j),
+  // byte 1 = e, byte 2 = region 1 + j / 2
+  const uint32_t lb0 = kTab + 4u * L, lb1 = lb0 + 128u, lb2 = lb0 + 0x10000u, lb3 = lb2 + 128u;
+  const Lanes ln{lb0, lb1, lb2, lb3, ssel, red, (uint32_t)P.words, (uint32_t)(P.nblk / 2)};
+  const uint32_t* pw0 = reinterpret_cast<const uint32_t*>(P.wq) + (size_t)ra * wrow + wl;
+  const uint32_t* qw0 = reinterpret_cast<const uint32_t*>(P.sc) + (size_t)ra * srow + pw;
+  float* out = P.part + (size_t)c * P.N;
+  int r0 = ra;
+  // batches whose 16 rows and 16 refills are all inside the warp's rows
+  for (; r0 + 2 * kRows <= rb; r0 += kRows) {
+    const size_t next = (size_t)(r0 - ra + kRows);
+    rows_batch<true>(wr, sr, kRows, kRows, pw0 + next * wrow, qw0 + next * srow, ln);
+    reduce_batch(red, L, out, r0, rb);
+  }
+  for (; r0 < rb; r0 += kRows) {
+    const size_t next = (size_t)(r0 - ra + kRows);
+    const int nrows = rb - r0 < kRows ? rb - r0 : kRows;
+    const int nref = rb - r0 - kRows;  // rows left to fetch (may be <= 0)
+    rows_batch<false>(wr, sr, nrows, nref, pw0 + next * wrow, qw0 + next * srow, ln);
+    reduce_batch(red, L, out, r0, rb);
+  }
+}
+
+// y[n] = sum over chunks c = 0..nch-1 of part[c][n], in that order.
+__global__ void __launch_bounds__(256) gemv_lut_reduce_kernel(const float* __restrict__ part,
+                                                              float* __restrict__ y, int N,
+                                                              int nch) {
+  pdl_release();
+  pdl_wait();
+  const int n = blockIdx.x * blockDim.x + threadIdx.x;
+  if (n >= N) return;
+  float acc = 0.0f;
+  for (int c = 0; c < nch; ++c) acc += __ldcg(part + (size_t)c * N + n);
+  y[n] = acc;
+}
+
+int g_sms[64];
+
+}  // namespace
+
+int64_t gemv_lut_chunks(int64_t K) {
+  const int64_t nblk = K / kBlockWeights;
+  if (K % kBlockWeights != 0 || nblk % 2 != 0) return 0;
+  const int64_t words = 13 * nblk / 2;
+  return (words + kChunkWords - 1) / kChunkWords;
+}
+
+size_t gemv_lut_workspace_bytes(int64_t N, int64_t K) {
+  const int64_t nch = gemv_lut_chunks(K);
+  if (nch <= 1) return 0;
+  return (size_t)(((nch * N * 4) + 255) / 256 * 256);
+}
+
+// cudaErrorNotSupported when the shape does not fit this kernel (odd K/128,
+// more chunks than SMs, sizes past int32); the caller then runs the general
+// GEMV.  `part` holds gemv_lut_workspace_bytes(N, K) bytes (unused when the
+// row has a single chunk).
+cudaError_t launch_gemv_lut(const uint8_t* wq, const uint16_t* scales, const float* x, float* y,
+                            float* part, int64_t N, int64_t K, cudaStream_t st) {
+  const int64_t nch = gemv_lut_chunks(K);
+  if (nch == 0 || N > INT32_MAX / 2 || K > (1 << 24)) return cudaErrorNotSupported;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (g_sms[dev] == 0) {
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(gemv_lut_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    g_sms[dev] = sms;
+  }
+  if (nch > g_sms[dev]) return cudaErrorNotSupported;
+  if (nch > 1 && part == nullptr) return cudaErrorInvalidValue;
+  int64_t cpc = g_sms[dev] / nch;
+  const int64_t by_rows = (N + kMinRowsPerCta - 1) / kMinRowsPerCta;
+  if (cpc > by_rows) cpc = by_rows;
+  if (cpc < 1) cpc = 1;
+  LutArgs A;
+  A.wq = wq;
+  A.sc = scales;
+  A.x = x;
+  A.part = nch == 1 ? y : part;
+  A.N = (int)N;
+  A.nblk = (int)(K / kBlockWeights);
+  A.words = 13 * A.nblk / 2;
+  A.nch = (int)nch;
+  A.cpc = (int)cpc;
+  e = launch_pdl(gemv_lut_kernel, dim3((unsigned)(nch * cpc)), dim3(kThreads), kSmemBytes, st, A);
+  if (e != cudaSuccess || nch == 1) return e;
+  return launch_pdl(gemv_lut_reduce_kernel, dim3((unsigned)((N + 255) / 256)), dim3(256), 0, st,
+                    (const float*)part, y, (int)N, (int)nch);
+}
+
+}  // namespace ptq

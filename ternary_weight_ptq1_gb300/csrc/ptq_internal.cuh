@@ -66,10 +66,13 @@ cudaError_t launch_fwht(const void* x, Act in, void* y, Act out,
 cudaError_t launch_gemv(const uint8_t* wq, const uint16_t* scales,
                         const float* x, float* y, int64_t M, int64_t N,
                         int64_t K, cudaStream_t st);
-// M = 1 decode on the tensor cores (k_gemv_tc.cu); cudaErrorNotSupported
-// when the shape does not fit it (K % 1024 != 0 or shared memory).
-cudaError_t launch_gemv_m1_tc(const uint8_t* wq, const uint16_t* scales, const float* x,
-                              float* y, int64_t N, int64_t K, cudaStream_t st);
+// M = 1 decode by lookup tables (k_gemv_lut.cu).  part: scratch of
+// gemv_lut_workspace_bytes(N, K) bytes.  cudaErrorNotSupported when the
+// shape does not fit it (K/128 odd, more K-chunks than SMs); the caller then
+// runs launch_gemv.
+cudaError_t launch_gemv_lut(const uint8_t* wq, const uint16_t* scales, const float* x, float* y,
+                            float* part, int64_t N, int64_t K, cudaStream_t st);
+size_t gemv_lut_workspace_bytes(int64_t N, int64_t K);
 // x is BF16 or F16; y is BF16 or F32.
 cudaError_t launch_gemm(const uint8_t* wq, const uint16_t* scales, const void* x, Act x_t,
                         void* y, Act y_t, int64_t M, int64_t N, int64_t K, cudaStream_t st);

@@ -73,16 +73,28 @@ def test_refusals_before_launch(P):
     p16 = ctypes.c_void_p(16 * 1024)   # never dereferenced: every call below is refused
     odd = ctypes.c_void_p(16 * 1024 + 4)
     # matmul
-    assert L.ptq_matmul(p16, p16, p16, p16, 1, 8, 100, P.PTQ_F32, None) == 2
-    assert L.ptq_matmul(p16, p16, p16, p16, -1, 8, 128, P.PTQ_F32, None) == 2
-    assert L.ptq_matmul(p16, p16, p16, p16, 9, 8, 128, P.PTQ_F32, None) == 5
+    mm = lambda *a: L.ptq_matmul(*a[:8], None, 0, None)  # no workspace
+    assert mm(p16, p16, p16, p16, 1, 8, 100, P.PTQ_F32) == 2
+    assert mm(p16, p16, p16, p16, -1, 8, 128, P.PTQ_F32) == 2
+    assert mm(p16, p16, p16, p16, 9, 8, 128, P.PTQ_F32) == 5
     assert b"M=9" in L.ptq_last_error()
-    assert L.ptq_matmul(p16, p16, p16, p16, 1, 8, 128, 7, None) == 4
-    assert L.ptq_matmul(None, p16, p16, p16, 1, 8, 128, P.PTQ_F32, None) == 1
-    assert L.ptq_matmul(p16, odd, p16, p16, 1, 8, 128, P.PTQ_F32, None) == 3
-    assert L.ptq_matmul(None, None, None, None, 0, 8, 128, P.PTQ_F32, None) == 0
-    assert L.ptq_matmul(None, None, None, None, 4, 0, 128, P.PTQ_BF16, None) == 0
-    assert L.ptq_matmul(p16, p16, p16, p16, 2 ** 40, 2 ** 40, 128, P.PTQ_BF16, None) == 2
+    assert mm(p16, p16, p16, p16, 1, 8, 128, 7) == 4
+    assert mm(None, p16, p16, p16, 1, 8, 128, P.PTQ_F32) == 1
+    assert mm(p16, odd, p16, p16, 1, 8, 128, P.PTQ_F32) == 3
+    assert mm(None, None, None, None, 0, 8, 128, P.PTQ_F32) == 0
+    assert mm(None, None, None, None, 4, 0, 128, P.PTQ_BF16) == 0
+    assert mm(p16, p16, p16, p16, 2 ** 40, 2 ** 40, 128, P.PTQ_BF16) == 2
+    # the M = 1 decode needs its scratch: refused by size before any launch
+    need = P.matmul_workspace_bytes(1, 17408, 5120, P.PTQ_F32)
+    assert need == 9 * 17408 * 4
+    args = (p16, p16, p16, p16, 1, 17408, 5120, P.PTQ_F32)
+    assert L.ptq_matmul(*args, None, need, None) == 6
+    assert L.ptq_matmul(*args, p16, need - 1, None) == 6
+    assert L.ptq_matmul(*args, odd, need, None) == 3
+    assert P.matmul_workspace_bytes(4, 17408, 5120, P.PTQ_F32) == 0
+    assert P.matmul_workspace_bytes(512, 17408, 5120, P.PTQ_BF16) == 0
+    assert P.matmul_workspace_bytes(1, 17408, 5120 + 128, P.PTQ_F32) == 0  # K/128 odd
+    assert P.matmul_workspace_bytes(1, 17408, 100, P.PTQ_F32) == 0
     # rotation
     assert L.ptq_fwht(p16, p16, p16, 1, 1000, P.PTQ_F32, None) == 2
     assert L.ptq_fwht(p16, odd, p16, 1, 1024, P.PTQ_F32, None) == 3
@@ -100,7 +112,7 @@ def test_refusals_before_launch(P):
 
 
 def test_routing_table(P):
-    assert P.route(1, P.PTQ_F32) == "gemv_ptq1_f32_m1_tc"
+    assert P.route(1, P.PTQ_F32) == "gemv_ptq1_f32_m1_lut"
     for M in range(2, 9):
         assert P.route(M, P.PTQ_F32) == "gemv_ptq1_f32"
     for M in (1, 8, 64, 128, 512, 2048, 10 ** 6):
@@ -122,4 +134,14 @@ def test_workspace_sizes(P):
     bf = P.ffn_workspace_bytes(M, H, I, P.PTQ_BF16)
     f = P.ffn_workspace_bytes(1, H, I, P.PTQ_F32)
     assert bf >= M * H * 2 + M * 2 * I * 4 + M * I * 4 + M * I * 2
-    assert f >= H * 4 + 2 * I * 4 + I * 4
+    # decode adds the row sums of the larger projection: 9 chunks of the
+    # gate/up rows (K = 5120) against 28 chunks of the down rows (K = 17408)
+    gu_part = 9 * 2 * I * 4
+    assert gu_part > 28 * H * 4
+    assert f >= H * 4 + 2 * I * 4 + I * 4 + gu_part
+    assert f <= P.FFN_NOALLOC_SCRATCH_BYTES
+    # chunk count: 13 K/256 words per row, at most 32 per chunk
+    for K in (256, 512, 1024, 2048, 5120, 17408):
+        words = 13 * K // 256
+        assert P.matmul_workspace_bytes(1, 100, K, P.PTQ_F32) == (
+            0 if words <= 32 else ((words + 31) // 32 * 100 * 4 + 255) // 256 * 256)

@@ -110,6 +110,71 @@ def test_gemv_deterministic_and_in_bounds(P, syn):
     assert torch.isfinite(out).all()
 
 
+# ---- the M = 1 table-lookup decode ----------------------------------------------
+# A row has 13 K/256 words of trits, cut into chunks of at most 32 words; each
+# chunk's row sums are added by a second kernel.
+
+@pytest.mark.parametrize("N,K", [(1, 256), (7, 512), (300, 768), (64, 1024), (513, 2560),
+                                 (40, 12800), (3, 17408), (2000, 4096)])
+def test_lut_chunking(P, orc, syn, N, K):
+    # K = 256, 512: one chunk (the GEMV writes y itself); 768: 39 words in
+    # chunks of 19 and 20; 12800: 20 chunks; N = 1..2000 spans one to many
+    # rows per warp
+    mv = syn.gaussian_matvec(200 + K // 128, 1, N, K)
+    y, _ = run(P, mv.trits, mv.scales, mv.x)
+    Q.check_f32(Q.host_f64(y), orc.matmul(orc.pack(mv.trits), mv.scales, Q.x_f64(mv.x)),
+                f"lut N={N} K={K}")
+
+
+@pytest.mark.parametrize("K", [128, 384, 640])
+def test_lut_odd_block_count_uses_general_gemv(P, orc, syn, K):
+    # K/128 odd leaves rows that are not whole 32-bit words apart
+    assert P.matmul_workspace_bytes(1, 50, K, P.PTQ_F32) == 0
+    mv = syn.gaussian_matvec(210 + K // 128, 1, 50, K)
+    y, _ = run(P, mv.trits, mv.scales, mv.x)
+    Q.check_f32(Q.host_f64(y), orc.matmul(orc.pack(mv.trits), mv.scales, Q.x_f64(mv.x)),
+                f"odd K={K}")
+
+
+def test_lut_every_byte_value(P, orc, syn):
+    # every byte value at every position of a block, including the 13 bytes
+    # the encoder never writes: the decode is the peel, total over 0..255
+    N, K = 512, 2048
+    nb = K // 128
+    wq = ((np.arange(N)[:, None] * 7 + np.arange(nb * 26)[None, :]) % 256).astype(np.uint8)
+    s = syn.scales_f16(11, 1, (N, nb))
+    x = syn.normal_f32(11, 2, (1, K))
+    y = P.matmul(Q.dev(wq), Q.dev(s), Q.dev(x))
+    Q.check_f32(Q.host_f64(y), orc.matmul(wq, s, Q.x_f64(x)), "all bytes")
+
+
+@pytest.mark.parametrize("scale", [2.0 ** 60, 2.0 ** -60])
+def test_lut_activation_range(P, orc, syn, scale):
+    # the tables hold sums of five activations: no fixed point, no overflow
+    mv = syn.gaussian_matvec(12, 1, 700, 5120)
+    x = (mv.x.astype(np.float64) * scale).astype(np.float32)
+    y, _ = run(P, mv.trits, mv.scales, x)
+    Q.check_f32(Q.host_f64(y), orc.matmul(orc.pack(mv.trits), mv.scales, Q.x_f64(x)),
+                f"x * {scale:g}")
+
+
+def test_lut_workspace(P, syn):
+    import torch
+
+    N, K = 3000, 5120
+    mv = syn.gaussian_matvec(13, 1, N, K)
+    wq, s, x = Q.dev(P.pack(mv.trits)), Q.dev(mv.scales), Q.dev(mv.x)
+    need = P.matmul_workspace_bytes(1, N, K, P.PTQ_F32)
+    assert need == (9 * N * 4 + 255) // 256 * 256
+    ref = P.matmul(wq, s, x)
+    # any initial contents; the same bits on every call
+    ws = torch.full((need // 4,), float("nan"), device="cuda").view(torch.uint8)
+    for _ in range(3):
+        assert torch.equal(P.matmul(wq, s, x, workspace=ws), ref)
+    with pytest.raises(P.PTQError, match="WORKSPACE"):
+        P.matmul(wq, s, x, workspace=ws[:need - 16])
+
+
 def test_f32_above_eight_rows_is_refused(P, syn):
     mv = syn.gaussian_matvec(9, 9, 16, 128)
     with pytest.raises(P.PTQError, match="UNSUPPORTED"):
