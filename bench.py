@@ -191,13 +191,12 @@ def run_ours(args, world, rank):
     xr = [torch.empty((1, K_COLS), device="cuda") for _ in range(R)]
     ys = [torch.empty((1, N_ROWS), device="cuda") for _ in range(R)]
     # one scratch for every call: they are ordered on one stream
-    ws = torch.empty(max(1, P.matmul_workspace_bytes(1, N_ROWS, K_COLS, P.PTQ_F32)),
+    ws = torch.empty(max(1, P.rotate_matmul_workspace_bytes(1, N_ROWS, K_COLS, P.PTQ_F32)),
                      dtype=torch.uint8, device="cuda")
 
-    def step(i):
+    def step(i):  # rotation fused into the table-lookup GEMV
         wq, sc, x = ring[i % R]
-        P.fwht(x, signs, out=xr[i % R])
-        P.matmul(wq, sc, xr[i % R], out=ys[i % R], workspace=ws)
+        P.rotate_matmul(wq, sc, x, signs, out=ys[i % R], workspace=ws)
 
     def gemv_only(i):
         wq, sc, _ = ring[i % R]
@@ -216,7 +215,8 @@ def run_ours(args, world, rank):
     value = world * WEIGHT_BYTES / (ms_per_step * 1e-3) / 1e9       # GB/s, all ranks
     gemv_bytes = WEIGHT_BYTES + K_COLS * 4 + N_ROWS * 4
     gemv_us = ms_gemv / K * 1e3
-    achieved = gemv_bytes / (gemv_us * 1e-6) / 1e9
+    step_us = ms_per_step * 1e3
+    achieved = gemv_bytes / (step_us * 1e-6) / 1e9
 
     # e2e through the public API: pinned host x -> device, rotate, GEMV, y -> host
     xh = torch.from_numpy(syn.normal_f32(77, 2, (1, K_COLS))).pin_memory()
@@ -225,8 +225,7 @@ def run_ours(args, world, rank):
     E = max(50, min(K, 2000))
     for i in range(5):
         xd.copy_(xh, non_blocking=True)
-        P.fwht(xd, signs, out=xr[0])
-        P.matmul(ring[0][0], ring[0][1], xr[0], out=ys[0], workspace=ws)
+        P.rotate_matmul(ring[0][0], ring[0][1], xd, signs, out=ys[0], workspace=ws)
         yh.copy_(ys[0], non_blocking=True)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
@@ -236,8 +235,7 @@ def run_ours(args, world, rank):
     for i in range(E):
         wq, sc, _ = ring[i % R]
         xd.copy_(xh, non_blocking=True)
-        P.fwht(xd, signs, out=xr[i % R])
-        P.matmul(wq, sc, xr[i % R], out=ys[i % R], workspace=ws)
+        P.rotate_matmul(wq, sc, xd, signs, out=ys[i % R], workspace=ws)
         yh.copy_(ys[i % R], non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -275,7 +273,8 @@ def run_ours(args, world, rank):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": round(ms_per_step, 6), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": "decode gate/up: rotate (5 signed 1024-blocks) + PTQ1_0 GEMV",
+        "config": {"workload": "decode gate/up: rotate (5 signed 1024-blocks) + PTQ1_0 GEMV, "
+                               "one ptq_rotate_matmul call",
                    "M": 1, "K": K_COLS, "N": N_ROWS, "weight_bytes_per_step": WEIGHT_BYTES,
                    "l2": f"inputs larger than L2: ring of {R} distinct weight sets "
                          f"({R * WEIGHT_BYTES / 1e6:.0f} MB)",
@@ -283,17 +282,18 @@ def run_ours(args, world, rank):
                    "timing": "CUDA graphs of <=500 steps, CUDA events on the launching stream"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm"],
                      "unit": "GB/s", "frac": round(achieved / pk["hbm"], 4), "traffic": None,
-                     "kernel": P.route(1, P.PTQ_F32), "kernel_us": round(gemv_us, 3),
-                     "timed": "one ptq_matmul call: the table-lookup GEMV and its chunk "
-                              "reduction kernel",
+                     "kernel": P.route(1, P.PTQ_F32), "kernel_us": round(step_us, 3),
+                     "timed": "one ptq_rotate_matmul call: the table-lookup GEMV with the "
+                              "rotation fused in, and its chunk-reduction kernel",
                      "bytes_per_launch": gemv_bytes, "peak_source": pk["source"] + " copy bandwidth"},
-        "stage_us": {"fwht": round(ms_fwht / K * 1e3, 3), "gemv": round(gemv_us, 3),
-                     "step": round(ms_per_step * 1e3, 3)},
+        "stage_us": {"step_rotate_gemv_fused": round(step_us, 3),
+                     "unfused_fwht": round(ms_fwht / K * 1e3, 3),
+                     "unfused_gemv_on_rotated_x": round(gemv_us, 3)},
         "tokens_per_s_equiv": round(value * 1e9 / 5.906e9, 1),
         "e2e": {"value": round(e2e, 2), "unit": "GB/s", "h2d_bytes_per_step": K_COLS * 4,
                 "d2h_bytes_per_step": N_ROWS * 4, "ms_per_step": round(ms_e2e, 5),
                 "path": "python ctypes binding, eager launches, pinned host buffers"},
-        "gpu_launches": 3 * K,   # rotation, table-lookup GEMV, chunk reduction
+        "gpu_launches": 2 * K,   # fused rotation + table-lookup GEMV, chunk reduction
         "clocks": clocks,
         "prefill": pre,
         "cpu_baseline": cpu,
@@ -353,7 +353,8 @@ def run_reference(args, world, rank):
         "n_gpus": world, "steps": steps, "warmup": min(W, 3), "ms_per_step": round(ms_per_step, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": "decode gate/up: rotate (5 signed 1024-blocks) + PTQ1_0 GEMV",
+        "config": {"workload": "decode gate/up: rotate (5 signed 1024-blocks) + PTQ1_0 GEMV, "
+                               "one ptq_rotate_matmul call",
                    "M": 1, "K": K_COLS, "N": N_ROWS, "weight_bytes_per_step": WEIGHT_BYTES},
         "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": orc.get_threads(),
                          "kind": "oracle",

@@ -139,6 +139,27 @@ PTQ_API PTQ_NODISCARD ptq_status ptq_matmul(const uint8_t* wq,
                                             size_t workspace_bytes,
                                             ptq_stream_t stream);
 
+/* ptq_rotate_matmul_workspace_bytes -- scratch size of ptq_rotate_matmul;
+ * 0 when the arguments are invalid. */
+PTQ_API size_t ptq_rotate_matmul_workspace_bytes(int64_t M, int64_t N,
+                                                 int64_t K, ptq_dtype dtype);
+
+/* ptq_rotate_matmul -- y = (R x) W^T: the signed rotation of ptq_fwht applied
+ * to x (un-rotated, not modified), then ptq_matmul.  This is the order the
+ * pages prescribe for a folded weight ("What Ferrox does with it": rotate
+ * the activation before every matmul).  On the fp32 M == 1 decode route the
+ * rotation runs inside the GEMV, on the activations each thread block reads;
+ * otherwise it is a separate kernel writing R x into the workspace.
+ * signs: K int8 (device, 4-byte aligned).  Requires K % 1024 == 0.
+ * workspace: at least ptq_rotate_matmul_workspace_bytes(...) bytes, 16-byte
+ * aligned, any initial contents.  Other arguments, routing and errors as
+ * ptq_matmul. */
+PTQ_API PTQ_NODISCARD ptq_status ptq_rotate_matmul(
+    const uint8_t* wq, const uint16_t* scales, const void* x,
+    const int8_t* signs, void* y, int64_t M, int64_t N, int64_t K,
+    ptq_dtype dtype, void* workspace, size_t workspace_bytes,
+    ptq_stream_t stream);
+
 /* ptq_ffn_workspace_bytes -- scratch size ptq_ffn needs for (M, H, I, dtype);
  * 0 when the arguments are invalid. */
 PTQ_API size_t ptq_ffn_workspace_bytes(int64_t M, int64_t H, int64_t I,

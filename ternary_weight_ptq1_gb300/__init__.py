@@ -27,7 +27,7 @@ STATUS = {
 
 # Every symbol include/ptq.h declares.
 EXPORTS = ("ptq1_pack", "ptq1_unpack", "ptq_fwht", "ptq_matmul_workspace_bytes", "ptq_matmul",
-           "ptq_ffn_workspace_bytes",
+           "ptq_rotate_matmul_workspace_bytes", "ptq_rotate_matmul", "ptq_ffn_workspace_bytes",
            "ptq_ffn", "ptq_ffn_noalloc", "ptq_route", "ptq_device_check", "ptq_status_str",
            "ptq_last_error")
 
@@ -63,6 +63,10 @@ def load(path: str | None = None):
     L.ptq_matmul_workspace_bytes.argtypes = [_I64, _I64, _I64, _I32]
     L.ptq_matmul_workspace_bytes.restype = ctypes.c_size_t
     L.ptq_matmul.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, ctypes.c_size_t, _P]
+    L.ptq_rotate_matmul_workspace_bytes.argtypes = [_I64, _I64, _I64, _I32]
+    L.ptq_rotate_matmul_workspace_bytes.restype = ctypes.c_size_t
+    L.ptq_rotate_matmul.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, ctypes.c_size_t,
+                                    _P]
     L.ptq_ffn_workspace_bytes.argtypes = [_I64, _I64, _I64, _I32]
     L.ptq_ffn_workspace_bytes.restype = ctypes.c_size_t
     L.ptq_ffn.argtypes = [_P] * 8 + [_I64, _I64, _I64, _I32, _P, ctypes.c_size_t, _P]
@@ -73,7 +77,8 @@ def load(path: str | None = None):
     L.ptq_status_str.restype = ctypes.c_char_p
     L.ptq_last_error.argtypes = []
     L.ptq_last_error.restype = ctypes.c_char_p
-    for name in ("ptq1_pack", "ptq1_unpack", "ptq_fwht", "ptq_matmul", "ptq_ffn", "ptq_ffn_noalloc",
+    for name in ("ptq1_pack", "ptq1_unpack", "ptq_fwht", "ptq_matmul", "ptq_rotate_matmul", "ptq_ffn",
+                 "ptq_ffn_noalloc",
                  "ptq_route", "ptq_device_check"):
         getattr(L, name).restype = _I32
     _lib = L
@@ -174,6 +179,32 @@ def matmul(wq, scales, x, out=None, workspace=None, stream=None):
     _check(load().ptq_matmul(_dev(wq, torch.uint8, "wq"), _dev(scales, torch.int16, "scales"),
                              _dev(x, None, "x"), _dev(y, x.dtype, "out"), M, N, K, dt, ws,
                              ws_bytes, _stream(stream)), "ptq_matmul")
+    return y
+
+
+def rotate_matmul_workspace_bytes(M: int, N: int, K: int, dtype: int) -> int:
+    return int(load().ptq_rotate_matmul_workspace_bytes(M, N, K, dtype))
+
+
+def rotate_matmul(wq, scales, x, signs, out=None, workspace=None, stream=None):
+    """y = (R x) W^T: the signed rotation of `x` (not modified), then the
+    PTQ1_0 matmul; fused into one kernel on the fp32 M = 1 route.  The
+    scratch is allocated by PyTorch here when `workspace` is not given."""
+    import torch
+
+    M, K = x.shape
+    N = wq.shape[0]
+    dt = _act_dtype(x)
+    y = torch.empty((M, N), dtype=x.dtype, device=x.device) if out is None else out
+    if workspace is None:
+        workspace = torch.empty(max(1, rotate_matmul_workspace_bytes(M, N, K, dt)),
+                                dtype=torch.uint8, device=x.device)
+    _check(load().ptq_rotate_matmul(_dev(wq, torch.uint8, "wq"),
+                                    _dev(scales, torch.int16, "scales"), _dev(x, None, "x"),
+                                    _dev(signs, torch.int8, "signs"), _dev(y, x.dtype, "out"), M, N,
+                                    K, dt, _dev(workspace, None, "workspace"),
+                                    workspace.numel() * workspace.element_size(), _stream(stream)),
+           "ptq_rotate_matmul")
     return y
 
 

@@ -227,9 +227,10 @@ static cudaError_t run_matmul(const Route* r, const uint8_t* wq, const uint16_t*
   switch (r->kernel) {
     case Kernel::GemvF32:
       if (M == 1) {  // table-lookup decode when the shape fits it
-        const cudaError_t e = launch_gemv_lut(wq, scales, static_cast<const float*>(x),
-                                              static_cast<float*>(y), static_cast<float*>(ws), N,
-                                              K, st);
+        const cudaError_t e =
+            launch_gemv_lut(wq, scales, static_cast<const float*>(x), nullptr,
+                            static_cast<float*>(y), static_cast<float*>(ws), N, K,
+                            LutEpilogue::Plain, st);
         if (e != cudaErrorNotSupported) return e;
       }
       return launch_gemv(wq, scales, static_cast<const float*>(x), static_cast<float*>(y), M, N,
@@ -272,6 +273,62 @@ PTQ_API ptq_status ptq_matmul(const uint8_t* wq, const uint16_t* scales, const v
   cudaError_t e = run_matmul(r, wq, scales, x, act_of(dtype), y, act_of(dtype), M, N, K,
                              need > 0 ? ws : nullptr, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq_matmul launch");
+}
+
+// ---- rotate + matmul ------------------------------------------------------
+// Workspace: [matmul scratch | R x (M x K of dtype), used when the rotation
+// runs as its own kernel], each rounded up to 256 bytes.
+static bool rotmm_layout(int64_t M, int64_t N, int64_t K, ptq_dtype dt, size_t* xr_off,
+                         size_t* total) {
+  int64_t xb;
+  if (!mul_ok(M, K, &xb) || !mul_ok(xb, (int64_t)dsize(dt), &xb)) return false;
+  *xr_off = (matmul_ws_bytes(M, N, K, dt) + 255) / 256 * 256;
+  *total = *xr_off + (size_t)((xb + 255) / 256 * 256);
+  return true;
+}
+
+PTQ_API size_t ptq_rotate_matmul_workspace_bytes(int64_t M, int64_t N, int64_t K,
+                                                 ptq_dtype dtype) {
+  int64_t t;
+  size_t off, total;
+  if (!dtype_ok(dtype) || M < 0 || N < 0 || K <= 0 || K % kRot != 0 || !mul_ok(N, K, &t) ||
+      !mul_ok(M, N, &t) || !mul_ok(t, 4, &t) || !rotmm_layout(M, N, K, dtype, &off, &total))
+    return 0;
+  return total;
+}
+
+PTQ_API ptq_status ptq_rotate_matmul(const uint8_t* wq, const uint16_t* scales, const void* x,
+                                     const int8_t* signs, void* y, int64_t M, int64_t N,
+                                     int64_t K, ptq_dtype dtype, void* ws, size_t ws_bytes,
+                                     ptq_stream_t stream) {
+  t_msg[0] = 0;
+  const char* who = "ptq_rotate_matmul";
+  if (dtype_ok(dtype) && K > 0 && K % kRot != 0)
+    return fail(PTQ_ERR_SHAPE, "%s: need K %% 1024 == 0 (K=%lld)", who, (long long)K);
+  const Route* r = nullptr;
+  ptq_status s = check_matmul(wq, scales, x, y, M, N, K, dtype, who, &r);
+  if (s != PTQ_OK || M == 0 || N == 0) return s;
+  if (!signs) return fail(PTQ_ERR_NULL, "%s: signs is NULL", who);
+  if (!aligned(signs, 4)) return fail(PTQ_ERR_ALIGN, "%s: signs need 4-byte alignment", who);
+  size_t xr_off, need;
+  if (!rotmm_layout(M, N, K, dtype, &xr_off, &need)) return fail(PTQ_ERR_SHAPE, "%s: size overflow", who);
+  if (!ws) return fail(PTQ_ERR_WORKSPACE, "%s: workspace is NULL (%zu bytes needed)", who, need);
+  if (ws_bytes < need)
+    return fail(PTQ_ERR_WORKSPACE, "%s: workspace has %zu bytes, %zu needed", who, ws_bytes, need);
+  if (!aligned(ws, 16)) return fail(PTQ_ERR_ALIGN, "%s: workspace needs 16-byte alignment", who);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (r->kernel == Kernel::GemvF32 && M == 1 && gemv_lut_supported(N, K, true)) {
+    // the rotation runs inside the GEMV, on the activations each CTA reads
+    e = launch_gemv_lut(wq, scales, static_cast<const float*>(x), signs, static_cast<float*>(y),
+                        static_cast<float*>(ws), N, K, LutEpilogue::Plain, st);
+  } else {
+    void* xr = static_cast<char*>(ws) + xr_off;
+    e = launch_fwht(x, act_of(dtype), xr, act_of(dtype), signs, M, K, st);
+    if (e == cudaSuccess)
+      e = run_matmul(r, wq, scales, xr, act_of(dtype), y, act_of(dtype), M, N, K, ws, st);
+  }
+  return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq_rotate_matmul launch");
 }
 
 // Workspace of ptq_ffn, each region rounded up to 256 bytes:
@@ -343,6 +400,17 @@ PTQ_API ptq_status ptq_ffn(const uint8_t* wgu_q, const uint16_t* wgu_s, const ui
   void* hr = bf ? static_cast<void*>(base + off[3]) : static_cast<void*>(h);
   void* part = base + off[4];
   const Act op = bf ? Act::F16 : Act::F32;  // tensor-core operand type
+  if (!bf && M == 1 && r_gu->kernel == Kernel::GemvF32 && gemv_lut_supported(2 * I, H, true) &&
+      gemv_lut_supported(H, I, true)) {
+    // decode: each table-lookup GEMV rotates its own activations, and the
+    // gate/up row sums are reduced straight into h = silu(g) * u
+    cudaError_t e = launch_gemv_lut(wgu_q, wgu_s, static_cast<const float*>(x), signs_in, h,
+                                    static_cast<float*>(part), 2 * I, H, LutEpilogue::SwiGLU, st);
+    if (e == cudaSuccess)
+      e = launch_gemv_lut(wd_q, wd_s, h, signs_mid, static_cast<float*>(y),
+                          static_cast<float*>(part), H, I, LutEpilogue::Plain, st);
+    return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq_ffn launch");
+  }
   cudaError_t e = launch_fwht(x, act_of(dtype), xr, op, signs_in, M, H, st);
   if (e == cudaSuccess)
     e = run_matmul(r_gu, wgu_q, wgu_s, xr, op, gu, Act::F32, M, 2 * I, H, part, st);

@@ -50,8 +50,9 @@ constexpr int kChunkWords = 32;            // one word per lane
 constexpr int kRows = 16;                  // rows per batch = prefetch distance
 constexpr int kRedPitch = 36;              // words per row of a reduction buffer
 constexpr int kRedBytes = kRows * kRedPitch * 4;             // 2304 per warp
-constexpr int kXBlocks = 6;                // blocks one chunk can touch
-constexpr int kLowBytes = kWarps * kRedBytes + kXBlocks * kBlockWeights * 4;
+constexpr int kXFloats = 2 * kRot;         // a chunk touches at most 6 blocks = 768
+                                           // weights, inside at most two 1024-blocks
+constexpr int kLowBytes = kWarps * kRedBytes + kXFloats * 4;
 constexpr uint32_t kTab = 0x10000u;        // shared address of the tables
 constexpr uint32_t kTabEnd = 0x30000u;     // 4 positions x 32 lanes x 256 x 4 B
 constexpr size_t kSmemBytes = kTabEnd;     // dynamic bytes requested (covers
@@ -62,6 +63,7 @@ struct LutArgs {
   const uint8_t* wq;
   const uint16_t* sc;
   const float* x;
+  const int8_t* signs;  // non-null: x is not rotated yet (K % 1024 == 0)
   float* part;   // nch x N row sums (y itself when nch == 1)
   int N, nblk, words, nch, cpc;  // cpc: CTAs per chunk
 };
@@ -168,6 +170,59 @@ __device__ __forceinline__ void build_entries(const float (&A)[9], const float (
   }
 }
 
+// The signed rotation of one 1024-block of x by the 256 threads of 8 warps
+// (g8: thread index within them), written to xs_blk (1024 floats):
+//   xs_blk[j] = (1/32) sum_i (-1)^popcount(i & j) s[i] x[i]
+// ("What Bonsai is": a 1024-wide butterfly with a sign pattern; sign first,
+// then the Sylvester-ordered Hadamard butterfly).  Bits 0-1 of the index are
+// done in registers, bits 2-6 across the lanes of a warp, bits 7-9 in
+// registers after a transpose through `exch` (1024 floats).  The caller
+// synchronises the 8 warps around it with bar(); `bar` is that barrier.
+template <typename Bar>
+__device__ __forceinline__ void rotate_block(const float* __restrict__ x, const int8_t* __restrict__ s,
+                                             uint32_t exch, uint32_t xs_blk, int g8, Bar bar) {
+  const int lane = g8 & 31;
+  const float4 xv = reinterpret_cast<const float4*>(x)[g8];
+  const uint32_t sv = reinterpret_cast<const uint32_t*>(s)[g8];
+  float v[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    if ((int8_t)(sv >> (8 * i)) < 0) v[i] = -v[i];
+  // bits 0, 1
+  float a = v[0] + v[1], b = v[0] - v[1], c = v[2] + v[3], d = v[2] - v[3];
+  v[0] = a + c; v[1] = b + d; v[2] = a - c; v[3] = b - d;
+  // bits 2..6: the lane bits
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const bool up = lane & m;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float o = __shfl_xor_sync(0xffffffffu, v[i], m);
+      v[i] = up ? o - v[i] : v[i] + o;
+    }
+  }
+  asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(exch + 16u * (uint32_t)g8),
+               "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3])
+               : "memory");
+  bar();
+  if (g8 < 128) {  // bits 7..9: elements g8 + 128 k, k = 0..7
+    float w[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) w[k] = lds_f32(exch + 4u * (uint32_t)(g8 + 128 * k));
+#pragma unroll
+    for (int m = 1; m < 8; m <<= 1)
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (!(k & m)) {
+          const float p = w[k], q = w[k + m];
+          w[k] = p + q;
+          w[k + m] = p - q;
+        }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) sts_f32(xs_blk + 4u * (uint32_t)(g8 + 128 * k), w[k] * 0.03125f);
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1) gemv_lut_kernel(const LutArgs P) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int L = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -220,9 +275,27 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_lut_kernel(const LutArgs P) 
   // ---- activations of the chunk, then its tables ---------------------------------
   pdl_wait();
   const int bx0 = (4 * ws) / kBlockBytes, bx1 = (4 * we - 1) / kBlockBytes;
-  const int nx = (bx1 - bx0 + 1) * kBlockWeights;  // <= kXBlocks * 128
-  for (int i = threadIdx.x; i < nx; i += kThreads)
-    sts_f32(xs + 4u * (uint32_t)i, P.x[(size_t)bx0 * kBlockWeights + i]);
+  int xbase;  // weight index of xs[0]
+  if (P.signs == nullptr) {
+    xbase = bx0 * kBlockWeights;
+    const int nx = (bx1 - bx0 + 1) * kBlockWeights;  // <= 6 * 128
+    for (int i = threadIdx.x; i < nx; i += kThreads)
+      sts_f32(xs + 4u * (uint32_t)i, P.x[(size_t)xbase + i]);
+  } else {
+    // the rotation blocks that hold this chunk's weights: one or two, one per
+    // half of the CTA; the reduction buffers are free to exchange through
+    const int f0 = bx0 * kBlockWeights / kRot, f1 = (bx1 * kBlockWeights + kBlockWeights - 1) / kRot;
+    xbase = f0 * kRot;
+    const int half = warp >> 3, g8 = threadIdx.x & 255;
+    auto bar = [half]() {
+      asm volatile("bar.sync %0, 256;" ::"r"(1 + half) : "memory");
+    };
+    if (f0 + half <= f1) {
+      const size_t off = (size_t)(f0 + half) * kRot;
+      rotate_block(P.x + off, P.signs + off, base + (uint32_t)(half * kRot * 4),
+                   xs + (uint32_t)(half * kRot * 4), g8, bar);
+    }
+  }
   __syncthreads();
   {
     // warp -> (position j of every lane's word, quarter R of the entries)
@@ -233,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_lut_kernel(const LutArgs P) 
 #pragma unroll
     for (int i = 0; i < 5; ++i) {
       const bool in = live && 5 * q + i < kBlockWeights;  // byte 25 holds three trits
-      xv[i] = in ? lds_f32(xs + 4u * (uint32_t)((b - bx0) * kBlockWeights + 5 * q + i)) : 0.0f;
+      xv[i] = in ? lds_f32(xs + 4u * (uint32_t)(b * kBlockWeights + 5 * q + i - xbase)) : 0.0f;
     }
     float A[9], B[27];
 #pragma unroll
@@ -285,6 +358,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_lut_kernel(const LutArgs P) 
   }
 }
 
+__device__ __forceinline__ float chunk_sum(const float* __restrict__ part, int N, int nch, int n) {
+  float acc = 0.0f;
+  for (int c = 0; c < nch; ++c) acc += __ldcg(part + (size_t)c * N + n);
+  return acc;
+}
+
 // y[n] = sum over chunks c = 0..nch-1 of part[c][n], in that order.
 __global__ void __launch_bounds__(256) gemv_lut_reduce_kernel(const float* __restrict__ part,
                                                               float* __restrict__ y, int N,
@@ -293,9 +372,21 @@ __global__ void __launch_bounds__(256) gemv_lut_reduce_kernel(const float* __res
   pdl_wait();
   const int n = blockIdx.x * blockDim.x + threadIdx.x;
   if (n >= N) return;
-  float acc = 0.0f;
-  for (int c = 0; c < nch; ++c) acc += __ldcg(part + (size_t)c * N + n);
-  y[n] = acc;
+  y[n] = chunk_sum(part, N, nch, n);
+}
+
+// The same sums for a fused gate+up weight (rows 0..I-1 gate, I..2I-1 up),
+// followed by h[i] = silu(g_i) * u_i with silu(a) = a / (1 + e^-a): the
+// feed-forward block of "Speed, and where it goes".
+__global__ void __launch_bounds__(256) gemv_lut_reduce_swiglu_kernel(
+    const float* __restrict__ part, float* __restrict__ h, int N, int nch) {
+  pdl_release();
+  pdl_wait();
+  const int I = N / 2;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= I) return;
+  const float g = chunk_sum(part, N, nch, i), u = chunk_sum(part, N, nch, i + I);
+  h[i] = g / (1.0f + expf(-g)) * u;
 }
 
 int g_sms[64];
@@ -315,14 +406,7 @@ size_t gemv_lut_workspace_bytes(int64_t N, int64_t K) {
   return (size_t)(((nch * N * 4) + 255) / 256 * 256);
 }
 
-// cudaErrorNotSupported when the shape does not fit this kernel (odd K/128,
-// more chunks than SMs, sizes past int32); the caller then runs the general
-// GEMV.  `part` holds gemv_lut_workspace_bytes(N, K) bytes (unused when the
-// row has a single chunk).
-cudaError_t launch_gemv_lut(const uint8_t* wq, const uint16_t* scales, const float* x, float* y,
-                            float* part, int64_t N, int64_t K, cudaStream_t st) {
-  const int64_t nch = gemv_lut_chunks(K);
-  if (nch == 0 || N > INT32_MAX / 2 || K > (1 << 24)) return cudaErrorNotSupported;
+static cudaError_t device_sms(int* out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -336,9 +420,37 @@ cudaError_t launch_gemv_lut(const uint8_t* wq, const uint16_t* scales, const flo
     if (e != cudaSuccess) return e;
     g_sms[dev] = sms;
   }
-  if (nch > g_sms[dev]) return cudaErrorNotSupported;
+  *out = g_sms[dev];
+  return cudaSuccess;
+}
+
+bool gemv_lut_supported(int64_t N, int64_t K, bool rotate) {
+  const int64_t nch = gemv_lut_chunks(K);
+  if (nch == 0 || N > INT32_MAX / 2 || K > (1 << 24)) return false;
+  if (rotate && K % kRot != 0) return false;
+  int sms = 0;
+  return device_sms(&sms) == cudaSuccess && nch <= sms;
+}
+
+// cudaErrorNotSupported when the shape does not fit this kernel (odd K/128,
+// more chunks than SMs, sizes past int32; with signs, K % 1024 != 0; with the
+// SwiGLU epilogue, odd N or a single chunk); the caller then runs the general
+// path.  `part` holds gemv_lut_workspace_bytes(N, K) bytes (unused when the
+// row has a single chunk).  signs != NULL: x is rotated inside the kernel.
+// SwiGLU: y receives h = silu(g) * u of the N/2 gate and N/2 up rows.
+cudaError_t launch_gemv_lut(const uint8_t* wq, const uint16_t* scales, const float* x,
+                            const int8_t* signs, float* y, float* part, int64_t N, int64_t K,
+                            LutEpilogue ep, cudaStream_t st) {
+  const int64_t nch = gemv_lut_chunks(K);
+  if (nch == 0 || N > INT32_MAX / 2 || K > (1 << 24)) return cudaErrorNotSupported;
+  if (signs != nullptr && K % kRot != 0) return cudaErrorNotSupported;
+  if (ep == LutEpilogue::SwiGLU && (N % 2 != 0 || nch == 1)) return cudaErrorNotSupported;
+  int sms = 0;
+  cudaError_t e = device_sms(&sms);
+  if (e != cudaSuccess) return e;
+  if (nch > sms) return cudaErrorNotSupported;
   if (nch > 1 && part == nullptr) return cudaErrorInvalidValue;
-  int64_t cpc = g_sms[dev] / nch;
+  int64_t cpc = sms / nch;
   const int64_t by_rows = (N + kMinRowsPerCta - 1) / kMinRowsPerCta;
   if (cpc > by_rows) cpc = by_rows;
   if (cpc < 1) cpc = 1;
@@ -346,6 +458,7 @@ cudaError_t launch_gemv_lut(const uint8_t* wq, const uint16_t* scales, const flo
   A.wq = wq;
   A.sc = scales;
   A.x = x;
+  A.signs = signs;
   A.part = nch == 1 ? y : part;
   A.N = (int)N;
   A.nblk = (int)(K / kBlockWeights);
@@ -354,6 +467,9 @@ cudaError_t launch_gemv_lut(const uint8_t* wq, const uint16_t* scales, const flo
   A.cpc = (int)cpc;
   e = launch_pdl(gemv_lut_kernel, dim3((unsigned)(nch * cpc)), dim3(kThreads), kSmemBytes, st, A);
   if (e != cudaSuccess || nch == 1) return e;
+  if (ep == LutEpilogue::SwiGLU)
+    return launch_pdl(gemv_lut_reduce_swiglu_kernel, dim3((unsigned)((N / 2 + 255) / 256)),
+                      dim3(256), 0, st, (const float*)part, y, (int)N, (int)nch);
   return launch_pdl(gemv_lut_reduce_kernel, dim3((unsigned)((N + 255) / 256)), dim3(256), 0, st,
                     (const float*)part, y, (int)N, (int)nch);
 }

@@ -70,9 +70,16 @@ cudaError_t launch_gemv(const uint8_t* wq, const uint16_t* scales,
 // gemv_lut_workspace_bytes(N, K) bytes.  cudaErrorNotSupported when the
 // shape does not fit it (K/128 odd, more K-chunks than SMs); the caller then
 // runs launch_gemv.
-cudaError_t launch_gemv_lut(const uint8_t* wq, const uint16_t* scales, const float* x, float* y,
-                            float* part, int64_t N, int64_t K, cudaStream_t st);
+// signs != NULL: x is not rotated yet and the kernel rotates it (K % 1024).
+// SwiGLU: the weight is the fused gate+up (N = 2I) and y receives h (I).
+enum class LutEpilogue { Plain, SwiGLU };
+cudaError_t launch_gemv_lut(const uint8_t* wq, const uint16_t* scales, const float* x,
+                            const int8_t* signs, float* y, float* part, int64_t N, int64_t K,
+                            LutEpilogue ep, cudaStream_t st);
 size_t gemv_lut_workspace_bytes(int64_t N, int64_t K);
+// Whether launch_gemv_lut serves (N, K) on the current device (with the
+// rotation when `rotate`).
+bool gemv_lut_supported(int64_t N, int64_t K, bool rotate);
 // x is BF16 or F16; y is BF16 or F32.
 cudaError_t launch_gemm(const uint8_t* wq, const uint16_t* scales, const void* x, Act x_t,
                         void* y, Act y_t, int64_t M, int64_t N, int64_t K, cudaStream_t st);
