@@ -323,10 +323,14 @@ PTQ_API ptq_status ptq_rotate_matmul(const uint8_t* wq, const uint16_t* scales, 
     e = launch_gemv_lut(wq, scales, static_cast<const float*>(x), signs, static_cast<float*>(y),
                         static_cast<float*>(ws), N, K, LutEpilogue::Plain, st);
   } else {
+    // R x is kept in fp32 (fp32 routes) or fp16 (bf16 route): with an fp16
+    // operand the GEMM's weight tile t * s is exact, so the one rounding of
+    // the rotated activation (2^-11) is the only error before the output's
+    // own bf16 rounding
     void* xr = static_cast<char*>(ws) + xr_off;
-    e = launch_fwht(x, act_of(dtype), xr, act_of(dtype), signs, M, K, st);
-    if (e == cudaSuccess)
-      e = run_matmul(r, wq, scales, xr, act_of(dtype), y, act_of(dtype), M, N, K, ws, st);
+    const Act op = dtype == PTQ_BF16 ? Act::F16 : Act::F32;
+    e = launch_fwht(x, act_of(dtype), xr, op, signs, M, K, st);
+    if (e == cudaSuccess) e = run_matmul(r, wq, scales, xr, op, y, act_of(dtype), M, N, K, ws, st);
   }
   return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq_rotate_matmul launch");
 }

@@ -8,26 +8,27 @@
 // decode matvec reads; the trits are peeled as floor(3^(n+1) u) - 3 floor(3^n
 // u), u = byte / 256.
 //
-// Operands.  A = activations (16-bit, M x K), B = the weight tile expanded in
-// shared memory to t * s.  Both are fp16: the block scale is an fp16 number,
-// so +-s and 0 are exact and the MMA (kind::f16, fp32 accumulation in TMEM)
-// needs no per-block epilogue.  Activations that arrive as bf16 are converted
-// to fp16 in shared memory, in place (exact for |x| in fp16's normal range;
-// bf16 values beyond +-65504 are outside the supported domain).
+// Operands.  A = activations (16-bit, M x K), read by the MMA straight from
+// the TMA-staged tile; B = the weight tile expanded in shared memory to t * s
+// in A's type (kind::f16 takes A and B of one type), so the block scale is
+// folded into B and the MMA (fp32 accumulation in TMEM) needs no per-block
+// epilogue.  bf16 activations give bf16 tiles t * bf16(s) -- the expansion to
+// bf16 tiles the decode/prefill split calls for; the scale's rounding to
+// bf16 is at most 2^-9 relative.  fp16 activations (the feed-forward block's
+// rotated operands) give exact fp16 tiles.
 //
 // Tile: 256 (M) x 128 (N): two 128-row accumulators in TMEM share every
 // expanded B slice, so each weight is peeled once per 256 activation rows.
-// K is consumed in 64-wide slices (one 128-byte swizzle atom of fp16),
-// kStages slices in flight.  Warp roles (14 warps):
+// K is consumed in 64-wide slices (one 128-byte swizzle atom of 16-bit
+// values), kStages slices in flight.  Warp roles (10 warps):
 //   warp 0      TMA producer: A slices (box 64 x 256, 128B swizzle) and, per
 //               1024-wide group, the packed trits (box 208 B x 128 rows) and
 //               scales (box 8 x 128) into a 2-deep group ring, one group ahead.
 //   warp 1      TMEM allocation; lane 0 issues tcgen05.mma (8 per slice).
-//   warps 2-5   convert bf16 A slices to fp16 in place (idle for fp16 A).
-//   warps 6-13  expansion: thread (row r, half h) peels the 64 weights of half
+//   warps 2-9   expansion: thread (row r, half h) peels the 64 weights of half
 //               h of each 128-weight block of row r.  A table built per CTA
 //               maps each byte value to byte-permute selectors, so every pair
-//               of fp16 outputs is one permute of the per-block bytes
+//               of 16-bit outputs is one permute of the per-block bytes
 //               {-s, 0, +s}.  Writes use the canonical K-major 128B-swizzled
 //               layout; afterwards these warps run the epilogue
 //               (TMEM -> registers -> y).
@@ -50,8 +51,8 @@ constexpr int kQsBytes = BN * kGroupBytes;                  // 26,624
 constexpr int kScBytes = BN * kGroupBlocks * 2;             // 2,048
 constexpr int kGroupBuf = kQsBytes + kScBytes;              // 28,672 = 28 * 1024
 constexpr int kLutBytes = 2 * 256 * 16;                     // even / odd selector tables
-constexpr int kThreads = 14 * 32;
-constexpr int kConvThreads = 128, kExpThreads = 256;
+constexpr int kThreads = 10 * 32;
+constexpr int kExpWarp0 = 2, kExpThreads = 256;
 constexpr uint32_t kWaitLimit = 1u << 22;
 
 // shared memory layout (offsets from a 1024-aligned base)
@@ -60,8 +61,8 @@ constexpr int kOffB = kOffA + kStages * kASlice;
 constexpr int kOffQ = kOffB + kStages * kBSlice;
 constexpr int kOffLut = kOffQ + 2 * kGroupBuf;
 constexpr int kOffBar = kOffLut + kLutBytes;
-// barriers: a_full[S], a_ready[S], b_full[S], empty[S], q_full[2], q_empty[2], acc
-constexpr int kNumBars = 4 * kStages + 4 + 1;
+// barriers: a_full[S], b_full[S], empty[S], q_full[2], q_empty[2], acc
+constexpr int kNumBars = 3 * kStages + 4 + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;            // tmem base, abort flag
 constexpr int kSmemBytes = kOffMisc + 16;
 
@@ -122,16 +123,21 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
   return d;
 }
 
-// Instruction descriptor: fp32 accumulator, fp16 A and B, both K-major,
-// N = 128, M = 128.
-constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(UM >> 4) << 24);
+// Instruction descriptor: fp32 accumulator (bits 4-5), A and B format
+// (bits 7-9, 10-12: 0 fp16, 1 bf16), both K-major, N = 128, M = 128.
+template <bool kBf16>
+__host__ __device__ constexpr uint32_t idesc() {
+  return (1u << 4) | (kBf16 ? (1u << 7) | (1u << 10) : 0u) | ((uint32_t)(BN >> 3) << 17) |
+         ((uint32_t)(UM >> 4) << 24);
+}
 
+template <bool kBf16>
 __device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
                                          uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      "l"(adesc), "l"(bdesc), "r"(idesc<kBf16>()), "r"(accumulate)
       : "memory");
 }
 
@@ -234,8 +240,9 @@ __device__ __forceinline__ void expand_half(const uint32_t win[12], uint32_t ta,
         make_uint4(out[4 * c], out[4 * c + 1], out[4 * c + 2], out[4 * c + 3]);
 }
 
-// The 8 blocks of one staged group for this thread's row and half.
-template <int h, int bb = 0>
+// The 8 blocks of one staged group for this thread's row and half, as fp16
+// or (kBf16) bf16 values t * s.
+template <bool kBf16, int h, int bb = 0>
 __device__ __forceinline__ bool expand_group(const unsigned char* qrow, const uint16_t* srow,
                                              const unsigned char* lut, unsigned char* smem,
                                              uint64_t* empty, uint64_t* b_full, int g, int r,
@@ -248,7 +255,9 @@ __device__ __forceinline__ bool expand_group(const unsigned char* qrow, const ui
       const uint4 v = *reinterpret_cast<const uint4*>(qrow + base16 + 16 * i);
       win[4 * i] = v.x; win[4 * i + 1] = v.y; win[4 * i + 2] = v.z; win[4 * i + 3] = v.w;
     }
-    const uint32_t s16 = srow[bb];
+    uint32_t s16 = srow[bb];
+    if constexpr (kBf16)  // the fp16 scale rounded to nearest-even bf16
+      s16 = __bfloat16_as_ushort(__float2bfloat16_rn(__half2float(__ushort_as_half((unsigned short)s16))));
     // PRMT sources: bytes 0-1 = -s, 2-3 = 0, 4-5 = +s
     const uint32_t ta = (s16 ^ 0x8000u), tb = s16;
     const int kb = g * 16 + bb * 2 + h;
@@ -257,12 +266,12 @@ __device__ __forceinline__ bool expand_group(const unsigned char* qrow, const ui
     expand_half<h, o>(win, ta, tb, lut, smem + kOffB + s * kBSlice, r);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     mbar_arrive(&b_full[s]);
-    return expand_group<h, bb + 1>(qrow, srow, lut, smem, empty, b_full, g, r, abort_flag);
+    return expand_group<kBf16, h, bb + 1>(qrow, srow, lut, smem, empty, b_full, g, r, abort_flag);
   }
   return true;
 }
 
-template <bool kConvertA, bool kOutF32>
+template <bool kBf16, bool kOutF32>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a,
                    const __grid_constant__ CUtensorMap map_q,
@@ -275,10 +284,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) unsigned char smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint64_t* a_full = bars;
-  uint64_t* a_ready = bars + kStages;
-  uint64_t* b_full = bars + 2 * kStages;
-  uint64_t* empty = bars + 3 * kStages;
-  uint64_t* q_full = bars + 4 * kStages;
+  uint64_t* b_full = bars + kStages;
+  uint64_t* empty = bars + 2 * kStages;
+  uint64_t* q_full = bars + 3 * kStages;
   uint64_t* q_empty = q_full + 2;
   uint64_t* acc_full = q_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
@@ -293,7 +301,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&a_full[s], 1);
-      mbar_init(&a_ready[s], kConvThreads);
       mbar_init(&b_full[s], kExpThreads / 2);
       mbar_init(&empty[s], 1);
     }
@@ -351,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       for (int kb = 0; kb < nk && ok; ++kb) {
         const int s = kb % kStages, round = kb / kStages;
-        ok = mbar_wait(kConvertA ? &a_ready[s] : &a_full[s], round & 1, abort_flag) &&
+        ok = mbar_wait(&a_full[s], round & 1, abort_flag) &&
              mbar_wait(&b_full[s], round & 1, abort_flag);
         if (!ok) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -361,39 +368,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int mh = 0; mh < 2; ++mh)
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)  // K = 16 per MMA: 32 bytes along the atom
-            umma_f16(tmem + mh * BN, sw128_desc(a_addr + mh * (UM * 128) + 32 * kk),
-                     sw128_desc(b_addr + 32 * kk), (kb | kk) != 0);
+            umma_f16<kBf16>(tmem + mh * BN, sw128_desc(a_addr + mh * (UM * 128) + 32 * kk),
+                            sw128_desc(b_addr + 32 * kk), (kb | kk) != 0);
         umma_commit(&empty[s]);  // frees the slice once these MMAs have read it
       }
       umma_commit(acc_full);     // all MMAs issued by this thread
     }
-  } else if (warp < 6) {
-    // ---- A conversion bf16 -> fp16, in place ---------------------------------------
-    if (kConvertA) {
-      const int t = threadIdx.x - 64;  // 0..127
-      for (int kb = 0; kb < nk && ok; ++kb) {
-        const int s = kb % kStages, round = kb / kStages;
-        ok = mbar_wait(&a_full[s], round & 1, abort_flag);
-        if (!ok) break;
-        uint4* a = reinterpret_cast<uint4*>(smem + kOffA + s * kASlice);
-#pragma unroll 4
-        for (int c = t; c < kASlice / 16; c += kConvThreads) {
-          uint4 v = a[c];
-          auto cv = [](uint32_t w) {
-            const __half2 h2 =
-                __floats2half2_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
-            return (uint32_t)__half_as_ushort(h2.x) | ((uint32_t)__half_as_ushort(h2.y) << 16);
-          };
-          v.x = cv(v.x); v.y = cv(v.y); v.z = cv(v.z); v.w = cv(v.w);
-          a[c] = v;
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive(&a_ready[s]);
-      }
-    }
   } else {
     // ---- B expansion: thread (row r, half h) ---------------------------------------
-    const int t = threadIdx.x - 192, r = t & (BN - 1), h = t >> 7;  // h is warp-uniform
+    const int t = threadIdx.x - 32 * kExpWarp0, r = t & (BN - 1), h = t >> 7;  // h: warp-uniform
     for (int g = 0; g < ng && ok; ++g) {
       const int qb = g & 1;
       ok = mbar_wait(&q_full[qb], (g >> 1) & 1, abort_flag);
@@ -401,8 +384,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const unsigned char* qrow = smem + kOffQ + qb * kGroupBuf + r * kGroupBytes;
       const uint16_t* srow =
           reinterpret_cast<const uint16_t*>(smem + kOffQ + qb * kGroupBuf + kQsBytes) + r * 8;
-      ok = h == 0 ? expand_group<0>(qrow, srow, lut, smem, empty, b_full, g, r, abort_flag)
-                  : expand_group<1>(qrow, srow, lut, smem, empty, b_full, g, r, abort_flag);
+      ok = h == 0 ? expand_group<kBf16, 0>(qrow, srow, lut, smem, empty, b_full, g, r, abort_flag)
+                  : expand_group<kBf16, 1>(qrow, srow, lut, smem, empty, b_full, g, r, abort_flag);
       if (ok) mbar_arrive(&q_empty[qb]);
     }
   }
@@ -411,13 +394,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) atomicOr(status, kDevTimeout);
   }
 
-  // ---- epilogue: warps 6-13; warp w reads TMEM lanes 32 (w % 4) .. + 31 of
-  // accumulator (w - 6) / 4 -------------------------------------------------------------
-  if (warp >= 6) {
+  // ---- epilogue: warps 2-9; warp w reads TMEM lanes 32 (w % 4) .. + 31 of
+  // accumulator (w - 2) / 4 -------------------------------------------------------------
+  if (warp >= kExpWarp0) {
     const bool done = !*abort_flag && mbar_wait(acc_full, 0, abort_flag);
     if (done) {
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const int q = warp & 3, mh = (warp - 6) >> 2;
+      const int q = warp & 3, mh = (warp - kExpWarp0) >> 2;
       const int row = m0 + mh * UM + 32 * q + lane;
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -490,10 +473,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---- host side -------------------------------------------------------------------------
-template <bool kConvertA, bool kOutF32>
+template <bool kBf16, bool kOutF32>
 cudaError_t launch_t(const CUtensorMap& ma, const CUtensorMap& mq, const CUtensorMap& ms, void* y,
                      int M, int N, int K, int* status, cudaStream_t st) {
-  auto kern = gemm_tc_kernel<kConvertA, kOutF32>;
+  auto kern = gemm_tc_kernel<kBf16, kOutF32>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -525,9 +508,9 @@ cudaError_t launch_gemm_tc(const uint8_t* wq, const uint16_t* scales, const void
   int* status = device_status_ptr();
   if (!status) return cudaErrorInvalidDevice;
   const int m = (int)M, n = (int)N, k = (int)K;
-  const bool conv = x_t == Act::BF16, f32 = y_t == Act::F32;
-  if (conv && f32) return launch_t<true, true>(ma, mq, ms, y, m, n, k, status, st);
-  if (conv) return launch_t<true, false>(ma, mq, ms, y, m, n, k, status, st);
+  const bool bf = x_t == Act::BF16, f32 = y_t == Act::F32;
+  if (bf && f32) return launch_t<true, true>(ma, mq, ms, y, m, n, k, status, st);
+  if (bf) return launch_t<true, false>(ma, mq, ms, y, m, n, k, status, st);
   if (f32) return launch_t<false, true>(ma, mq, ms, y, m, n, k, status, st);
   return launch_t<false, false>(ma, mq, ms, y, m, n, k, status, st);
 }

@@ -71,8 +71,8 @@ def test_rotate_matmul_unfused_routes(P, orc, syn, M, dtype):
     if dtype == "f32":
         Q.check_f32(Q.host_f64(y), ref, f"rotate+matmul M={M}")
     else:
-        # the rotated operand is stored in bf16 before the GEMM: one more
-        # rounding of 2^-9 relative, far inside 1e-2 rms
+        # the rotated operand is held in fp16 before the GEMM (2^-11), whose
+        # weight tile is then exact
         Q.check_bf16(Q.host_f64(y), ref, f"rotate+gemm M={M}")
 
 
