@@ -17,23 +17,27 @@
 // bf16 is at most 2^-9 relative.  fp16 activations (the feed-forward block's
 // rotated operands) give exact fp16 tiles.
 //
-// Tile: 256 (M) x 128 (N): two 128-row accumulators in TMEM share every
-// expanded B slice, so each weight is peeled once per 256 activation rows.
-// K is consumed in 64-wide slices (one 128-byte swizzle atom of 16-bit
-// values), kStages slices in flight.  Warp roles (10 warps):
-//   warp 0      TMA producer: A slices (box 64 x 256, 128B swizzle) and, per
-//               1024-wide group, the packed trits (box 208 B x 128 rows) and
-//               scales (box 8 x 128) into a 2-deep group ring, one group ahead.
+// Tile: 256 (M) x 128 (N): two 128-row accumulators in TMEM (256 columns)
+// share every expanded B slice, so each weight is peeled once per 256
+// activation rows.  K is consumed in 64-wide slices (one 128-byte swizzle atom
+// of 16-bit values) through a 2-deep ring of A and B slices.  The CTA holds
+// about 98 KB of shared memory, so two CTAs share an SM: the MMAs of one
+// cover the load and expansion latency of the other.  Warp roles (10 warps):
+//   warp 0      TMA producer of the A slices (box 64 x 256, 128B swizzle).
 //   warp 1      TMEM allocation; lane 0 issues tcgen05.mma (8 per slice).
 //   warps 2-9   expansion: thread (row r, half h) peels the 64 weights of half
-//               h of each 128-weight block of row r.  A table built per CTA
-//               maps each byte value to byte-permute selectors, so every pair
-//               of 16-bit outputs is one permute of the per-block bytes
+//               h of every 128-weight block of row r in registers (two bytes
+//               per integer multiply, see expand_half), reading the packed
+//               row with 16-byte loads kept two blocks ahead; every pair of
+//               16-bit outputs is one permute of the per-block bytes
 //               {-s, 0, +s}.  Writes use the canonical K-major 128B-swizzled
 //               layout; afterwards these warps run the epilogue
 //               (TMEM -> registers -> y).
-// Every mbarrier wait is bounded; a wait that runs out raises the device
-// status word, the CTA drains what it has in flight (bounded) and exits.
+// The weights do not depend on the previous kernel in the stream, so the
+// expansion starts before griddepcontrol.wait; the A loads and the output
+// stores wait for it.  Every mbarrier wait is bounded; a wait that runs out
+// raises the device status word, the CTA drains what it has in flight
+// (bounded) and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -44,13 +48,9 @@ namespace ptq {
 namespace {
 
 constexpr int BM = 256, BN = 128, BK = 64, UM = 128;   // UM: rows per MMA
-constexpr int kStages = 3;
+constexpr int kStages = 2;
 constexpr int kASlice = BM * BK * 2;                        // 32 KB
 constexpr int kBSlice = BN * BK * 2;                        // 16 KB
-constexpr int kQsBytes = BN * kGroupBytes;                  // 26,624
-constexpr int kScBytes = BN * kGroupBlocks * 2;             // 2,048
-constexpr int kGroupBuf = kQsBytes + kScBytes;              // 28,672 = 28 * 1024
-constexpr int kLutBytes = 2 * 256 * 16;                     // even / odd selector tables
 constexpr int kThreads = 10 * 32;
 constexpr int kExpWarp0 = 2, kExpThreads = 256;
 constexpr uint32_t kWaitLimit = 1u << 22;
@@ -58,13 +58,12 @@ constexpr uint32_t kWaitLimit = 1u << 22;
 // shared memory layout (offsets from a 1024-aligned base)
 constexpr int kOffA = 0;
 constexpr int kOffB = kOffA + kStages * kASlice;
-constexpr int kOffQ = kOffB + kStages * kBSlice;
-constexpr int kOffLut = kOffQ + 2 * kGroupBuf;
-constexpr int kOffBar = kOffLut + kLutBytes;
-// barriers: a_full[S], b_full[S], empty[S], q_full[2], q_empty[2], acc
-constexpr int kNumBars = 3 * kStages + 4 + 1;
+constexpr int kOffBar = kOffB + kStages * kBSlice;
+// barriers: a_full[S], b_full[S], empty[S], acc
+constexpr int kNumBars = 3 * kStages + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;            // tmem base, abort flag
 constexpr int kSmemBytes = kOffMisc + 16;
+static_assert(2 * (kSmemBytes + 1024) <= 228 * 1024, "two CTAs per SM");
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -148,135 +147,188 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
       : "memory");
 }
 
-// Byte offset of element (r, k) (k < 64) inside a 128-row, 64-wide fp16 tile
+// Byte offset of element (r, k) (k < 64) inside a 128-row, 64-wide 16-bit tile
 // in the canonical K-major 128B-swizzled layout.
 __device__ __forceinline__ uint32_t sw128_off(int r, int k) {
   return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + (((k >> 3) ^ (r & 7)) << 4) + (k & 7) * 2);
 }
 
-// Selector tables.  PRMT picks each output byte from 8 source bytes; the
-// per-block sources are {-s, 0, +s} as fp16 (bytes 0-1, 2-3, 4-5), so digit
-// d = t + 1 of a weight selects bytes 2d and 2d + 1.  For a byte value v with
-// digits d0..d4 (weights 5j .. 5j+4): an even-positioned byte (5j even) is
-// emitted as pairs (d0,d1), (d2,d3) and a low half d4; an odd-positioned
-// byte as a high half d0 and pairs (d1,d2), (d3,d4).  Entry = 4 words:
-// {pair selector, pair selector, half selector, 0}; the straddling pair is
-// the OR of the two half selectors.
-__device__ __forceinline__ uint32_t sel_pair(uint32_t da, uint32_t db) {
-  return (2 * da) | ((2 * da + 1) << 4) | ((2 * db) << 8) | ((2 * db + 1) << 12);
-}
-
-__device__ void build_luts(uint4* lut) {
-  for (int i = threadIdx.x; i < 512; i += blockDim.x) {
-    const uint32_t v = i & 255;
-    uint32_t d[5], fprev = 0;
+// Expansion arithmetic.  PRMT picks each output byte from 8 source bytes; the
+// per-block sources are {-s, 0, +s} as 16-bit values (bytes 0-1, 2-3, 4-5), so
+// a weight with digit d = t + 1 selects bytes 2d and 2d + 1, and a pair of
+// weights with digits (da, db) -- one 32-bit output word -- uses the selector
+//   (2da) | (2da+1) << 4 | (2db) << 8 | (2db+1) << 12 = 34 (da + 256 db) + 0x1010.
+// Digits come from the peel of "What Ferrox does with it",
+//   d_n = floor(3^(n+1) u) - 3 floor(3^n u),  u = byte / 256,
+// computed for two bytes at once: with byte A in bits 0-7 and byte B in bits
+// 16-23 of S, S * 3^n holds 3^n A and 3^n B in its two 16-bit lanes
+// (3^5 * 255 < 2^16), their floors (/256) are bytes 1 and 3, and
+// F_{n+1} - 3 F_n never borrows across lanes (it is the digit, 0..2).
+// digits2(S) returns D_n = dA_n | dB_n << 16 for n = 0..4.
+__device__ __forceinline__ void digits2(uint32_t S, uint32_t D[5]) {
+  uint32_t F = 0u;  // F_0 = floor(byte / 256) = 0
+  uint32_t P = S;
 #pragma unroll
-    for (int n = 0; n < 5; ++n) {  // digit n = floor(3^(n+1) v/256) - 3 floor(3^n v/256)
-      const uint32_t p = n == 0 ? 3u : n == 1 ? 9u : n == 2 ? 27u : n == 3 ? 81u : 243u;
-      const uint32_t fnext = (v * p) >> 8;
-      d[n] = fnext - 3u * fprev;
-      fprev = fnext;
-    }
-    lut[i] = i < 256 ? make_uint4(sel_pair(d[0], d[1]), sel_pair(d[2], d[3]),
-                                  (2 * d[4]) | ((2 * d[4] + 1) << 4), 0u)
-                     : make_uint4(sel_pair(d[1], d[2]), sel_pair(d[3], d[4]),
-                                  ((2 * d[0]) | ((2 * d[0] + 1) << 4)) << 8, 0u);
+  for (int n = 0; n < 5; ++n) {
+    P *= 3u;                                         // 3^(n+1) byte, per lane
+    const uint32_t Fn = __byte_perm(P, 0u, 0x4341);  // floor(.../256), per lane
+    D[n] = Fn - 3u * F;
+    F = Fn;
   }
 }
 
-// Half h of one 128-weight block of one row: 64 fp16 values t * s written as
-// 8 swizzled 16-byte chunks.  `win` holds the 16-byte-aligned 48 bytes that
-// contain the block, which starts at byte `o` of the window.
+// Output word for the digit pair picked from Da and Db: the pair's selector
+// applied to the {-s, 0, +s} sources.
+__device__ __forceinline__ uint32_t word_of(uint32_t Da, uint32_t Db, uint32_t pick, uint32_t ta,
+                                            uint32_t tb) {
+  const uint32_t pair = __byte_perm(Da, Db, pick);  // da | db << 8
+  return __byte_perm(ta, tb, 34u * pair + 0x1010u);
+}
+// picks: digit of byte A (lane 0) or B (lane 1) of Da, then of Db
+constexpr uint32_t kAA = 0x1140, kBB = 0x1162, kAB = 0x1160;
+
+// Half h of one 128-weight block of one row: 64 16-bit values t * s written as
+// 8 swizzled 16-byte chunks.  `win` holds the 16-byte-aligned bytes that
+// contain the block, which starts at byte `o` of the window.  Bytes (2i, 2i+1)
+// of the block are peeled together and give the ten weights 10i..10i+9 as five
+// words: (d0,d1)A (d2,d3)A (d4A,d0B) (d1,d2)B (d3,d4)B.
 template <int h, int o>
 __device__ __forceinline__ void expand_half(const uint32_t win[12], uint32_t ta, uint32_t tb,
-                                            const unsigned char* lut, unsigned char* bslice,
-                                            int r) {
-  auto byte_of = [&](int j) -> uint32_t {
-    return __byte_perm(win[(o + j) >> 2], 0u, 0x4440u | ((o + j) & 3));
+                                            uint32_t bslice, int r) {
+  auto pair_of = [&](int i) -> uint32_t {  // bytes 2i, 2i+1 of the block in lanes 0, 1
+    const int j0 = o + 2 * i, j1 = o + 2 * i + 1;
+    const uint32_t sel = (uint32_t)(j0 & 3) | ((uint32_t)(4 + (j1 & 3)) << 8);
+    return __byte_perm(win[j0 >> 2], win[j1 >> 2], sel) & 0x00FF00FFu;
   };
-  auto even = [&](int j) { return *reinterpret_cast<const uint4*>(lut + byte_of(j) * 16); };
-  auto odd = [&](int j) { return *reinterpret_cast<const uint4*>(lut + 4096 + byte_of(j) * 16); };
-  auto P = [&](uint32_t sel) { return __byte_perm(ta, tb, sel); };
   uint32_t out[32];
   int n = 0;
   if constexpr (h == 0) {
 #pragma unroll
-    for (int j = 0; j < 12; j += 2) {  // bytes 0..11: weights 0..59
-      const uint4 e = even(j), q = odd(j + 1);
-      out[n++] = P(e.x);
-      out[n++] = P(e.y);
-      out[n++] = P(e.z | q.z);
-      out[n++] = P(q.x);
-      out[n++] = P(q.y);
+    for (int i = 0; i < 6; ++i) {  // weights 0..59
+      uint32_t D[5];
+      digits2(pair_of(i), D);
+      out[n++] = word_of(D[0], D[1], kAA, ta, tb);
+      out[n++] = word_of(D[2], D[3], kAA, ta, tb);
+      out[n++] = word_of(D[4], D[0], kAB, ta, tb);
+      out[n++] = word_of(D[1], D[2], kBB, ta, tb);
+      out[n++] = word_of(D[3], D[4], kBB, ta, tb);
     }
-    const uint4 e = even(12);  // weights 60..63
-    out[n++] = P(e.x);
-    out[n++] = P(e.y);
+    uint32_t D[5];
+    digits2(pair_of(6), D);  // weights 60..63
+    out[n++] = word_of(D[0], D[1], kAA, ta, tb);
+    out[n++] = word_of(D[2], D[3], kAA, ta, tb);
   } else {
     {
-      const uint4 e = even(12), q = odd(13);  // weights 64..69
-      out[n++] = P(e.z | q.z);
-      out[n++] = P(q.x);
-      out[n++] = P(q.y);
+      uint32_t D[5];
+      digits2(pair_of(6), D);  // weights 64..69
+      out[n++] = word_of(D[4], D[0], kAB, ta, tb);
+      out[n++] = word_of(D[1], D[2], kBB, ta, tb);
+      out[n++] = word_of(D[3], D[4], kBB, ta, tb);
     }
 #pragma unroll
-    for (int j = 14; j < 24; j += 2) {  // bytes 14..23: weights 70..119
-      const uint4 e = even(j), q = odd(j + 1);
-      out[n++] = P(e.x);
-      out[n++] = P(e.y);
-      out[n++] = P(e.z | q.z);
-      out[n++] = P(q.x);
-      out[n++] = P(q.y);
+    for (int i = 7; i < 12; ++i) {  // weights 70..119
+      uint32_t D[5];
+      digits2(pair_of(i), D);
+      out[n++] = word_of(D[0], D[1], kAA, ta, tb);
+      out[n++] = word_of(D[2], D[3], kAA, ta, tb);
+      out[n++] = word_of(D[4], D[0], kAB, ta, tb);
+      out[n++] = word_of(D[1], D[2], kBB, ta, tb);
+      out[n++] = word_of(D[3], D[4], kBB, ta, tb);
     }
-    const uint4 e = even(24), q = odd(25);  // weights 120..127 (byte 25 holds 3)
-    out[n++] = P(e.x);
-    out[n++] = P(e.y);
-    out[n++] = P(e.z | q.z);
-    out[n++] = P(q.x);
+    uint32_t D[5];
+    digits2(pair_of(12), D);  // weights 120..127; byte 25's last two digits are padding
+    out[n++] = word_of(D[0], D[1], kAA, ta, tb);
+    out[n++] = word_of(D[2], D[3], kAA, ta, tb);
+    out[n++] = word_of(D[4], D[0], kAB, ta, tb);
+    out[n++] = word_of(D[1], D[2], kBB, ta, tb);
   }
 #pragma unroll
   for (int c = 0; c < 8; ++c)
-    *reinterpret_cast<uint4*>(bslice + sw128_off(r, 8 * c)) =
-        make_uint4(out[4 * c], out[4 * c + 1], out[4 * c + 2], out[4 * c + 3]);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(bslice + sw128_off(r, 8 * c)),
+                 "r"(out[4 * c]), "r"(out[4 * c + 1]), "r"(out[4 * c + 2]), "r"(out[4 * c + 3])
+                 : "memory");
 }
 
-// The 8 blocks of one staged group for this thread's row and half, as fp16
-// or (kBf16) bf16 values t * s.
-template <bool kBf16, int h, int bb = 0>
-__device__ __forceinline__ bool expand_group(const unsigned char* qrow, const uint16_t* srow,
-                                             const unsigned char* lut, unsigned char* smem,
-                                             uint64_t* empty, uint64_t* b_full, int g, int r,
-                                             volatile int* abort_flag) {
-  if constexpr (bb < kGroupBlocks) {
-    constexpr int base16 = (kBlockBytes * bb) & ~15, o = (kBlockBytes * bb) & 15;
-    uint32_t win[12];
+// The packed bytes of one block of one row: the 16-byte chunks of the row
+// that the block's 26 bytes touch (two or three), and the block's scale.
+// Block kb of a row starts at byte 26 kb; rows are whole multiples of 208 =
+// 13 * 16 bytes (K % 1024 == 0), so with q = kb % 8 the block starts at byte
+// (26 q) % 16 of the chunk (26 kb) / 16 and no chunk past the block is read.
+template <int q>
+__device__ __forceinline__ void load_block(const uint8_t* row, const uint16_t* srow, int kb,
+                                           uint32_t win[12], uint32_t& sc) {
+  constexpr int o = (kBlockBytes * q) & 15;
+  constexpr int nc = (o + kBlockBytes + 15) / 16;
+  const uint4* p = reinterpret_cast<const uint4*>(row + ((kBlockBytes * kb) & ~15));
 #pragma unroll
-    for (int i = 0; i < 3; ++i) {
-      const uint4 v = *reinterpret_cast<const uint4*>(qrow + base16 + 16 * i);
-      win[4 * i] = v.x; win[4 * i + 1] = v.y; win[4 * i + 2] = v.z; win[4 * i + 3] = v.w;
-    }
-    uint32_t s16 = srow[bb];
-    if constexpr (kBf16)  // the fp16 scale rounded to nearest-even bf16
-      s16 = __bfloat16_as_ushort(__float2bfloat16_rn(__half2float(__ushort_as_half((unsigned short)s16))));
-    // PRMT sources: bytes 0-1 = -s, 2-3 = 0, 4-5 = +s
-    const uint32_t ta = (s16 ^ 0x8000u), tb = s16;
-    const int kb = g * 16 + bb * 2 + h;
-    const int s = kb % kStages, round = kb / kStages;
-    if (round > 0 && !mbar_wait(&empty[s], (round - 1) & 1, abort_flag)) return false;
-    expand_half<h, o>(win, ta, tb, lut, smem + kOffB + s * kBSlice, r);
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    mbar_arrive(&b_full[s]);
-    return expand_group<kBf16, h, bb + 1>(qrow, srow, lut, smem, empty, b_full, g, r, abort_flag);
+  for (int i = 0; i < nc; ++i) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p + i));
+    win[4 * i] = v.x; win[4 * i + 1] = v.y; win[4 * i + 2] = v.z; win[4 * i + 3] = v.w;
+  }
+  unsigned short s;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(s) : "l"(srow + kb));
+  sc = s;
+}
+
+struct ExpCtx {
+  const uint8_t* row;     // this thread's packed row
+  const uint16_t* srow;   // its scales
+  int nblk;
+  uint32_t bbase;         // shared address of B slice h
+  uint64_t* empty;        // empty[h]
+  uint64_t* b_full;       // b_full[h]
+  int r;
+  volatile int* abort_flag;
+};
+
+// One block kb = 8 g + q of the expansion: prefetch block kb + 2 into ring
+// slot (q + 2) % 4, wait for B slice h to be free, expand, publish.
+template <bool kBf16, int h, int q>
+__device__ __forceinline__ bool expand_step(const ExpCtx& c, int g, uint32_t (&win)[4][12],
+                                            uint32_t (&sc)[4]) {
+  const int kb = 8 * g + q;
+  if (kb + 2 < c.nblk)
+    load_block<(q + 2) % 8>(c.row, c.srow, kb + 2, win[(q + 2) % 4], sc[(q + 2) % 4]);
+  uint32_t s16 = sc[q % 4];
+  if constexpr (kBf16)  // the fp16 scale rounded to nearest-even bf16
+    s16 = __bfloat16_as_ushort(
+        __float2bfloat16_rn(__half2float(__ushort_as_half((unsigned short)s16))));
+  // PRMT sources: bytes 0-1 = -s, 2-3 = 0, 4-5 = +s
+  const uint32_t ta = (s16 ^ 0x8000u), tb = s16;
+  if (kb > 0 && !mbar_wait(c.empty, (kb - 1) & 1, c.abort_flag)) return false;
+  expand_half<h, (kBlockBytes * q) & 15>(win[q % 4], ta, tb, c.bbase, c.r);
+  // every writer makes its stores visible to the tensor core's (async) proxy
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  mbar_arrive(c.b_full);
+  return true;
+}
+
+template <bool kBf16, int h>
+__device__ bool expand_all(const ExpCtx& c) {
+  uint32_t win[4][12], sc[4];
+  load_block<0>(c.row, c.srow, 0, win[0], sc[0]);
+  load_block<1>(c.row, c.srow, 1, win[1], sc[1]);  // K >= 1024: at least 8 blocks
+  for (int g = 0; 8 * g < c.nblk; ++g) {
+    if (!expand_step<kBf16, h, 0>(c, g, win, sc)) return false;
+    if (!expand_step<kBf16, h, 1>(c, g, win, sc)) return false;
+    if (!expand_step<kBf16, h, 2>(c, g, win, sc)) return false;
+    if (!expand_step<kBf16, h, 3>(c, g, win, sc)) return false;
+    if (!expand_step<kBf16, h, 4>(c, g, win, sc)) return false;
+    if (!expand_step<kBf16, h, 5>(c, g, win, sc)) return false;
+    if (!expand_step<kBf16, h, 6>(c, g, win, sc)) return false;
+    if (!expand_step<kBf16, h, 7>(c, g, win, sc)) return false;
   }
   return true;
 }
 
 template <bool kBf16, bool kOutF32>
-__global__ void __launch_bounds__(kThreads, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a,
-                   const __grid_constant__ CUtensorMap map_q,
-                   const __grid_constant__ CUtensorMap map_s, void* __restrict__ y, int M, int N,
-                   int K, int* status) {
+__global__ void __launch_bounds__(kThreads, 2)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const uint8_t* __restrict__ wq,
+                   const uint16_t* __restrict__ scales, void* __restrict__ y, int M, int N, int K,
+                   int* status) {
   // No static shared variables: the dynamic window starts at offset 0, so the
   // declared 1024-byte alignment holds, and every access below stays a
   // shared-memory instruction (an address laundered through an integer
@@ -286,17 +338,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* a_full = bars;
   uint64_t* b_full = bars + kStages;
   uint64_t* empty = bars + 2 * kStages;
-  uint64_t* q_full = bars + 3 * kStages;
-  uint64_t* q_empty = q_full + 2;
-  uint64_t* acc_full = q_empty + 2;
+  uint64_t* acc_full = bars + 3 * kStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 8);
-  const unsigned char* lut = smem + kOffLut;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
-  const int nk = K / BK;            // 64-wide slices
-  const int ng = K / kRot;          // 1024-wide groups
+  const int nk = K / BK;             // 64-wide slices
+  const int nblk = K / kBlockWeights;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -304,15 +353,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&b_full[s], kExpThreads / 2);
       mbar_init(&empty[s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&q_full[i], 1);
-      mbar_init(&q_empty[i], kExpThreads);
-    }
     mbar_init(acc_full, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  build_luts(reinterpret_cast<uint4*>(smem + kOffLut));
   if (warp == 1) {  // TMEM: two 128-column fp32 accumulators x 128 lanes
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
@@ -324,28 +368,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tmem_slot;
-  pdl_wait();  // A may come from the previous kernel
 
   bool ok = true;
   int a_issued = 0;
   if (warp == 0) {
-    // ---- TMA producer ----------------------------------------------------------
+    // ---- TMA producer of A --------------------------------------------------------
     if (lane == 0) {
-      // packed weights run one 1024-wide group ahead of the A slices
-      auto issue_group = [&](int g) {
-        const int qb = g & 1;
-        if (g >= 2 && !mbar_wait(&q_empty[qb], ((g >> 1) - 1) & 1, abort_flag)) return false;
-        const uint32_t qdst = smem_u32(smem + kOffQ + qb * kGroupBuf);
-        mbar_expect_tx(&q_full[qb], kGroupBuf);
-        tma_2d(qdst, &map_q, g * kGroupBytes, n0, &q_full[qb]);
-        tma_2d(qdst + kQsBytes, &map_s, g * kGroupBlocks, n0, &q_full[qb]);
-        return true;
-      };
-      ok = issue_group(0) && (ng < 2 || issue_group(1));
+      pdl_wait();  // A may come from the previous kernel
       for (int kb = 0; kb < nk && ok; ++kb) {
         const int s = kb % kStages, round = kb / kStages;
-        if (kb % 16 == 0 && kb > 0 && kb / 16 + 1 < ng) ok = issue_group(kb / 16 + 1);
-        if (!ok) break;
         if (round > 0) ok = mbar_wait(&empty[s], (round - 1) & 1, abort_flag);
         if (!ok) break;
         mbar_expect_tx(&a_full[s], kASlice);
@@ -375,19 +406,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(acc_full);     // all MMAs issued by this thread
     }
   } else {
-    // ---- B expansion: thread (row r, half h) ---------------------------------------
+    // ---- B expansion: thread (row r, half h); slice 2 kb + h uses stage h ----------
     const int t = threadIdx.x - 32 * kExpWarp0, r = t & (BN - 1), h = t >> 7;  // h: warp-uniform
-    for (int g = 0; g < ng && ok; ++g) {
-      const int qb = g & 1;
-      ok = mbar_wait(&q_full[qb], (g >> 1) & 1, abort_flag);
-      if (!ok) break;
-      const unsigned char* qrow = smem + kOffQ + qb * kGroupBuf + r * kGroupBytes;
-      const uint16_t* srow =
-          reinterpret_cast<const uint16_t*>(smem + kOffQ + qb * kGroupBuf + kQsBytes) + r * 8;
-      ok = h == 0 ? expand_group<kBf16, 0>(qrow, srow, lut, smem, empty, b_full, g, r, abort_flag)
-                  : expand_group<kBf16, 1>(qrow, srow, lut, smem, empty, b_full, g, r, abort_flag);
-      if (ok) mbar_arrive(&q_empty[qb]);
-    }
+    const int n = n0 + r < N ? n0 + r : N - 1;  // rows past N expand a valid row; never stored
+    ExpCtx c;
+    c.row = wq + (size_t)n * nblk * kBlockBytes;
+    c.srow = scales + (size_t)n * nblk;
+    c.nblk = nblk;
+    c.bbase = smem_u32(smem + kOffB + h * kBSlice);
+    c.empty = &empty[h];
+    c.b_full = &b_full[h];
+    c.r = r;
+    c.abort_flag = abort_flag;
+    ok = h == 0 ? expand_all<kBf16, 0>(c) : expand_all<kBf16, 1>(c);
   }
   if (!ok) {
     *abort_flag = 1;
@@ -399,6 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp >= kExpWarp0) {
     const bool done = !*abort_flag && mbar_wait(acc_full, 0, abort_flag);
     if (done) {
+      pdl_wait();  // the previous kernel may still read y
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const int q = warp & 3, mh = (warp - kExpWarp0) >> 2;
       const int row = m0 + mh * UM + 32 * q + lane;
@@ -428,7 +460,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
                                 __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
             } else {
-              for (int i = 0; i < 32 && ncol + i < N; ++i) out[i] = __uint_as_float(v[i]);
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (ncol + i < N) out[i] = __uint_as_float(v[i]);
             }
           } else {
             uint16_t* out = static_cast<uint16_t*>(y) + (size_t)row * N + ncol;
@@ -444,8 +478,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *reinterpret_cast<uint4*>(out + 2 * i) =
                     make_uint4(pk[i], pk[i + 1], pk[i + 2], pk[i + 3]);
             } else {
-              for (int i = 0; i < 32 && ncol + i < N; ++i)
-                out[i] = (uint16_t)(pk[i >> 1] >> (16 * (i & 1)));
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (ncol + i < N) out[i] = (uint16_t)(pk[i >> 1] >> (16 * (i & 1)));
             }
           }
         }
@@ -474,15 +509,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---- host side -------------------------------------------------------------------------
 template <bool kBf16, bool kOutF32>
-cudaError_t launch_t(const CUtensorMap& ma, const CUtensorMap& mq, const CUtensorMap& ms, void* y,
+cudaError_t launch_t(const CUtensorMap& ma, const uint8_t* wq, const uint16_t* scales, void* y,
                      int M, int N, int K, int* status, cudaStream_t st) {
   auto kern = gemm_tc_kernel<kBf16, kOutF32>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmemBytes);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM));
-  return launch_pdl(kern, grid, dim3(kThreads), (size_t)kSmemBytes, st, ma, mq, ms, y, M, N, K,
-                    status);
+  return launch_pdl(kern, grid, dim3(kThreads), (size_t)kSmemBytes, st, ma, wq, scales, y, M, N,
+                    K, status);
 }
 
 }  // namespace
@@ -494,25 +529,18 @@ cudaError_t launch_gemm_tc(const uint8_t* wq, const uint16_t* scales, const void
       (M + BM - 1) / BM > 65535)
     return cudaErrorNotSupported;
   cudaError_t e;
-  const int64_t nblk = K / kBlockWeights, row_bytes = nblk * kBlockBytes;
-  CUtensorMap ma, mq, ms;
+  CUtensorMap ma;
   if ((e = encode_tma_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT16, x, K, M, K * 2, BK, BM,
                          CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)  // box 64 x 256
-    return e;
-  if ((e = encode_tma_2d(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, row_bytes, N, row_bytes,
-                         kGroupBytes, BN, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
-    return e;
-  if ((e = encode_tma_2d(&ms, CU_TENSOR_MAP_DATA_TYPE_UINT16, scales, nblk, N, nblk * 2,
-                         kGroupBlocks, BN, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
     return e;
   int* status = device_status_ptr();
   if (!status) return cudaErrorInvalidDevice;
   const int m = (int)M, n = (int)N, k = (int)K;
   const bool bf = x_t == Act::BF16, f32 = y_t == Act::F32;
-  if (bf && f32) return launch_t<true, true>(ma, mq, ms, y, m, n, k, status, st);
-  if (bf) return launch_t<true, false>(ma, mq, ms, y, m, n, k, status, st);
-  if (f32) return launch_t<false, true>(ma, mq, ms, y, m, n, k, status, st);
-  return launch_t<false, false>(ma, mq, ms, y, m, n, k, status, st);
+  if (bf && f32) return launch_t<true, true>(ma, wq, scales, y, m, n, k, status, st);
+  if (bf) return launch_t<true, false>(ma, wq, scales, y, m, n, k, status, st);
+  if (f32) return launch_t<false, true>(ma, wq, scales, y, m, n, k, status, st);
+  return launch_t<false, false>(ma, wq, scales, y, m, n, k, status, st);
 }
 
 }  // namespace ptq
