@@ -176,6 +176,16 @@ def max_over_ranks(v: float) -> float:
     return float(t.item())
 
 
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
+# dominant kernel, from the ncu capture of the matching `bench.py --profile`
+# case; None when the kernel has changed since those counters were taken.
+# Prefill: the capture is this exact launch (M=512, N=17408, K=5120).
+TRAFFIC_PREFILL = 24_840_448 + 7_168
+# Decode: the capture runs eight stacked gate/up matrices; the per-launch
+# figure is that capture's bytes / 8 (traffic grows with the rows streamed).
+TRAFFIC_DECODE = (156_069_376 + 4_433_920) // 8
+
+
 def run_ours(args, world, rank):
     import torch
 
@@ -265,7 +275,7 @@ def run_ours(args, world, rank):
                "kernel": P.route(PREFILL_M, P.PTQ_BF16),
                "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": pk["bf16"],
                             "unit": "TFLOP/s", "frac": round(tf / pk["bf16"], 4),
-                            "traffic": None, "peak_source": pk["source"] + " burst bf16"}}
+                            "traffic": TRAFFIC_PREFILL, "peak_source": pk["source"] + " burst bf16"}}
 
     cpu = cpu_baseline(args) if rank == 0 and not args.skip_cpu else None
     clocks = clk.summary()
@@ -281,7 +291,8 @@ def run_ours(args, world, rank):
                    "parallelism": f"{world} independent replicas" if world > 1 else "single GPU",
                    "timing": "CUDA graphs of <=500 steps, CUDA events on the launching stream"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm"],
-                     "unit": "GB/s", "frac": round(achieved / pk["hbm"], 4), "traffic": None,
+                     "unit": "GB/s", "frac": round(achieved / pk["hbm"], 4),
+                     "traffic": TRAFFIC_DECODE,
                      "kernel": P.route(1, P.PTQ_F32), "kernel_us": round(step_us, 3),
                      "timed": "one ptq_rotate_matmul call: the table-lookup GEMV with the "
                               "rotation fused in, and its chunk-reduction kernel",
@@ -383,18 +394,21 @@ def run_profile_case(which: str):
     mv = syn.gaussian_matvec(7, M, N, K_COLS, dtype=dt)
     wq = torch.from_numpy(P.pack(mv.trits)).cuda()
     sc = torch.from_numpy(mv.scales.view(np.int16)).cuda()
-    if dt == "f32":
+    if dt == "f32":  # the bench's decode call: rotation fused into the GEMV
         x = torch.from_numpy(mv.x).cuda()
         y = torch.empty((M, N), device="cuda")
+        signs = torch.from_numpy(syn.signs(7, 3, K_COLS)).cuda()
+        call = lambda: P.rotate_matmul(wq, sc, x, signs, out=y)
     else:
         x = torch.from_numpy(mv.x.view(np.int16)).cuda().view(torch.bfloat16)
         y = torch.empty((M, N), device="cuda", dtype=torch.bfloat16)
+        call = lambda: P.matmul(wq, sc, x, out=y)
     for _ in range(3):
-        P.matmul(wq, sc, x, out=y)
+        call()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    P.matmul(wq, sc, x, out=y)
+    call()
     e1.record()
     torch.cuda.synchronize()
     P.device_check()
@@ -408,8 +422,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=100)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-reps", type=int, default=20)
-    ap.add_argument("--reference-max-steps", type=int, default=40)
+    ap.add_argument("--cpu-reps", type=int, default=1000)       # about 10 s of oracle work
+    ap.add_argument("--reference-max-steps", type=int, default=1000)
     ap.add_argument("--skip-prefill", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--profile", choices=["gemv", "gemm"],
