@@ -107,8 +107,9 @@ PTQ_API PTQ_NODISCARD ptq_status ptq_fwht(const void* x, void* y,
 
 /* ptq_matmul_workspace_bytes -- scratch size ptq_matmul needs for
  * (M, N, K, dtype); 0 when it needs none or the arguments are invalid.
- * Only the M = 1 fp32 decode path with K/128 even needs scratch: one fp32
- * partial row sum per (K-chunk of at most 640 weights, output row). */
+ * Only the fp32 decode path (M <= 8) with K/128 even needs scratch: one fp32
+ * partial row sum per (K-chunk of at most 640 weights, output row), reused
+ * by the tokens in turn. */
 PTQ_API size_t ptq_matmul_workspace_bytes(int64_t M, int64_t N, int64_t K,
                                           ptq_dtype dtype);
 
@@ -116,10 +117,9 @@ PTQ_API size_t ptq_matmul_workspace_bytes(int64_t M, int64_t N, int64_t K,
  *     y[m, n] = sum_b scale[n, b] * sum_{i<128} trit[n, 128b + i] * x[m, 128b + i]
  * x is M x K and must already be rotated (ptq_fwht) when W carries the fold.
  * Routing (one table, queryable with ptq_route):
- *   PTQ_F32,  M == 1      : decode GEMV by per-position lookup tables of the
- *                           five-trit sums (K/128 even; otherwise the
- *                           general GEMV below), fp32 throughout
- *   PTQ_F32,  2 <= M <= 8 : decode GEMV with the fp32 peel, fp32 throughout
+ *   PTQ_F32,  1 <= M <= 8 : decode GEMV by per-position lookup tables of the
+ *                           five-trit sums, one token after the other, fp32
+ *                           throughout (K/128 odd: a GEMV with the fp32 peel)
  *   PTQ_BF16, M >= 1      : prefill GEMM, bf16 in / fp32 accumulate / bf16 out
  *   PTQ_F32,  M > 8       : refused with PTQ_ERR_UNSUPPORTED
  * M == 0 or N == 0 is a no-op.  Requires K % 128 == 0 (fastest at
@@ -147,7 +147,7 @@ PTQ_API size_t ptq_rotate_matmul_workspace_bytes(int64_t M, int64_t N,
 /* ptq_rotate_matmul -- y = (R x) W^T: the signed rotation of ptq_fwht applied
  * to x (un-rotated, not modified), then ptq_matmul.  This is the order the
  * pages prescribe for a folded weight ("What Ferrox does with it": rotate
- * the activation before every matmul).  On the fp32 M == 1 decode route the
+ * the activation before every matmul).  On the fp32 decode route (M <= 8) the
  * rotation runs inside the GEMV, on the activations each thread block reads;
  * otherwise it is a separate kernel writing R x into the workspace.
  * signs: K int8 (device, 4-byte aligned).  Requires K % 1024 == 0.

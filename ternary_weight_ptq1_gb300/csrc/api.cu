@@ -64,8 +64,7 @@ struct Route {
   const char* name;
 };
 static const Route kRoutes[] = {
-    {PTQ_F32, 1, 1, Kernel::GemvF32, "gemv_ptq1_f32_m1_lut"},
-    {PTQ_F32, 2, 8, Kernel::GemvF32, "gemv_ptq1_f32"},
+    {PTQ_F32, 1, 8, Kernel::GemvF32, "gemv_ptq1_f32_lut"},
     {PTQ_BF16, 1, INT64_MAX, Kernel::GemmBf16, "gemm_ptq1_bf16"},
 };
 
@@ -220,19 +219,26 @@ static ptq_status check_matmul(const uint8_t* wq, const uint16_t* scales, const 
 // x_t / y_t: the GEMV is fp32 in and out; the GEMM reads bf16 (public call)
 // or fp16 (inside the feed-forward block) and writes bf16 (public call) or
 // fp32 (the feed-forward block keeps gate/up in fp32).
+// The table-lookup GEMV for each of the M tokens in turn (its tables hold one
+// token's activations); the calls share the scratch, in stream order.
+static cudaError_t gemv_lut_tokens(const uint8_t* wq, const uint16_t* scales, const float* x,
+                                   const int8_t* signs, float* y, float* part, int64_t M,
+                                   int64_t N, int64_t K, cudaStream_t st) {
+  cudaError_t e = cudaSuccess;
+  for (int64_t m = 0; m < M && e == cudaSuccess; ++m)
+    e = launch_gemv_lut(wq, scales, x + m * K, signs, y + m * N, part, N, K, LutEpilogue::Plain, st);
+  return e;
+}
+
 // ws: matmul_ws_bytes(M, N, K, dtype) bytes of scratch (NULL when that is 0).
 static cudaError_t run_matmul(const Route* r, const uint8_t* wq, const uint16_t* scales,
                               const void* x, Act x_t, void* y, Act y_t, int64_t M, int64_t N,
                               int64_t K, void* ws, cudaStream_t st) {
   switch (r->kernel) {
     case Kernel::GemvF32:
-      if (M == 1) {  // table-lookup decode when the shape fits it
-        const cudaError_t e =
-            launch_gemv_lut(wq, scales, static_cast<const float*>(x), nullptr,
-                            static_cast<float*>(y), static_cast<float*>(ws), N, K,
-                            LutEpilogue::Plain, st);
-        if (e != cudaErrorNotSupported) return e;
-      }
+      if (gemv_lut_supported(N, K, false))  // table-lookup decode, one token at a time
+        return gemv_lut_tokens(wq, scales, static_cast<const float*>(x), nullptr,
+                               static_cast<float*>(y), static_cast<float*>(ws), M, N, K, st);
       return launch_gemv(wq, scales, static_cast<const float*>(x), static_cast<float*>(y), M, N,
                          K, st);
     case Kernel::GemmBf16:
@@ -243,7 +249,7 @@ static cudaError_t run_matmul(const Route* r, const uint8_t* wq, const uint16_t*
 
 // Scratch of ptq_matmul for valid arguments: the GEMV's per-chunk row sums.
 static size_t matmul_ws_bytes(int64_t M, int64_t N, int64_t K, ptq_dtype dt) {
-  return (dt == PTQ_F32 && M == 1) ? gemv_lut_workspace_bytes(N, K) : 0;
+  return (dt == PTQ_F32 && M >= 1 && M <= 8) ? gemv_lut_workspace_bytes(N, K) : 0;
 }
 
 PTQ_API size_t ptq_matmul_workspace_bytes(int64_t M, int64_t N, int64_t K, ptq_dtype dtype) {
@@ -318,10 +324,10 @@ PTQ_API ptq_status ptq_rotate_matmul(const uint8_t* wq, const uint16_t* scales, 
   if (!aligned(ws, 16)) return fail(PTQ_ERR_ALIGN, "%s: workspace needs 16-byte alignment", who);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (r->kernel == Kernel::GemvF32 && M == 1 && gemv_lut_supported(N, K, true)) {
+  if (r->kernel == Kernel::GemvF32 && gemv_lut_supported(N, K, true)) {
     // the rotation runs inside the GEMV, on the activations each CTA reads
-    e = launch_gemv_lut(wq, scales, static_cast<const float*>(x), signs, static_cast<float*>(y),
-                        static_cast<float*>(ws), N, K, LutEpilogue::Plain, st);
+    e = gemv_lut_tokens(wq, scales, static_cast<const float*>(x), signs, static_cast<float*>(y),
+                        static_cast<float*>(ws), M, N, K, st);
   } else {
     // R x is kept in fp32 (fp32 routes) or fp16 (bf16 route): with an fp16
     // operand the GEMM's weight tile t * s is exact, so the one rounding of
@@ -404,15 +410,20 @@ PTQ_API ptq_status ptq_ffn(const uint8_t* wgu_q, const uint16_t* wgu_s, const ui
   void* hr = bf ? static_cast<void*>(base + off[3]) : static_cast<void*>(h);
   void* part = base + off[4];
   const Act op = bf ? Act::F16 : Act::F32;  // tensor-core operand type
-  if (!bf && M == 1 && r_gu->kernel == Kernel::GemvF32 && gemv_lut_supported(2 * I, H, true) &&
+  if (!bf && r_gu->kernel == Kernel::GemvF32 && gemv_lut_supported(2 * I, H, true) &&
       gemv_lut_supported(H, I, true)) {
-    // decode: each table-lookup GEMV rotates its own activations, and the
-    // gate/up row sums are reduced straight into h = silu(g) * u
-    cudaError_t e = launch_gemv_lut(wgu_q, wgu_s, static_cast<const float*>(x), signs_in, h,
-                                    static_cast<float*>(part), 2 * I, H, LutEpilogue::SwiGLU, st);
-    if (e == cudaSuccess)
-      e = launch_gemv_lut(wd_q, wd_s, h, signs_mid, static_cast<float*>(y),
-                          static_cast<float*>(part), H, I, LutEpilogue::Plain, st);
+    // decode, token by token: each table-lookup GEMV rotates its own
+    // activations, and the gate/up row sums are reduced straight into
+    // h = silu(g) * u
+    cudaError_t e = cudaSuccess;
+    for (int64_t m = 0; m < M && e == cudaSuccess; ++m) {
+      float* hm = h + m * I;
+      e = launch_gemv_lut(wgu_q, wgu_s, static_cast<const float*>(x) + m * H, signs_in, hm,
+                          static_cast<float*>(part), 2 * I, H, LutEpilogue::SwiGLU, st);
+      if (e == cudaSuccess)
+        e = launch_gemv_lut(wd_q, wd_s, hm, signs_mid, static_cast<float*>(y) + m * H,
+                            static_cast<float*>(part), H, I, LutEpilogue::Plain, st);
+    }
     return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq_ffn launch");
   }
   cudaError_t e = launch_fwht(x, act_of(dtype), xr, op, signs_in, M, H, st);

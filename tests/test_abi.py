@@ -91,7 +91,8 @@ def test_refusals_before_launch(P):
     assert L.ptq_matmul(*args, None, need, None) == 6
     assert L.ptq_matmul(*args, p16, need - 1, None) == 6
     assert L.ptq_matmul(*args, odd, need, None) == 3
-    assert P.matmul_workspace_bytes(4, 17408, 5120, P.PTQ_F32) == 0
+    assert P.matmul_workspace_bytes(4, 17408, 5120, P.PTQ_F32) == need  # reused per token
+    assert P.matmul_workspace_bytes(9, 17408, 5120, P.PTQ_F32) == 0
     assert P.matmul_workspace_bytes(512, 17408, 5120, P.PTQ_BF16) == 0
     assert P.matmul_workspace_bytes(1, 17408, 5120 + 128, P.PTQ_F32) == 0  # K/128 odd
     assert P.matmul_workspace_bytes(1, 17408, 100, P.PTQ_F32) == 0
@@ -112,9 +113,8 @@ def test_refusals_before_launch(P):
 
 
 def test_routing_table(P):
-    assert P.route(1, P.PTQ_F32) == "gemv_ptq1_f32_m1_lut"
-    for M in range(2, 9):
-        assert P.route(M, P.PTQ_F32) == "gemv_ptq1_f32"
+    for M in range(1, 9):
+        assert P.route(M, P.PTQ_F32) == "gemv_ptq1_f32_lut"
     for M in (1, 8, 64, 128, 512, 2048, 10 ** 6):
         assert P.route(M, P.PTQ_BF16).startswith("gemm_ptq1_bf16")
     with pytest.raises(P.PTQError, match="UNSUPPORTED"):
