@@ -107,9 +107,11 @@ PTQ_API PTQ_NODISCARD ptq_status ptq_fwht(const void* x, void* y,
 
 /* ptq_matmul_workspace_bytes -- scratch size ptq_matmul needs for
  * (M, N, K, dtype); 0 when it needs none or the arguments are invalid.
- * Only the fp32 decode path (M <= 8) with K/128 even needs scratch: one fp32
- * partial row sum per (K-chunk of at most 640 weights, output row), reused
- * by the tokens in turn. */
+ * fp32 decode (M <= 8, K/128 even): one fp32 partial row sum per (K-chunk of
+ * at most 640 weights, output row), reused by the tokens in turn; required.
+ * bf16 GEMM: fp32 partial sums for shapes with too few output tiles to fill
+ * the GPU, whose K is then split in up to 6 parts; optional (with less, the
+ * product runs with fewer splits). */
 PTQ_API size_t ptq_matmul_workspace_bytes(int64_t M, int64_t N, int64_t K,
                                           ptq_dtype dtype);
 
@@ -124,9 +126,9 @@ PTQ_API size_t ptq_matmul_workspace_bytes(int64_t M, int64_t N, int64_t K,
  *   PTQ_F32,  M > 8       : refused with PTQ_ERR_UNSUPPORTED
  * M == 0 or N == 0 is a no-op.  Requires K % 128 == 0 (fastest at
  * K % 1024 == 0).  All pointers are device pointers.
- * workspace: device scratch of at least ptq_matmul_workspace_bytes(...) bytes,
- * 16-byte aligned, caller-owned, any initial contents, unspecified contents
- * on return; may be NULL when that size is 0.  Calls whose kernels overlap
+ * workspace: device scratch of ptq_matmul_workspace_bytes(...) bytes, 16-byte
+ * aligned, caller-owned, any initial contents, unspecified contents on
+ * return; may be NULL when that size is 0 or the route is the bf16 GEMM.  Calls whose kernels overlap
  * on the GPU need separate workspaces.  Results are bitwise reproducible:
  * the same inputs give the same bits on every run.
  * Errors: PTQ_ERR_NULL, PTQ_ERR_SHAPE, PTQ_ERR_ALIGN, PTQ_ERR_VALUE (dtype),

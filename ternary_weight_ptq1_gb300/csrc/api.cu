@@ -230,10 +230,11 @@ static cudaError_t gemv_lut_tokens(const uint8_t* wq, const uint16_t* scales, co
   return e;
 }
 
-// ws: matmul_ws_bytes(M, N, K, dtype) bytes of scratch (NULL when that is 0).
+// ws: ws_bytes of scratch, matmul_ws_bytes(M, N, K, dtype) for full speed
+// (NULL when that is 0).  The GEMM runs with fewer K splits when it gets less.
 static cudaError_t run_matmul(const Route* r, const uint8_t* wq, const uint16_t* scales,
                               const void* x, Act x_t, void* y, Act y_t, int64_t M, int64_t N,
-                              int64_t K, void* ws, cudaStream_t st) {
+                              int64_t K, void* ws, size_t ws_bytes, cudaStream_t st) {
   switch (r->kernel) {
     case Kernel::GemvF32:
       if (gemv_lut_supported(N, K, false))  // table-lookup decode, one token at a time
@@ -242,14 +243,15 @@ static cudaError_t run_matmul(const Route* r, const uint8_t* wq, const uint16_t*
       return launch_gemv(wq, scales, static_cast<const float*>(x), static_cast<float*>(y), M, N,
                          K, st);
     case Kernel::GemmBf16:
-      return launch_gemm(wq, scales, x, x_t, y, y_t, M, N, K, st);
+      return launch_gemm(wq, scales, x, x_t, y, y_t, M, N, K, ws, ws_bytes, st);
   }
   return cudaErrorInvalidValue;
 }
 
 // Scratch of ptq_matmul for valid arguments: the GEMV's per-chunk row sums.
 static size_t matmul_ws_bytes(int64_t M, int64_t N, int64_t K, ptq_dtype dt) {
-  return (dt == PTQ_F32 && M >= 1 && M <= 8) ? gemv_lut_workspace_bytes(N, K) : 0;
+  if (dt == PTQ_F32) return (M >= 1 && M <= 8) ? gemv_lut_workspace_bytes(N, K) : 0;
+  return gemm_tc_workspace_bytes(M, N, K);  // split-K partial sums
 }
 
 PTQ_API size_t ptq_matmul_workspace_bytes(int64_t M, int64_t N, int64_t K, ptq_dtype dtype) {
@@ -268,16 +270,18 @@ PTQ_API ptq_status ptq_matmul(const uint8_t* wq, const uint16_t* scales, const v
   const Route* r = nullptr;
   ptq_status s = check_matmul(wq, scales, x, y, M, N, K, dtype, who, &r);
   if (s != PTQ_OK || M == 0 || N == 0) return s;
+  // the decode GEMV needs its scratch; the GEMM runs unsplit (or with fewer
+  // K splits) on less
   const size_t need = matmul_ws_bytes(M, N, K, dtype);
-  if (need > 0) {
-    if (!ws) return fail(PTQ_ERR_WORKSPACE, "%s: workspace is NULL (%zu bytes needed)", who, need);
-    if (ws_bytes < need)
-      return fail(PTQ_ERR_WORKSPACE, "%s: workspace has %zu bytes, %zu needed", who, ws_bytes,
-                  need);
-    if (!aligned(ws, 16)) return fail(PTQ_ERR_ALIGN, "%s: workspace needs 16-byte alignment", who);
-  }
+  const bool required = dtype == PTQ_F32 && need > 0;
+  if (required && !ws)
+    return fail(PTQ_ERR_WORKSPACE, "%s: workspace is NULL (%zu bytes needed)", who, need);
+  if (required && ws_bytes < need)
+    return fail(PTQ_ERR_WORKSPACE, "%s: workspace has %zu bytes, %zu needed", who, ws_bytes, need);
+  if (ws && !aligned(ws, 16))
+    return fail(PTQ_ERR_ALIGN, "%s: workspace needs 16-byte alignment", who);
   cudaError_t e = run_matmul(r, wq, scales, x, act_of(dtype), y, act_of(dtype), M, N, K,
-                             need > 0 ? ws : nullptr, reinterpret_cast<cudaStream_t>(stream));
+                             ws, ws ? ws_bytes : 0, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq_matmul launch");
 }
 
@@ -336,15 +340,17 @@ PTQ_API ptq_status ptq_rotate_matmul(const uint8_t* wq, const uint16_t* scales, 
     void* xr = static_cast<char*>(ws) + xr_off;
     const Act op = dtype == PTQ_BF16 ? Act::F16 : Act::F32;
     e = launch_fwht(x, act_of(dtype), xr, op, signs, M, K, st);
-    if (e == cudaSuccess) e = run_matmul(r, wq, scales, xr, op, y, act_of(dtype), M, N, K, ws, st);
+    if (e == cudaSuccess)
+      e = run_matmul(r, wq, scales, xr, op, y, act_of(dtype), M, N, K, ws, xr_off, st);
   }
   return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq_rotate_matmul launch");
 }
 
 // Workspace of ptq_ffn, each region rounded up to 256 bytes:
 //   xr (M x H) | gu (M x 2I, fp32) | h (M x I, fp32) [| hr (M x I, fp16)]
-//   | part (the decode GEMV's row sums; shared by the two projections,
-//     which never hold it at the same time)
+//   | part (the decode GEMV's row sums, shared by the two projections, which
+//     never hold it at the same time; for the prefill GEMM, gate/up's split-K
+//     partial sums)
 // fp32 path: xr fp32, h rotated in place.  bf16 path: xr and hr are fp16
 // (the tensor-core operands; 11 significant bits against bf16's 8, and the
 // block scale times a trit is exact in fp16), gate/up and SwiGLU stay fp32,
@@ -363,8 +369,10 @@ static bool ffn_layout(int64_t M, int64_t H, int64_t I, ptq_dtype dt, size_t off
   off[2] = off[1] + (size_t)up(b);
   off[3] = off[2] + (size_t)up(c);
   off[4] = off[3] + (size_t)up(d);
+  // decode: the larger of the two projections' row sums; prefill: gate/up's
+  // split-K sums (the down projection's use the gate/up region, dead by then)
   const size_t p1 = matmul_ws_bytes(M, 2 * I, H, dt), p2 = matmul_ws_bytes(M, H, I, dt);
-  *total = off[4] + (p1 > p2 ? p1 : p2);
+  *total = off[4] + (dt == PTQ_BF16 ? p1 : (p1 > p2 ? p1 : p2));
   return true;
 }
 
@@ -428,11 +436,13 @@ PTQ_API ptq_status ptq_ffn(const uint8_t* wgu_q, const uint16_t* wgu_s, const ui
   }
   cudaError_t e = launch_fwht(x, act_of(dtype), xr, op, signs_in, M, H, st);
   if (e == cudaSuccess)
-    e = run_matmul(r_gu, wgu_q, wgu_s, xr, op, gu, Act::F32, M, 2 * I, H, part, st);
+    e = run_matmul(r_gu, wgu_q, wgu_s, xr, op, gu, Act::F32, M, 2 * I, H, part, need - off[4], st);
   if (e == cudaSuccess) e = launch_swiglu(gu, h, M, I, st);
   if (e == cudaSuccess) e = launch_fwht(h, Act::F32, hr, op, signs_mid, M, I, st);
+  // the down projection's split-K partials go where gate/up was (dead after
+  // SwiGLU)
   if (e == cudaSuccess)
-    e = run_matmul(r_d, wd_q, wd_s, hr, op, y, act_of(dtype), M, H, I, part, st);
+    e = run_matmul(r_d, wd_q, wd_s, hr, op, y, act_of(dtype), M, H, I, gu, off[2] - off[1], st);
   return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq_ffn launch");
 }
 

@@ -94,8 +94,9 @@ __global__ void __launch_bounds__(256) gemm_ptq1_bf16_simt(const uint8_t* __rest
 }  // namespace
 
 cudaError_t launch_gemm(const uint8_t* wq, const uint16_t* scales, const void* xv, Act x_t,
-                        void* y, Act y_t, int64_t M, int64_t N, int64_t K, cudaStream_t st) {
-  const cudaError_t tc = launch_gemm_tc(wq, scales, xv, x_t, y, y_t, M, N, K, st);
+                        void* y, Act y_t, int64_t M, int64_t N, int64_t K, void* ws,
+                        size_t ws_bytes, cudaStream_t st) {
+  const cudaError_t tc = launch_gemm_tc(wq, scales, xv, x_t, y, y_t, M, N, K, ws, ws_bytes, st);
   if (tc != cudaErrorNotSupported) return tc;  // K % 1024 != 0 falls through to SIMT
   const uint16_t* x = static_cast<const uint16_t*>(xv);
   if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return cudaErrorInvalidValue;

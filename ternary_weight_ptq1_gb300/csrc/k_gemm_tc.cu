@@ -276,7 +276,7 @@ __device__ __forceinline__ void load_block(const uint8_t* row, const uint16_t* s
 struct ExpCtx {
   const uint8_t* row;     // this thread's packed row
   const uint16_t* srow;   // its scales
-  int nblk;
+  int g_lo, nblk;         // first group, and the end of this split's blocks
   uint32_t bbase;         // shared address of B slice h
   uint64_t* empty;        // empty[h]
   uint64_t* b_full;       // b_full[h]
@@ -289,7 +289,8 @@ struct ExpCtx {
 template <bool kBf16, int h, int q>
 __device__ __forceinline__ bool expand_step(const ExpCtx& c, int g, uint32_t (&win)[4][12],
                                             uint32_t (&sc)[4]) {
-  const int kb = 8 * g + q;
+  const int kb = 8 * g + q;           // block index within the row
+  const int lb = kb - 8 * c.g_lo;      // block index within this split
   if (kb + 2 < c.nblk)
     load_block<(q + 2) % 8>(c.row, c.srow, kb + 2, win[(q + 2) % 4], sc[(q + 2) % 4]);
   uint32_t s16 = sc[q % 4];
@@ -298,7 +299,7 @@ __device__ __forceinline__ bool expand_step(const ExpCtx& c, int g, uint32_t (&w
         __float2bfloat16_rn(__half2float(__ushort_as_half((unsigned short)s16))));
   // PRMT sources: bytes 0-1 = -s, 2-3 = 0, 4-5 = +s
   const uint32_t ta = (s16 ^ 0x8000u), tb = s16;
-  if (kb > 0 && !mbar_wait(c.empty, (kb - 1) & 1, c.abort_flag)) return false;
+  if (lb > 0 && !mbar_wait(c.empty, (lb - 1) & 1, c.abort_flag)) return false;
   expand_half<h, (kBlockBytes * q) & 15>(win[q % 4], ta, tb, c.bbase, c.r);
   // every writer makes its stores visible to the tensor core's (async) proxy
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -309,9 +310,9 @@ __device__ __forceinline__ bool expand_step(const ExpCtx& c, int g, uint32_t (&w
 template <bool kBf16, int h>
 __device__ bool expand_all(const ExpCtx& c) {
   uint32_t win[4][12], sc[4];
-  load_block<0>(c.row, c.srow, 0, win[0], sc[0]);
-  load_block<1>(c.row, c.srow, 1, win[1], sc[1]);  // K >= 1024: at least 8 blocks
-  for (int g = 0; 8 * g < c.nblk; ++g) {
+  load_block<0>(c.row, c.srow, 8 * c.g_lo, win[0], sc[0]);
+  load_block<1>(c.row, c.srow, 8 * c.g_lo + 1, win[1], sc[1]);  // a split holds >= 8 blocks
+  for (int g = c.g_lo; 8 * g < c.nblk; ++g) {
     if (!expand_step<kBf16, h, 0>(c, g, win, sc)) return false;
     if (!expand_step<kBf16, h, 1>(c, g, win, sc)) return false;
     if (!expand_step<kBf16, h, 2>(c, g, win, sc)) return false;
@@ -324,11 +325,14 @@ __device__ bool expand_all(const ExpCtx& c) {
   return true;
 }
 
+// blockIdx.z = split of K: split z covers the 1024-wide groups
+// [z G / S, (z + 1) G / S) and, when S > 1, writes fp32 partial sums to
+// y + z M N (kOutF32).
 template <bool kBf16, bool kOutF32>
 __global__ void __launch_bounds__(kThreads, 2)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const uint8_t* __restrict__ wq,
                    const uint16_t* __restrict__ scales, void* __restrict__ y, int M, int N, int K,
-                   int* status) {
+                   int splits, int* status) {
   // No static shared variables: the dynamic window starts at offset 0, so the
   // declared 1024-byte alignment holds, and every access below stays a
   // shared-memory instruction (an address laundered through an integer
@@ -344,8 +348,13 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
-  const int nk = K / BK;             // 64-wide slices
   const int nblk = K / kBlockWeights;
+  const int G = K / kRot, z = blockIdx.z;
+  const int g_lo = (int)((long long)z * G / splits), g_hi = (int)((long long)(z + 1) * G / splits);
+  const int kb0 = g_lo * (kRot / BK), kb1 = g_hi * (kRot / BK);  // this split's 64-wide slices
+  const int nk = kb1 - kb0;
+  const int nmh = M - m0 > UM ? 2 : 1;  // the second 128-row half only when it holds rows
+  if (kOutF32 && splits > 1) y = static_cast<float*>(y) + (size_t)z * M * N;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -380,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (round > 0) ok = mbar_wait(&empty[s], (round - 1) & 1, abort_flag);
         if (!ok) break;
         mbar_expect_tx(&a_full[s], kASlice);
-        tma_2d(smem_u32(smem + kOffA + s * kASlice), &map_a, kb * BK, m0, &a_full[s]);
+        tma_2d(smem_u32(smem + kOffA + s * kASlice), &map_a, (kb0 + kb) * BK, m0, &a_full[s]);
         ++a_issued;
       }
     }
@@ -395,8 +404,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t a_addr = smem_u32(smem + kOffA + s * kASlice);
         const uint32_t b_addr = smem_u32(smem + kOffB + s * kBSlice);
-#pragma unroll
-        for (int mh = 0; mh < 2; ++mh)
+        for (int mh = 0; mh < nmh; ++mh)
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)  // K = 16 per MMA: 32 bytes along the atom
             umma_f16<kBf16>(tmem + mh * BN, sw128_desc(a_addr + mh * (UM * 128) + 32 * kk),
@@ -412,7 +420,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     ExpCtx c;
     c.row = wq + (size_t)n * nblk * kBlockBytes;
     c.srow = scales + (size_t)n * nblk;
-    c.nblk = nblk;
+    c.g_lo = g_lo;
+    c.nblk = g_hi * kGroupBlocks;
     c.bbase = smem_u32(smem + kOffB + h * kBSlice);
     c.empty = &empty[h];
     c.b_full = &b_full[h];
@@ -507,24 +516,67 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
+// y[i] = sum over splits z = 0..S-1 of part[z][i], in that order, stored as
+// bf16 (kOutF32 false) or fp32.
+template <bool kOutF32>
+__global__ void __launch_bounds__(256) gemm_split_reduce_kernel(const float* __restrict__ part,
+                                                                void* __restrict__ y, size_t MN,
+                                                                int S) {
+  pdl_release();
+  pdl_wait();
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= MN) return;
+  float acc = 0.0f;
+  for (int z = 0; z < S; ++z) acc += __ldcg(part + (size_t)z * MN + i);
+  if constexpr (kOutF32)
+    static_cast<float*>(y)[i] = acc;
+  else
+    static_cast<uint16_t*>(y)[i] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
+}
+
 // ---- host side -------------------------------------------------------------------------
 template <bool kBf16, bool kOutF32>
 cudaError_t launch_t(const CUtensorMap& ma, const uint8_t* wq, const uint16_t* scales, void* y,
-                     int M, int N, int K, int* status, cudaStream_t st) {
+                     int M, int N, int K, int splits, int* status, cudaStream_t st) {
   auto kern = gemm_tc_kernel<kBf16, kOutF32>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmemBytes);
   if (e != cudaSuccess) return e;
-  const dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM));
+  const dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM), (unsigned)splits);
   return launch_pdl(kern, grid, dim3(kThreads), (size_t)kSmemBytes, st, ma, wq, scales, y, M, N,
-                    K, status);
+                    K, splits, status);
 }
 
 }  // namespace
 
+// Number of K splits for an M x N x K product.  Splitting pays only when most
+// SMs of a 152-SM part would otherwise idle (fewer tiles than half the SMs:
+// measured, 136 tiles of M=128 ran 40 us unsplit and 54 us in two splits);
+// then enough splits to fill two CTAs per SM, at most one per 1024-wide group
+// and at most kMaxSplits.  A function of the shape alone, so the workspace
+// query and the launch agree.
+int gemm_tc_splits(int64_t M, int64_t N, int64_t K) {
+  constexpr int64_t kSms = 152, kMaxSplits = 6;
+  if (K % kRot != 0 || M <= 0 || N <= 0) return 1;
+  const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  if (2 * tiles > kSms) return 1;
+  int64_t s = 2 * kSms / tiles;
+  if (s > kMaxSplits) s = kMaxSplits;
+  if (s > K / kRot) s = K / kRot;
+  return s < 2 ? 1 : (int)s;
+}
+
+size_t gemm_tc_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  const int s = gemm_tc_splits(M, N, K);
+  return s > 1 ? (size_t)s * (size_t)M * (size_t)N * 4 : 0;
+}
+
 // Tensor-core GEMM for K % 1024 == 0 (cudaErrorNotSupported otherwise).
+// ws/ws_bytes: scratch for split-K partial sums; with less than
+// gemm_tc_workspace_bytes the product runs with as many splits as fit.
 cudaError_t launch_gemm_tc(const uint8_t* wq, const uint16_t* scales, const void* x, Act x_t,
-                           void* y, Act y_t, int64_t M, int64_t N, int64_t K, cudaStream_t st) {
+                           void* y, Act y_t, int64_t M, int64_t N, int64_t K, void* ws,
+                           size_t ws_bytes, cudaStream_t st) {
   if (K % kRot != 0 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX ||
       (M + BM - 1) / BM > 65535)
     return cudaErrorNotSupported;
@@ -537,10 +589,25 @@ cudaError_t launch_gemm_tc(const uint8_t* wq, const uint16_t* scales, const void
   if (!status) return cudaErrorInvalidDevice;
   const int m = (int)M, n = (int)N, k = (int)K;
   const bool bf = x_t == Act::BF16, f32 = y_t == Act::F32;
-  if (bf && f32) return launch_t<true, true>(ma, wq, scales, y, m, n, k, status, st);
-  if (bf) return launch_t<true, false>(ma, wq, scales, y, m, n, k, status, st);
-  if (f32) return launch_t<false, true>(ma, wq, scales, y, m, n, k, status, st);
-  return launch_t<false, false>(ma, wq, scales, y, m, n, k, status, st);
+  int splits = gemm_tc_splits(M, N, K);
+  const size_t per = (size_t)M * (size_t)N * 4;
+  if (splits > 1 && (ws == nullptr || ws_bytes / per < 2)) splits = 1;
+  if (splits > 1 && ws_bytes / per < (size_t)splits) splits = (int)(ws_bytes / per);
+  if (splits > 1) {  // fp32 partials, then the fixed-order sum
+    e = bf ? launch_t<true, true>(ma, wq, scales, ws, m, n, k, splits, status, st)
+           : launch_t<false, true>(ma, wq, scales, ws, m, n, k, splits, status, st);
+    if (e != cudaSuccess) return e;
+    const size_t mn = (size_t)M * (size_t)N;
+    const dim3 grid((unsigned)((mn + 255) / 256));
+    return f32 ? launch_pdl(gemm_split_reduce_kernel<true>, grid, dim3(256), 0, st,
+                            (const float*)ws, y, mn, splits)
+               : launch_pdl(gemm_split_reduce_kernel<false>, grid, dim3(256), 0, st,
+                            (const float*)ws, y, mn, splits);
+  }
+  if (bf && f32) return launch_t<true, true>(ma, wq, scales, y, m, n, k, 1, status, st);
+  if (bf) return launch_t<true, false>(ma, wq, scales, y, m, n, k, 1, status, st);
+  if (f32) return launch_t<false, true>(ma, wq, scales, y, m, n, k, 1, status, st);
+  return launch_t<false, false>(ma, wq, scales, y, m, n, k, 1, status, st);
 }
 
 }  // namespace ptq

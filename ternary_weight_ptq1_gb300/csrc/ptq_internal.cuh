@@ -80,9 +80,11 @@ size_t gemv_lut_workspace_bytes(int64_t N, int64_t K);
 // Whether launch_gemv_lut serves (N, K) on the current device (with the
 // rotation when `rotate`).
 bool gemv_lut_supported(int64_t N, int64_t K, bool rotate);
-// x is BF16 or F16; y is BF16 or F32.
+// x is BF16 or F16; y is BF16 or F32.  ws: split-K scratch (may be NULL;
+// then, or when it is smaller than gemm_tc_workspace_bytes, fewer splits).
 cudaError_t launch_gemm(const uint8_t* wq, const uint16_t* scales, const void* x, Act x_t,
-                        void* y, Act y_t, int64_t M, int64_t N, int64_t K, cudaStream_t st);
+                        void* y, Act y_t, int64_t M, int64_t N, int64_t K, void* ws,
+                        size_t ws_bytes, cudaStream_t st);
 // gu: M x 2I fp32 (gate half first) -> h: M x I fp32.
 cudaError_t launch_swiglu(const float* gu, float* h, int64_t M, int64_t I,
                           cudaStream_t st);
@@ -90,7 +92,12 @@ cudaError_t launch_swiglu(const float* gu, float* h, int64_t M, int64_t I,
 // Tensor-core GEMM (k_gemm_tc.cu); cudaErrorNotSupported when the shape does
 // not fit it (the caller then uses the SIMT kernel).
 cudaError_t launch_gemm_tc(const uint8_t* wq, const uint16_t* scales, const void* x, Act x_t,
-                           void* y, Act y_t, int64_t M, int64_t N, int64_t K, cudaStream_t st);
+                           void* y, Act y_t, int64_t M, int64_t N, int64_t K, void* ws,
+                           size_t ws_bytes, cudaStream_t st);
+// K splits of the tensor-core GEMM for a shape, and the fp32 partial-sum
+// scratch they need (0 when the product runs unsplit).
+int gemm_tc_splits(int64_t M, int64_t N, int64_t K);
+size_t gemm_tc_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 // 2-D TMA tensor map over a row-major array (tma_util.cu): `inner` elements
 // per row, `rows` rows `row_bytes` apart, boxes of box_inner x box_rows.

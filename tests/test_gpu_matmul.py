@@ -209,6 +209,29 @@ def test_prefill_small_shapes(P, orc, syn, M, N, K):
     Q.check_bf16(Q.host_f64(y), orc.matmul(wq, mv.scales, Q.x_f64(mv.x)), f"bf16 {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("M,N,K", [(64, 1000, 6144), (256, 5120, 17408), (300, 640, 3072)])
+def test_prefill_split_k(P, orc, syn, M, N, K):
+    # few output tiles: K is split over several CTAs whose fp32 partial sums
+    # a second kernel adds in a fixed order; with too little scratch the
+    # product runs unsplit -- both match the oracle, and each is reproducible
+    import torch
+
+    need = P.matmul_workspace_bytes(M, N, K, P.PTQ_BF16)
+    assert need > 0
+    mv = syn.gaussian_matvec(50 + M, M, N, K, dtype="bf16")
+    wq = P.pack(mv.trits)
+    args = (Q.dev(wq), Q.dev(mv.scales), Q.dev_bf16(mv.x))
+    rng = np.random.default_rng(M)
+    rows = np.unique(np.concatenate([rng.integers(0, N, 64), [0, N - 1]]))
+    ref = orc.matmul_rows(wq, mv.scales, Q.x_f64(mv.x), rows)
+    ws = torch.full((need,), 0x7F, dtype=torch.uint8, device="cuda")
+    split = P.matmul(*args, workspace=ws)
+    unsplit = P.matmul(*args, workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
+    Q.check_bf16(Q.host_f64(split)[:, rows], ref, f"split-K {M}x{N}x{K}")
+    Q.check_bf16(Q.host_f64(unsplit)[:, rows], ref, f"unsplit {M}x{N}x{K}")
+    assert torch.equal(P.matmul(*args, workspace=ws), split)
+
+
 def test_prefill_in_bounds(P, syn):
     import torch
 
