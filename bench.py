@@ -186,6 +186,50 @@ TRAFFIC_PREFILL = 24_840_448 + 7_168
 TRAFFIC_DECODE = (156_069_376 + 4_433_920) // 8
 
 
+def ffn_lines(P, torch, syn, pk, world, args):
+    """The feed-forward block (rotate, fused gate+up, SwiGLU, rotate, down),
+    H=5120, I=17408, 64 layers per step: decode (M=1, fp32) and prefill
+    (M=256, bf16).  The 64 layers cycle through 8 distinct seeded layers
+    (470 MB of weights, more than the L2), so every layer streams its weights
+    from HBM as 64 distinct layers would."""
+    H, I, LAYERS, RING = 5120, 17408, 64, 8
+    layers = []
+    for l in range(RING):
+        L = syn.ffn_layer(4, l, H, I)
+        layers.append(tuple(torch.from_numpy(a).cuda() for a in (
+            P.pack(L.wgu_trits), L.wgu_scales.view(np.int16), P.pack(L.wd_trits),
+            L.wd_scales.view(np.int16), L.signs_in, L.signs_mid)))
+    wbytes = LAYERS * 3 * H * I * 7 // 32                 # 3,743,416,320 B per token-step
+    out = {}
+    for name, M, dt, pdt in (("decode", 1, torch.float32, P.PTQ_F32),
+                             ("prefill", 256, torch.bfloat16, P.PTQ_BF16)):
+        xa = syn.ffn_input(4, 0, M, H, "f32" if M == 1 else "bf16")
+        x = torch.from_numpy(xa if M == 1 else xa.view(np.int16)).cuda()
+        if dt == torch.bfloat16:
+            x = x.view(torch.bfloat16)
+        y = torch.empty((M, H), device="cuda", dtype=dt)
+        ws = torch.empty(P.ffn_workspace_bytes(M, H, I, pdt), dtype=torch.uint8, device="cuda")
+
+        def step(i, x=x, y=y, ws=ws):  # one token-step: all 64 layers
+            for l in range(LAYERS):
+                P.ffn(*layers[l % RING], x, out=y, workspace=ws)
+
+        K = max(3, min(args.steps, 40 if M == 1 else 8))
+        ms = timed_steps(torch, step, K, 3, chunk=2) / K
+        line = {"workload": f"feed-forward block x {LAYERS} layers, M={M}", "M": M, "H": H, "I": I,
+                "dtype": "f32" if M == 1 else "bf16 in/out, fp16 rotated operands",
+                "ms_per_step": round(ms, 4), "weight_bytes_per_step": wbytes,
+                "weight_GB/s": round(world * wbytes / (ms * 1e-3) / 1e9, 1)}
+        if M == 1:
+            line["tokens_per_s"] = round(world * 1e3 / ms, 1)
+        else:
+            tf = 2.0 * M * LAYERS * 3 * H * I / (ms * 1e-3) / 1e12
+            line["TFLOP/s"] = round(world * tf, 1)
+            line["frac_of_bf16_peak"] = round(tf / pk["bf16"], 4)
+        out[name] = line
+    return out
+
+
 def run_ours(args, world, rank):
     import torch
 
@@ -277,6 +321,8 @@ def run_ours(args, world, rank):
                             "unit": "TFLOP/s", "frac": round(tf / pk["bf16"], 4),
                             "traffic": TRAFFIC_PREFILL, "peak_source": pk["source"] + " burst bf16"}}
 
+    ffn = None if args.skip_ffn else ffn_lines(P, torch, syn, pk, world, args)
+
     cpu = cpu_baseline(args) if rank == 0 and not args.skip_cpu else None
     clocks = clk.summary()
     line = {
@@ -307,6 +353,7 @@ def run_ours(args, world, rank):
         "gpu_launches": 2 * K,   # fused rotation + table-lookup GEMV, chunk reduction
         "clocks": clocks,
         "prefill": pre,
+        "ffn": ffn,
         "cpu_baseline": cpu,
     }
     if rank == 0:
@@ -425,6 +472,7 @@ def main():
     ap.add_argument("--cpu-reps", type=int, default=1000)       # about 10 s of oracle work
     ap.add_argument("--reference-max-steps", type=int, default=1000)
     ap.add_argument("--skip-prefill", action="store_true")
+    ap.add_argument("--skip-ffn", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--profile", choices=["gemv", "gemm"],
                     help="run a small case of one kernel for an ncu capture, then exit")
