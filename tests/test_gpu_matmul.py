@@ -168,11 +168,48 @@ def test_lut_workspace(P, syn):
     assert need == (9 * N * 4 + 255) // 256 * 256
     ref = P.matmul(wq, s, x)
     # any initial contents; the same bits on every call
-    ws = torch.full((need // 4,), float("nan"), device="cuda").view(torch.uint8)
-    for _ in range(3):
-        assert torch.equal(P.matmul(wq, s, x, workspace=ws), ref)
+    g = torch.Generator(device="cuda").manual_seed(5)
+    fills = [torch.full((need // 4,), float("nan"), device="cuda").view(torch.uint8),
+             torch.zeros(need, dtype=torch.uint8, device="cuda"),
+             torch.full((need,), 255, dtype=torch.uint8, device="cuda"),
+             torch.randint(0, 256, (need,), dtype=torch.uint8, device="cuda", generator=g)]
+    for ws in fills:
+        for _ in range(3):
+            assert torch.equal(P.matmul(wq, s, x, workspace=ws), ref)
     with pytest.raises(P.PTQError, match="WORKSPACE"):
         P.matmul(wq, s, x, workspace=ws[:need - 16])
+
+
+def test_lut_graph_replay(P, syn):
+    """A captured decode call (the GEMV and its chunk reduction) replays with
+    the same launch arguments every time, also after another call or other
+    data used the workspace in between."""
+    import torch
+
+    N, K = 4096, 5120
+    mv = syn.gaussian_matvec(17, 1, N, K)
+    wq, s, x = Q.dev(P.pack(mv.trits)), Q.dev(mv.scales), Q.dev(mv.x)
+    ref = P.matmul(wq, s, x)
+    ws = torch.empty(P.matmul_workspace_bytes(1, N, K, P.PTQ_F32), dtype=torch.uint8,
+                     device="cuda")
+    y = torch.empty_like(ref)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        P.matmul(wq, s, x, out=y, workspace=ws)  # warm-up outside the capture
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        P.matmul(wq, s, x, out=y, workspace=ws)
+    for i in range(6):
+        y.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y, ref), f"replay {i}"
+        if i == 2:
+            P.matmul(wq, s, x, workspace=ws)  # an uncaptured call in between
+        if i == 4:
+            ws.fill_(7)
 
 
 def test_f32_above_eight_rows_is_refused(P, syn):
