@@ -61,6 +61,12 @@ def lib():
         for name in ("orc_fwht_def", "orc_fwht_fast"):
             getattr(L, name).argtypes = [_P, _P, _P, _I64, _I64]
             getattr(L, name).restype = None
+        L.orc_unrotate_def.argtypes = [_P, _P, _P, _I64, _I64]
+        L.orc_unrotate_def.restype = None
+        L.orc_embed.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64]
+        L.orc_embed.restype = None
+        L.orc_embed_ptq1.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64]
+        L.orc_embed_ptq1.restype = ctypes.c_int
         L.orc_matmul.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64]
         L.orc_matmul.restype = None
         L.orc_matmul_rows.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _P, _I64]
@@ -160,6 +166,42 @@ def fwht(x: np.ndarray, signs: np.ndarray) -> np.ndarray:
     y = np.empty_like(x2)
     lib().orc_fwht_fast(_ptr(x2), _ptr(signs), _ptr(y), x2.shape[0], x2.shape[1])
     return y.reshape(x.shape)
+
+
+def unrotate_def(y: np.ndarray, signs: np.ndarray) -> np.ndarray:
+    """R^T y per 1024-block, by the definition (O(1024^2) per block)."""
+    y = _c(y, np.float64)
+    y2 = y.reshape(-1, y.shape[-1])
+    signs = _c(signs, np.int8)
+    x = np.empty_like(y2)
+    lib().orc_unrotate_def(_ptr(y2), _ptr(signs), _ptr(x), y2.shape[0], y2.shape[1])
+    return x.reshape(y.shape)
+
+
+def embed(table: np.ndarray, ids: np.ndarray, signs: np.ndarray) -> np.ndarray:
+    """out[m] = R^T table[ids[m]] (V x H float64 table); NaN rows for bad ids."""
+    table = _c(table, np.float64)
+    ids = _c(np.asarray(ids, np.int32), np.int32)
+    signs = _c(signs, np.int8)
+    V, H = table.shape
+    out = np.empty((ids.size, H), np.float64)
+    lib().orc_embed(_ptr(table), _ptr(ids), _ptr(signs), _ptr(out), ids.size, V, H)
+    return out
+
+
+def embed_ptq1(wq: np.ndarray, scales: np.ndarray, ids: np.ndarray,
+               signs: np.ndarray) -> np.ndarray:
+    """The same for a PTQ1_0 table (wq V x H/128*26, scales V x H/128)."""
+    wq = _c(wq, np.uint8)
+    scales = _c(scales, np.uint16)
+    ids = _c(np.asarray(ids, np.int32), np.int32)
+    signs = _c(signs, np.int8)
+    V, H = scales.shape[0], scales.shape[1] * 128
+    out = np.empty((ids.size, H), np.float64)
+    if lib().orc_embed_ptq1(_ptr(wq), _ptr(scales), _ptr(ids), _ptr(signs), _ptr(out),
+                            ids.size, V, H) != 0:
+        raise ValueError("orc_embed_ptq1: H % 1024 != 0 or allocation failure")
+    return out
 
 
 def matmul(wq: np.ndarray, scales: np.ndarray, x: np.ndarray) -> np.ndarray:

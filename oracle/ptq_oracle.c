@@ -192,6 +192,80 @@ void orc_fwht_fast(const double* x, const int8_t* signs, double* y, int64_t M,
   }
 }
 
+/* The inverse rotation.  R = H D_s / 32 with H symmetric and H H = 1024 I,
+   so R is orthonormal and R^T = D_s H / 32: per block,
+   x_i = (1/32) s_i sum_j (-1)^popcount(i&j) y_j.  The definition, O(1024^2)
+   per block. */
+void orc_unrotate_def(const double* y, const int8_t* signs, double* x,
+                      int64_t M, int64_t K) {
+  int64_t nblk = K / ORC_ROT;
+#pragma omp parallel for schedule(static)
+  for (int64_t mb = 0; mb < M * nblk; ++mb) {
+    int64_t m = mb / nblk, b = mb % nblk;
+    const double* yb = y + m * K + b * ORC_ROT;
+    const int8_t* sb = signs + b * ORC_ROT;
+    double* xb = x + m * K + b * ORC_ROT;
+    for (int i = 0; i < ORC_ROT; ++i) {
+      double acc = 0.0;
+      for (int j = 0; j < ORC_ROT; ++j) {
+        double h = (popcount_u32((unsigned)(i & j)) & 1) ? -1.0 : 1.0;
+        acc += h * yb[j];
+      }
+      xb[i] = (double)sb[i] * acc / 32.0;
+    }
+  }
+}
+
+/* ---- embedding lookup on a rotated table -------------------------------- */
+
+/* [P1] "What Bonsai is": the rotation folded into the stored weights is
+   undone on the embedding table after each lookup.  The stored row of token
+   v is R e_v, so out[m] = R^T table[ids[m]].  A row whose id lies outside
+   [0, V) is all NaN. */
+void orc_embed(const double* table, const int32_t* ids, const int8_t* signs,
+               double* out, int64_t M, int64_t V, int64_t H) {
+  for (int64_t m = 0; m < M; ++m) {
+    double* om = out + m * H;
+    if (ids[m] < 0 || ids[m] >= V) {
+      for (int64_t k = 0; k < H; ++k) om[k] = NAN;
+      continue;
+    }
+    orc_unrotate_def(table + (int64_t)ids[m] * H, signs, om, 1, H);
+  }
+}
+
+/* The same with a PTQ1_0 table: row v is t[v,k] * s[v, k/128], its trits
+   peeled from wq.  Returns 0, or -1 on a bad shape or allocation failure. */
+int orc_embed_ptq1(const uint8_t* wq, const uint16_t* scales,
+                   const int32_t* ids, const int8_t* signs, double* out,
+                   int64_t M, int64_t V, int64_t H) {
+  if (H % ORC_ROT != 0 || M < 0 || V < 0) return -1;
+  int64_t nb = H / ORC_WEIGHTS_PER_BLOCK;
+  int8_t* t = (int8_t*)malloc((size_t)H);
+  double* row = (double*)malloc(sizeof(double) * (size_t)H);
+  if (!t || !row) {
+    free(t);
+    free(row);
+    return -1;
+  }
+  for (int64_t m = 0; m < M; ++m) {
+    double* om = out + m * H;
+    if (ids[m] < 0 || ids[m] >= V) {
+      for (int64_t k = 0; k < H; ++k) om[k] = NAN;
+      continue;
+    }
+    int64_t v = ids[m];
+    orc_unpack(wq + v * nb * ORC_BYTES_PER_BLOCK, t, 1, H);
+    for (int64_t k = 0; k < H; ++k)
+      row[k] = (double)t[k] *
+               orc_half_to_double(scales[v * nb + k / ORC_WEIGHTS_PER_BLOCK]);
+    orc_unrotate_def(row, signs, om, 1, H);
+  }
+  free(t);
+  free(row);
+  return 0;
+}
+
 /* ---- the block-scaled ternary matmul ------------------------------------ */
 
 /* One output row n for all M activation rows: peel the row, then

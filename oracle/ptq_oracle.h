@@ -29,7 +29,10 @@
  *     Hadamard matrix H[i][j] = (-1)^popcount(i & j), then scales by 1/32;
  *     the sign vector has one entry per element (block b uses its own 1024);
  *   - the gate/up weight of the fused feed-forward block stacks the gate rows
- *     (0..I-1) above the up rows (I..2I-1); h = silu(gate) * up.
+ *     (0..I-1) above the up rows (I..2I-1); h = silu(gate) * up;
+ *   - the embedding table is stored rotated like the weights (row v holds
+ *     R e_v), so a lookup returns R^T of the stored row; an id outside the
+ *     table gives a row of NaN.
  *
  * Storage (the same on both sides of the parity tests):
  *   wq     : N x (K/128) x 26 bytes, row-major (row n is (K/128)*26 bytes)
@@ -78,6 +81,25 @@ void orc_fwht_def(const double* x, const int8_t* signs, double* y,
    y may alias x. */
 void orc_fwht_fast(const double* x, const int8_t* signs, double* y,
                    int64_t M, int64_t K);
+
+/* The inverse rotation R^T = D_s H / 32 (R is orthonormal), the definition:
+   per 1024-block, x_i = (1/32) s_i sum_j (-1)^popcount(i&j) y_j.
+   O(1024^2) per block; x may not alias y. */
+void orc_unrotate_def(const double* y, const int8_t* signs, double* x,
+                      int64_t M, int64_t K);
+
+/* Embedding lookup on a rotated table ([P1] "What Bonsai is": the rotation
+   is undone on the embedding row after each lookup):
+   out[m] = R^T table[ids[m]], table V x H, out M x H.  Rows with an id
+   outside [0, V) are NaN. */
+void orc_embed(const double* table, const int32_t* ids, const int8_t* signs,
+               double* out, int64_t M, int64_t V, int64_t H);
+
+/* The same for a PTQ1_0 table (wq V x (H/128) x 26, scales V x H/128): the
+   row is the peeled trits times their block scales.  Returns 0 or -1. */
+int orc_embed_ptq1(const uint8_t* wq, const uint16_t* scales,
+                   const int32_t* ids, const int8_t* signs, double* out,
+                   int64_t M, int64_t V, int64_t H);
 
 /* y[m,n] = sum_b s[n,b] * sum_{i<128} t[n,128b+i] * x[m,128b+i], where the
    trits are peeled from wq.  x is M x K, y is M x N, both row-major. */

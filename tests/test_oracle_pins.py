@@ -190,6 +190,81 @@ def test_weight_fold_identity(orc):
         np.testing.assert_allclose(folded @ xr[0], W @ x[0], rtol=1e-12, atol=1e-12)
 
 
+# ---- inverse rotation and the embedding lookup -------------------------------
+
+def _signs(rng, n):
+    return np.where(rng.random(n) < 0.5, -1, 1).astype(np.int8)
+
+
+def test_unrotate_is_transpose_of_sylvester_rotation(orc):
+    # R = H D_s / 32 with the textbook Sylvester H (scipy), so R^T = D_s H / 32:
+    # the butterfly first, then the signs -- not the forward transform again.
+    rng = np.random.default_rng(21)
+    y = rng.standard_normal((2, 2048))
+    s = _signs(rng, 2048)
+    H = scipy.linalg.hadamard(1024).astype(np.float64)
+    x = orc.unrotate_def(y, s)
+    for b in range(2):
+        sl = slice(1024 * b, 1024 * (b + 1))
+        np.testing.assert_allclose(x[:, sl], (y[:, sl] @ H / 32) * s[sl], rtol=0, atol=1e-12)
+    assert np.abs(x - orc.fwht(y, s)).max() > 0.1  # signed R is not symmetric
+
+
+def test_unrotate_inverts_the_rotation(orc):
+    rng = np.random.default_rng(22)
+    x = rng.standard_normal((3, 3072))
+    s = _signs(rng, 3072)
+    np.testing.assert_allclose(orc.unrotate_def(orc.fwht_def(x, s), s), x, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(orc.fwht_def(orc.unrotate_def(x, s), s), x, rtol=0, atol=1e-12)
+
+
+def test_unrotate_closed_forms(orc):
+    # R^T (32 e_j) = s * H[:, j], i.e. x_i = s_i (-1)^popcount(i & j); for
+    # j = 0 that is the sign vector itself.  With all signs +1 the all-ones
+    # block goes to 32 e_0.
+    s = np.where(np.arange(1024) % 5 == 1, -1, 1).astype(np.int8)
+    i = np.arange(1024)
+    for j in (0, 1, 7, 640, 1023):
+        y = np.zeros((1, 1024))
+        y[0, j] = 32.0
+        parity = np.array([bin(v & j).count("1") & 1 for v in i])
+        np.testing.assert_array_equal(orc.unrotate_def(y, s)[0], s * np.where(parity, -1.0, 1.0))
+    ones = np.ones(1024, np.int8)
+    e0 = np.zeros(1024)
+    e0[0] = 32.0
+    np.testing.assert_array_equal(orc.unrotate_def(np.ones((1, 1024)), ones)[0], e0)
+
+
+def test_embed_undoes_the_fold(orc):
+    # "What Bonsai is": the rotation is folded into the stored table and
+    # undone after each lookup.  A table stored as R e_v returns e_v.
+    rng = np.random.default_rng(23)
+    V, H = 9, 2048
+    E = rng.standard_normal((V, H))
+    s = _signs(rng, H)
+    stored = orc.fwht_def(E, s)
+    ids = np.array([3, 0, 8, 3, 9, -1, 2 ** 31 - 1], np.int32)
+    out = orc.embed(stored, ids, s)
+    np.testing.assert_allclose(out[:4], E[[3, 0, 8, 3]], rtol=0, atol=1e-12)
+    assert np.isnan(out[4:]).all()  # ids outside [0, V)
+
+
+def test_embed_ptq1_row_is_trits_times_block_scales(orc):
+    # the table row decoded straight from the trits and scales the encoder
+    # was given (numpy here, not the oracle's peel), then un-rotated
+    rng = np.random.default_rng(24)
+    V, H = 5, 1024
+    t = rng.integers(-1, 2, size=(V, H)).astype(np.int8)
+    sbits = (np.abs(rng.standard_normal((V, H // 128))) * 0.02).astype(np.float16).view(np.uint16)
+    dense = t * np.repeat(_f16(sbits), 128, axis=1)
+    s = _signs(rng, H)
+    ids = np.array([4, 1, 1, 5], np.int32)
+    out = orc.embed_ptq1(orc.pack(t), sbits, ids, s)
+    H1 = scipy.linalg.hadamard(1024).astype(np.float64)
+    np.testing.assert_allclose(out[:3], (dense[[4, 1, 1]] @ H1 / 32) * s, rtol=0, atol=1e-12)
+    assert np.isnan(out[3]).all()
+
+
 # ---- ternary matmul --------------------------------------------------------
 
 def test_ternary_dot_brute_force(orc):
