@@ -209,6 +209,39 @@ PTQ_API PTQ_NODISCARD ptq_status ptq_ffn_noalloc(
     const void* x, void* y, int64_t M, int64_t H, int64_t I, ptq_dtype dtype,
     ptq_stream_t stream);
 
+/* ptq_embed -- token-embedding lookup on a rotated table.
+ * "What Bonsai is": the rotation folded into the weights is undone on the
+ * embedding table after each lookup.  Row v of the table holds R e_v, with R
+ * the signed rotation of ptq_fwht; this call gathers the rows ids[0..M-1] and
+ * returns out[m] = R^T table[ids[m]] = D_s H table[ids[m]] / 32 per
+ * 1024-block (the butterfly first, then the signs: R is orthonormal).
+ *   table  V x H, dtype (PTQ_F32 float, PTQ_BF16 bfloat16), row-major
+ *   ids    M int32 token ids (device)
+ *   signs  H values, +1 or -1 (those of the rotation folded into the table)
+ *   out    M x H, dtype; must not overlap the table
+ * Arithmetic is fp32; a bf16 output is rounded to nearest-even once.  An id
+ * outside [0, V) gives a row of quiet NaN (nothing is read for it): the
+ * ids are on the device, so the call cannot refuse them.
+ * Requires H % 1024 == 0, V >= 1; table and out 16-byte aligned, ids and
+ * signs 4-byte aligned.  M = 0 is a no-op.
+ * Errors: PTQ_ERR_NULL, PTQ_ERR_SHAPE, PTQ_ERR_ALIGN, PTQ_ERR_VALUE (dtype),
+ * PTQ_ERR_CUDA. */
+PTQ_API PTQ_NODISCARD ptq_status ptq_embed(const void* table,
+                                           const int32_t* ids,
+                                           const int8_t* signs, void* out,
+                                           int64_t M, int64_t V, int64_t H,
+                                           ptq_dtype dtype,
+                                           ptq_stream_t stream);
+
+/* ptq_embed_ptq1 -- ptq_embed for a PTQ1_0 table: wq V x (H/128) x 26
+ * bytes and scales V x (H/128) binary16 patterns (the layouts above); row v
+ * is trit x block scale, decoded exactly in fp32.  out (M x H) is
+ * out_dtype.  wq and scales 16-byte aligned; everything else as ptq_embed. */
+PTQ_API PTQ_NODISCARD ptq_status ptq_embed_ptq1(
+    const uint8_t* wq, const uint16_t* scales, const int32_t* ids,
+    const int8_t* signs, void* out, int64_t M, int64_t V, int64_t H,
+    ptq_dtype out_dtype, ptq_stream_t stream);
+
 /* ptq_route -- the kernel ptq_matmul would run for (M, dtype) when K/128 is
  * even: writes its name to *kernel_name (static storage) and returns PTQ_OK,
  * or returns PTQ_ERR_UNSUPPORTED / PTQ_ERR_VALUE.  Host only. */

@@ -53,8 +53,9 @@ def lib():
         L.syn_normal_f32.argtypes = [_U64, _U64, _P, _I64]
         L.syn_normal_bf16.argtypes = [_U64, _U64, _P, _I64]
         L.syn_abs_normal_f16.argtypes = [_U64, _U64, ctypes.c_double, _P, _I64]
+        L.syn_token_ids.argtypes = [_U64, _U64, _I64, _P, _I64]
         for f in ("syn_trits_uniform", "syn_trits_sparse", "syn_signs", "syn_normal_f64",
-                  "syn_normal_f32", "syn_normal_bf16", "syn_abs_normal_f16"):
+                  "syn_normal_f32", "syn_normal_bf16", "syn_abs_normal_f16", "syn_token_ids"):
             getattr(L, f).restype = None
         L.syn_half_bits.argtypes = [ctypes.c_double]
         L.syn_half_bits.restype = ctypes.c_uint16
@@ -109,6 +110,13 @@ def scales_f16(seed: int, stream: int, shape, sigma: float = 0.02, out=None) -> 
     """fp16 bit patterns (uint16) of sigma * |N(0,1)|."""
     a = np.empty(shape, np.uint16) if out is None else out
     lib().syn_abs_normal_f16(seed, stream, float(sigma), _p(a), a.size)
+    return a
+
+
+def token_ids(seed: int, stream: int, n: int, V: int) -> np.ndarray:
+    """n int32 token ids, uniform over [0, V)."""
+    a = np.empty(n, np.int32)
+    lib().syn_token_ids(seed, stream, int(V), _p(a), n)
     return a
 
 

@@ -152,5 +152,13 @@ void syn_abs_normal_f16(uint64_t seed, uint64_t stream, double sigma, uint16_t* 
 }
 
 /* storage rounding helpers, exported so the tests can pin them */
+/* token ids uniform over [0, V): draw mod V (the bias, below V / 2^64, is
+   immaterial for a test input) */
+void syn_token_ids(uint64_t seed, uint64_t stream, int64_t V, int32_t* out, int64_t n) {
+  uint64_t key = key_of(seed, stream);
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < n; ++i) out[i] = (int32_t)(draw(key, (uint64_t)i) % (uint64_t)V);
+}
+
 uint16_t syn_half_bits(double v) { return to_half_bits(v); }
 uint16_t syn_bf16_bits(float f) { return to_bf16_bits(f); }

@@ -28,8 +28,8 @@ STATUS = {
 # Every symbol include/ptq.h declares.
 EXPORTS = ("ptq1_pack", "ptq1_unpack", "ptq_fwht", "ptq_matmul_workspace_bytes", "ptq_matmul",
            "ptq_rotate_matmul_workspace_bytes", "ptq_rotate_matmul", "ptq_ffn_workspace_bytes",
-           "ptq_ffn", "ptq_ffn_noalloc", "ptq_route", "ptq_device_check", "ptq_status_str",
-           "ptq_last_error")
+           "ptq_ffn", "ptq_ffn_noalloc", "ptq_embed", "ptq_embed_ptq1", "ptq_route",
+           "ptq_device_check", "ptq_status_str", "ptq_last_error")
 
 # Size of the built-in scratch array behind ptq_ffn_noalloc (include/ptq.h).
 FFN_NOALLOC_SCRATCH_BYTES = 4 * 1024 * 1024
@@ -71,6 +71,8 @@ def load(path: str | None = None):
     L.ptq_ffn_workspace_bytes.restype = ctypes.c_size_t
     L.ptq_ffn.argtypes = [_P] * 8 + [_I64, _I64, _I64, _I32, _P, ctypes.c_size_t, _P]
     L.ptq_ffn_noalloc.argtypes = [_P] * 8 + [_I64, _I64, _I64, _I32, _P]
+    L.ptq_embed.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _P]
+    L.ptq_embed_ptq1.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _P]
     L.ptq_route.argtypes = [_I64, _I32, ctypes.POINTER(ctypes.c_char_p)]
     L.ptq_device_check.argtypes = [_P]
     L.ptq_status_str.argtypes = [_I32]
@@ -78,8 +80,7 @@ def load(path: str | None = None):
     L.ptq_last_error.argtypes = []
     L.ptq_last_error.restype = ctypes.c_char_p
     for name in ("ptq1_pack", "ptq1_unpack", "ptq_fwht", "ptq_matmul", "ptq_rotate_matmul", "ptq_ffn",
-                 "ptq_ffn_noalloc",
-                 "ptq_route", "ptq_device_check"):
+                 "ptq_ffn_noalloc", "ptq_embed", "ptq_embed_ptq1", "ptq_route", "ptq_device_check"):
         getattr(L, name).restype = _I32
     _lib = L
     return L
@@ -251,6 +252,42 @@ def ffn_noalloc(wgu_q, wgu_s, wd_q, wd_s, signs_in, signs_mid, x, out=None, stre
                                   _dev(signs_mid, torch.int8, "signs_mid"), _dev(x, None, "x"),
                                   _dev(y, x.dtype, "out"), M, H, I, _act_dtype(x), _stream(stream)),
            "ptq_ffn_noalloc")
+    return y
+
+
+def embed(table, ids, signs, out=None, stream=None):
+    """out[m] = R^T table[ids[m]]: the lookup on a rotated embedding table
+    (ptq_embed).  table: V x H float32 or bfloat16; ids: M int32 token ids;
+    ids outside [0, V) give rows of NaN."""
+    import torch
+
+    dt = _act_dtype(table)
+    V, H = table.shape
+    M = ids.numel()
+    y = torch.empty((M, H), dtype=table.dtype, device=table.device) if out is None else out
+    _check(load().ptq_embed(_dev(table, None, "table"), _dev(ids, torch.int32, "ids"),
+                            _dev(signs, torch.int8, "signs"), _dev(y, table.dtype, "out"), M, V, H,
+                            dt, _stream(stream)), "ptq_embed")
+    return y
+
+
+def embed_ptq1(wq, scales, ids, signs, out_dtype=None, out=None, stream=None):
+    """ptq_embed_ptq1: the same lookup on a PTQ1_0 table (wq V x H/128*26
+    uint8, scales V x H/128 int16 bit patterns); out_dtype float32 (default)
+    or bfloat16."""
+    import torch
+
+    out_dtype = out_dtype or (out.dtype if out is not None else torch.float32)
+    dt = PTQ_F32 if out_dtype == torch.float32 else PTQ_BF16 if out_dtype == torch.bfloat16 else None
+    if dt is None:
+        raise TypeError(f"out_dtype must be float32 or bfloat16, got {out_dtype}")
+    V, H = scales.shape[0], scales.shape[1] * 128
+    M = ids.numel()
+    y = torch.empty((M, H), dtype=out_dtype, device=wq.device) if out is None else out
+    _check(load().ptq_embed_ptq1(_dev(wq, torch.uint8, "wq"), _dev(scales, None, "scales"),
+                                 _dev(ids, torch.int32, "ids"), _dev(signs, torch.int8, "signs"),
+                                 _dev(y, out_dtype, "out"), M, V, H, dt, _stream(stream)),
+           "ptq_embed_ptq1")
     return y
 
 

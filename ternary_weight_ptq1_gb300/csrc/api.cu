@@ -196,6 +196,48 @@ PTQ_API ptq_status ptq_fwht(const void* x, void* y, const int8_t* signs, int64_t
   return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq_fwht launch");
 }
 
+static ptq_status check_embed(const void* table, const void* scales, const int32_t* ids,
+                              const int8_t* signs, const void* out, int64_t M, int64_t V,
+                              int64_t H, ptq_dtype dt, bool ptq1, const char* who) {
+  if (!dtype_ok(dt)) return fail(PTQ_ERR_VALUE, "%s: unknown dtype %d", who, (int)dt);
+  int64_t t;
+  if (M < 0 || V < 1 || H <= 0 || H % kRot != 0 || !mul_ok(V, H, &t) || !mul_ok(t, 4, &t) ||
+      !mul_ok(M, H, &t) || !mul_ok(t, 4, &t))
+    return fail(PTQ_ERR_SHAPE, "%s: need M >= 0, V >= 1, H > 0, H %% 1024 == 0 (M=%lld V=%lld H=%lld)",
+                who, (long long)M, (long long)V, (long long)H);
+  if (M == 0) return PTQ_OK;
+  if (!table || !ids || !signs || !out || (ptq1 && !scales))
+    return fail(PTQ_ERR_NULL, "%s: NULL pointer", who);
+  if (!aligned(table, 16) || !aligned(out, 16) || !aligned(ids, 4) || !aligned(signs, 4) ||
+      (ptq1 && !aligned(scales, 16)))
+    return fail(PTQ_ERR_ALIGN, "%s: the table%s and out need 16-byte, ids and signs 4-byte alignment",
+                who, ptq1 ? " (wq and scales)" : "");
+  return PTQ_OK;
+}
+
+PTQ_API ptq_status ptq_embed(const void* table, const int32_t* ids, const int8_t* signs, void* out,
+                             int64_t M, int64_t V, int64_t H, ptq_dtype dtype,
+                             ptq_stream_t stream) {
+  t_msg[0] = 0;
+  ptq_status s = check_embed(table, nullptr, ids, signs, out, M, V, H, dtype, false, "ptq_embed");
+  if (s != PTQ_OK || M == 0) return s;
+  cudaError_t e = launch_embed(table, act_of(dtype), ids, signs, out, act_of(dtype), M, V, H,
+                               reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq_embed launch");
+}
+
+PTQ_API ptq_status ptq_embed_ptq1(const uint8_t* wq, const uint16_t* scales, const int32_t* ids,
+                                  const int8_t* signs, void* out, int64_t M, int64_t V, int64_t H,
+                                  ptq_dtype out_dtype, ptq_stream_t stream) {
+  t_msg[0] = 0;
+  ptq_status s =
+      check_embed(wq, scales, ids, signs, out, M, V, H, out_dtype, true, "ptq_embed_ptq1");
+  if (s != PTQ_OK || M == 0) return s;
+  cudaError_t e = launch_embed_ptq1(wq, scales, ids, signs, out, act_of(out_dtype), M, V, H,
+                                    reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq_embed_ptq1 launch");
+}
+
 static ptq_status check_matmul(const uint8_t* wq, const uint16_t* scales, const void* x,
                                const void* y, int64_t M, int64_t N, int64_t K, ptq_dtype dt,
                                const char* who, const Route** route) {

@@ -5,11 +5,8 @@
 // pattern, so every activation is flipped by the signs, pushed through the
 // Sylvester-ordered Hadamard butterfly and scaled by 1/32 (orthonormal).
 //
-// One warp owns one 1024-element block.  Lane l holds elements
-// 128 j + 4 l + c (j = 0..7, c = 0..3): index bits 0-1 (c) and 7-9 (j) live
-// in registers, bits 2-6 are the lane id.  The ten butterfly stages are the
-// five in-register ones plus five xor-shuffles; H is a tensor product over
-// the index bits, so the stage order is free.  Loads and stores are 16-byte
+// One warp owns one 1024-element block, laid out over the lanes as
+// warp_hadamard_1024 (fwht_warp.cuh) wants it.  Loads and stores are 16-byte
 // (fp32) or 8-byte (16-bit types) vectors, 512 (256) contiguous bytes per warp
 // instruction.  Arithmetic is fp32 (16-bit outputs are rounded
 // to nearest-even once, at the end); y may alias x because a warp reads its
@@ -20,6 +17,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "fwht_warp.cuh"
 #include "ptq_internal.cuh"
 
 namespace ptq {
@@ -72,41 +70,7 @@ __global__ void __launch_bounds__(256) fwht1024_kernel(const void* x, void* y,
         v[j][c] = s < 0 ? -a[c] : a[c];
       }
     }
-    // index bits 0 and 1 (c)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      float a0 = v[j][0] + v[j][1], a1 = v[j][0] - v[j][1];
-      float a2 = v[j][2] + v[j][3], a3 = v[j][2] - v[j][3];
-      v[j][0] = a0 + a2; v[j][2] = a0 - a2;
-      v[j][1] = a1 + a3; v[j][3] = a1 - a3;
-    }
-    // index bits 7, 8, 9 (j)
-#pragma unroll
-    for (int h = 1; h < 8; h <<= 1) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (j & h) continue;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const float a = v[j][c], d = v[j + h][c];
-          v[j][c] = a + d;
-          v[j + h][c] = a - d;
-        }
-      }
-    }
-    // index bits 2..6 (lane): partner holds the other element of the pair
-#pragma unroll
-    for (int mask = 1; mask < 32; mask <<= 1) {
-      const float sgn = (lane & mask) ? -1.0f : 1.0f;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const float p = __shfl_xor_sync(0xffffffffu, v[j][c], mask);
-          v[j][c] = fmaf(sgn, v[j][c], p);  // low: v + p, high: p - v
-        }
-      }
-    }
+    warp_hadamard_1024(v, lane);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int64_t e = base + 128 * j + 4 * lane;

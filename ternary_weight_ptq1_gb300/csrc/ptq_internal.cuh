@@ -66,6 +66,13 @@ cudaError_t launch_fwht(const void* x, Act in, void* y, Act out,
 cudaError_t launch_gemv(const uint8_t* wq, const uint16_t* scales,
                         const float* x, float* y, int64_t M, int64_t N,
                         int64_t K, cudaStream_t st);
+// Embedding lookup on a rotated table (k_embed.cu): out[m] = R^T table[ids[m]].
+// Dense tables: (F32, F32) or (BF16, BF16).  PTQ1_0 tables: out F32 or BF16.
+cudaError_t launch_embed(const void* table, Act table_t, const int32_t* ids, const int8_t* signs,
+                         void* out, Act out_t, int64_t M, int64_t V, int64_t H, cudaStream_t st);
+cudaError_t launch_embed_ptq1(const uint8_t* wq, const uint16_t* scales, const int32_t* ids,
+                              const int8_t* signs, void* out, Act out_t, int64_t M, int64_t V,
+                              int64_t H, cudaStream_t st);
 // M = 1 decode by lookup tables (k_gemv_lut.cu).  part: scratch of
 // gemv_lut_workspace_bytes(N, K) bytes.  cudaErrorNotSupported when the
 // shape does not fit it (K/128 odd, more K-chunks than SMs); the caller then

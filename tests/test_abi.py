@@ -101,6 +101,22 @@ def test_refusals_before_launch(P):
     assert L.ptq_fwht(p16, odd, p16, 1, 1024, P.PTQ_F32, None) == 3
     assert L.ptq_fwht(p16, p16, None, 1, 1024, P.PTQ_F32, None) == 1
     assert L.ptq_fwht(None, None, None, 0, 1024, P.PTQ_BF16, None) == 0
+    # embedding lookup: shape, NULL, alignment, dtype; M = 0 is a no-op
+    em = L.ptq_embed
+    assert em(p16, p16, p16, p16, 1, 10, 1000, P.PTQ_F32, None) == 2     # H % 1024
+    assert em(p16, p16, p16, p16, 1, 0, 1024, P.PTQ_F32, None) == 2      # V < 1
+    assert em(p16, p16, p16, p16, -1, 10, 1024, P.PTQ_F32, None) == 2
+    assert em(p16, None, p16, p16, 1, 10, 1024, P.PTQ_F32, None) == 1
+    odd2 = ctypes.c_void_p(16 * 1024 + 2)
+    assert em(p16, odd2, p16, p16, 1, 10, 1024, P.PTQ_F32, None) == 3    # ids 4-aligned
+    assert em(odd, p16, p16, p16, 1, 10, 1024, P.PTQ_BF16, None) == 3
+    assert em(p16, p16, p16, p16, 1, 10, 1024, 5, None) == 4
+    assert em(None, None, None, None, 0, 10, 1024, P.PTQ_F32, None) == 0
+    ep = L.ptq_embed_ptq1
+    assert ep(p16, None, p16, p16, p16, 1, 10, 1024, P.PTQ_F32, None) == 1  # scales
+    assert ep(p16, odd, p16, p16, p16, 1, 10, 1024, P.PTQ_F32, None) == 3
+    assert ep(p16, p16, p16, p16, p16, 1, 10, 2048 + 128, P.PTQ_F32, None) == 2
+    assert ep(p16, p16, p16, p16, p16, 1, 2 ** 62, 1024, P.PTQ_F32, None) == 2  # V H overflows
     # feed-forward block
     need = P.ffn_workspace_bytes(1, 1024, 2048, P.PTQ_F32)
     assert need > 0

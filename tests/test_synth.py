@@ -42,3 +42,12 @@ def test_distributions(syn):
     assert abs(s.mean() - 0.02 * np.sqrt(2 / np.pi)) < 2e-4 and (s >= 0).all()
     # about 0.24% of 0.02|z| fall below the smallest normal fp16 (2^-14)
     assert 0.001 < (s < 2.0 ** -14).mean() < 0.005
+
+
+def test_token_ids_uniform_in_range(syn):
+    V = 1000
+    ids = syn.token_ids(4, 3, 200000, V)
+    assert ids.dtype == np.int32 and ids.min() >= 0 and ids.max() < V
+    counts = np.bincount(ids, minlength=V)
+    assert counts.min() > 120 and counts.max() < 290  # expected 200 per id
+    np.testing.assert_array_equal(syn.token_ids(4, 3, 50, V), ids[:50])
