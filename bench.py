@@ -230,6 +230,43 @@ def ffn_lines(P, torch, syn, pk, world, args):
     return out
 
 
+def embed_lines(P, torch, syn, pk, world, args):
+    """The token-embedding lookup on a rotated table (gather + inverse signed
+    rotation), V=131,072 x H=5,120: one token (decode) and 2,048 (prefill),
+    from a PTQ1_0 table (147 MB) and a bf16 one (1.34 GB); ids change every
+    step (a ring of 16 seeded id sets)."""
+    V, H, RING = 131072, 5120, 16
+    s = torch.from_numpy(syn.signs(9, 2, H)).cuda()
+    t, sc = syn.weights(9, V, H)
+    tabs = {"ptq1": (torch.from_numpy(P.pack(t)).cuda(), torch.from_numpy(sc.view(np.int16)).cuda())}
+    del t
+    tabs["bf16"] = torch.from_numpy(syn.normal_bf16(9, 8, (V, H)).view(np.int16)).cuda().view(
+        torch.bfloat16)
+    out = {}
+    for name, M in (("decode", 1), ("prefill", 2048)):
+        ids = [torch.from_numpy(syn.token_ids(9, 100 + r, M, V)).cuda() for r in range(RING)]
+        for kind in ("ptq1", "bf16"):
+            y = torch.empty((M, H), device="cuda",
+                            dtype=torch.float32 if kind == "ptq1" else torch.bfloat16)
+            if kind == "ptq1":
+                wq, scd = tabs["ptq1"]
+                fn = lambda i, y=y: P.embed_ptq1(wq, scd, ids[i % RING], s, out=y)  # noqa: E731
+                nbytes = M * (H // 128 * 28 + H * 4) + M * 4 + H
+            else:
+                tb = tabs["bf16"]
+                fn = lambda i, y=y: P.embed(tb, ids[i % RING], s, out=y)  # noqa: E731
+                nbytes = M * H * 2 * 2 + M * 4 + H
+            K = max(3, min(args.steps, 2000 if M == 1 else 200))
+            us = timed_steps(torch, fn, K, 3) / K * 1e3
+            gbs = nbytes / (us * 1e-6) / 1e9
+            out[f"{name}_{kind}"] = {
+                "workload": f"embedding lookup + inverse rotation, {kind} table {V} x {H}, M={M}",
+                "us_per_call": round(us, 3), "bytes_per_call": nbytes,
+                "GB/s": round(world * gbs, 1), "frac_of_hbm": round(gbs / pk["hbm"], 4),
+                "out_dtype": "f32" if kind == "ptq1" else "bf16"}
+    return out
+
+
 def run_ours(args, world, rank):
     import torch
 
@@ -322,6 +359,7 @@ def run_ours(args, world, rank):
                             "traffic": TRAFFIC_PREFILL, "peak_source": pk["source"] + " burst bf16"}}
 
     ffn = None if args.skip_ffn else ffn_lines(P, torch, syn, pk, world, args)
+    emb = None if args.skip_embed else embed_lines(P, torch, syn, pk, world, args)
 
     cpu = cpu_baseline(args) if rank == 0 and not args.skip_cpu else None
     clocks = clk.summary()
@@ -354,6 +392,7 @@ def run_ours(args, world, rank):
         "clocks": clocks,
         "prefill": pre,
         "ffn": ffn,
+        "embed": emb,
         "cpu_baseline": cpu,
     }
     if rank == 0:
@@ -473,6 +512,7 @@ def main():
     ap.add_argument("--reference-max-steps", type=int, default=1000)
     ap.add_argument("--skip-prefill", action="store_true")
     ap.add_argument("--skip-ffn", action="store_true")
+    ap.add_argument("--skip-embed", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--profile", choices=["gemv", "gemm"],
                     help="run a small case of one kernel for an ncu capture, then exit")

@@ -8,15 +8,17 @@
 // butterfly first, then the signs and 1/32 -- the reverse order of the
 // forward rotation.
 //
-// One warp owns one (token m, 1024-block b) pair, laid out over the lanes as
-// warp_hadamard_1024 (fwht_warp.cuh) wants it.  The table is dense (fp32 or
-// bf16 rows, read with 16- or 8-byte vector loads) or PTQ1_0: a lane's four
-// weights 4l..4l+3 of a 128-weight block sit in one or two of its 26 bytes,
-// and each is the pages' peel (section "What Ferrox does with it": digit n
-// of byte e is floor(3^(n+1) u) - 3 floor(3^n u), u = e / 256, exact in fp32)
-// minus one, times the block's fp16 scale.  Arithmetic is fp32; a bf16 output
-// is rounded to nearest-even once, at the end.  An id outside [0, V) makes
-// the warp write quiet NaN and read nothing from the table.
+// A (token m, 1024-block b) pair goes to one CTA of 256 threads, 4 values
+// each, which keeps the dependent chain short (a decode step has only
+// H / 1024 pairs); for dense tables and many pairs, to one warp instead, laid
+// out over the lanes as warp_hadamard_1024 (fwht_warp.cuh) wants it.  The
+// table is dense (fp32 or bf16 rows, read with 16- or 8-byte vector loads) or
+// PTQ1_0: a thread's four weights 4l..4l+3 of a 128-weight block sit in one
+// or two of its 26 bytes, and each is the pages' peel (section "What Ferrox
+// does with it": digit n of byte e is floor(3^(n+1) u) - 3 floor(3^n u),
+// u = e / 256, exact in fp32) minus one, times the block's fp16 scale.
+// Arithmetic is fp32; a bf16 output is rounded to nearest-even once, at the
+// end.  An id outside [0, V) gives quiet NaN and reads nothing from the table.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -28,21 +30,81 @@ namespace {
 
 enum class Tab { F32, BF16, PTQ1 };
 
-// Weight w (0..127) of a PTQ1_0 block whose 26 bytes start at `blk`.
-__device__ __forceinline__ float ptq1_trit(const uint8_t* blk, int w) {
-  const int q = w / 5, n = w % 5;
-  const float u = (float)blk[q] * (1.0f / 256.0f);
-  const float p = n == 0 ? 1.0f : n == 1 ? 3.0f : n == 2 ? 9.0f : n == 3 ? 27.0f : 81.0f;  // 3^n
-  return floorf(3.0f * p * u) - 3.0f * floorf(p * u) - 1.0f;
+// Digit n of byte e by the pages' peel, exact in fp32: u = e / 256 and p = 3^n,
+// so 3 p u <= 243 * 255 / 256 needs no rounding.
+__device__ __forceinline__ float peel(uint32_t e, float p) {
+  const float u = (float)e * (1.0f / 256.0f);
+  return floorf(3.0f * p * u) - 3.0f * floorf(p * u);
 }
 
+__device__ __forceinline__ float pow3(int n) {
+  return n == 0 ? 1.0f : n == 1 ? 3.0f : n == 2 ? 9.0f : n == 3 ? 27.0f : 81.0f;
+}
+
+// The four values at weights 4l..4l+3 of 128-weight block j of 1024-group g
+// of table row `id` (dense: elements 128 j + 4 l + c of that group).  For
+// PTQ1_0 the group's 8 blocks are 208 contiguous bytes starting at
+// 208 (id bpr + g) and its 8 scales 16 contiguous bytes.
+template <Tab kT>
+__device__ __forceinline__ void load4(const void* __restrict__ table,
+                                      const uint16_t* __restrict__ scales, int64_t row_group,
+                                      int j, int l, float (&v)[4]) {
+  if constexpr (kT == Tab::F32) {
+    const float4 r = *reinterpret_cast<const float4*>(static_cast<const float*>(table) +
+                                                      row_group * kRot + 128 * j + 4 * l);
+    v[0] = r.x; v[1] = r.y; v[2] = r.z; v[3] = r.w;
+  } else if constexpr (kT == Tab::BF16) {
+    const uint2 r = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(table) +
+                                                    row_group * kRot + 128 * j + 4 * l);
+    v[0] = __uint_as_float(r.x << 16);
+    v[1] = __uint_as_float(r.x & 0xffff0000u);
+    v[2] = __uint_as_float(r.y << 16);
+    v[3] = __uint_as_float(r.y & 0xffff0000u);
+  } else {
+    const uint8_t* blk = static_cast<const uint8_t*>(table) + row_group * kGroupBytes + j * kBlockBytes;
+    const float s = __half2float(__ushort_as_half(scales[row_group * kGroupBlocks + j]));
+    const int w0 = 4 * l, q0 = w0 / 5, q1 = (w0 + 3) / 5;  // the one or two bytes
+    const uint32_t e0 = blk[q0], e1 = blk[q1];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int w = w0 + c;
+      v[c] = (peel(w / 5 == q0 ? e0 : e1, pow3(w % 5)) - 1.0f) * s;
+    }
+  }
+}
+
+template <Act kOut>
+__device__ __forceinline__ void store4(void* out, int64_t e, const float (&o)[4]) {
+  if constexpr (kOut == Act::BF16) {
+    uint2 r;
+    r.x = __bfloat16_as_ushort(__float2bfloat16_rn(o[0])) |
+          ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(o[1])) << 16);
+    r.y = __bfloat16_as_ushort(__float2bfloat16_rn(o[2])) |
+          ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(o[3])) << 16);
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + e) = r;
+  } else {
+    *reinterpret_cast<float4*>(static_cast<float*>(out) + e) = make_float4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+template <Act kOut>
+__device__ __forceinline__ void store1(void* out, int64_t e, float o) {
+  if constexpr (kOut == Act::BF16)
+    static_cast<uint16_t*>(out)[e] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+  else
+    static_cast<float*>(out)[e] = o;
+}
+
+constexpr float kQNaN = __builtin_nanf("");
+
+// Many (token, block) pairs: one warp each, 32 values a lane.
 template <Tab kT, Act kOut>
-__global__ void __launch_bounds__(256) embed_kernel(const void* __restrict__ table,
-                                                    const uint16_t* __restrict__ scales,
-                                                    const int32_t* ids,
-                                                    const int8_t* __restrict__ signs, void* out,
-                                                    int64_t total_blocks, int64_t blocks_per_row,
-                                                    int64_t V) {
+__global__ void __launch_bounds__(256) embed_warp_kernel(const void* __restrict__ table,
+                                                         const uint16_t* __restrict__ scales,
+                                                         const int32_t* ids,
+                                                         const int8_t* __restrict__ signs,
+                                                         void* out, int64_t total_blocks,
+                                                         int64_t blocks_per_row, int64_t V) {
   const int lane = threadIdx.x & 31;
   const int64_t H = blocks_per_row * kRot;
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
@@ -56,25 +118,7 @@ __global__ void __launch_bounds__(256) embed_kernel(const void* __restrict__ tab
     float v[8][4] = {};
     if (ok) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int64_t e = (int64_t)id * H + b * kRot + 128 * j + 4 * lane;
-        if constexpr (kT == Tab::F32) {
-          const float4 r = *reinterpret_cast<const float4*>(static_cast<const float*>(table) + e);
-          v[j][0] = r.x; v[j][1] = r.y; v[j][2] = r.z; v[j][3] = r.w;
-        } else if constexpr (kT == Tab::BF16) {
-          const uint2 r = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(table) + e);
-          v[j][0] = __uint_as_float(r.x << 16);
-          v[j][1] = __uint_as_float(r.x & 0xffff0000u);
-          v[j][2] = __uint_as_float(r.y << 16);
-          v[j][3] = __uint_as_float(r.y & 0xffff0000u);
-        } else {
-          const int64_t blk = (int64_t)id * (H / kBlockWeights) + b * kGroupBlocks + j;
-          const uint8_t* bytes = static_cast<const uint8_t*>(table) + blk * kBlockBytes;
-          const float s = __half2float(__ushort_as_half(scales[blk]));
-#pragma unroll
-          for (int c = 0; c < 4; ++c) v[j][c] = ptq1_trit(bytes, 4 * lane + c) * s;
-        }
-      }
+      for (int j = 0; j < 8; ++j) load4<kT>(table, scales, (int64_t)id * blocks_per_row + b, j, lane, v[j]);
       warp_hadamard_1024(v, lane);
     }
 #pragma unroll
@@ -85,18 +129,71 @@ __global__ void __launch_bounds__(256) embed_kernel(const void* __restrict__ tab
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const float f = v[j][c] * (1.0f / 32.0f);
-        o[c] = ok ? ((int8_t)(sg >> (8 * c)) < 0 ? -f : f) : __uint_as_float(0x7fc00000u);
+        o[c] = ok ? ((int8_t)(sg >> (8 * c)) < 0 ? -f : f) : kQNaN;
       }
-      const int64_t e = m * H + k;
-      if constexpr (kOut == Act::BF16) {
-        uint2 r;
-        r.x = __bfloat16_as_ushort(__float2bfloat16_rn(o[0])) |
-              ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(o[1])) << 16);
-        r.y = __bfloat16_as_ushort(__float2bfloat16_rn(o[2])) |
-              ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(o[3])) << 16);
-        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + e) = r;
-      } else {
-        *reinterpret_cast<float4*>(static_cast<float*>(out) + e) = make_float4(o[0], o[1], o[2], o[3]);
+      store4<kOut>(out, m * H + k, o);
+    }
+  }
+}
+
+// Few pairs (a decode step): one CTA of 256 threads each, 4 values a thread.
+// Thread (warp j, lane l) holds elements 128 j + 4 l + c: index bits 0-1 in
+// registers, bits 2-6 across the lanes; bits 7-9 (the warp) are done after a
+// transpose through shared memory, by 128 threads holding elements t + 128 k.
+template <Tab kT, Act kOut>
+__global__ void __launch_bounds__(256) embed_cta_kernel(const void* __restrict__ table,
+                                                        const uint16_t* __restrict__ scales,
+                                                        const int32_t* ids,
+                                                        const int8_t* __restrict__ signs,
+                                                        void* out, int64_t total_blocks,
+                                                        int64_t blocks_per_row, int64_t V) {
+  __shared__ float4 exch[kRot / 4];
+  const int t = threadIdx.x, lane = t & 31, j = t >> 5;
+  const int64_t H = blocks_per_row * kRot;
+  pdl_release();
+  pdl_wait();
+  for (int64_t wb = blockIdx.x; wb < total_blocks; wb += gridDim.x) {
+    const int64_t m = wb / blocks_per_row, b = wb % blocks_per_row;
+    const int32_t id = ids[m];
+    const bool ok = id >= 0 && (int64_t)id < V;  // the same for the whole CTA
+    if (!ok) {
+      for (int i = t; i < kRot; i += 256) store1<kOut>(out, m * H + b * kRot + i, kQNaN);
+      continue;
+    }
+    float v[4];
+    load4<kT>(table, scales, (int64_t)id * blocks_per_row + b, j, lane, v);
+    {  // bits 0, 1
+      const float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
+      v[0] = a0 + a2; v[2] = a0 - a2; v[1] = a1 + a3; v[3] = a1 - a3;
+    }
+#pragma unroll
+    for (int mask = 1; mask < 32; mask <<= 1) {  // bits 2..6
+      const float sgn = (lane & mask) ? -1.0f : 1.0f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) v[c] = fmaf(sgn, v[c], __shfl_xor_sync(0xffffffffu, v[c], mask));
+    }
+    __syncthreads();  // the previous pair's readers are done with exch
+    exch[t] = make_float4(v[0], v[1], v[2], v[3]);
+    __syncthreads();
+    if (t < 128) {  // bits 7..9: elements t + 128 k
+      const float* ex = reinterpret_cast<const float*>(exch);
+      float w[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) w[k] = ex[t + 128 * k];
+#pragma unroll
+      for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (!(k & h)) {
+            const float p = w[k], q = w[k + h];
+            w[k] = p + q;
+            w[k + h] = p - q;
+          }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int64_t i = b * kRot + t + 128 * k;
+        const float f = w[k] * (1.0f / 32.0f);
+        store1<kOut>(out, m * H + i, signs[i] < 0 ? -f : f);
       }
     }
   }
@@ -107,11 +204,21 @@ cudaError_t launch_embed_t(const void* table, const uint16_t* scales, const int3
                            const int8_t* signs, void* out, int64_t M, int64_t V, int64_t H,
                            cudaStream_t st) {
   const int64_t bpr = H / kRot, total = M * bpr;
+  constexpr int64_t kSms = 152;
+  // Measured on a GB300 (V = 131072, H = 5120): a CTA per pair is faster for
+  // PTQ1_0 tables at every M (2.5 against 7.5 us at M = 1, 31 against 42 us
+  // at M = 2048) and for dense tables up to M = 256 (1280 pairs); a warp per
+  // pair is faster for dense tables at M = 2048 (12 against 18 us).
+  if (kT == Tab::PTQ1 || total < 16 * kSms) {
+    const int64_t grid = total < kSms * 512 ? total : kSms * 512;
+    return launch_pdl(embed_cta_kernel<kT, kOut>, dim3((unsigned)grid), dim3(256), 0, st, table,
+                      scales, ids, signs, out, total, bpr, V);
+  }
   const int warps = 8;
   int64_t grid = (total + warps - 1) / warps;
-  if (grid > 152 * 64) grid = 152 * 64;
-  return launch_pdl(embed_kernel<kT, kOut>, dim3((unsigned)grid), dim3(32 * warps), 0, st, table,
-                    scales, ids, signs, out, total, bpr, V);
+  if (grid > kSms * 64) grid = kSms * 64;
+  return launch_pdl(embed_warp_kernel<kT, kOut>, dim3((unsigned)grid), dim3(32 * warps), 0, st,
+                    table, scales, ids, signs, out, total, bpr, V);
 }
 
 }  // namespace

@@ -120,6 +120,28 @@ def test_empty_and_in_bounds(P, syn):
     assert torch.isfinite(out).all()
 
 
+def test_dispatch_paths(P, orc, syn):
+    # a dense table with many (token, block) pairs runs a warp per pair; a
+    # PTQ1_0 table past 152 x 512 pairs makes each CTA take several pairs
+    import torch
+
+    V, H = 97, 5120
+    table = syn.normal_f32(38, 0, (V, H))
+    s = syn.signs(38, 2, H)
+    ids = syn.token_ids(38, 1, 600, V)            # 3000 pairs
+    y = P.embed(Q.dev(table), _ids_dev(ids), Q.dev(s))
+    Q.check_fwht(Q.host_f64(y), orc.embed(orc.decode_f32(table), ids, s), what="warp per pair")
+    t, sc = syn.weights(38, V, H)
+    wq = P.pack(t)
+    ids = syn.token_ids(38, 3, 16000, V)          # 80000 pairs
+    ids[-1] = V                                   # a bad id in the last pass
+    y = P.embed_ptq1(Q.dev(wq), Q.dev(sc), _ids_dev(ids), Q.dev(s))
+    rows = np.array([0, 1, 7777, 15197, 15198, 15998])
+    Q.check_fwht(Q.host_f64(y[torch.from_numpy(rows).cuda()]), orc.embed_ptq1(wq, sc, ids[rows], s),
+                 what="several pairs per CTA")
+    assert torch.isnan(y[-1]).all() and torch.isfinite(y[:-1]).all()
+
+
 def test_full_size_sampled(P, orc, syn):
     # the bench's shape: a 131,072 x 5,120 PTQ1_0 table (147 MB) and a bf16
     # one (1.34 GB), 2,048 ids; 24 rows checked against the oracle
