@@ -42,6 +42,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "async_util.cuh"
 #include "ptq_internal.cuh"
 
 namespace ptq {
@@ -53,7 +54,6 @@ constexpr int kASlice = BM * BK * 2;                        // 32 KB
 constexpr int kBSlice = BN * BK * 2;                        // 16 KB
 constexpr int kThreads = 10 * 32;
 constexpr int kExpWarp0 = 2, kExpThreads = 256;
-constexpr uint32_t kWaitLimit = 1u << 22;
 
 // shared memory layout (offsets from a 1024-aligned base)
 constexpr int kOffA = 0;
@@ -65,50 +65,7 @@ constexpr int kOffMisc = kOffBar + kNumBars * 8;            // tmem base, abort 
 constexpr int kSmemBytes = kOffMisc + 16;
 static_assert(2 * (kSmemBytes + 1024) <= 228 * 1024, "two CTAs per SM");
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-               "r"(bytes)
-               : "memory");
-}
-
-// Bounded wait for phase `parity`.  Returns false when the limit ran out or
-// (when `abort` is given) another role has already aborted the CTA.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  const uint32_t a = smem_u32(bar);
-  for (uint32_t i = 0; i < kWaitLimit; ++i) {
-    uint32_t done;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(done)
-        : "r"(a), "r"(parity)
-        : "memory");
-    if (done) return true;
-    if (abort && (i & 1023) == 1023 && *abort) return false;
-  }
-  return false;
-}
-
-__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                       uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return smem_addr(p); }
 
 // Shared-memory matrix descriptor of a K-major, 128B-swizzled tile whose
 // 8-row x 128-byte atoms are stacked every 1024 bytes (SBO).

@@ -39,6 +39,7 @@
 // bitwise reproducible.  No kernel here waits on another CTA.
 #include <cuda_fp16.h>
 
+#include "async_util.cuh"
 #include "ptq_internal.cuh"
 
 namespace ptq {
@@ -223,6 +224,72 @@ __device__ __forceinline__ void rotate_block(const float* __restrict__ x, const 
   }
 }
 
+// The activations a chunk (words [ws, we) of every row) touches, rotated
+// first when `signs` is given, staged at `xs`; then the lane tables.  All
+// threads of the CTA take part; `exch` is 8 KB of scratch for the rotation.
+__device__ __forceinline__ void stage_tables(const float* __restrict__ x,
+                                             const int8_t* __restrict__ signs, int ws, int we,
+                                             bool live, uint32_t exch, uint32_t xs) {
+  const int L = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int bx0 = (4 * ws) / kBlockBytes, bx1 = (4 * we - 1) / kBlockBytes;
+  int xbase;  // weight index of xs[0]
+  if (signs == nullptr) {
+    xbase = bx0 * kBlockWeights;
+    const int nx = (bx1 - bx0 + 1) * kBlockWeights;  // <= 6 * 128
+    for (int i = threadIdx.x; i < nx; i += kThreads)
+      sts_f32(xs + 4u * (uint32_t)i, x[(size_t)xbase + i]);
+  } else {
+    // the rotation blocks that hold this chunk's weights: one or two, one per
+    // half of the CTA
+    const int f0 = bx0 * kBlockWeights / kRot, f1 = (bx1 * kBlockWeights + kBlockWeights - 1) / kRot;
+    xbase = f0 * kRot;
+    const int half = warp >> 3, g8 = threadIdx.x & 255;
+    auto bar = [half]() {
+      asm volatile("bar.sync %0, 256;" ::"r"(1 + half) : "memory");
+    };
+    if (f0 + half <= f1) {
+      const size_t off = (size_t)(f0 + half) * kRot;
+      rotate_block(x + off, signs + off, exch + (uint32_t)(half * kRot * 4),
+                   xs + (uint32_t)(half * kRot * 4), g8, bar);
+    }
+  }
+  __syncthreads();
+  {
+    // warp -> (position j of every lane's word, quarter R of the entries)
+    const int j = warp & 3;
+    const int Pj = 4 * (ws + L) + j;
+    const int b = Pj / kBlockBytes, q = Pj % kBlockBytes;
+    float xv[5];
+#pragma unroll
+    for (int i = 0; i < 5; ++i) {
+      const bool in = live && 5 * q + i < kBlockWeights;  // byte 25 holds three trits
+      xv[i] = in ? lds_f32(xs + 4u * (uint32_t)(b * kBlockWeights + 5 * q + i - xbase)) : 0.0f;
+    }
+    float A[9], B[27];
+#pragma unroll
+    for (int a = 0; a < 9; ++a) {
+      // digits d0 = a / 3, d1 = a % 3 contribute (d - 1) x
+      const int d0 = a / 3 - 1, d1 = a % 3 - 1;
+      const float t0 = d0 > 0 ? xv[0] : (d0 < 0 ? -xv[0] : 0.0f);
+      A[a] = d1 > 0 ? t0 + xv[1] : (d1 < 0 ? t0 - xv[1] : t0);
+    }
+#pragma unroll
+    for (int bb = 0; bb < 27; ++bb) {
+      const int d2 = bb / 9 - 1, d3 = (bb / 3) % 3 - 1, d4 = bb % 3 - 1;
+      float t = d2 > 0 ? xv[2] : (d2 < 0 ? -xv[2] : 0.0f);
+      t = d3 > 0 ? t + xv[3] : (d3 < 0 ? t - xv[3] : t);
+      B[bb] = d4 > 0 ? t + xv[4] : (d4 < 0 ? t - xv[4] : t);
+    }
+    const uint32_t dst = kTab + 0x10000u * (uint32_t)(j >> 1) + 128u * (uint32_t)(j & 1) + 4u * L;
+    switch (warp >> 2) {
+      case 0: build_entries<0>(A, B, dst); break;
+      case 1: build_entries<1>(A, B, dst); break;
+      case 2: build_entries<2>(A, B, dst); break;
+      default: build_entries<3>(A, B, dst); break;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1) gemv_lut_kernel(const LutArgs P) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int L = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -274,63 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_lut_kernel(const LutArgs P) 
 
   // ---- activations of the chunk, then its tables ---------------------------------
   pdl_wait();
-  const int bx0 = (4 * ws) / kBlockBytes, bx1 = (4 * we - 1) / kBlockBytes;
-  int xbase;  // weight index of xs[0]
-  if (P.signs == nullptr) {
-    xbase = bx0 * kBlockWeights;
-    const int nx = (bx1 - bx0 + 1) * kBlockWeights;  // <= 6 * 128
-    for (int i = threadIdx.x; i < nx; i += kThreads)
-      sts_f32(xs + 4u * (uint32_t)i, P.x[(size_t)xbase + i]);
-  } else {
-    // the rotation blocks that hold this chunk's weights: one or two, one per
-    // half of the CTA; the reduction buffers are free to exchange through
-    const int f0 = bx0 * kBlockWeights / kRot, f1 = (bx1 * kBlockWeights + kBlockWeights - 1) / kRot;
-    xbase = f0 * kRot;
-    const int half = warp >> 3, g8 = threadIdx.x & 255;
-    auto bar = [half]() {
-      asm volatile("bar.sync %0, 256;" ::"r"(1 + half) : "memory");
-    };
-    if (f0 + half <= f1) {
-      const size_t off = (size_t)(f0 + half) * kRot;
-      rotate_block(P.x + off, P.signs + off, base + (uint32_t)(half * kRot * 4),
-                   xs + (uint32_t)(half * kRot * 4), g8, bar);
-    }
-  }
-  __syncthreads();
-  {
-    // warp -> (position j of every lane's word, quarter R of the entries)
-    const int j = warp & 3;
-    const int Pj = 4 * (ws + L) + j;
-    const int b = Pj / kBlockBytes, q = Pj % kBlockBytes;
-    float xv[5];
-#pragma unroll
-    for (int i = 0; i < 5; ++i) {
-      const bool in = live && 5 * q + i < kBlockWeights;  // byte 25 holds three trits
-      xv[i] = in ? lds_f32(xs + 4u * (uint32_t)(b * kBlockWeights + 5 * q + i - xbase)) : 0.0f;
-    }
-    float A[9], B[27];
-#pragma unroll
-    for (int a = 0; a < 9; ++a) {
-      // digits d0 = a / 3, d1 = a % 3 contribute (d - 1) x
-      const int d0 = a / 3 - 1, d1 = a % 3 - 1;
-      const float t0 = d0 > 0 ? xv[0] : (d0 < 0 ? -xv[0] : 0.0f);
-      A[a] = d1 > 0 ? t0 + xv[1] : (d1 < 0 ? t0 - xv[1] : t0);
-    }
-#pragma unroll
-    for (int bb = 0; bb < 27; ++bb) {
-      const int d2 = bb / 9 - 1, d3 = (bb / 3) % 3 - 1, d4 = bb % 3 - 1;
-      float t = d2 > 0 ? xv[2] : (d2 < 0 ? -xv[2] : 0.0f);
-      t = d3 > 0 ? t + xv[3] : (d3 < 0 ? t - xv[3] : t);
-      B[bb] = d4 > 0 ? t + xv[4] : (d4 < 0 ? t - xv[4] : t);
-    }
-    const uint32_t dst = kTab + 0x10000u * (uint32_t)(j >> 1) + 128u * (uint32_t)(j & 1) + 4u * L;
-    switch (warp >> 2) {
-      case 0: build_entries<0>(A, B, dst); break;
-      case 1: build_entries<1>(A, B, dst); break;
-      case 2: build_entries<2>(A, B, dst); break;
-      default: build_entries<3>(A, B, dst); break;
-    }
-  }
+  stage_tables(P.x, P.signs, ws, we, live, base, xs);
   __syncthreads();
   pdl_release();  // the reduction kernel may start its prologue
 
@@ -355,6 +366,181 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_lut_kernel(const LutArgs P) 
     const int nref = rb - r0 - kRows;  // rows left to fetch (may be <= 0)
     rows_batch<false>(wr, sr, nrows, nref, pw0 + next * wrow, qw0 + next * srow, ln);
     reduce_batch(red, L, out, r0, rb);
+  }
+}
+
+// ---- the same GEMV with the weights staged by TMA (K % 1024 == 0) --------------
+// Rows are 26 nblk / 8 ... bytes apart: with nblk % 8 == 0 both weight planes
+// have 16-byte aligned rows, and chunks cut at multiples of 4 words start on
+// 16-byte boundaries, so a chunk's trits of 16 rows (16 x 128 bytes) and the
+// 8 scale words that cover its blocks (16 x 32 bytes) are two TMA boxes.
+// Each warp owns a ring of two such slots: while it works on one batch, the
+// next is landing and the one after is on its way -- twice the register
+// ring's depth, with no register cost.  The first two boxes of every warp
+// are requested before griddepcontrol.wait, so they stream in while the
+// previous kernel finishes and the tables are built.  The 32 lane values of
+// a row are summed by a butterfly of shuffles (no shared memory), whose
+// space the ring takes.
+
+constexpr int kBoxRows = 16;                          // rows per box = per batch
+constexpr int kBoxScaleWords = 8;                     // scale words per row in a box
+constexpr int kSlotTrits = kBoxRows * kChunkWords * 4;     // 2048
+constexpr int kSlotBytes = kSlotTrits + kBoxRows * kBoxScaleWords * 4;  // 2560
+constexpr int kSlotsPerWarp = 2;
+constexpr int kSlots = kWarps * kSlotsPerWarp;       // 32
+constexpr int kLowSlots = 18;                        // below the tables; the rest above them
+constexpr int kExchBytes = 2 * kRot * 4;             // rotation scratch (two blocks)
+constexpr int kBarOff = kExchBytes + kXFloats * 4;   // after the exchange and x
+constexpr int kRingOff = (kBarOff + kSlots * 8 + 127) / 128 * 128;
+constexpr size_t kSmemTma = 227 * 1024;               // the whole window
+static_assert(kTabEnd + (kSlots - kLowSlots) * kSlotBytes <= kSmemTma, "upper ring fits");
+
+struct LutTmaArgs {
+  CUtensorMap tw;      // trits: N rows of `words` 32-bit words, boxes 32 x 16
+  CUtensorMap ts;      // scales: N rows of nblk / 2 words (fp16 pairs), boxes 8 x 16
+  const float* x;
+  const int8_t* signs;  // non-null: x is not rotated yet
+  float* part;          // nch x N row sums (y itself when nch == 1)
+  int* status;          // device status word (a wait that ran out)
+  int N, nblk, words, nch, cpc;
+};
+
+__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+
+__device__ __forceinline__ float lane_value(uint32_t w, uint32_t sw, const Lanes& ln) {
+  const uint32_t a0 = __byte_perm(w, ln.lb0, 0x7604), a1 = __byte_perm(w, ln.lb1, 0x7614);
+  const uint32_t a2 = __byte_perm(w, ln.lb2, 0x7624), a3 = __byte_perm(w, ln.lb3, 0x7634);
+  const uint32_t s2 = __byte_perm(sw, 0u, ln.ssel);
+  const float t0 = lds_f32(a0), t1 = lds_f32(a1), t2 = lds_f32(a2), t3 = lds_f32(a3);
+  const float sA = __half2float(__ushort_as_half((unsigned short)(s2 & 0xffffu)));
+  const float sB = __half2float(__ushort_as_half((unsigned short)(s2 >> 16)));
+  return fmaf(t2 + t3, sB, (t0 + t1) * sA);
+}
+
+// lo/hi: this lane's values of two rows; the lane keeps the one its bit m
+// selects and adds the partner lane's copy of it
+__device__ __forceinline__ float fold(float lo, float hi, bool up, int m) {
+  const float keep = up ? hi : lo, send = up ? lo : hi;
+  return keep + __shfl_xor_sync(0xffffffffu, send, m);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) gemv_lut_tma_kernel(const __grid_constant__ LutTmaArgs P) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int L = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t raw = smem_u32(smem);
+  const uint32_t base = (raw + 127u) & ~127u;
+  const uint32_t exch = base, xs = base + (uint32_t)kExchBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (base - raw) + kBarOff);
+  const uint32_t ring_lo = base + (uint32_t)kRingOff;
+  // The tables and the upper slots sit at fixed addresses: the window must
+  // start low enough for the lower slots to end below the tables (it starts
+  // after the 1 KB the driver reserves); otherwise nothing runs.
+  if (ring_lo + (uint32_t)(kLowSlots * kSlotBytes) > kTab ||
+      kTabEnd + (uint32_t)((kSlots - kLowSlots) * kSlotBytes) > raw + (uint32_t)kSmemTma)
+    return;
+
+  // ---- this CTA's chunk and rows ------------------------------------------------
+  const int c = blockIdx.x / P.cpc, k = blockIdx.x % P.cpc;
+  const int R0 = (int)((long long)k * P.N / P.cpc);
+  const int R1 = (int)((long long)(k + 1) * P.N / P.cpc);
+  const int Q = P.words / 4;                   // 4-word quads per row
+  const int ws = 4 * (int)((long long)c * Q / P.nch);
+  const int we = 4 * (int)((long long)(c + 1) * Q / P.nch);
+  const int Wc = we - ws;                      // 4..32 words
+  const bool live = L < Wc;
+  const int wl = ws + (live ? L : Wc - 1);     // lanes past the chunk take its last word's scales
+  const int P0 = 4 * wl;
+  const int bA = P0 / kBlockBytes, bB = (P0 + 2) / kBlockBytes;
+  const uint32_t ssel = (bB != bA) ? 0x3210u : ((bA & 1) ? 0x3232u : 0x1010u);
+  // the scale box starts at the chunk's first scale word rounded down to a
+  // multiple of 4; a chunk spans at most 6 blocks, so 8 words cover it
+  const int xsw = ((4 * ws / kBlockBytes) >> 1) & ~3;
+  const uint32_t soff = 4u * (uint32_t)((bA >> 1) - xsw);
+
+  const int nr = R1 - R0;
+  const int ra = R0 + (int)((long long)warp * nr / kWarps);
+  const int rb = R0 + (int)((long long)(warp + 1) * nr / kWarps);
+  const int nbat = (rb - ra + kBoxRows - 1) / kBoxRows;
+
+  // ---- this warp's ring; its first two boxes (weights only) -----------------------
+  uint64_t* full = bars + kSlotsPerWarp * warp;
+  auto slot_of = [&](int s) -> uint32_t {
+    const int g = kSlotsPerWarp * warp + s;
+    return g < kLowSlots ? ring_lo + (uint32_t)(g * kSlotBytes)
+                         : kTabEnd + (uint32_t)((g - kLowSlots) * kSlotBytes);
+  };
+  auto request = [&](int b) {  // lane 0: batch b into slot b % 2
+    const int s = b & 1;
+    const uint32_t dst = slot_of(s);
+    mbar_expect_tx(&full[s], (uint32_t)kSlotBytes);
+    tma_2d(dst, &P.tw, ws, ra + kBoxRows * b, &full[s]);
+    tma_2d(dst + (uint32_t)kSlotTrits, &P.ts, xsw, ra + kBoxRows * b, &full[s]);
+  };
+  if (L == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (nbat > 0) request(0);
+    if (nbat > 1) request(1);
+  }
+  __syncwarp();
+
+  // ---- activations of the chunk, then its tables ---------------------------------
+  pdl_wait();
+  stage_tables(P.x, P.signs, ws, we, live, exch, xs);
+  __syncthreads();
+  pdl_release();  // the reduction kernel may start its prologue
+
+  // ---- main loop: one box of 16 rows per batch -------------------------------------
+  const uint32_t lb0 = kTab + 4u * L, lb1 = lb0 + 128u, lb2 = lb0 + 0x10000u, lb3 = lb2 + 128u;
+  const Lanes ln{lb0, lb1, lb2, lb3, ssel, 0u, 0u, 0u};
+  float* out = P.part + (size_t)c * P.N;
+  int b = 0;
+  bool ok = true;
+  for (; b < nbat; ++b) {
+    const int s = b & 1;
+    ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (uint32_t)((b >> 1) & 1), nullptr));
+    if (!ok) break;
+    const uint32_t slot = slot_of(s);
+    uint32_t w[kBoxRows], sw[kBoxRows];
+    uint32_t seen = 0u;
+#pragma unroll
+    for (int r = 0; r < kBoxRows; ++r) {
+      w[r] = lds_u32(slot + (uint32_t)(r * kChunkWords * 4) + 4u * (uint32_t)L);
+      sw[r] = lds_u32(slot + (uint32_t)kSlotTrits + (uint32_t)(r * kBoxScaleWords * 4) + soff);
+      seen ^= w[r] ^ sw[r];
+    }
+    // The slot is read (`seen` waits for every load); hand it to the TMA for
+    // the batch two ahead.  The proxy fence orders these reads before the
+    // asynchronous writes.
+    asm volatile("" ::"r"(seen));
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (L == 0 && b + 2 < nbat) request(b + 2);
+    // rows j and j + 8 meet first (lane bit 4), then the halves fold over
+    // lane bits 3, 2, 1, 0: lanes 2i and 2i + 1 end with row i of the batch
+    float k1[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      k1[j] = fold(lane_value(w[j], sw[j], ln), lane_value(w[j + 8], sw[j + 8], ln), L & 16, 16);
+    float k2[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) k2[j] = fold(k1[j], k1[j + 4], L & 8, 8);
+    const float k3a = fold(k2[0], k2[2], L & 4, 4), k3b = fold(k2[1], k2[3], L & 4, 4);
+    float v = fold(k3a, k3b, L & 2, 2);
+    v += __shfl_xor_sync(0xffffffffu, v, 1);
+    const int row = ra + kBoxRows * b + (L >> 1);
+    if (!(L & 1) && row < rb) out[row] = v;
+  }
+  if (!ok) {
+    if (L == 0) atomicOr(P.status, kDevTimeout);
+    // let the boxes still in flight land before the CTA's shared memory goes
+    for (int bb = b; bb < nbat && bb < b + 2; ++bb)
+      static_cast<void>(mbar_wait(&full[bb & 1], (uint32_t)((bb >> 1) & 1), nullptr));
   }
 }
 
@@ -418,6 +604,9 @@ static cudaError_t device_sms(int* out) {
     e = cudaFuncSetAttribute(gemv_lut_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemBytes);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(gemv_lut_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemTma);
+    if (e != cudaSuccess) return e;
     g_sms[dev] = sms;
   }
   *out = g_sms[dev];
@@ -454,18 +643,47 @@ cudaError_t launch_gemv_lut(const uint8_t* wq, const uint16_t* scales, const flo
   const int64_t by_rows = (N + kMinRowsPerCta - 1) / kMinRowsPerCta;
   if (cpc > by_rows) cpc = by_rows;
   if (cpc < 1) cpc = 1;
-  LutArgs A;
-  A.wq = wq;
-  A.sc = scales;
-  A.x = x;
-  A.signs = signs;
-  A.part = nch == 1 ? y : part;
-  A.N = (int)N;
-  A.nblk = (int)(K / kBlockWeights);
-  A.words = 13 * A.nblk / 2;
-  A.nch = (int)nch;
-  A.cpc = (int)cpc;
-  e = launch_pdl(gemv_lut_kernel, dim3((unsigned)(nch * cpc)), dim3(kThreads), kSmemBytes, st, A);
+  const int nblk = (int)(K / kBlockWeights), words = 13 * nblk / 2;
+  // With K % 1024 == 0 both weight planes have 16-byte aligned rows: the
+  // TMA-fed kernel (its 4-word aligned chunks number the same nch).
+  bool tma = K % kRot == 0 && device_status_ptr() != nullptr;
+  if (tma) {
+    LutTmaArgs T;
+    tma = encode_tma_2d(&T.tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, wq, (uint64_t)words, (uint64_t)N,
+                        (uint64_t)words * 4, kChunkWords, kBoxRows,
+                        CU_TENSOR_MAP_SWIZZLE_NONE) == cudaSuccess &&
+          encode_tma_2d(&T.ts, CU_TENSOR_MAP_DATA_TYPE_UINT32, scales, (uint64_t)(nblk / 2),
+                        (uint64_t)N, (uint64_t)nblk * 2, kBoxScaleWords, kBoxRows,
+                        CU_TENSOR_MAP_SWIZZLE_NONE) == cudaSuccess;
+    if (tma) {
+      T.x = x;
+      T.signs = signs;
+      T.part = nch == 1 ? y : part;
+      T.status = device_status_ptr();
+      T.N = (int)N;
+      T.nblk = nblk;
+      T.words = words;
+      T.nch = (int)nch;
+      T.cpc = (int)cpc;
+      e = launch_pdl(gemv_lut_tma_kernel, dim3((unsigned)(nch * cpc)), dim3(kThreads), kSmemTma,
+                     st, T);
+    }
+  }
+  if (!tma) {
+    LutArgs A;
+    A.wq = wq;
+    A.sc = scales;
+    A.x = x;
+    A.signs = signs;
+    A.part = nch == 1 ? y : part;
+    A.N = (int)N;
+    A.nblk = nblk;
+    A.words = words;
+    A.nch = (int)nch;
+    A.cpc = (int)cpc;
+    e = launch_pdl(gemv_lut_kernel, dim3((unsigned)(nch * cpc)), dim3(kThreads), kSmemBytes, st,
+                   A);
+  }
   if (e != cudaSuccess || nch == 1) return e;
   if (ep == LutEpilogue::SwiGLU)
     return launch_pdl(gemv_lut_reduce_swiglu_kernel, dim3((unsigned)((N / 2 + 255) / 256)),
