@@ -183,7 +183,7 @@ def max_over_ranks(v: float) -> float:
 TRAFFIC_PREFILL = 24_840_448 + 7_168
 # Decode: the capture runs eight stacked gate/up matrices; the per-launch
 # figure is that capture's bytes / 8 (traffic grows with the rows streamed).
-TRAFFIC_DECODE = None
+TRAFFIC_DECODE = (156_060_416 + 5_802_496) // 8
 
 
 def ffn_lines(P, torch, syn, pk, world, args):
