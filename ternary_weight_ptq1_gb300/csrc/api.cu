@@ -477,9 +477,18 @@ PTQ_API ptq_status ptq_ffn(const uint8_t* wgu_q, const uint16_t* wgu_s, const ui
     return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq_ffn launch");
   }
   cudaError_t e = launch_fwht(x, act_of(dtype), xr, op, signs_in, M, H, st);
-  if (e == cudaSuccess)
+  // prefill: SwiGLU in the gate/up GEMM's epilogue when that GEMM runs
+  // unsplit; otherwise gate/up into fp32, then the SwiGLU kernel
+  bool fused = false;
+  if (e == cudaSuccess && r_gu->kernel == Kernel::GemmBf16) {
+    e = launch_gemm_tc_swiglu(wgu_q, wgu_s, xr, op, h, M, I, H, st);
+    fused = e == cudaSuccess;
+    if (e == cudaErrorNotSupported) e = cudaSuccess;
+  }
+  if (e == cudaSuccess && !fused) {
     e = run_matmul(r_gu, wgu_q, wgu_s, xr, op, gu, Act::F32, M, 2 * I, H, part, need - off[4], st);
-  if (e == cudaSuccess) e = launch_swiglu(gu, h, M, I, st);
+    if (e == cudaSuccess) e = launch_swiglu(gu, h, M, I, st);
+  }
   if (e == cudaSuccess) e = launch_fwht(h, Act::F32, hr, op, signs_mid, M, I, st);
   // the down projection's split-K partials go where gate/up was (dead after
   // SwiGLU)

@@ -282,14 +282,32 @@ __device__ bool expand_all(const ExpCtx& c) {
   return true;
 }
 
+// 16 consecutive fp32 accumulator columns of this warp's 32 TMEM lanes
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr));
+}
+
 // blockIdx.z = split of K: split z covers the 1024-wide groups
 // [z G / S, (z + 1) G / S) and, when S > 1, writes fp32 partial sums to
 // y + z M N (kOutF32).
-template <bool kBf16, bool kOutF32>
+// kSwiGLU: the weight is a fused gate+up of N = 2I rows (gate rows 0..I-1,
+// then up rows), and y is h = silu(g) * u, M x I fp32, with
+// silu(a) = a / (1 + e^-a) (the feed-forward block of "Speed, and where it
+// goes").  Tile x then covers gate rows [64 x, 64 x + 64) in its first 64
+// columns and the matching up rows in the other 64, so the epilogue holds
+// both factors of each output; no split.
+template <bool kBf16, bool kOutF32, bool kSwiGLU = false>
 __global__ void __launch_bounds__(kThreads, 2)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const uint8_t* __restrict__ wq,
                    const uint16_t* __restrict__ scales, void* __restrict__ y, int M, int N, int K,
                    int splits, int* status) {
+  static_assert(!kSwiGLU || kOutF32, "h is fp32");
   // No static shared variables: the dynamic window starts at offset 0, so the
   // declared 1024-byte alignment holds, and every access below stays a
   // shared-memory instruction (an address laundered through an integer
@@ -304,7 +322,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * (kSwiGLU ? BN / 2 : BN);
+  const int I = N / 2;  // kSwiGLU: gate rows, up rows, and the columns of h
   const int nblk = K / kBlockWeights;
   const int G = K / kRot, z = blockIdx.z;
   const int g_lo = (int)((long long)z * G / splits), g_hi = (int)((long long)(z + 1) * G / splits);
@@ -373,7 +392,13 @@ __global__ void __launch_bounds__(kThreads, 2)
   } else {
     // ---- B expansion: thread (row r, half h); slice 2 kb + h uses stage h ----------
     const int t = threadIdx.x - 32 * kExpWarp0, r = t & (BN - 1), h = t >> 7;  // h: warp-uniform
-    const int n = n0 + r < N ? n0 + r : N - 1;  // rows past N expand a valid row; never stored
+    int n;
+    if constexpr (kSwiGLU) {  // columns 0-63: gate rows n0.., 64-127: up rows I + n0..
+      const int i = n0 + (r & (BN / 2 - 1));
+      n = (r < BN / 2 ? 0 : I) + (i < I ? i : I - 1);  // past I: a valid row, never stored
+    } else {
+      n = n0 + r < N ? n0 + r : N - 1;  // rows past N expand a valid row; never stored
+    }
     ExpCtx c;
     c.row = wq + (size_t)n * nblk * kBlockBytes;
     c.srow = scales + (size_t)n * nblk;
@@ -400,6 +425,34 @@ __global__ void __launch_bounds__(kThreads, 2)
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const int q = warp & 3, mh = (warp - kExpWarp0) >> 2;
       const int row = m0 + mh * UM + 32 * q + lane;
+      if constexpr (kSwiGLU) {
+        const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(mh * BN);
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN / 2; c0 += 16) {
+          uint32_t g[16], u[16];
+          tmem_ld16(taddr + (uint32_t)c0, g);
+          tmem_ld16(taddr + (uint32_t)(BN / 2 + c0), u);
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+          if (row < M) {
+            float* out = static_cast<float*>(y) + (size_t)row * I + n0 + c0;
+            float hv[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float a = __uint_as_float(g[i]);
+              hv[i] = a / (1.0f + expf(-a)) * __uint_as_float(u[i]);
+            }
+            if (n0 + c0 + 16 <= I && (I & 3) == 0) {
+#pragma unroll
+              for (int i = 0; i < 16; i += 4)
+                *reinterpret_cast<float4*>(out + i) = make_float4(hv[i], hv[i + 1], hv[i + 2], hv[i + 3]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                if (n0 + c0 + i < I) out[i] = hv[i];
+            }
+          }
+        }
+      } else
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 32) {
         uint32_t v[32];
@@ -492,14 +545,17 @@ __global__ void __launch_bounds__(256) gemm_split_reduce_kernel(const float* __r
 }
 
 // ---- host side -------------------------------------------------------------------------
-template <bool kBf16, bool kOutF32>
+template <bool kBf16, bool kOutF32, bool kSwiGLU = false>
 cudaError_t launch_t(const CUtensorMap& ma, const uint8_t* wq, const uint16_t* scales, void* y,
                      int M, int N, int K, int splits, int* status, cudaStream_t st) {
-  auto kern = gemm_tc_kernel<kBf16, kOutF32>;
+  auto kern = gemm_tc_kernel<kBf16, kOutF32, kSwiGLU>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmemBytes);
   if (e != cudaSuccess) return e;
-  const dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM), (unsigned)splits);
+  const int cols = kSwiGLU ? BN / 2 : BN;  // output columns per tile
+  const int ncols = kSwiGLU ? N / 2 : N;
+  const dim3 grid((unsigned)((ncols + cols - 1) / cols), (unsigned)((M + BM - 1) / BM),
+                  (unsigned)splits);
   return launch_pdl(kern, grid, dim3(kThreads), (size_t)kSmemBytes, st, ma, wq, scales, y, M, N,
                     K, splits, status);
 }
@@ -565,6 +621,25 @@ cudaError_t launch_gemm_tc(const uint8_t* wq, const uint16_t* scales, const void
   if (bf) return launch_t<true, false>(ma, wq, scales, y, m, n, k, 1, status, st);
   if (f32) return launch_t<false, true>(ma, wq, scales, y, m, n, k, 1, status, st);
   return launch_t<false, false>(ma, wq, scales, y, m, n, k, 1, status, st);
+}
+
+cudaError_t launch_gemm_tc_swiglu(const uint8_t* wq, const uint16_t* scales, const void* x,
+                                  Act x_t, float* h, int64_t M, int64_t I, int64_t K,
+                                  cudaStream_t st) {
+  const int64_t N = 2 * I;
+  if (K % kRot != 0 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX ||
+      (M + BM - 1) / BM > 65535 || gemm_tc_splits(M, N, K) != 1)
+    return cudaErrorNotSupported;
+  cudaError_t e;
+  CUtensorMap ma;
+  if ((e = encode_tma_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT16, x, K, M, K * 2, BK, BM,
+                         CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+    return e;
+  int* status = device_status_ptr();
+  if (!status) return cudaErrorInvalidDevice;
+  const int m = (int)M, n = (int)N, k = (int)K;
+  return x_t == Act::BF16 ? launch_t<true, true, true>(ma, wq, scales, h, m, n, k, 1, status, st)
+                          : launch_t<false, true, true>(ma, wq, scales, h, m, n, k, 1, status, st);
 }
 
 }  // namespace ptq

@@ -101,6 +101,13 @@ cudaError_t launch_swiglu(const float* gu, float* h, int64_t M, int64_t I,
 cudaError_t launch_gemm_tc(const uint8_t* wq, const uint16_t* scales, const void* x, Act x_t,
                            void* y, Act y_t, int64_t M, int64_t N, int64_t K, void* ws,
                            size_t ws_bytes, cudaStream_t st);
+// The gate+up GEMM of the feed-forward block with SwiGLU in its epilogue:
+// wq/scales hold 2I rows (gate then up), h = silu(g) * u is M x I fp32.
+// cudaErrorNotSupported when the shape would be split along K (the caller
+// then runs the GEMM into fp32 and launch_swiglu).
+cudaError_t launch_gemm_tc_swiglu(const uint8_t* wq, const uint16_t* scales, const void* x,
+                                  Act x_t, float* h, int64_t M, int64_t I, int64_t K,
+                                  cudaStream_t st);
 // K splits of the tensor-core GEMM for a shape, and the fp32 partial-sum
 // scratch they need (0 when the product runs unsplit).
 int gemm_tc_splits(int64_t M, int64_t N, int64_t K);

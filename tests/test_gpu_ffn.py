@@ -58,6 +58,19 @@ def test_ffn_small(P, orc, syn, M, dtype):
     (Q.check_f32 if dtype == "f32" else Q.check_bf16)(y, ref, f"ffn small {M} {dtype}")
 
 
+@pytest.mark.parametrize("M", [70, 300])
+def test_ffn_prefill_swiglu_in_the_gemm_epilogue(P, orc, syn, M):
+    # I = 9216 gives 144 gate/up tiles: the GEMM runs unsplit, with SwiGLU in
+    # its epilogue (a tile pairs 64 gate rows with the matching 64 up rows);
+    # M = 70 leaves most of a row tile empty, M = 300 spans two
+    L = syn.ffn_layer(10, M, 1024, 9216)
+    x = syn.ffn_input(10, M, M, 1024, "bf16")
+    y = Q.host_f64(P.ffn(*device_layer(P, L), Q.dev_bf16(x)))
+    tokens = [0, 1, M // 2, M - 2, M - 1] + ([255, 256] if M > 256 else [])
+    ref = oracle_ffn(orc, P, L, Q.x_f64(x)[tokens])
+    Q.check_bf16(y[tokens], ref, f"ffn fused SwiGLU M={M}")
+
+
 def test_ffn_leaves_x_alone_and_rejects_small_workspace(P, syn):
     import torch
 
