@@ -61,6 +61,14 @@ def lib():
         for name in ("orc_fwht_def", "orc_fwht_fast"):
             getattr(L, name).argtypes = [_P, _P, _P, _I64, _I64]
             getattr(L, name).restype = None
+        L.orc_pq2_pack.argtypes = [_P, _P, _I64, _I64]
+        L.orc_pq2_pack.restype = ctypes.c_int
+        L.orc_pq2_unpack.argtypes = [_P, _P, _I64, _I64]
+        L.orc_pq2_unpack.restype = ctypes.c_int
+        L.orc_pq2_matmul.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64]
+        L.orc_pq2_matmul.restype = None
+        L.orc_pq2_matmul_rows.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _P, _I64]
+        L.orc_pq2_matmul_rows.restype = None
         L.orc_unrotate_def.argtypes = [_P, _P, _P, _I64, _I64]
         L.orc_unrotate_def.restype = None
         L.orc_embed.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64]
@@ -148,6 +156,49 @@ def unpack(wq: np.ndarray, K: int) -> np.ndarray:
     if lib().orc_unpack(_ptr(wq), _ptr(trits), N, K) != 0:
         raise ValueError("orc_unpack: K % 128 != 0")
     return trits
+
+
+def pq2_pack(trits: np.ndarray) -> np.ndarray:
+    """N x K int8 trits -> N x (K/128*32) uint8 PQ2_0 codes (raises on invalid input)."""
+    trits = _c(trits, np.int8)
+    N, K = trits.shape
+    wq = np.empty((N, (K // 128) * 32), np.uint8)
+    if lib().orc_pq2_pack(_ptr(trits), _ptr(wq), N, K) != 0:
+        raise ValueError("orc_pq2_pack: trit outside {-1,0,1} or K % 128 != 0")
+    return wq
+
+
+def pq2_unpack(wq: np.ndarray, K: int) -> np.ndarray:
+    wq = _c(wq, np.uint8)
+    N = wq.shape[0]
+    trits = np.empty((N, K), np.int8)
+    if lib().orc_pq2_unpack(_ptr(wq), _ptr(trits), N, K) != 0:
+        raise ValueError("orc_pq2_unpack: K % 128 != 0")
+    return trits
+
+
+def pq2_matmul(wq: np.ndarray, scales: np.ndarray, x: np.ndarray) -> np.ndarray:
+    """x (M x K float64) -> y (M x N float64), PQ2_0 weights."""
+    wq = _c(wq, np.uint8)
+    scales = _c(scales, np.uint16)
+    x = _c(x, np.float64)
+    M, K = x.shape
+    N = wq.shape[0]
+    y = np.empty((M, N), np.float64)
+    lib().orc_pq2_matmul(_ptr(wq), _ptr(scales), _ptr(x), _ptr(y), M, N, K)
+    return y
+
+
+def pq2_matmul_rows(wq, scales, x, rows) -> np.ndarray:
+    wq = _c(wq, np.uint8)
+    scales = _c(scales, np.uint16)
+    x = _c(x, np.float64)
+    rows = _c(np.asarray(rows, np.int64), np.int64)
+    M, K = x.shape
+    y = np.empty((M, rows.size), np.float64)
+    lib().orc_pq2_matmul_rows(_ptr(wq), _ptr(scales), _ptr(x), _ptr(y), M, wq.shape[0], K,
+                              _ptr(rows), rows.size)
+    return y
 
 
 def fwht_def(x: np.ndarray, signs: np.ndarray) -> np.ndarray:

@@ -19,7 +19,9 @@ enum {
   ORC_WEIGHTS_PER_BLOCK = 128, /* [P1] "What Bonsai is" */
   ORC_TRITS_PER_BYTE = 5,      /* [P1] "What Bonsai is" */
   ORC_BYTES_PER_BLOCK = 26,    /* ceil(128 / 5) */
-  ORC_ROT = 1024               /* [P1] "What Bonsai is": 1024-wide butterfly */
+  ORC_ROT = 1024,              /* [P1] "What Bonsai is": 1024-wide butterfly */
+  ORC_PQ2_PER_BYTE = 4,        /* [P2] "Level 2": 2 bits per weight */
+  ORC_PQ2_BYTES_PER_BLOCK = 32 /* 128 weights x 2 bits */
 };
 
 static int g_threads = 0; /* 0 = OpenMP default */
@@ -134,6 +136,33 @@ int orc_unpack(const uint8_t* wq, int8_t* trits, int64_t N, int64_t K) {
       }
     }
   }
+  return 0;
+}
+
+/* ---- PQ2_0: two bits per trit ------------------------------------------ */
+
+/* [P2] "Why I Am Building Another Inference Engine", "Level 2: The short
+   answer": each ternary weight in 2 bits plus one 16-bit scale per 128
+   weights.  Readings: code = trit + 1; weight 4j + i of a block sits in
+   byte j, bits 2i and 2i + 1; a block is 32 bytes; the decode is
+   trit = code - 1 for all four codes (an encoder never writes code 3). */
+int orc_pq2_pack(const int8_t* trits, uint8_t* wq, int64_t N, int64_t K) {
+  if (K % ORC_WEIGHTS_PER_BLOCK != 0 || N < 0) return -1;
+  for (int64_t i = 0; i < N * K; ++i)
+    if (trits[i] < -1 || trits[i] > 1) return -1;
+  for (int64_t i = 0; i < N * K / ORC_PQ2_PER_BYTE; ++i) {
+    int v = 0;
+    for (int k = 0; k < ORC_PQ2_PER_BYTE; ++k)
+      v |= (trits[ORC_PQ2_PER_BYTE * i + k] + 1) << (2 * k);
+    wq[i] = (uint8_t)v;
+  }
+  return 0;
+}
+
+int orc_pq2_unpack(const uint8_t* wq, int8_t* trits, int64_t N, int64_t K) {
+  if (K % ORC_WEIGHTS_PER_BLOCK != 0 || N < 0) return -1;
+  for (int64_t i = 0; i < N * K; ++i)
+    trits[i] = (int8_t)(((wq[i / ORC_PQ2_PER_BYTE] >> (2 * (i % ORC_PQ2_PER_BYTE))) & 3) - 1);
   return 0;
 }
 
@@ -268,13 +297,16 @@ int orc_embed_ptq1(const uint8_t* wq, const uint16_t* scales,
 
 /* ---- the block-scaled ternary matmul ------------------------------------ */
 
-/* One output row n for all M activation rows: peel the row, then
-   y[m] = sum_b s_b * (sum_i t_i x_i). */
+/* One output row n for all M activation rows: decode the row's trits (PTQ1_0
+   or PQ2_0), then y[m] = sum_b s_b * (sum_i t_i x_i). */
 static void matmul_row(const uint8_t* wq, const uint16_t* scales,
                        const double* x, double* out, int64_t out_stride,
-                       int64_t M, int64_t n, int64_t K, int8_t* trow) {
+                       int64_t M, int64_t n, int64_t K, int8_t* trow, int pq2) {
   int64_t nb = K / ORC_WEIGHTS_PER_BLOCK;
-  orc_unpack(wq + n * nb * ORC_BYTES_PER_BLOCK, trow, 1, K);
+  if (pq2)
+    orc_pq2_unpack(wq + n * nb * ORC_PQ2_BYTES_PER_BLOCK, trow, 1, K);
+  else
+    orc_unpack(wq + n * nb * ORC_BYTES_PER_BLOCK, trow, 1, K);
   for (int64_t m = 0; m < M; ++m) {
     const double* xm = x + m * K;
     double y = 0.0;
@@ -291,30 +323,54 @@ static void matmul_row(const uint8_t* wq, const uint16_t* scales,
   }
 }
 
-void orc_matmul(const uint8_t* wq, const uint16_t* scales, const double* x,
-                double* y, int64_t M, int64_t N, int64_t K) {
+static void matmul_fmt(const uint8_t* wq, const uint16_t* scales,
+                       const double* x, double* y, int64_t M, int64_t N,
+                       int64_t K, int pq2) {
 #pragma omp parallel
   {
     int8_t* trow = (int8_t*)malloc((size_t)K);
 #pragma omp for schedule(static)
     for (int64_t n = 0; n < N; ++n)
-      matmul_row(wq, scales, x, y + n, N, M, n, K, trow);
+      matmul_row(wq, scales, x, y + n, N, M, n, K, trow, pq2);
     free(trow);
   }
+}
+
+static void matmul_rows_fmt(const uint8_t* wq, const uint16_t* scales,
+                            const double* x, double* y, int64_t M, int64_t K,
+                            const int64_t* rows, int64_t nrows, int pq2) {
+#pragma omp parallel
+  {
+    int8_t* trow = (int8_t*)malloc((size_t)K);
+#pragma omp for schedule(static)
+    for (int64_t r = 0; r < nrows; ++r)
+      matmul_row(wq, scales, x, y + r, nrows, M, rows[r], K, trow, pq2);
+    free(trow);
+  }
+}
+
+void orc_matmul(const uint8_t* wq, const uint16_t* scales, const double* x,
+                double* y, int64_t M, int64_t N, int64_t K) {
+  matmul_fmt(wq, scales, x, y, M, N, K, 0);
 }
 
 void orc_matmul_rows(const uint8_t* wq, const uint16_t* scales,
                      const double* x, double* y, int64_t M, int64_t N,
                      int64_t K, const int64_t* rows, int64_t nrows) {
   (void)N;
-#pragma omp parallel
-  {
-    int8_t* trow = (int8_t*)malloc((size_t)K);
-#pragma omp for schedule(static)
-    for (int64_t r = 0; r < nrows; ++r)
-      matmul_row(wq, scales, x, y + r, nrows, M, rows[r], K, trow);
-    free(trow);
-  }
+  matmul_rows_fmt(wq, scales, x, y, M, K, rows, nrows, 0);
+}
+
+void orc_pq2_matmul(const uint8_t* wq, const uint16_t* scales, const double* x,
+                    double* y, int64_t M, int64_t N, int64_t K) {
+  matmul_fmt(wq, scales, x, y, M, N, K, 1);
+}
+
+void orc_pq2_matmul_rows(const uint8_t* wq, const uint16_t* scales,
+                         const double* x, double* y, int64_t M, int64_t N,
+                         int64_t K, const int64_t* rows, int64_t nrows) {
+  (void)N;
+  matmul_rows_fmt(wq, scales, x, y, M, K, rows, nrows, 1);
 }
 
 /* ---- SwiGLU and the feed-forward block ---------------------------------- */

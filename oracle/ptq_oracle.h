@@ -18,6 +18,9 @@
  *          floor(3^(n+1) u) - 3 floor(3^n u) with u = byte/256.
  *        - "Speed, and where it goes": the feed-forward block is rotate,
  *          gate (+ up), SwiGLU, rotate, down.
+ *   [P2] "Why I Am Building Another Inference Engine"
+ *        - "Level 2: The short answer": PQ2_0 stores each ternary weight in
+ *          2 bits plus one 16-bit scale per 128 weights (2.125 bits/weight).
  *   The encode rule (digit = trit + 1, v = sum d_i 3^(4-i),
  *   byte = ceil(256 v / 243), last byte of a block holds 3 trits padded with
  *   digit 1) is the workload definition of the tiny PTQ1_0 matvec case.
@@ -30,6 +33,9 @@
  *     the sign vector has one entry per element (block b uses its own 1024);
  *   - the gate/up weight of the fused feed-forward block stacks the gate rows
  *     (0..I-1) above the up rows (I..2I-1); h = silu(gate) * up;
+ *   - PQ2_0: code = trit + 1; weight 4j + i of a block is bits 2i, 2i + 1
+ *     of byte j; 32 bytes per block; decode trit = code - 1 for all four
+ *     codes (no encoder writes code 3);
  *   - the embedding table is stored rotated like the weights (row v holds
  *     R e_v), so a lookup returns R^T of the stored row; an id outside the
  *     table gives a row of NaN.
@@ -71,6 +77,11 @@ int orc_pack(const int8_t* trits, uint8_t* wq, int64_t N, int64_t K);
    Returns 0, or -1 if K % 128 != 0. */
 int orc_unpack(const uint8_t* wq, int8_t* trits, int64_t N, int64_t K);
 
+/* PQ2_0 codec: N x K trits <-> N x (K/128) x 32 bytes.  Return 0, or -1 on
+   a trit outside {-1,0,1} (pack) or K % 128 != 0. */
+int orc_pq2_pack(const int8_t* trits, uint8_t* wq, int64_t N, int64_t K);
+int orc_pq2_unpack(const uint8_t* wq, int8_t* trits, int64_t N, int64_t K);
+
 /* Signed rotation, the definition: for every row m and 1024-block b,
    y_j = (1/32) sum_i (-1)^popcount(i&j) s_i x_i.  O(1024^2) per block.
    x and y are M x K row-major; y may not alias x. */
@@ -111,6 +122,14 @@ void orc_matmul(const uint8_t* wq, const uint16_t* scales, const double* x,
 void orc_matmul_rows(const uint8_t* wq, const uint16_t* scales,
                      const double* x, double* y, int64_t M, int64_t N,
                      int64_t K, const int64_t* rows, int64_t nrows);
+
+/* The block-scaled ternary matmul over PQ2_0 weights (the same definition,
+   trits decoded from 2-bit codes), and the same for listed rows. */
+void orc_pq2_matmul(const uint8_t* wq, const uint16_t* scales, const double* x,
+                    double* y, int64_t M, int64_t N, int64_t K);
+void orc_pq2_matmul_rows(const uint8_t* wq, const uint16_t* scales,
+                         const double* x, double* y, int64_t M, int64_t N,
+                         int64_t K, const int64_t* rows, int64_t nrows);
 
 /* h = silu(g) * u, silu(a) = a / (1 + exp(-a)). */
 void orc_swiglu(const double* g, const double* u, double* h, int64_t n);

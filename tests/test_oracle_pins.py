@@ -102,6 +102,71 @@ def test_geometry_matches_pages(orc):
     assert abs(gib - float(g["model_gb_on_disk"])) < 0.05
 
 
+# ---- PQ2_0 ------------------------------------------------------------------
+
+def test_pq2_geometry_matches_pages(orc):
+    g = {k: v for k, v in read_golden("pq2_geometry.txt")}
+    block = int(g["weights_per_block"])
+    K = 4 * block
+    wq = orc.pq2_pack(np.zeros((3, K), np.int8))
+    bytes_per_block = wq.shape[1] // (K // block)
+    assert bytes_per_block * 8 == block * int(g["bits_per_code"])
+    bits = (bytes_per_block * 8 + int(g["scale_bits"])) / block
+    assert bits == float(g["bits_per_weight"])
+    # 27e9 weights at 2.125 bits: 7.17e9 bytes, "7.2 GB"; 16 bits: 54 GB
+    assert abs(float(g["model_params"]) * bits / 8 / 1e9 - float(g["model_gb"])) < 0.05
+    assert float(g["model_params"]) * 16 / 8 / 1e9 == float(g["model_gb_16bit"])
+
+
+def test_pq2_fields_are_independent(orc):
+    # changing one weight changes one 2-bit field of one byte, and a byte's
+    # four fields are its four weights in order
+    rng = np.random.default_rng(30)
+    t = rng.integers(-1, 2, size=(2, 256)).astype(np.int8)
+    w0 = orc.pq2_pack(t)
+    for k in (0, 1, 3, 4, 127, 128, 255):
+        t2 = t.copy()
+        t2[1, k] = (t2[1, k] + 2) % 3 - 1
+        diff = np.argwhere(orc.pq2_pack(t2) != w0)
+        assert diff.tolist() == [[1, k // 4]]
+        bits = int(orc.pq2_pack(t2)[1, k // 4]) ^ int(w0[1, k // 4])
+        assert bits & ~(3 << (2 * (k % 4))) == 0
+    np.testing.assert_array_equal(orc.pq2_unpack(w0, 256), t)
+
+
+def test_pq2_decode_of_every_byte(orc):
+    # 256 bytes x 4 fields: exactly 81 = 3^4 bytes decode to four trits, the
+    # rest hold at least one code 3, which decodes to +2
+    codes = np.arange(256, dtype=np.uint8).reshape(8, 32)  # 8 one-block rows
+    allb = orc.pq2_unpack(codes, 128).reshape(256, 4)      # byte b -> its 4 weights
+    assert set(np.unique(allb).tolist()) == {-1, 0, 1, 2}
+    assert int((allb <= 1).all(axis=1).sum()) == 81
+    # byte 0b11100100 holds codes 0, 1, 2, 3 from the low bits up
+    np.testing.assert_array_equal(allb[0b11100100], [-1, 0, 1, 2])
+
+
+def test_pq2_matmul_brute_force(orc):
+    # against a dense product built from the trits and scales directly
+    rng = np.random.default_rng(31)
+    N, K, M = 6, 512, 3
+    t = rng.integers(-1, 2, size=(N, K)).astype(np.int8)
+    sbits = (np.abs(rng.standard_normal((N, K // 128))) * 0.02).astype(np.float16).view(np.uint16)
+    x = rng.standard_normal((M, K))
+    W = t * np.repeat(_f16(sbits), 128, axis=1)
+    y = orc.pq2_matmul(orc.pq2_pack(t), sbits, x)
+    np.testing.assert_allclose(y, x @ W.T, rtol=1e-12, atol=1e-12)
+    rows = [5, 0, 3]
+    np.testing.assert_allclose(orc.pq2_matmul_rows(orc.pq2_pack(t), sbits, x, rows), (x @ W.T)[:, rows],
+                               rtol=1e-12, atol=1e-12)
+
+
+def test_pq2_pack_refuses_invalid(orc):
+    with pytest.raises(ValueError):
+        orc.pq2_pack(np.full((1, 128), 2, np.int8))
+    with pytest.raises(ValueError):
+        orc.pq2_pack(np.zeros((1, 100), np.int8))
+
+
 # ---- storage decodes -------------------------------------------------------
 
 def test_half_decode_all_patterns(orc):
