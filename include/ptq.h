@@ -209,6 +209,42 @@ PTQ_API PTQ_NODISCARD ptq_status ptq_ffn_noalloc(
     const void* x, void* y, int64_t M, int64_t H, int64_t I, ptq_dtype dtype,
     ptq_stream_t stream);
 
+/* ---- PQ2_0 ("Why I Am Building Another Inference Engine", section
+ * "Level 2: The short answer"): each ternary weight in 2 bits plus one
+ * 16-bit scale per 128 weights, 2.125 bits per weight.  The page fixes only
+ * that much; this library reads it as:
+ *   wq     uint8  N x (K/128) x 32: weight 4j + i of a block is bits 2i and
+ *                 2i + 1 of its byte j, code = trit + 1; the decode is
+ *                 trit = code - 1 for all four codes (no encoder writes 3,
+ *                 which therefore decodes to +2);
+ *   scales uint16 N x (K/128) binary16 patterns, as for PTQ1_0.
+ * The rotation, x and y are as for PTQ1_0. */
+
+/* ptq2_pack -- host-side PQ2_0 encoder.  Errors as ptq1_pack. */
+PTQ_API PTQ_NODISCARD ptq_status ptq2_pack(const int8_t* trits, uint8_t* wq,
+                                           int64_t N, int64_t K);
+
+/* ptq2_unpack -- device decode of PQ2_0 codes into N x K int8 trits
+ * (bit-exact test export).  trits 4-byte aligned.  Errors as ptq1_unpack,
+ * plus PTQ_ERR_ALIGN. */
+PTQ_API PTQ_NODISCARD ptq_status ptq2_unpack(const uint8_t* wq, int8_t* trits,
+                                             int64_t N, int64_t K,
+                                             ptq_stream_t stream);
+
+/* ptq_matmul_pq2_workspace_bytes -- scratch ptq_matmul_pq2 needs (or, for
+ * the bf16 GEMM, can use for K splits); 0 for invalid arguments or none. */
+PTQ_API size_t ptq_matmul_pq2_workspace_bytes(int64_t M, int64_t N,
+                                              int64_t K, ptq_dtype dtype);
+
+/* ptq_matmul_pq2 -- ptq_matmul over PQ2_0 weights: the same definition
+ * (y = x W^T with W = trit x block scale), dtype routing and workspace rules.
+ * Both routes use the TMA-fed kernels, so K % 1024 == 0 is required
+ * (otherwise PTQ_ERR_UNSUPPORTED); every other error as ptq_matmul. */
+PTQ_API PTQ_NODISCARD ptq_status ptq_matmul_pq2(
+    const uint8_t* wq, const uint16_t* scales, const void* x, void* y,
+    int64_t M, int64_t N, int64_t K, ptq_dtype dtype, void* workspace,
+    size_t workspace_bytes, ptq_stream_t stream);
+
 /* ptq_embed -- token-embedding lookup on a rotated table.
  * "What Bonsai is": the rotation folded into the weights is undone on the
  * embedding table after each lookup.  Row v of the table holds R e_v, with R

@@ -28,7 +28,9 @@ STATUS = {
 # Every symbol include/ptq.h declares.
 EXPORTS = ("ptq1_pack", "ptq1_unpack", "ptq_fwht", "ptq_matmul_workspace_bytes", "ptq_matmul",
            "ptq_rotate_matmul_workspace_bytes", "ptq_rotate_matmul", "ptq_ffn_workspace_bytes",
-           "ptq_ffn", "ptq_ffn_noalloc", "ptq_embed", "ptq_embed_ptq1", "ptq_route",
+           "ptq_ffn", "ptq_ffn_noalloc", "ptq2_pack", "ptq2_unpack",
+           "ptq_matmul_pq2_workspace_bytes", "ptq_matmul_pq2", "ptq_embed", "ptq_embed_ptq1",
+           "ptq_route",
            "ptq_device_check", "ptq_status_str", "ptq_last_error")
 
 # Size of the built-in scratch array behind ptq_ffn_noalloc (include/ptq.h).
@@ -71,6 +73,11 @@ def load(path: str | None = None):
     L.ptq_ffn_workspace_bytes.restype = ctypes.c_size_t
     L.ptq_ffn.argtypes = [_P] * 8 + [_I64, _I64, _I64, _I32, _P, ctypes.c_size_t, _P]
     L.ptq_ffn_noalloc.argtypes = [_P] * 8 + [_I64, _I64, _I64, _I32, _P]
+    L.ptq2_pack.argtypes = [_P, _P, _I64, _I64]
+    L.ptq2_unpack.argtypes = [_P, _P, _I64, _I64, _P]
+    L.ptq_matmul_pq2_workspace_bytes.argtypes = [_I64, _I64, _I64, _I32]
+    L.ptq_matmul_pq2_workspace_bytes.restype = ctypes.c_size_t
+    L.ptq_matmul_pq2.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, ctypes.c_size_t, _P]
     L.ptq_embed.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _P]
     L.ptq_embed_ptq1.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _P]
     L.ptq_route.argtypes = [_I64, _I32, ctypes.POINTER(ctypes.c_char_p)]
@@ -80,7 +87,8 @@ def load(path: str | None = None):
     L.ptq_last_error.argtypes = []
     L.ptq_last_error.restype = ctypes.c_char_p
     for name in ("ptq1_pack", "ptq1_unpack", "ptq_fwht", "ptq_matmul", "ptq_rotate_matmul", "ptq_ffn",
-                 "ptq_ffn_noalloc", "ptq_embed", "ptq_embed_ptq1", "ptq_route", "ptq_device_check"):
+                 "ptq_ffn_noalloc", "ptq2_pack", "ptq2_unpack", "ptq_matmul_pq2", "ptq_embed",
+                 "ptq_embed_ptq1", "ptq_route", "ptq_device_check"):
         getattr(L, name).restype = _I32
     _lib = L
     return L
@@ -180,6 +188,51 @@ def matmul(wq, scales, x, out=None, workspace=None, stream=None):
     _check(load().ptq_matmul(_dev(wq, torch.uint8, "wq"), _dev(scales, torch.int16, "scales"),
                              _dev(x, None, "x"), _dev(y, x.dtype, "out"), M, N, K, dt, ws,
                              ws_bytes, _stream(stream)), "ptq_matmul")
+    return y
+
+
+def pq2_pack(trits: np.ndarray) -> np.ndarray:
+    """ptq2_pack: N x K int8 trits -> N x (K/128*32) uint8 PQ2_0 codes (host)."""
+    trits = np.ascontiguousarray(trits, dtype=np.int8)
+    if trits.ndim != 2:
+        raise ValueError("trits must be 2-D")
+    N, K = trits.shape
+    out = np.empty((N, K // 4 if K % 128 == 0 else 0), np.uint8)
+    _check(load().ptq2_pack(ctypes.c_void_p(trits.ctypes.data), ctypes.c_void_p(out.ctypes.data),
+                            N, K), "ptq2_pack")
+    return out
+
+
+def pq2_unpack(wq, K: int, stream=None):
+    import torch
+
+    N = wq.shape[0]
+    out = torch.empty((N, K), dtype=torch.int8, device=wq.device)
+    _check(load().ptq2_unpack(_dev(wq, torch.uint8, "wq"), _dev(out), N, K, _stream(stream)),
+           "ptq2_unpack")
+    return out
+
+
+def matmul_pq2_workspace_bytes(M: int, N: int, K: int, dtype: int) -> int:
+    return int(load().ptq_matmul_pq2_workspace_bytes(M, N, K, dtype))
+
+
+def matmul_pq2(wq, scales, x, out=None, workspace=None, stream=None):
+    """y = x W^T over PQ2_0 weights (ptq_matmul_pq2); as matmul otherwise."""
+    import torch
+
+    M, K = x.shape
+    N = wq.shape[0]
+    dt = _act_dtype(x)
+    y = torch.empty((M, N), dtype=x.dtype, device=x.device) if out is None else out
+    need = matmul_pq2_workspace_bytes(M, N, K, dt)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    ws = _dev(workspace, None, "workspace") if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load().ptq_matmul_pq2(_dev(wq, torch.uint8, "wq"), _dev(scales, torch.int16, "scales"),
+                                 _dev(x, None, "x"), _dev(y, x.dtype, "out"), M, N, K, dt, ws,
+                                 ws_bytes, _stream(stream)), "ptq_matmul_pq2")
     return y
 
 

@@ -327,6 +327,94 @@ PTQ_API ptq_status ptq_matmul(const uint8_t* wq, const uint16_t* scales, const v
   return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq_matmul launch");
 }
 
+// ---- PQ2_0 ----------------------------------------------------------------
+// "Why I Am Building Another Inference Engine", section "Level 2: The short
+// answer": two bits per ternary weight plus one 16-bit scale per 128
+// weights.  Same routing as PTQ1_0 (fp32 M <= 8: the table-lookup GEMV,
+// bf16: the tensor-core GEMM), both on the TMA-fed paths, so K % 1024 == 0.
+
+PTQ_API ptq_status ptq2_pack(const int8_t* trits, uint8_t* wq, int64_t N, int64_t K) {
+  t_msg[0] = 0;
+  if (N < 0 || K <= 0 || K % kBlockWeights != 0)
+    return fail(PTQ_ERR_SHAPE, "ptq2_pack: need N >= 0, K > 0, K %% 128 == 0 (N=%lld K=%lld)",
+                (long long)N, (long long)K);
+  int64_t total;
+  if (!mul_ok(N, K, &total)) return fail(PTQ_ERR_SHAPE, "ptq2_pack: N*K overflows");
+  if (total == 0) return PTQ_OK;
+  if (!trits || !wq) return fail(PTQ_ERR_NULL, "ptq2_pack: NULL pointer");
+  for (int64_t i = 0; i < total; ++i)
+    if (trits[i] < -1 || trits[i] > 1)
+      return fail(PTQ_ERR_VALUE, "ptq2_pack: trit %d at index %lld is not in {-1,0,1}",
+                  (int)trits[i], (long long)i);
+  for (int64_t i = 0; i < total / 4; ++i) {  // weight 4j + k: bits 2k, 2k+1 of byte j
+    uint32_t v = 0;
+    for (int k = 0; k < 4; ++k) v |= (uint32_t)(trits[4 * i + k] + 1) << (2 * k);
+    wq[i] = static_cast<uint8_t>(v);
+  }
+  return PTQ_OK;
+}
+
+PTQ_API ptq_status ptq2_unpack(const uint8_t* wq, int8_t* trits, int64_t N, int64_t K,
+                               ptq_stream_t stream) {
+  t_msg[0] = 0;
+  int64_t total;
+  if (N < 0 || K <= 0 || K % kBlockWeights != 0 || !mul_ok(N, K, &total))
+    return fail(PTQ_ERR_SHAPE, "ptq2_unpack: bad shape N=%lld K=%lld", (long long)N,
+                (long long)K);
+  if (total == 0) return PTQ_OK;
+  if (!wq || !trits) return fail(PTQ_ERR_NULL, "ptq2_unpack: NULL pointer");
+  if (!aligned(trits, 4)) return fail(PTQ_ERR_ALIGN, "ptq2_unpack: trits need 4-byte alignment");
+  cudaError_t e = launch_unpack_pq2(wq, trits, N, K, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq2_unpack launch");
+}
+
+static size_t matmul_pq2_ws_bytes(int64_t M, int64_t N, int64_t K, ptq_dtype dt) {
+  if (dt == PTQ_F32) return (M >= 1 && M <= 8) ? gemv_lut_pq2_workspace_bytes(N, K) : 0;
+  return gemm_tc_workspace_bytes(M, N, K);
+}
+
+PTQ_API size_t ptq_matmul_pq2_workspace_bytes(int64_t M, int64_t N, int64_t K, ptq_dtype dtype) {
+  int64_t t;
+  if (!dtype_ok(dtype) || M < 0 || N < 0 || K <= 0 || K % kRot != 0 || !mul_ok(N, K, &t) ||
+      !mul_ok(M, N, &t) || !mul_ok(t, 4, &t))
+    return 0;
+  return matmul_pq2_ws_bytes(M, N, K, dtype);
+}
+
+PTQ_API ptq_status ptq_matmul_pq2(const uint8_t* wq, const uint16_t* scales, const void* x,
+                                  void* y, int64_t M, int64_t N, int64_t K, ptq_dtype dtype,
+                                  void* ws, size_t ws_bytes, ptq_stream_t stream) {
+  t_msg[0] = 0;
+  const char* who = "ptq_matmul_pq2";
+  const Route* r = nullptr;
+  ptq_status s = check_matmul(wq, scales, x, y, M, N, K, dtype, who, &r);
+  if (s != PTQ_OK || M == 0 || N == 0) return s;
+  if (K % kRot != 0)
+    return fail(PTQ_ERR_UNSUPPORTED, "%s: PQ2_0 is served for K %% 1024 == 0 only (K=%lld)", who,
+                (long long)K);
+  const size_t need = matmul_pq2_ws_bytes(M, N, K, dtype);
+  const bool required = dtype == PTQ_F32 && need > 0;
+  if (required && !ws)
+    return fail(PTQ_ERR_WORKSPACE, "%s: workspace is NULL (%zu bytes needed)", who, need);
+  if (required && ws_bytes < need)
+    return fail(PTQ_ERR_WORKSPACE, "%s: workspace has %zu bytes, %zu needed", who, ws_bytes, need);
+  if (ws && !aligned(ws, 16))
+    return fail(PTQ_ERR_ALIGN, "%s: workspace needs 16-byte alignment", who);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (r->kernel == Kernel::GemvF32) {  // one token at a time, as for PTQ1_0
+    for (int64_t m = 0; m < M && e == cudaSuccess; ++m)
+      e = launch_gemv_lut_pq2(wq, scales, static_cast<const float*>(x) + m * K, nullptr,
+                              static_cast<float*>(y) + m * N, static_cast<float*>(ws), N, K, st);
+  } else {
+    e = launch_gemm_tc_pq2(wq, scales, x, y, M, N, K, ws, ws ? ws_bytes : 0, st);
+  }
+  if (e == cudaErrorNotSupported)
+    return fail(PTQ_ERR_UNSUPPORTED, "%s: shape N=%lld K=%lld not served for PQ2_0", who,
+                (long long)N, (long long)K);
+  return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq_matmul_pq2 launch");
+}
+
 // ---- rotate + matmul ------------------------------------------------------
 // Workspace: [matmul scratch | R x (M x K of dtype), used when the rotation
 // runs as its own kernel], each rounded up to 256 bytes.

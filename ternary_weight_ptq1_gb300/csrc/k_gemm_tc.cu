@@ -230,6 +230,44 @@ __device__ __forceinline__ void load_block(const uint8_t* row, const uint16_t* s
   sc = s;
 }
 
+// PQ2_0 (two bits a weight, 32 bytes a block): half h of block kb of a row is
+// the 16 aligned bytes at 32 kb + 16 h -- one 16-byte load -- and weight
+// 4j + i of the half is bits 2i, 2i+1 of its byte j.
+__device__ __forceinline__ void load_half_pq2(const uint8_t* row, const uint16_t* srow, int kb,
+                                              int h, uint32_t (&win)[4], uint32_t& sc) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(row + 32 * kb + 16 * h));
+  win[0] = v.x; win[1] = v.y; win[2] = v.z; win[3] = v.w;
+  unsigned short s;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(s) : "l"(srow + kb));
+  sc = s;
+}
+
+// The 64 weights of a PQ2_0 half-block as 32 output words.  Nibble k of the
+// half holds the codes (ca, cb) of weights 2k, 2k+1, and the pair's selector
+// over the sources {-s, 0, +s, +2s} is 34 (ca + 256 cb) + 0x1010, where
+// ca + 256 cb = n + 63 (n & 12) for the nibble n = ca + 4 cb.  (Code 3, which
+// no encoder writes, decodes as trit + 2 like every other code: c - 1.)
+__device__ __forceinline__ void expand_half_pq2(const uint32_t (&win)[4], uint32_t ta, uint32_t tb,
+                                                uint32_t bslice, int r) {
+  uint32_t out[32];
+#pragma unroll
+  for (int w = 0; w < 4; ++w)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t m = win[w] >> (4 * i);
+      const uint32_t n = m & 15u;
+      out[8 * w + i] = __byte_perm(ta, tb, 34u * (n + 63u * (m & 12u)) + 0x1010u);
+    }
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(bslice + sw128_off(r, 8 * c)),
+                 "r"(out[4 * c]), "r"(out[4 * c + 1]), "r"(out[4 * c + 2]), "r"(out[4 * c + 3])
+                 : "memory");
+}
+
 struct ExpCtx {
   const uint8_t* row;     // this thread's packed row
   const uint16_t* srow;   // its scales
@@ -261,6 +299,48 @@ __device__ __forceinline__ bool expand_step(const ExpCtx& c, int g, uint32_t (&w
   // every writer makes its stores visible to the tensor core's (async) proxy
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   mbar_arrive(c.b_full);
+  return true;
+}
+
+// PQ2_0: block kb of this thread's half, with half-blocks kb + 1, kb + 2
+// prefetched into ring slots (q + 1) % 4, (q + 2) % 4.
+template <bool kBf16, int h, int q>
+__device__ __forceinline__ bool expand_step_pq2(const ExpCtx& c, int g, uint32_t (&win)[4][4],
+                                                uint32_t (&sc)[4]) {
+  const int kb = 8 * g + q;
+  const int lb = kb - 8 * c.g_lo;
+  if (kb + 2 < c.nblk) load_half_pq2(c.row, c.srow, kb + 2, h, win[(q + 2) % 4], sc[(q + 2) % 4]);
+  uint32_t s16 = sc[q % 4];
+  float sf = __half2float(__ushort_as_half((unsigned short)s16));
+  if constexpr (kBf16) {  // the fp16 scale rounded to nearest-even bf16
+    s16 = __bfloat16_as_ushort(__float2bfloat16_rn(sf));
+    sf = __uint_as_float(s16 << 16);
+  }
+  const uint32_t s2 = kBf16 ? (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(2.0f * sf))
+                            : (uint32_t)__half_as_ushort(__float2half_rn(2.0f * sf));
+  const uint32_t ta = (s16 ^ 0x8000u), tb = s16 | (s2 << 16);
+  if (lb > 0 && !mbar_wait(c.empty, (lb - 1) & 1, c.abort_flag)) return false;
+  expand_half_pq2(win[q % 4], ta, tb, c.bbase, c.r);
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  mbar_arrive(c.b_full);
+  return true;
+}
+
+template <bool kBf16, int h>
+__device__ bool expand_all_pq2(const ExpCtx& c) {
+  uint32_t win[4][4], sc[4];
+  load_half_pq2(c.row, c.srow, 8 * c.g_lo, h, win[0], sc[0]);
+  load_half_pq2(c.row, c.srow, 8 * c.g_lo + 1, h, win[1], sc[1]);
+  for (int g = c.g_lo; 8 * g < c.nblk; ++g) {
+    if (!expand_step_pq2<kBf16, h, 0>(c, g, win, sc)) return false;
+    if (!expand_step_pq2<kBf16, h, 1>(c, g, win, sc)) return false;
+    if (!expand_step_pq2<kBf16, h, 2>(c, g, win, sc)) return false;
+    if (!expand_step_pq2<kBf16, h, 3>(c, g, win, sc)) return false;
+    if (!expand_step_pq2<kBf16, h, 4>(c, g, win, sc)) return false;
+    if (!expand_step_pq2<kBf16, h, 5>(c, g, win, sc)) return false;
+    if (!expand_step_pq2<kBf16, h, 6>(c, g, win, sc)) return false;
+    if (!expand_step_pq2<kBf16, h, 7>(c, g, win, sc)) return false;
+  }
   return true;
 }
 
@@ -302,7 +382,8 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
 // goes").  Tile x then covers gate rows [64 x, 64 x + 64) in its first 64
 // columns and the matching up rows in the other 64, so the epilogue holds
 // both factors of each output; no split.
-template <bool kBf16, bool kOutF32, bool kSwiGLU = false>
+// kPQ2: the weights are PQ2_0 (2-bit codes, 32 bytes a block).
+template <bool kBf16, bool kOutF32, bool kSwiGLU = false, bool kPQ2 = false>
 __global__ void __launch_bounds__(kThreads, 2)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const uint8_t* __restrict__ wq,
                    const uint16_t* __restrict__ scales, void* __restrict__ y, int M, int N, int K,
@@ -400,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       n = n0 + r < N ? n0 + r : N - 1;  // rows past N expand a valid row; never stored
     }
     ExpCtx c;
-    c.row = wq + (size_t)n * nblk * kBlockBytes;
+    c.row = wq + (size_t)n * nblk * (kPQ2 ? 32 : kBlockBytes);
     c.srow = scales + (size_t)n * nblk;
     c.g_lo = g_lo;
     c.nblk = g_hi * kGroupBlocks;
@@ -409,7 +490,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     c.b_full = &b_full[h];
     c.r = r;
     c.abort_flag = abort_flag;
-    ok = h == 0 ? expand_all<kBf16, 0>(c) : expand_all<kBf16, 1>(c);
+    if constexpr (kPQ2)
+      ok = h == 0 ? expand_all_pq2<kBf16, 0>(c) : expand_all_pq2<kBf16, 1>(c);
+    else
+      ok = h == 0 ? expand_all<kBf16, 0>(c) : expand_all<kBf16, 1>(c);
   }
   if (!ok) {
     *abort_flag = 1;
@@ -545,10 +629,10 @@ __global__ void __launch_bounds__(256) gemm_split_reduce_kernel(const float* __r
 }
 
 // ---- host side -------------------------------------------------------------------------
-template <bool kBf16, bool kOutF32, bool kSwiGLU = false>
+template <bool kBf16, bool kOutF32, bool kSwiGLU = false, bool kPQ2 = false>
 cudaError_t launch_t(const CUtensorMap& ma, const uint8_t* wq, const uint16_t* scales, void* y,
                      int M, int N, int K, int splits, int* status, cudaStream_t st) {
-  auto kern = gemm_tc_kernel<kBf16, kOutF32, kSwiGLU>;
+  auto kern = gemm_tc_kernel<kBf16, kOutF32, kSwiGLU, kPQ2>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -621,6 +705,35 @@ cudaError_t launch_gemm_tc(const uint8_t* wq, const uint16_t* scales, const void
   if (bf) return launch_t<true, false>(ma, wq, scales, y, m, n, k, 1, status, st);
   if (f32) return launch_t<false, true>(ma, wq, scales, y, m, n, k, 1, status, st);
   return launch_t<false, false>(ma, wq, scales, y, m, n, k, 1, status, st);
+}
+
+// The GEMM over PQ2_0 weights: x bf16, y bf16 (K % 1024 == 0).
+cudaError_t launch_gemm_tc_pq2(const uint8_t* wq, const uint16_t* scales, const void* x, void* y,
+                               int64_t M, int64_t N, int64_t K, void* ws, size_t ws_bytes,
+                               cudaStream_t st) {
+  if (K % kRot != 0 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX ||
+      (M + BM - 1) / BM > 65535)
+    return cudaErrorNotSupported;
+  cudaError_t e;
+  CUtensorMap ma;
+  if ((e = encode_tma_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT16, x, K, M, K * 2, BK, BM,
+                         CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+    return e;
+  int* status = device_status_ptr();
+  if (!status) return cudaErrorInvalidDevice;
+  const int m = (int)M, n = (int)N, k = (int)K;
+  int splits = gemm_tc_splits(M, N, K);
+  const size_t per = (size_t)M * (size_t)N * 4;
+  if (splits > 1 && (ws == nullptr || ws_bytes / per < 2)) splits = 1;
+  if (splits > 1 && ws_bytes / per < (size_t)splits) splits = (int)(ws_bytes / per);
+  if (splits > 1) {
+    e = launch_t<true, true, false, true>(ma, wq, scales, ws, m, n, k, splits, status, st);
+    if (e != cudaSuccess) return e;
+    const size_t mn = (size_t)M * (size_t)N;
+    return launch_pdl(gemm_split_reduce_kernel<false>, dim3((unsigned)((mn + 255) / 256)),
+                      dim3(256), 0, st, (const float*)ws, y, mn, splits);
+  }
+  return launch_t<true, false, false, true>(ma, wq, scales, y, m, n, k, 1, status, st);
 }
 
 cudaError_t launch_gemm_tc_swiglu(const uint8_t* wq, const uint16_t* scales, const void* x,

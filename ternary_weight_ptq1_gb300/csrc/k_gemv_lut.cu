@@ -171,6 +171,20 @@ __device__ __forceinline__ void build_entries(const float (&A)[9], const float (
   }
 }
 
+// Entries e = 64 R .. 64 R + 63 of one PQ2_0 table: a byte holds four 2-bit
+// codes, weights 4q..4q+3 from the low bits up, so T[e] = Lo[e & 15] +
+// Hi[e >> 4] with Lo / Hi the sums over the low / high two codes.
+template <int R>
+__device__ __forceinline__ void build_entries_pq2(const float (&Lo)[16], const float (&Hi)[16],
+                                                  uint32_t dst) {
+#pragma unroll
+  for (int i = 0; i < 64; ++i) {
+    constexpr int e0 = 64 * R;
+    const int e = e0 + i;
+    sts_f32(dst + 256u * (uint32_t)e, Lo[e & 15] + Hi[e >> 4]);
+  }
+}
+
 // The signed rotation of one 1024-block of x by the 256 threads of 8 warps
 // (g8: thread index within them), written to xs_blk (1024 floats):
 //   xs_blk[j] = (1/32) sum_i (-1)^popcount(i & j) s[i] x[i]
@@ -227,11 +241,14 @@ __device__ __forceinline__ void rotate_block(const float* __restrict__ x, const 
 // The activations a chunk (words [ws, we) of every row) touches, rotated
 // first when `signs` is given, staged at `xs`; then the lane tables.  All
 // threads of the CTA take part; `exch` is 8 KB of scratch for the rotation.
+// kPQ2: the weights are PQ2_0 (32 bytes per block, four 2-bit codes a byte).
+template <bool kPQ2 = false>
 __device__ __forceinline__ void stage_tables(const float* __restrict__ x,
                                              const int8_t* __restrict__ signs, int ws, int we,
                                              bool live, uint32_t exch, uint32_t xs) {
+  constexpr int kBB = kPQ2 ? 32 : kBlockBytes;  // bytes per block
   const int L = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int bx0 = (4 * ws) / kBlockBytes, bx1 = (4 * we - 1) / kBlockBytes;
+  const int bx0 = (4 * ws) / kBB, bx1 = (4 * we - 1) / kBB;
   int xbase;  // weight index of xs[0]
   if (signs == nullptr) {
     xbase = bx0 * kBlockWeights;
@@ -254,7 +271,30 @@ __device__ __forceinline__ void stage_tables(const float* __restrict__ x,
     }
   }
   __syncthreads();
-  {
+  if constexpr (kPQ2) {
+    const int j = warp & 3;
+    const int Pj = 4 * (ws + L) + j;
+    const int b = Pj / kBB, q = Pj % kBB;
+    float xv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      xv[i] = live ? lds_f32(xs + 4u * (uint32_t)(b * kBlockWeights + 4 * q + i - xbase)) : 0.0f;
+    float Lo[16], Hi[16];
+#pragma unroll
+    for (int n = 0; n < 16; ++n) {
+      // code c contributes (c - 1) x; code 3 (never written) gives 2 x
+      const float c0 = (float)((n & 3) - 1), c1 = (float)(((n >> 2) & 3) - 1);
+      Lo[n] = fmaf(c1, xv[1], c0 * xv[0]);
+      Hi[n] = fmaf(c1, xv[3], c0 * xv[2]);
+    }
+    const uint32_t dst = kTab + 0x10000u * (uint32_t)(j >> 1) + 128u * (uint32_t)(j & 1) + 4u * L;
+    switch (warp >> 2) {
+      case 0: build_entries_pq2<0>(Lo, Hi, dst); break;
+      case 1: build_entries_pq2<1>(Lo, Hi, dst); break;
+      case 2: build_entries_pq2<2>(Lo, Hi, dst); break;
+      default: build_entries_pq2<3>(Lo, Hi, dst); break;
+    }
+  } else {
     // warp -> (position j of every lane's word, quarter R of the entries)
     const int j = warp & 3;
     const int Pj = 4 * (ws + L) + j;
@@ -428,7 +468,9 @@ __device__ __forceinline__ float fold(float lo, float hi, bool up, int m) {
   return keep + __shfl_xor_sync(0xffffffffu, send, m);
 }
 
+template <bool kPQ2>
 __global__ void __launch_bounds__(kThreads, 1) gemv_lut_tma_kernel(const __grid_constant__ LutTmaArgs P) {
+  constexpr int kBB = kPQ2 ? 32 : kBlockBytes;  // bytes per 128-weight block
   extern __shared__ __align__(16) unsigned char smem[];
   const int L = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t raw = smem_u32(smem);
@@ -454,11 +496,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_lut_tma_kernel(const __grid_
   const bool live = L < Wc;
   const int wl = ws + (live ? L : Wc - 1);     // lanes past the chunk take its last word's scales
   const int P0 = 4 * wl;
-  const int bA = P0 / kBlockBytes, bB = (P0 + 2) / kBlockBytes;
+  // PTQ1_0: a block boundary falls mid-word at most, so the word's two halves
+  // have scales s[bA], s[bB]; PQ2_0: a word (16 weights) lies in one block
+  const int bA = P0 / kBB, bB = kPQ2 ? bA : (P0 + 2) / kBB;
   const uint32_t ssel = (bB != bA) ? 0x3210u : ((bA & 1) ? 0x3232u : 0x1010u);
   // the scale box starts at the chunk's first scale word rounded down to a
   // multiple of 4; a chunk spans at most 6 blocks, so 8 words cover it
-  const int xsw = ((4 * ws / kBlockBytes) >> 1) & ~3;
+  const int xsw = ((4 * ws / kBB) >> 1) & ~3;
   const uint32_t soff = 4u * (uint32_t)((bA >> 1) - xsw);
 
   const int nr = R1 - R0;
@@ -491,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_lut_tma_kernel(const __grid_
 
   // ---- activations of the chunk, then its tables ---------------------------------
   pdl_wait();
-  stage_tables(P.x, P.signs, ws, we, live, exch, xs);
+  stage_tables<kPQ2>(P.x, P.signs, ws, we, live, exch, xs);
   __syncthreads();
   pdl_release();  // the reduction kernel may start its prologue
 
@@ -604,8 +648,11 @@ static cudaError_t device_sms(int* out) {
     e = cudaFuncSetAttribute(gemv_lut_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(gemv_lut_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemTma);
+    e = cudaFuncSetAttribute(gemv_lut_tma_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemTma);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(gemv_lut_tma_kernel<true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemTma);
     if (e != cudaSuccess) return e;
     g_sms[dev] = sms;
   }
@@ -619,6 +666,54 @@ bool gemv_lut_supported(int64_t N, int64_t K, bool rotate) {
   if (rotate && K % kRot != 0) return false;
   int sms = 0;
   return device_sms(&sms) == cudaSuccess && nch <= sms;
+}
+
+// CTAs per chunk: enough to fill the SMs, but at least kMinRowsPerCta rows each.
+static int64_t ctas_per_chunk(int64_t sms, int64_t nch, int64_t N) {
+  int64_t cpc = sms / nch;
+  const int64_t by_rows = (N + kMinRowsPerCta - 1) / kMinRowsPerCta;
+  if (cpc > by_rows) cpc = by_rows;
+  return cpc < 1 ? 1 : cpc;
+}
+
+// The TMA-fed kernel for `words` 32-bit words of codes per row (both planes
+// need 16-byte aligned rows: K % 1024 == 0).  cudaErrorNotSupported when a
+// tensor map cannot be made.
+template <bool kPQ2>
+static cudaError_t launch_lut_tma(const void* wq, const uint16_t* scales, const float* x,
+                                  const int8_t* signs, float* y, float* part, int64_t N, int nblk,
+                                  int words, int64_t nch, int64_t cpc, cudaStream_t st) {
+  int* status = device_status_ptr();
+  if (status == nullptr) return cudaErrorNotSupported;
+  LutTmaArgs T;
+  if (encode_tma_2d(&T.tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, wq, (uint64_t)words, (uint64_t)N,
+                    (uint64_t)words * 4, kChunkWords, kBoxRows,
+                    CU_TENSOR_MAP_SWIZZLE_NONE) != cudaSuccess ||
+      encode_tma_2d(&T.ts, CU_TENSOR_MAP_DATA_TYPE_UINT32, scales, (uint64_t)(nblk / 2), (uint64_t)N,
+                    (uint64_t)nblk * 2, kBoxScaleWords, kBoxRows,
+                    CU_TENSOR_MAP_SWIZZLE_NONE) != cudaSuccess)
+    return cudaErrorNotSupported;
+  T.x = x;
+  T.signs = signs;
+  T.part = nch == 1 ? y : part;
+  T.status = status;
+  T.N = (int)N;
+  T.nblk = nblk;
+  T.words = words;
+  T.nch = (int)nch;
+  T.cpc = (int)cpc;
+  return launch_pdl(gemv_lut_tma_kernel<kPQ2>, dim3((unsigned)(nch * cpc)), dim3(kThreads),
+                    kSmemTma, st, T);
+}
+
+// The fixed-order sum of the nch chunk sums of every row (or h = silu(g) u).
+static cudaError_t launch_chunk_sums(const float* part, float* y, int64_t N, int64_t nch,
+                                     LutEpilogue ep, cudaStream_t st) {
+  if (ep == LutEpilogue::SwiGLU)
+    return launch_pdl(gemv_lut_reduce_swiglu_kernel, dim3((unsigned)((N / 2 + 255) / 256)),
+                      dim3(256), 0, st, part, y, (int)N, (int)nch);
+  return launch_pdl(gemv_lut_reduce_kernel, dim3((unsigned)((N + 255) / 256)), dim3(256), 0, st,
+                    part, y, (int)N, (int)nch);
 }
 
 // cudaErrorNotSupported when the shape does not fit this kernel (odd K/128,
@@ -639,35 +734,14 @@ cudaError_t launch_gemv_lut(const uint8_t* wq, const uint16_t* scales, const flo
   if (e != cudaSuccess) return e;
   if (nch > sms) return cudaErrorNotSupported;
   if (nch > 1 && part == nullptr) return cudaErrorInvalidValue;
-  int64_t cpc = sms / nch;
-  const int64_t by_rows = (N + kMinRowsPerCta - 1) / kMinRowsPerCta;
-  if (cpc > by_rows) cpc = by_rows;
-  if (cpc < 1) cpc = 1;
+  const int64_t cpc = ctas_per_chunk(sms, nch, N);
   const int nblk = (int)(K / kBlockWeights), words = 13 * nblk / 2;
   // With K % 1024 == 0 both weight planes have 16-byte aligned rows: the
   // TMA-fed kernel (its 4-word aligned chunks number the same nch).
-  bool tma = K % kRot == 0 && device_status_ptr() != nullptr;
-  if (tma) {
-    LutTmaArgs T;
-    tma = encode_tma_2d(&T.tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, wq, (uint64_t)words, (uint64_t)N,
-                        (uint64_t)words * 4, kChunkWords, kBoxRows,
-                        CU_TENSOR_MAP_SWIZZLE_NONE) == cudaSuccess &&
-          encode_tma_2d(&T.ts, CU_TENSOR_MAP_DATA_TYPE_UINT32, scales, (uint64_t)(nblk / 2),
-                        (uint64_t)N, (uint64_t)nblk * 2, kBoxScaleWords, kBoxRows,
-                        CU_TENSOR_MAP_SWIZZLE_NONE) == cudaSuccess;
-    if (tma) {
-      T.x = x;
-      T.signs = signs;
-      T.part = nch == 1 ? y : part;
-      T.status = device_status_ptr();
-      T.N = (int)N;
-      T.nblk = nblk;
-      T.words = words;
-      T.nch = (int)nch;
-      T.cpc = (int)cpc;
-      e = launch_pdl(gemv_lut_tma_kernel, dim3((unsigned)(nch * cpc)), dim3(kThreads), kSmemTma,
-                     st, T);
-    }
+  bool tma = false;
+  if (K % kRot == 0) {
+    e = launch_lut_tma<false>(wq, scales, x, signs, y, part, N, nblk, words, nch, cpc, st);
+    tma = e != cudaErrorNotSupported;
   }
   if (!tma) {
     LutArgs A;
@@ -685,11 +759,38 @@ cudaError_t launch_gemv_lut(const uint8_t* wq, const uint16_t* scales, const flo
                    A);
   }
   if (e != cudaSuccess || nch == 1) return e;
-  if (ep == LutEpilogue::SwiGLU)
-    return launch_pdl(gemv_lut_reduce_swiglu_kernel, dim3((unsigned)((N / 2 + 255) / 256)),
-                      dim3(256), 0, st, (const float*)part, y, (int)N, (int)nch);
-  return launch_pdl(gemv_lut_reduce_kernel, dim3((unsigned)((N + 255) / 256)), dim3(256), 0, st,
-                    (const float*)part, y, (int)N, (int)nch);
+  return launch_chunk_sums(part, y, N, nch, ep, st);
+}
+
+// ---- PQ2_0 ------------------------------------------------------------------------
+// A row is 8 nblk words of 2-bit codes, cut into chunks of at most 32 words.
+int64_t gemv_lut_pq2_chunks(int64_t K) {
+  if (K % kRot != 0 || K <= 0) return 0;
+  const int64_t words = 8 * (K / kBlockWeights);
+  return (words + kChunkWords - 1) / kChunkWords;
+}
+
+size_t gemv_lut_pq2_workspace_bytes(int64_t N, int64_t K) {
+  const int64_t nch = gemv_lut_pq2_chunks(K);
+  if (nch <= 1) return 0;
+  return (size_t)(((nch * N * 4) + 255) / 256 * 256);
+}
+
+cudaError_t launch_gemv_lut_pq2(const uint8_t* wq, const uint16_t* scales, const float* x,
+                                const int8_t* signs, float* y, float* part, int64_t N, int64_t K,
+                                cudaStream_t st) {
+  const int64_t nch = gemv_lut_pq2_chunks(K);
+  if (nch == 0 || N > INT32_MAX / 2 || K > (1 << 24)) return cudaErrorNotSupported;
+  int sms = 0;
+  cudaError_t e = device_sms(&sms);
+  if (e != cudaSuccess) return e;
+  if (nch > sms) return cudaErrorNotSupported;
+  if (nch > 1 && part == nullptr) return cudaErrorInvalidValue;
+  const int nblk = (int)(K / kBlockWeights);
+  e = launch_lut_tma<true>(wq, scales, x, signs, y, part, N, nblk, 8 * nblk, nch,
+                           ctas_per_chunk(sms, nch, N), st);
+  if (e != cudaSuccess || nch == 1) return e;
+  return launch_chunk_sums(part, y, N, nch, LutEpilogue::Plain, st);
 }
 
 }  // namespace ptq

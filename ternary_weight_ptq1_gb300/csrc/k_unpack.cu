@@ -32,7 +32,32 @@ __global__ void __launch_bounds__(256) unpack_kernel(const uint8_t* __restrict__
   (void)K;
 }
 
+// PQ2_0 ("Why I Am Building Another Inference Engine", section "Level 2: The
+// short answer": two bits per ternary weight): weight 4j + i of a row is bits
+// 2i, 2i+1 of byte j, trit = code - 1.
+__global__ void __launch_bounds__(256) unpack_pq2_kernel(const uint8_t* __restrict__ wq,
+                                                         int8_t* __restrict__ trits,
+                                                         int64_t total_bytes) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total_bytes; i += stride) {
+    const uint32_t b = wq[i];
+    const uint32_t c = (b & 3u) | ((b & 0x0cu) << 6) | ((b & 0x30u) << 12) | ((b & 0xc0u) << 18);
+    const uint32_t t = __vsub4(c, 0x01010101u);  // code - 1 in each byte, no borrow between them
+    *reinterpret_cast<uint32_t*>(trits + 4 * i) = t;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_unpack_pq2(const uint8_t* wq, int8_t* trits, int64_t N, int64_t K,
+                              cudaStream_t st) {
+  const int64_t total = N * K / 4;
+  int64_t grid = (total + 255) / 256;
+  if (grid > 152 * 32) grid = 152 * 32;
+  if (grid < 1) return cudaSuccess;
+  unpack_pq2_kernel<<<(unsigned)grid, 256, 0, st>>>(wq, trits, total);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_unpack(const uint8_t* wq, int8_t* trits, int64_t N, int64_t K,
                           cudaStream_t st) {

@@ -60,6 +60,8 @@ ptq_status cuda_fail(cudaError_t e, const char* what);
 // ---- launchers (arguments already validated) -------------------------------
 cudaError_t launch_unpack(const uint8_t* wq, int8_t* trits, int64_t N,
                           int64_t K, cudaStream_t st);
+cudaError_t launch_unpack_pq2(const uint8_t* wq, int8_t* trits, int64_t N, int64_t K,
+                              cudaStream_t st);
 // Supported (in, out): (F32, F32), (BF16, BF16), (BF16, F16), (F32, F16).
 cudaError_t launch_fwht(const void* x, Act in, void* y, Act out,
                         const int8_t* signs, int64_t M, int64_t K, cudaStream_t st);
@@ -84,6 +86,12 @@ cudaError_t launch_gemv_lut(const uint8_t* wq, const uint16_t* scales, const flo
                             const int8_t* signs, float* y, float* part, int64_t N, int64_t K,
                             LutEpilogue ep, cudaStream_t st);
 size_t gemv_lut_workspace_bytes(int64_t N, int64_t K);
+// The same decode for PQ2_0 weights (k_gemv_lut.cu): K % 1024 == 0 only.
+cudaError_t launch_gemv_lut_pq2(const uint8_t* wq, const uint16_t* scales, const float* x,
+                                const int8_t* signs, float* y, float* part, int64_t N, int64_t K,
+                                cudaStream_t st);
+int64_t gemv_lut_pq2_chunks(int64_t K);
+size_t gemv_lut_pq2_workspace_bytes(int64_t N, int64_t K);
 // Whether launch_gemv_lut serves (N, K) on the current device (with the
 // rotation when `rotate`).
 bool gemv_lut_supported(int64_t N, int64_t K, bool rotate);
@@ -101,6 +109,11 @@ cudaError_t launch_swiglu(const float* gu, float* h, int64_t M, int64_t I,
 cudaError_t launch_gemm_tc(const uint8_t* wq, const uint16_t* scales, const void* x, Act x_t,
                            void* y, Act y_t, int64_t M, int64_t N, int64_t K, void* ws,
                            size_t ws_bytes, cudaStream_t st);
+// The tensor-core GEMM over PQ2_0 weights (bf16 x, bf16 y; K % 1024 == 0);
+// ws as launch_gemm_tc.
+cudaError_t launch_gemm_tc_pq2(const uint8_t* wq, const uint16_t* scales, const void* x, void* y,
+                               int64_t M, int64_t N, int64_t K, void* ws, size_t ws_bytes,
+                               cudaStream_t st);
 // The gate+up GEMM of the feed-forward block with SwiGLU in its epilogue:
 // wq/scales hold 2I rows (gate then up), h = silu(g) * u is M x I fp32.
 // cudaErrorNotSupported when the shape would be split along K (the caller

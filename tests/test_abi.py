@@ -161,3 +161,26 @@ def test_workspace_sizes(P):
         words = 13 * K // 256
         assert P.matmul_workspace_bytes(1, 100, K, P.PTQ_F32) == (
             0 if words <= 32 else ((words + 31) // 32 * 100 * 4 + 255) // 256 * 256)
+
+
+def test_pq2_host_side(P, orc, syn):
+    # the library's PQ2_0 encoder writes the oracle's bytes; refusals before
+    # any launch
+    L = P.load()
+    t, _ = syn.weights(40, 7, 1024)
+    np.testing.assert_array_equal(P.pq2_pack(t), orc.pq2_pack(t))
+    with pytest.raises(P.PTQError, match="VALUE"):
+        P.pq2_pack(np.full((1, 128), 2, np.int8))
+    with pytest.raises(P.PTQError, match="SHAPE"):
+        P.pq2_pack(np.zeros((1, 100), np.int8))
+    p16 = ctypes.c_void_p(16 * 1024)
+    mm = lambda *a: L.ptq_matmul_pq2(*a[:8], None, 0, None)  # noqa: E731
+    assert mm(p16, p16, p16, p16, 1, 8, 1152, P.PTQ_F32) == 5     # K % 1024
+    assert mm(p16, p16, p16, p16, 9, 8, 1024, P.PTQ_F32) == 5     # fp32 serves M <= 8
+    assert mm(p16, p16, p16, p16, 1, 8, 100, P.PTQ_F32) == 2
+    assert mm(None, p16, p16, p16, 1, 8, 1024, P.PTQ_BF16) == 1
+    need = P.matmul_pq2_workspace_bytes(1, 17408, 5120, P.PTQ_F32)
+    assert need == 10 * 17408 * 4                                  # 320 words a row: 10 chunks
+    assert mm(p16, p16, p16, p16, 1, 17408, 5120, P.PTQ_F32) == 6  # no workspace
+    assert P.matmul_pq2_workspace_bytes(1, 100, 1152, P.PTQ_F32) == 0
+
