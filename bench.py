@@ -267,6 +267,41 @@ def embed_lines(P, torch, syn, pk, world, args):
     return out
 
 
+def pq2_lines(P, torch, syn, pk, world, args):
+    """The same hot path over PQ2_0 weights (2 bits a weight + a 16-bit scale
+    per 128: 34 bytes a block): the decode GEMV at the gate/up shape (M=1,
+    K=5120, N=17408; x already rotated; a ring of 16 weight sets, 357 MB > L2)
+    and the prefill GEMM at M=512."""
+    N, K = N_ROWS, K_COLS
+    wbytes = N * K // 128 * 34
+    R = 16
+    ring = []
+    for r in range(R):
+        t, s = syn.weights(2000 + r, N, K)
+        ring.append((torch.from_numpy(P.pq2_pack(t)).cuda(), torch.from_numpy(s.view(np.int16)).cuda()))
+    x = torch.from_numpy(syn.normal_f32(2000, 2, (1, K))).cuda()
+    ys = [torch.empty((1, N), device="cuda") for _ in range(R)]
+    ws = torch.empty(P.matmul_pq2_workspace_bytes(1, N, K, P.PTQ_F32), dtype=torch.uint8,
+                     device="cuda")
+    K1 = max(3, min(args.steps, 2000))
+    us = timed_steps(torch, lambda i: P.matmul_pq2(ring[i % R][0], ring[i % R][1], x, out=ys[i % R],
+                                                    workspace=ws), K1, 3) / K1 * 1e3
+    gbs = (wbytes + 4 * K + 4 * N) / (us * 1e-6) / 1e9
+    dec = {"workload": "PQ2_0 decode GEMV, M=1, K=5120, N=17408 (x rotated)", "us_per_call": round(us, 3),
+           "weight_bytes": wbytes, "GB/s": round(world * gbs, 1), "frac_of_hbm": round(gbs / pk["hbm"], 4),
+           "kernels": "gemv_lut_tma_kernel<PQ2_0> + gemv_lut_reduce_kernel"}
+    M = PREFILL_M
+    xb = torch.from_numpy(syn.normal_bf16(2000, 2, (M, K)).view(np.int16)).cuda().view(torch.bfloat16)
+    yb = [torch.empty((M, N), device="cuda", dtype=torch.bfloat16) for _ in range(8)]
+    K2 = max(3, min(args.steps, 200))
+    ms = timed_steps(torch, lambda i: P.matmul_pq2(ring[i % 8][0], ring[i % 8][1], xb, out=yb[i % 8]),
+                     K2, 3, chunk=50) / K2
+    tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+    pre = {"workload": "PQ2_0 prefill GEMM, M=512, K=5120, N=17408, bf16", "us_per_call": round(ms * 1e3, 2),
+           "TFLOP/s": round(world * tf, 1), "frac_of_bf16_peak": round(tf / pk["bf16"], 4)}
+    return {"decode": dec, "prefill": pre}
+
+
 def run_ours(args, world, rank):
     import torch
 
@@ -360,6 +395,7 @@ def run_ours(args, world, rank):
 
     ffn = None if args.skip_ffn else ffn_lines(P, torch, syn, pk, world, args)
     emb = None if args.skip_embed else embed_lines(P, torch, syn, pk, world, args)
+    pq2 = None if args.skip_pq2 else pq2_lines(P, torch, syn, pk, world, args)
 
     cpu = cpu_baseline(args) if rank == 0 and not args.skip_cpu else None
     clocks = clk.summary()
@@ -393,6 +429,7 @@ def run_ours(args, world, rank):
         "prefill": pre,
         "ffn": ffn,
         "embed": emb,
+        "pq2": pq2,
         "cpu_baseline": cpu,
     }
     if rank == 0:
@@ -513,6 +550,7 @@ def main():
     ap.add_argument("--skip-prefill", action="store_true")
     ap.add_argument("--skip-ffn", action="store_true")
     ap.add_argument("--skip-embed", action="store_true")
+    ap.add_argument("--skip-pq2", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--profile", choices=["gemv", "gemm"],
                     help="run a small case of one kernel for an ncu capture, then exit")
