@@ -311,7 +311,7 @@ def run_ours(args, world, rank):
     P.load()
     pk = peaks()
     dev_index = torch.cuda.current_device()
-    R = max(8, int(np.ceil(4 * L2_BYTES / WEIGHT_BYTES)))       # 27 sets, 526 MB
+    R = max(8, int(np.ceil(4 * L2_BYTES / WEIGHT_BYTES)))       # 28 sets, 546 MB
     ring = make_ring(P, torch, syn, R, 1, N_ROWS, K_COLS, "f32")
     signs = torch.from_numpy(syn.signs(1, 3, K_COLS)).cuda()
     xr = [torch.empty((1, K_COLS), device="cuda") for _ in range(R)]
