@@ -290,6 +290,14 @@ PTQ_API PTQ_NODISCARD ptq_status ptq_route(int64_t M, ptq_dtype dtype,
  * then invalid), PTQ_ERR_CUDA if the stream reports an error, else PTQ_OK. */
 PTQ_API PTQ_NODISCARD ptq_status ptq_device_check(ptq_stream_t stream);
 
+/* ptq_selftest_timeout -- test export for the timeout path.  Launches one
+ * CTA that waits, with the library's bounded mbarrier wait and a short poll
+ * limit, on a barrier that nothing arrives on; the wait runs out and the
+ * kernel raises the device status word and returns (no fault, no hang).  The
+ * next ptq_device_check on the stream then returns PTQ_ERR_TIMEOUT and
+ * clears the word.  Errors: PTQ_ERR_CUDA. */
+PTQ_API PTQ_NODISCARD ptq_status ptq_selftest_timeout(ptq_stream_t stream);
+
 /* ptq_status_str -- static name of a status code. */
 PTQ_API const char* ptq_status_str(ptq_status status);
 

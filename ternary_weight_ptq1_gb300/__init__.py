@@ -30,7 +30,7 @@ EXPORTS = ("ptq1_pack", "ptq1_unpack", "ptq_fwht", "ptq_matmul_workspace_bytes",
            "ptq_rotate_matmul_workspace_bytes", "ptq_rotate_matmul", "ptq_ffn_workspace_bytes",
            "ptq_ffn", "ptq_ffn_noalloc", "ptq2_pack", "ptq2_unpack",
            "ptq_matmul_pq2_workspace_bytes", "ptq_matmul_pq2", "ptq_embed", "ptq_embed_ptq1",
-           "ptq_route",
+           "ptq_route", "ptq_selftest_timeout",
            "ptq_device_check", "ptq_status_str", "ptq_last_error")
 
 # Size of the built-in scratch array behind ptq_ffn_noalloc (include/ptq.h).
@@ -82,13 +82,14 @@ def load(path: str | None = None):
     L.ptq_embed_ptq1.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _P]
     L.ptq_route.argtypes = [_I64, _I32, ctypes.POINTER(ctypes.c_char_p)]
     L.ptq_device_check.argtypes = [_P]
+    L.ptq_selftest_timeout.argtypes = [_P]
     L.ptq_status_str.argtypes = [_I32]
     L.ptq_status_str.restype = ctypes.c_char_p
     L.ptq_last_error.argtypes = []
     L.ptq_last_error.restype = ctypes.c_char_p
     for name in ("ptq1_pack", "ptq1_unpack", "ptq_fwht", "ptq_matmul", "ptq_rotate_matmul", "ptq_ffn",
                  "ptq_ffn_noalloc", "ptq2_pack", "ptq2_unpack", "ptq_matmul_pq2", "ptq_embed",
-                 "ptq_embed_ptq1", "ptq_route", "ptq_device_check"):
+                 "ptq_embed_ptq1", "ptq_route", "ptq_device_check", "ptq_selftest_timeout"):
         getattr(L, name).restype = _I32
     _lib = L
     return L
@@ -348,6 +349,12 @@ def route(M: int, dtype: int) -> str:
     name = ctypes.c_char_p()
     _check(load().ptq_route(M, dtype, ctypes.byref(name)), "ptq_route")
     return name.value.decode()
+
+
+def selftest_timeout(stream=None) -> None:
+    """Runs the bounded wait that is made to run out (ptq_selftest_timeout);
+    the next device_check raises PTQ_ERR_TIMEOUT."""
+    _check(load().ptq_selftest_timeout(_stream(stream)), "ptq_selftest_timeout")
 
 
 def device_check(stream=None) -> None:

@@ -585,6 +585,12 @@ PTQ_API ptq_status ptq_ffn(const uint8_t* wgu_q, const uint16_t* wgu_s, const ui
   return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq_ffn launch");
 }
 
+PTQ_API ptq_status ptq_selftest_timeout(ptq_stream_t stream) {
+  t_msg[0] = 0;
+  cudaError_t e = launch_selftest_timeout(reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq_selftest_timeout launch");
+}
+
 PTQ_API ptq_status ptq_device_check(ptq_stream_t stream) {
   t_msg[0] = 0;
   int v = 0;

@@ -132,6 +132,10 @@ cudaError_t encode_tma_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* 
                           uint64_t inner, uint64_t rows, uint64_t row_bytes, uint32_t box_inner,
                           uint32_t box_rows, CUtensorMapSwizzle swizzle);
 
+// One CTA waits (bounded) on an mbarrier nothing arrives on and raises the
+// device status word when the wait runs out (k_selftest.cu).
+cudaError_t launch_selftest_timeout(cudaStream_t st);
+
 // Device status word access (defined in api.cu).
 cudaError_t read_and_clear_device_status(int* out, cudaStream_t st);
 int* device_status_ptr();
