@@ -445,7 +445,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int s = kb % kStages, round = kb / kStages;
         if (round > 0) ok = mbar_wait(&empty[s], (round - 1) & 1, abort_flag);
         if (!ok) break;
-        mbar_expect_tx(&a_full[s], kASlice);
+        // M <= 128: the A box is 128 rows (no zero fill for the empty half)
+        mbar_expect_tx(&a_full[s], M <= UM ? kASlice / 2 : kASlice);
         tma_2d(smem_u32(smem + kOffA + s * kASlice), &map_a, (kb0 + kb) * BK, m0, &a_full[s]);
         ++a_issued;
       }
@@ -629,6 +630,14 @@ __global__ void __launch_bounds__(256) gemm_split_reduce_kernel(const float* __r
 }
 
 // ---- host side -------------------------------------------------------------------------
+// The TMA map of A (M x K, 16-bit): boxes of 64 x 256 rows, or 64 x 128 when
+// M <= 128 -- then only the lower accumulator has rows, and the upper 128
+// rows of the box would only be zero fill.
+static cudaError_t encode_a(CUtensorMap* ma, const void* x, int64_t M, int64_t K) {
+  return encode_tma_2d(ma, CU_TENSOR_MAP_DATA_TYPE_UINT16, x, K, M, K * 2, BK, M <= UM ? UM : BM,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 template <bool kBf16, bool kOutF32, bool kSwiGLU = false, bool kPQ2 = false>
 cudaError_t launch_t(const CUtensorMap& ma, const uint8_t* wq, const uint16_t* scales, void* y,
                      int M, int N, int K, int splits, int* status, cudaStream_t st) {
@@ -679,9 +688,7 @@ cudaError_t launch_gemm_tc(const uint8_t* wq, const uint16_t* scales, const void
     return cudaErrorNotSupported;
   cudaError_t e;
   CUtensorMap ma;
-  if ((e = encode_tma_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT16, x, K, M, K * 2, BK, BM,
-                         CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)  // box 64 x 256
-    return e;
+  if ((e = encode_a(&ma, x, M, K)) != cudaSuccess) return e;
   int* status = device_status_ptr();
   if (!status) return cudaErrorInvalidDevice;
   const int m = (int)M, n = (int)N, k = (int)K;
@@ -716,9 +723,7 @@ cudaError_t launch_gemm_tc_pq2(const uint8_t* wq, const uint16_t* scales, const 
     return cudaErrorNotSupported;
   cudaError_t e;
   CUtensorMap ma;
-  if ((e = encode_tma_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT16, x, K, M, K * 2, BK, BM,
-                         CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
-    return e;
+  if ((e = encode_a(&ma, x, M, K)) != cudaSuccess) return e;
   int* status = device_status_ptr();
   if (!status) return cudaErrorInvalidDevice;
   const int m = (int)M, n = (int)N, k = (int)K;
@@ -745,9 +750,7 @@ cudaError_t launch_gemm_tc_swiglu(const uint8_t* wq, const uint16_t* scales, con
     return cudaErrorNotSupported;
   cudaError_t e;
   CUtensorMap ma;
-  if ((e = encode_tma_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT16, x, K, M, K * 2, BK, BM,
-                         CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
-    return e;
+  if ((e = encode_a(&ma, x, M, K)) != cudaSuccess) return e;
   int* status = device_status_ptr();
   if (!status) return cudaErrorInvalidDevice;
   const int m = (int)M, n = (int)N, k = (int)K;
