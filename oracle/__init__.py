@@ -83,6 +83,8 @@ def lib():
         L.orc_swiglu.restype = None
         L.orc_ffn.argtypes = [_P] * 8 + [_I64] * 3
         L.orc_ffn.restype = ctypes.c_int
+        L.orc_ffn_stack.argtypes = [_P] * 7 + [_I64, ctypes.c_double, _P, _I64, _I64, _I64]
+        L.orc_ffn_stack.restype = ctypes.c_int
         L.orc_set_threads.argtypes = [ctypes.c_int]
         L.orc_set_threads.restype = None
         L.orc_get_threads.argtypes = []
@@ -305,3 +307,26 @@ def ffn(wgu_q, wgu_s, wd_q, wd_s, signs_in, signs_mid, x) -> np.ndarray:
     if rc != 0:
         raise ValueError("orc_ffn: H and I must be multiples of 1024")
     return y
+
+
+def ffn_stack(layers, norm_w, x, eps: float) -> np.ndarray:
+    """The pre-norm residual stack: for each layer l,
+    x = x + ffn_l(x / sqrt(mean(x^2) + eps) * g_l).  `layers` is a list of
+    (wgu_q, wgu_s, wd_q, wd_s, signs_in, signs_mid); norm_w a list of H-vectors."""
+    Lc = len(layers)
+    if Lc == 0:
+        return np.array(x, dtype=np.float64, copy=True, order="C")
+    cols = [[_c(lay[i], dt) for lay in layers]
+            for i, dt in enumerate((np.uint8, np.uint16, np.uint8, np.uint16, np.int8, np.int8))]
+    gs = [_c(np.asarray(g, np.float64), np.float64) for g in norm_w]
+    arrs = [(ctypes.c_void_p * Lc)(*[a.ctypes.data for a in col]) for col in cols]
+    garr = (ctypes.c_void_p * Lc)(*[g.ctypes.data for g in gs])
+    x = np.array(x, dtype=np.float64, copy=True, order="C")
+    M, H = x.shape
+    I = cols[5][0].size
+    rc = lib().orc_ffn_stack(*[ctypes.cast(a, ctypes.c_void_p) for a in arrs],
+                             ctypes.cast(garr, ctypes.c_void_p), Lc, float(eps), _ptr(x), M, H, I)
+    if rc != 0:
+        raise ValueError("orc_ffn_stack: H and I must be multiples of 1024")
+    return x
+

@@ -404,3 +404,43 @@ int orc_ffn(const uint8_t* wgu_q, const uint16_t* wgu_s, const uint8_t* wd_q,
   free(h);
   return 0;
 }
+
+/* ---- the chained feed-forward stack ----------------------------------- */
+
+/* [P1] "Speed, and where it goes": the next step named there is to run a
+   whole layer on the device, the norms and the residual adds included.
+   Reading: a pre-norm residual stack, for l = 0..L-1
+     xn = x / sqrt(mean(x^2) + eps) * g_l,   x = x + FFN_l(xn),
+   with FFN_l the block of orc_ffn.  wgu_q[l] etc. are per-layer arrays;
+   x (M x H) is updated in place.  Returns 0 or -1. */
+int orc_ffn_stack(const uint8_t* const* wgu_q, const uint16_t* const* wgu_s,
+                  const uint8_t* const* wd_q, const uint16_t* const* wd_s,
+                  const int8_t* const* signs_in, const int8_t* const* signs_mid,
+                  const double* const* norm_w, int64_t L, double eps, double* x,
+                  int64_t M, int64_t H, int64_t I) {
+  if (H % ORC_ROT != 0 || I % ORC_ROT != 0 || M < 0 || L < 0) return -1;
+  double* xn = (double*)malloc(sizeof(double) * (size_t)(M * H));
+  double* y = (double*)malloc(sizeof(double) * (size_t)(M * H));
+  if (!xn || !y) {
+    free(xn);
+    free(y);
+    return -1;
+  }
+  int rc = 0;
+  for (int64_t l = 0; l < L && rc == 0; ++l) {
+    for (int64_t m = 0; m < M; ++m) {
+      const double* xm = x + m * H;
+      double ss = 0.0;
+      for (int64_t k = 0; k < H; ++k) ss += xm[k] * xm[k];
+      const double inv = 1.0 / sqrt(ss / (double)H + eps);
+      for (int64_t k = 0; k < H; ++k) xn[m * H + k] = xm[k] * inv * norm_w[l][k];
+    }
+    rc = orc_ffn(wgu_q[l], wgu_s[l], wd_q[l], wd_s[l], signs_in[l], signs_mid[l], xn, y, M,
+                 H, I);
+    for (int64_t i = 0; i < M * H && rc == 0; ++i) x[i] += y[i];
+  }
+  free(xn);
+  free(y);
+  return rc;
+}
+

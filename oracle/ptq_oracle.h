@@ -144,6 +144,17 @@ int orc_ffn(const uint8_t* wgu_q, const uint16_t* wgu_s, const uint8_t* wd_q,
             const int8_t* signs_mid, const double* x, double* y, int64_t M,
             int64_t H, int64_t I);
 
+/* A chained stack of L feed-forward blocks, pre-norm with residual adds
+   (a reading of the next step [P1] "Speed, and where it goes" names):
+     xn = x / sqrt(mean(x^2) + eps) * g_l;  x = x + FFN_l(xn),  l = 0..L-1.
+   Per-layer arguments are arrays of L pointers; x (M x H) is updated in
+   place, in double.  Returns 0 or -1. */
+int orc_ffn_stack(const uint8_t* const* wgu_q, const uint16_t* const* wgu_s,
+                  const uint8_t* const* wd_q, const uint16_t* const* wd_s,
+                  const int8_t* const* signs_in, const int8_t* const* signs_mid,
+                  const double* const* norm_w, int64_t L, double eps, double* x,
+                  int64_t M, int64_t H, int64_t I);
+
 #ifdef __cplusplus
 }
 #endif

@@ -433,3 +433,53 @@ def test_ffn_against_dense_numpy(orc, syn):
     h = gu[:, :I_] * scipy.special.expit(gu[:, :I_]) * gu[:, I_:]
     ref = rot(h, s_mid) @ dense(t_d, s_d).T
     np.testing.assert_allclose(y, ref, rtol=1e-10, atol=1e-10 * np.abs(ref).max())
+
+
+# ---- the chained feed-forward stack ------------------------------------------
+
+def _stack_layer(syn, seed, l, H, I):
+    L = syn.ffn_layer(seed, l, H, I)
+    return (np.ascontiguousarray(__import__("oracle").pack(L.wgu_trits)), L.wgu_scales,
+            np.ascontiguousarray(__import__("oracle").pack(L.wd_trits)), L.wd_scales,
+            L.signs_in, L.signs_mid)
+
+
+def test_stack_identities(orc, syn):
+    H, I = 1024, 1024
+    x = syn.normal_f64(60, 2, (2, H))
+    lay = _stack_layer(syn, 60, 0, H, I)
+    g = np.ones(H)
+    np.testing.assert_array_equal(orc.ffn_stack([], [], x, 1e-6), x)  # no layers
+    zero = (orc.pack(np.zeros((2 * I, H), np.int8)), lay[1], orc.pack(np.zeros((H, I), np.int8)),
+            lay[3], lay[4], lay[5])
+    np.testing.assert_array_equal(orc.ffn_stack([zero], [g], x, 1e-6), x)  # residual only
+
+
+def test_stack_composes_and_is_scale_free(orc, syn):
+    H, I = 1024, 2048
+    x = syn.normal_f64(61, 2, (3, H))
+    l0, l1 = _stack_layer(syn, 61, 0, H, I), _stack_layer(syn, 61, 1, H, I)
+    g0 = 1.0 + 0.1 * syn.normal_f64(61, 7, (H,))
+    g1 = 1.0 + 0.1 * syn.normal_f64(61, 8, (H,))
+    two = orc.ffn_stack([l0, l1], [g0, g1], x, 1e-5)
+    one_one = orc.ffn_stack([l1], [g1], orc.ffn_stack([l0], [g0], x, 1e-5), 1e-5)
+    np.testing.assert_allclose(two, one_one, rtol=0, atol=1e-12)
+    # eps = 0: the norm removes any positive scale of x, so the block adds the
+    # same increment to c x as to x
+    c = 3.7
+    inc = orc.ffn_stack([l0], [g0], x, 0.0) - x
+    inc_c = orc.ffn_stack([l0], [g0], c * x, 0.0) - c * x
+    np.testing.assert_allclose(inc_c, inc, rtol=1e-12, atol=1e-12)
+
+
+def test_stack_rmsnorm_worked_values(orc, syn):
+    # rows of 3s and 4s have mean square 12.5: with eps = 0 and unit gains
+    # the block's input is x / sqrt(12.5), i.e. 0.8485... and 1.1313...
+    H, I = 1024, 1024
+    x = np.tile([3.0, 4.0], (1, H // 2))
+    lay = _stack_layer(syn, 62, 0, H, I)
+    xn = np.tile([3.0 / np.sqrt(12.5), 4.0 / np.sqrt(12.5)], (1, H // 2))
+    expect = x + orc.ffn(*lay, xn)
+    np.testing.assert_allclose(orc.ffn_stack([lay], [np.ones(H)], x, 0.0), expect, rtol=1e-12,
+                               atol=1e-12)
+
