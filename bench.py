@@ -189,9 +189,10 @@ TRAFFIC_DECODE = (156_060_416 + 5_802_496) // 8
 def ffn_lines(P, torch, syn, pk, world, args):
     """The feed-forward block (rotate, fused gate+up, SwiGLU, rotate, down),
     H=5120, I=17408, 64 layers per step: decode (M=1, fp32) and prefill
-    (M=256, bf16).  The 64 layers cycle through 8 distinct seeded layers
-    (470 MB of weights, more than the L2), so every layer streams its weights
-    from HBM as 64 distinct layers would."""
+    (M=256, bf16); then the same 64 blocks chained as a pre-norm residual
+    stack (RMSNorm and residual add between blocks).  The 64 layers cycle
+    through 8 distinct seeded layers (470 MB of weights, more than the L2), so
+    every layer streams its weights from HBM as 64 distinct layers would."""
     H, I, LAYERS, RING = 5120, 17408, 64, 8
     layers = []
     for l in range(RING):
@@ -226,6 +227,33 @@ def ffn_lines(P, torch, syn, pk, world, args):
             tf = 2.0 * M * LAYERS * 3 * H * I / (ms * 1e-3) / 1e12
             line["TFLOP/s"] = round(world * tf, 1)
             line["frac_of_bf16_peak"] = round(tf / pk["bf16"], 4)
+        out[name] = line
+    # the chained stack: the same 64 blocks, each preceded by the residual add
+    # and RMSNorm kernel, over an fp32 residual stream updated in place
+    gains = [torch.from_numpy(syn.norm_gain(4, l, H)).cuda() for l in range(RING)]
+    for name, M, act in (("stack_decode", 1, torch.float32), ("stack_prefill", 256, torch.bfloat16)):
+        xs = torch.from_numpy(syn.ffn_input(4, 0, M, H, "f32")).cuda()
+        pdt = P.PTQ_F32 if act == torch.float32 else P.PTQ_BF16
+        ws = torch.empty(P.ffn_stack_workspace_bytes(M, H, I, pdt), dtype=torch.uint8, device="cuda")
+        lays = [layers[l % RING] for l in range(LAYERS)]
+        gs = [gains[l % RING] for l in range(LAYERS)]
+
+        def step(i, xs=xs, ws=ws, act=act, lays=lays, gs=gs):
+            P.ffn_stack(lays, gs, xs, 1e-6, act=act, workspace=ws)
+
+        K = max(3, min(args.steps, 40 if M == 1 else 8))
+        ms = timed_steps(torch, step, K, 3, chunk=2) / K
+        base = out["decode" if M == 1 else "prefill"]["ms_per_step"]
+        line = {"workload": f"pre-norm residual stack of {LAYERS} feed-forward blocks, M={M}",
+                "M": M, "H": H, "I": I, "dtype": "f32 residual stream, "
+                + ("f32 activations" if M == 1 else "bf16 activations"),
+                "ms_per_step": round(ms, 4),
+                "norm_and_residual_ms": round(ms - base, 4),
+                "weight_GB/s": round(world * wbytes / (ms * 1e-3) / 1e9, 1)}
+        if M == 1:
+            line["tokens_per_s"] = round(world * 1e3 / ms, 1)
+        else:
+            line["TFLOP/s"] = round(world * 2.0 * M * LAYERS * 3 * H * I / (ms * 1e-3) / 1e12, 1)
         out[name] = line
     return out
 

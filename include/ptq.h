@@ -183,6 +183,50 @@ PTQ_API PTQ_NODISCARD ptq_status ptq_ffn(
     const void* x, void* y, int64_t M, int64_t H, int64_t I, ptq_dtype dtype,
     void* workspace, size_t workspace_bytes, ptq_stream_t stream);
 
+/* ---- the chained feed-forward stack ("A 27B model in 5.5 GB: Bonsai ternary
+ * on Ferrox, locally", section "Speed, and where it goes", which names running
+ * the whole layer on the device, norms and residual adds included, as the
+ * next step).  The page gives no formula; this library reads it as the usual
+ * pre-norm residual stack, for l = 0 .. L-1:
+ *     xn = x / sqrt(mean_k x_k^2 + eps) * g_l;   x = x + FFN_l(xn)
+ * with FFN_l the block of ptq_ffn and g_l a per-layer gain vector. */
+
+/* One layer of the stack: ptq_ffn's weights and signs (same shapes and
+ * formats) and the RMSNorm gains, H fp32 values, 16-byte aligned.  All
+ * pointers are device pointers owned by the caller. */
+typedef struct ptq_ffn_layer {
+  const uint8_t* wgu_q;
+  const uint16_t* wgu_s;
+  const uint8_t* wd_q;
+  const uint16_t* wd_s;
+  const int8_t* signs_in;
+  const int8_t* signs_mid;
+  const float* norm_w;
+} ptq_ffn_layer;
+
+/* ptq_ffn_stack_workspace_bytes -- scratch ptq_ffn_stack needs; 0 when the
+ * arguments are invalid. */
+PTQ_API size_t ptq_ffn_stack_workspace_bytes(int64_t M, int64_t H, int64_t I,
+                                             ptq_dtype dtype);
+
+/* ptq_ffn_stack -- L chained pre-norm feed-forward blocks over the residual
+ * stream x (M x H fp32, device, 16-byte aligned, updated in place).
+ * layers: a HOST array of L entries, read during the call only.  eps: the
+ * RMSNorm's epsilon, finite and >= 0.  dtype selects the blocks' routing and
+ * activation type as in ptq_ffn: PTQ_F32 (M <= 8) keeps xn and the block
+ * output in fp32; PTQ_BF16 stores them in bf16 (the residual stream stays
+ * fp32 either way).  Per layer the call launches one add-and-norm kernel
+ * and the block's kernels; one final kernel adds the last block's output.
+ * workspace: device scratch of ptq_ffn_stack_workspace_bytes(...) bytes,
+ * 16-byte aligned, caller-owned, contents unspecified on return.  Every
+ * layer is validated before the first launch, so a refused call leaves x
+ * unchanged.  L == 0 or M == 0 is a no-op.  Errors as ptq_ffn (the message
+ * names the layer), plus PTQ_ERR_VALUE for a bad eps. */
+PTQ_API PTQ_NODISCARD ptq_status ptq_ffn_stack(
+    const ptq_ffn_layer* layers, int64_t L, float* x, int64_t M, int64_t H,
+    int64_t I, float eps, ptq_dtype dtype, void* workspace,
+    size_t workspace_bytes, ptq_stream_t stream);
+
 /* ptq_ffn_noalloc -- ptq_ffn without a workspace argument; it allocates
  * nothing.  (The source pages have no counterpart: this exists for callers,
  * not for the method.)

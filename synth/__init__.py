@@ -189,3 +189,8 @@ def ffn_layer(seed: int, layer: int, H: int, I: int) -> FfnLayer:
 def ffn_input(seed: int, layer: int, M: int, H: int, dtype: str = "f32") -> np.ndarray:
     base = 16 * layer
     return normal_f32(seed, base + 6, (M, H)) if dtype == "f32" else normal_bf16(seed, base + 6, (M, H))
+
+
+def norm_gain(seed: int, layer: int, H: int) -> np.ndarray:
+    """RMSNorm gains of one layer, fp32: 1 + 0.1 N(0, 1) (stream 16 * layer + 7)."""
+    return (1.0 + 0.1 * normal_f64(seed, 16 * layer + 7, (H,))).astype(np.float32)

@@ -28,7 +28,7 @@ STATUS = {
 # Every symbol include/ptq.h declares.
 EXPORTS = ("ptq1_pack", "ptq1_unpack", "ptq_fwht", "ptq_matmul_workspace_bytes", "ptq_matmul",
            "ptq_rotate_matmul_workspace_bytes", "ptq_rotate_matmul", "ptq_ffn_workspace_bytes",
-           "ptq_ffn", "ptq_ffn_noalloc", "ptq2_pack", "ptq2_unpack",
+           "ptq_ffn", "ptq_ffn_noalloc", "ptq_ffn_stack_workspace_bytes", "ptq_ffn_stack", "ptq2_pack", "ptq2_unpack",
            "ptq_matmul_pq2_workspace_bytes", "ptq_matmul_pq2", "ptq_embed", "ptq_embed_ptq1",
            "ptq_route", "ptq_selftest_timeout",
            "ptq_device_check", "ptq_status_str", "ptq_last_error")
@@ -73,6 +73,10 @@ def load(path: str | None = None):
     L.ptq_ffn_workspace_bytes.restype = ctypes.c_size_t
     L.ptq_ffn.argtypes = [_P] * 8 + [_I64, _I64, _I64, _I32, _P, ctypes.c_size_t, _P]
     L.ptq_ffn_noalloc.argtypes = [_P] * 8 + [_I64, _I64, _I64, _I32, _P]
+    L.ptq_ffn_stack_workspace_bytes.argtypes = [_I64, _I64, _I64, _I32]
+    L.ptq_ffn_stack_workspace_bytes.restype = ctypes.c_size_t
+    L.ptq_ffn_stack.argtypes = [_P, _I64, _P, _I64, _I64, _I64, ctypes.c_float, _I32, _P,
+                                ctypes.c_size_t, _P]
     L.ptq2_pack.argtypes = [_P, _P, _I64, _I64]
     L.ptq2_unpack.argtypes = [_P, _P, _I64, _I64, _P]
     L.ptq_matmul_pq2_workspace_bytes.argtypes = [_I64, _I64, _I64, _I32]
@@ -88,7 +92,7 @@ def load(path: str | None = None):
     L.ptq_last_error.argtypes = []
     L.ptq_last_error.restype = ctypes.c_char_p
     for name in ("ptq1_pack", "ptq1_unpack", "ptq_fwht", "ptq_matmul", "ptq_rotate_matmul", "ptq_ffn",
-                 "ptq_ffn_noalloc", "ptq2_pack", "ptq2_unpack", "ptq_matmul_pq2", "ptq_embed",
+                 "ptq_ffn_noalloc", "ptq_ffn_stack", "ptq2_pack", "ptq2_unpack", "ptq_matmul_pq2", "ptq_embed",
                  "ptq_embed_ptq1", "ptq_route", "ptq_device_check", "ptq_selftest_timeout"):
         getattr(L, name).restype = _I32
     _lib = L
@@ -286,6 +290,47 @@ def ffn(wgu_q, wgu_s, wd_q, wd_s, signs_in, signs_mid, x, out=None, workspace=No
                           workspace.numel() * workspace.element_size(), _stream(stream)),
            "ptq_ffn")
     return y
+
+
+class FfnLayer(ctypes.Structure):
+    """One layer of ptq_ffn_stack (include/ptq.h): device addresses."""
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("wgu_q", "wgu_s", "wd_q", "wd_s", "signs_in", "signs_mid", "norm_w")]
+
+
+def ffn_stack_workspace_bytes(M: int, H: int, I: int, dtype: int) -> int:
+    return int(load().ptq_ffn_stack_workspace_bytes(M, H, I, dtype))
+
+
+def ffn_stack(layers, norm_w, x, eps: float, act=None, workspace=None, stream=None):
+    """L chained pre-norm feed-forward blocks over the fp32 residual stream x
+    (M x H, updated in place and returned): x += ffn_l(rmsnorm(x) * g_l).
+    `layers`: per layer (wgu_q, wgu_s, wd_q, wd_s, signs_in, signs_mid) as for
+    ffn(); `norm_w`: per layer an H-vector of fp32 gains.  `act` is the
+    blocks' activation dtype, torch.float32 (default) or torch.bfloat16."""
+    import torch
+
+    if len(layers) != len(norm_w):
+        raise ValueError("layers and norm_w differ in length")
+    M, H = x.shape
+    L = len(layers)
+    I = layers[0][5].shape[0] if L else 1024
+    dt = _act_dtype(torch.empty(0, dtype=act or torch.float32))
+    need = ffn_stack_workspace_bytes(M, H, I, dt)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
+    arr = (FfnLayer * max(L, 1))()
+    names = ("wgu_q", "wgu_s", "wd_q", "wd_s", "signs_in", "signs_mid")
+    types = (torch.uint8, torch.int16, torch.uint8, torch.int16, torch.int8, torch.int8)
+    for l, (lay, g) in enumerate(zip(layers, norm_w)):
+        ptrs = [_dev(t, ty, f"layers[{l}].{n}") for t, ty, n in zip(lay, types, names)]
+        ptrs.append(_dev(g, torch.float32, f"norm_w[{l}]"))
+        arr[l] = FfnLayer(*[p.value for p in ptrs])
+    _check(load().ptq_ffn_stack(ctypes.cast(arr, ctypes.c_void_p), L, _dev(x, torch.float32, "x"),
+                                M, H, I, float(eps), dt, _dev(workspace, None, "workspace"),
+                                workspace.numel() * workspace.element_size(), _stream(stream)),
+           "ptq_ffn_stack")
+    return x
 
 
 def ffn_noalloc(wgu_q, wgu_s, wd_q, wd_s, signs_in, signs_mid, x, out=None, stream=None):

@@ -1,6 +1,7 @@
 // api.cu -- the C ABI: argument validation, the (M, dtype) routing table,
 // the host-side PTQ1_0 encoder and error reporting.  Every public entry point
 // validates everything before it launches anything.
+#include <math.h>
 #include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
@@ -514,33 +515,34 @@ PTQ_API size_t ptq_ffn_workspace_bytes(int64_t M, int64_t H, int64_t I, ptq_dtyp
   return total;
 }
 
-PTQ_API ptq_status ptq_ffn(const uint8_t* wgu_q, const uint16_t* wgu_s, const uint8_t* wd_q,
-                           const uint16_t* wd_s, const int8_t* signs_in, const int8_t* signs_mid,
-                           const void* x, void* y, int64_t M, int64_t H, int64_t I,
-                           ptq_dtype dtype, void* ws, size_t ws_bytes, ptq_stream_t stream) {
-  t_msg[0] = 0;
-  const char* who = "ptq_ffn";
-  if (!dtype_ok(dtype)) return fail(PTQ_ERR_VALUE, "%s: unknown dtype %d", who, (int)dtype);
-  if (M < 0 || H <= 0 || I <= 0 || H % kRot || I % kRot || I > INT64_MAX / 4)
-    return fail(PTQ_ERR_SHAPE, "%s: need M >= 0, H and I positive multiples of 1024", who);
-  size_t off[5], need;
-  if (!ffn_layout(M, H, I, dtype, off, &need)) return fail(PTQ_ERR_SHAPE, "%s: size overflow", who);
-  if (M == 0) return PTQ_OK;
-  const Route *r_gu = nullptr, *r_d = nullptr;
-  ptq_status s = check_matmul(wgu_q, wgu_s, x, y, M, 2 * I, H, dtype, who, &r_gu);
+// The per-block checks of ptq_ffn (weights, signs, dtype routing); the
+// shape and workspace checks are the caller's.
+struct FfnRoutes {
+  const Route* gu;
+  const Route* d;
+};
+
+static ptq_status check_ffn_block(const uint8_t* wgu_q, const uint16_t* wgu_s, const uint8_t* wd_q,
+                                  const uint16_t* wd_s, const int8_t* signs_in,
+                                  const int8_t* signs_mid, const void* x, const void* y,
+                                  int64_t M, int64_t H, int64_t I, ptq_dtype dtype, const char* who,
+                                  FfnRoutes* r) {
+  ptq_status s = check_matmul(wgu_q, wgu_s, x, y, M, 2 * I, H, dtype, who, &r->gu);
   if (s != PTQ_OK) return s;
-  s = check_matmul(wd_q, wd_s, x, y, M, H, I, dtype, who, &r_d);
+  s = check_matmul(wd_q, wd_s, x, y, M, H, I, dtype, who, &r->d);
   if (s != PTQ_OK) return s;
   if (!signs_in || !signs_mid) return fail(PTQ_ERR_NULL, "%s: NULL signs", who);
   if (!aligned(signs_in, 4) || !aligned(signs_mid, 4))
     return fail(PTQ_ERR_ALIGN, "%s: signs need 4-byte alignment", who);
-  if (!ws) return fail(PTQ_ERR_WORKSPACE, "%s: workspace is NULL (%zu bytes needed)", who, need);
-  if (ws_bytes < need)
-    return fail(PTQ_ERR_WORKSPACE, "%s: workspace has %zu bytes, %zu needed", who, ws_bytes, need);
-  if (!aligned(ws, 16)) return fail(PTQ_ERR_ALIGN, "%s: workspace needs 16-byte alignment", who);
+  return PTQ_OK;
+}
 
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  char* base = static_cast<char*>(ws);
+// Launches one feed-forward block; base/off/need are ffn_layout's regions.
+static cudaError_t run_ffn_block(const FfnRoutes& r, const uint8_t* wgu_q, const uint16_t* wgu_s,
+                                 const uint8_t* wd_q, const uint16_t* wd_s,
+                                 const int8_t* signs_in, const int8_t* signs_mid, const void* x,
+                                 void* y, int64_t M, int64_t H, int64_t I, ptq_dtype dtype,
+                                 char* base, const size_t off[5], size_t need, cudaStream_t st) {
   void* xr = base + off[0];
   float* gu = reinterpret_cast<float*>(base + off[1]);
   float* h = reinterpret_cast<float*>(base + off[2]);
@@ -548,7 +550,7 @@ PTQ_API ptq_status ptq_ffn(const uint8_t* wgu_q, const uint16_t* wgu_s, const ui
   void* hr = bf ? static_cast<void*>(base + off[3]) : static_cast<void*>(h);
   void* part = base + off[4];
   const Act op = bf ? Act::F16 : Act::F32;  // tensor-core operand type
-  if (!bf && r_gu->kernel == Kernel::GemvF32 && gemv_lut_supported(2 * I, H, true) &&
+  if (!bf && r.gu->kernel == Kernel::GemvF32 && gemv_lut_supported(2 * I, H, true) &&
       gemv_lut_supported(H, I, true)) {
     // decode, token by token: each table-lookup GEMV rotates its own
     // activations, and the gate/up row sums are reduced straight into
@@ -562,27 +564,138 @@ PTQ_API ptq_status ptq_ffn(const uint8_t* wgu_q, const uint16_t* wgu_s, const ui
         e = launch_gemv_lut(wd_q, wd_s, hm, signs_mid, static_cast<float*>(y) + m * H,
                             static_cast<float*>(part), H, I, LutEpilogue::Plain, st);
     }
-    return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq_ffn launch");
+    return e;
   }
   cudaError_t e = launch_fwht(x, act_of(dtype), xr, op, signs_in, M, H, st);
   // prefill: SwiGLU in the gate/up GEMM's epilogue when that GEMM runs
   // unsplit; otherwise gate/up into fp32, then the SwiGLU kernel
   bool fused = false;
-  if (e == cudaSuccess && r_gu->kernel == Kernel::GemmBf16) {
+  if (e == cudaSuccess && r.gu->kernel == Kernel::GemmBf16) {
     e = launch_gemm_tc_swiglu(wgu_q, wgu_s, xr, op, h, M, I, H, st);
     fused = e == cudaSuccess;
     if (e == cudaErrorNotSupported) e = cudaSuccess;
   }
   if (e == cudaSuccess && !fused) {
-    e = run_matmul(r_gu, wgu_q, wgu_s, xr, op, gu, Act::F32, M, 2 * I, H, part, need - off[4], st);
+    e = run_matmul(r.gu, wgu_q, wgu_s, xr, op, gu, Act::F32, M, 2 * I, H, part, need - off[4], st);
     if (e == cudaSuccess) e = launch_swiglu(gu, h, M, I, st);
   }
   if (e == cudaSuccess) e = launch_fwht(h, Act::F32, hr, op, signs_mid, M, I, st);
   // the down projection's split-K partials go where gate/up was (dead after
   // SwiGLU)
   if (e == cudaSuccess)
-    e = run_matmul(r_d, wd_q, wd_s, hr, op, y, act_of(dtype), M, H, I, gu, off[2] - off[1], st);
+    e = run_matmul(r.d, wd_q, wd_s, hr, op, y, act_of(dtype), M, H, I, gu, off[2] - off[1], st);
+  return e;
+}
+
+static bool ffn_shape_ok(int64_t M, int64_t H, int64_t I) {
+  return M >= 0 && H > 0 && I > 0 && H % kRot == 0 && I % kRot == 0 && I <= INT64_MAX / 4;
+}
+
+PTQ_API ptq_status ptq_ffn(const uint8_t* wgu_q, const uint16_t* wgu_s, const uint8_t* wd_q,
+                           const uint16_t* wd_s, const int8_t* signs_in, const int8_t* signs_mid,
+                           const void* x, void* y, int64_t M, int64_t H, int64_t I,
+                           ptq_dtype dtype, void* ws, size_t ws_bytes, ptq_stream_t stream) {
+  t_msg[0] = 0;
+  const char* who = "ptq_ffn";
+  if (!dtype_ok(dtype)) return fail(PTQ_ERR_VALUE, "%s: unknown dtype %d", who, (int)dtype);
+  if (!ffn_shape_ok(M, H, I))
+    return fail(PTQ_ERR_SHAPE, "%s: need M >= 0, H and I positive multiples of 1024", who);
+  size_t off[5], need;
+  if (!ffn_layout(M, H, I, dtype, off, &need)) return fail(PTQ_ERR_SHAPE, "%s: size overflow", who);
+  if (M == 0) return PTQ_OK;
+  FfnRoutes r;
+  ptq_status s =
+      check_ffn_block(wgu_q, wgu_s, wd_q, wd_s, signs_in, signs_mid, x, y, M, H, I, dtype, who, &r);
+  if (s != PTQ_OK) return s;
+  if (!ws) return fail(PTQ_ERR_WORKSPACE, "%s: workspace is NULL (%zu bytes needed)", who, need);
+  if (ws_bytes < need)
+    return fail(PTQ_ERR_WORKSPACE, "%s: workspace has %zu bytes, %zu needed", who, ws_bytes, need);
+  if (!aligned(ws, 16)) return fail(PTQ_ERR_ALIGN, "%s: workspace needs 16-byte alignment", who);
+  const cudaError_t e = run_ffn_block(r, wgu_q, wgu_s, wd_q, wd_s, signs_in, signs_mid, x, y, M, H,
+                                      I, dtype, static_cast<char*>(ws), off, need,
+                                      reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq_ffn launch");
+}
+
+// Workspace of ptq_ffn_stack, each region rounded up to 256 bytes:
+//   xn (M x H, dtype: the block input) | y (M x H, dtype: the block output)
+//   | ptq_ffn's workspace
+static bool stack_layout(int64_t M, int64_t H, int64_t I, ptq_dtype dt, size_t off[3],
+                         size_t ffn_off[5], size_t* ffn_need, size_t* total) {
+  int64_t a;
+  if (!mul_ok(M, H, &a) || !mul_ok(a, (int64_t)dsize(dt), &a) || a > INT64_MAX / 4) return false;
+  if (!ffn_layout(M, H, I, dt, ffn_off, ffn_need)) return false;
+  const size_t r = (size_t)((a + 255) / 256 * 256);
+  off[0] = 0;
+  off[1] = r;
+  off[2] = 2 * r;
+  if (*ffn_need > SIZE_MAX - off[2]) return false;
+  *total = off[2] + *ffn_need;
+  return true;
+}
+
+PTQ_API size_t ptq_ffn_stack_workspace_bytes(int64_t M, int64_t H, int64_t I, ptq_dtype dtype) {
+  size_t off[3], foff[5], fneed, total;
+  if (!dtype_ok(dtype) || !ffn_shape_ok(M, H, I) ||
+      !stack_layout(M, H, I, dtype, off, foff, &fneed, &total))
+    return 0;
+  return total;
+}
+
+PTQ_API ptq_status ptq_ffn_stack(const ptq_ffn_layer* layers, int64_t L, float* x, int64_t M,
+                                 int64_t H, int64_t I, float eps, ptq_dtype dtype, void* ws,
+                                 size_t ws_bytes, ptq_stream_t stream) {
+  t_msg[0] = 0;
+  const char* who = "ptq_ffn_stack";
+  if (!dtype_ok(dtype)) return fail(PTQ_ERR_VALUE, "%s: unknown dtype %d", who, (int)dtype);
+  if (L < 0 || !ffn_shape_ok(M, H, I))
+    return fail(PTQ_ERR_SHAPE, "%s: need L >= 0, M >= 0, H and I positive multiples of 1024",
+                who);
+  if (!(eps >= 0.0f) || !(eps < INFINITY))
+    return fail(PTQ_ERR_VALUE, "%s: eps must be finite and >= 0", who);
+  size_t off[3], foff[5], fneed, need;
+  if (!stack_layout(M, H, I, dtype, off, foff, &fneed, &need))
+    return fail(PTQ_ERR_SHAPE, "%s: size overflow", who);
+  if (M == 0 || L == 0) return PTQ_OK;
+  if (!layers) return fail(PTQ_ERR_NULL, "%s: layers is NULL", who);
+  if (!x) return fail(PTQ_ERR_NULL, "%s: x is NULL", who);
+  if (!aligned(x, 16)) return fail(PTQ_ERR_ALIGN, "%s: x needs 16-byte alignment", who);
+  if (!ws) return fail(PTQ_ERR_WORKSPACE, "%s: workspace is NULL (%zu bytes needed)", who, need);
+  if (ws_bytes < need)
+    return fail(PTQ_ERR_WORKSPACE, "%s: workspace has %zu bytes, %zu needed", who, ws_bytes, need);
+  if (!aligned(ws, 16)) return fail(PTQ_ERR_ALIGN, "%s: workspace needs 16-byte alignment", who);
+  char* base = static_cast<char*>(ws);
+  void* xn = base + off[0];
+  void* y = base + off[1];
+  char* fbase = base + off[2];
+  // every layer is checked before the first launch, so a refused call leaves
+  // x untouched
+  FfnRoutes r0 = {nullptr, nullptr};
+  for (int64_t l = 0; l < L; ++l) {
+    const ptq_ffn_layer& ly = layers[l];
+    char lw[64];
+    snprintf(lw, sizeof lw, "%s: layer %lld", who, (long long)l);
+    FfnRoutes r;
+    ptq_status s = check_ffn_block(ly.wgu_q, ly.wgu_s, ly.wd_q, ly.wd_s, ly.signs_in,
+                                   ly.signs_mid, xn, y, M, H, I, dtype, lw, &r);
+    if (s != PTQ_OK) return s;
+    if (!ly.norm_w) return fail(PTQ_ERR_NULL, "%s: norm_w is NULL", lw);
+    if (!aligned(ly.norm_w, 16)) return fail(PTQ_ERR_ALIGN, "%s: norm_w needs 16-byte alignment", lw);
+    if (l == 0) r0 = r;
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const Act t = act_of(dtype);
+  cudaError_t e = cudaSuccess;
+  for (int64_t l = 0; l < L && e == cudaSuccess; ++l) {
+    const ptq_ffn_layer& ly = layers[l];
+    // x += y (from the second layer on); xn = RMSNorm(x) * g_l
+    e = launch_add_rmsnorm(x, l ? y : nullptr, ly.norm_w, xn, t, M, H, eps, st);
+    if (e == cudaSuccess)
+      e = run_ffn_block(r0, ly.wgu_q, ly.wgu_s, ly.wd_q, ly.wd_s, ly.signs_in, ly.signs_mid, xn, y,
+                        M, H, I, dtype, fbase, foff, fneed, st);
+  }
+  if (e == cudaSuccess) e = launch_add_rmsnorm(x, y, nullptr, nullptr, t, M, H, eps, st);
+  return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq_ffn_stack launch");
 }
 
 PTQ_API ptq_status ptq_selftest_timeout(ptq_stream_t stream) {

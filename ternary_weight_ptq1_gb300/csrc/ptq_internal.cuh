@@ -104,6 +104,13 @@ cudaError_t launch_gemm(const uint8_t* wq, const uint16_t* scales, const void* x
 cudaError_t launch_swiglu(const float* gu, float* h, int64_t M, int64_t I,
                           cudaStream_t st);
 
+// Residual add and RMSNorm between chained blocks (k_norm.cu): per row of
+// x (M x H fp32, in place) x += y, then xn = x / sqrt(mean(x^2) + eps) * g.
+// y and xn are F32 or BF16 (t); y == nullptr skips the add, xn == nullptr
+// the norm.  H % 4 == 0; x, y, g, xn 16-byte aligned.
+cudaError_t launch_add_rmsnorm(float* x, const void* y, const float* g, void* xn, Act t,
+                               int64_t M, int64_t H, float eps, cudaStream_t st);
+
 // Tensor-core GEMM (k_gemm_tc.cu); cudaErrorNotSupported when the shape does
 // not fit it (the caller then uses the SIMT kernel).
 cudaError_t launch_gemm_tc(const uint8_t* wq, const uint16_t* scales, const void* x, Act x_t,

@@ -128,6 +128,52 @@ def test_refusals_before_launch(P):
     assert P.ffn_workspace_bytes(1, 1000, 2048, P.PTQ_F32) == 0
 
 
+
+def test_stack_refusals_before_launch(P):
+    L = P.load()
+    p16 = ctypes.c_void_p(16 * 1024)   # never dereferenced: every call below is refused
+    odd = ctypes.c_void_p(16 * 1024 + 4)
+    H, I = 1024, 2048
+    need = P.ffn_stack_workspace_bytes(1, H, I, P.PTQ_F32)
+    # xn and y regions (256-byte rounded) ahead of the block's own scratch
+    assert need == 2 * H * 4 + P.ffn_workspace_bytes(1, H, I, P.PTQ_F32)
+    assert P.ffn_stack_workspace_bytes(3, H, I, P.PTQ_BF16) == (
+        2 * ((3 * H * 2 + 255) // 256 * 256) + P.ffn_workspace_bytes(3, H, I, P.PTQ_BF16))
+    assert P.ffn_stack_workspace_bytes(1, 1000, I, P.PTQ_F32) == 0
+    assert P.ffn_stack_workspace_bytes(1, H, I, 9) == 0
+    good = P.FfnLayer(*([16 * 1024] * 7))
+    bad_w = P.FfnLayer(*([16 * 1024] * 6 + [16 * 1024 + 4]))      # misaligned gains
+    no_w = P.FfnLayer(*([16 * 1024] * 6 + [None]))
+    no_q = P.FfnLayer(*([None] + [16 * 1024] * 6))
+
+    def st(layers, nL, x=p16, M=1, h=H, eps=1e-6, dt=P.PTQ_F32, ws=p16, wsb=need):
+        arr = (P.FfnLayer * max(len(layers), 1))(*layers)
+        return L.ptq_ffn_stack(ctypes.cast(arr, ctypes.c_void_p), nL, x, M, h, I, eps, dt, ws, wsb,
+                               None)
+
+    assert st([good], 1, dt=7) == 4
+    assert st([good], -1) == 2
+    assert st([good], 1, h=1000) == 2
+    assert st([good], 1, eps=-1.0) == 4
+    assert st([good], 1, eps=float("nan")) == 4
+    assert st([good], 1, eps=float("inf")) == 4
+    assert st([good], 1, x=None) == 1
+    assert st([good], 1, x=odd) == 3
+    assert st([good], 1, ws=None) == 6
+    assert st([good], 1, wsb=need - 1) == 6
+    assert st([good], 1, ws=odd) == 3
+    assert st([good], 1, M=9, wsb=10 ** 9) == 5         # fp32 serves M <= 8
+    assert L.ptq_ffn_stack(None, 1, p16, 1, H, I, 1e-6, P.PTQ_F32, p16, need, None) == 1
+    # every layer is checked before the first launch; the message names it
+    assert st([good, no_q], 2) == 1
+    assert b"layer 1" in L.ptq_last_error()
+    assert st([good, good, no_w], 3) == 1
+    assert b"layer 2" in L.ptq_last_error()
+    assert st([bad_w], 1) == 3
+    # no layers or no rows: nothing to do
+    assert st([], 0, x=None, ws=None, wsb=0) == 0
+    assert st([good], 1, M=0, x=None, ws=None, wsb=0) == 0
+
 def test_routing_table(P):
     for M in range(1, 9):
         assert P.route(M, P.PTQ_F32) == "gemv_ptq1_f32_lut"

@@ -1,0 +1,164 @@
+"""GPU parity of ptq_ffn_stack (L chained pre-norm feed-forward blocks over
+an fp32 residual stream) against the oracle's fp64 stack.
+
+Tolerance.  The stack's error is the sum of its blocks' errors plus what the
+later blocks do with the earlier ones.  Block l adds y_l to x; its own error
+is within the single-block tolerance of y_l (fp32 path: 1e-4 (|y_l| +
+rms(y_l)); bf16 path: 1e-2 rms(y_l) + 2^-8 |y_l|).  An error d in x reaches
+the next block's output scaled by at most 2 rho, with
+rho = max_l rms(y_l) / rms(x_l): the norm divides d by rms(x), and SwiGLU's
+product of two linear maps at most doubles a relative change.  So after L
+blocks
+    |x - x_ref| <= (1 + 2 rho)^(L-1) * sum_l tol(y_l),
+with every y_l and x_l taken from the oracle, layer by layer."""
+import numpy as np
+import pytest
+
+import parity as Q
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def P():
+    import torch
+
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import ternary_weight_ptq1_gb300 as P
+
+    P.load()
+    return P
+
+
+def make_layers(P, orc, syn, seed, Lc, H, I):
+    """Device tuples, oracle tuples and fp32 gains of Lc seeded layers."""
+    dev, host, gains = [], [], []
+    for l in range(Lc):
+        F = syn.ffn_layer(seed, l, H, I)
+        gq, dq = P.pack(F.wgu_trits), P.pack(F.wd_trits)
+        dev.append((Q.dev(gq), Q.dev(F.wgu_scales), Q.dev(dq), Q.dev(F.wd_scales),
+                    Q.dev(F.signs_in), Q.dev(F.signs_mid)))
+        host.append((orc.pack(F.wgu_trits), F.wgu_scales, orc.pack(F.wd_trits), F.wd_scales,
+                     F.signs_in, F.signs_mid))
+        del F
+        gains.append(syn.norm_gain(seed, l, H))
+    return dev, host, gains
+
+
+def oracle_with_bound(orc, host, gains, x64, eps, bf16):
+    """The oracle's stack output and the elementwise bound of the docstring."""
+    x = x64.copy()
+    tol = np.zeros_like(x)
+    rho = 0.0
+    for lay, g in zip(host, gains):
+        nx = orc.ffn_stack([lay], [g.astype(np.float64)], x, eps)
+        y = nx - x
+        r = Q.rms(y)
+        tol += (1e-2 * r + 2.0 ** -8 * np.abs(y)) if bf16 else 1e-4 * (np.abs(y) + r)
+        rho = max(rho, r / Q.rms(x))
+        x = nx
+    return x, tol * (1.0 + 2.0 * rho) ** (len(host) - 1)
+
+
+def check_stack(y, ref, bound, what):
+    y = np.asarray(y, np.float64)
+    assert np.isfinite(y).all(), f"{what}: non-finite output"
+    err = np.abs(y - ref)
+    bad = err > bound
+    if bad.any():
+        i = np.unravel_index(np.argmax(err - bound), err.shape)
+        raise AssertionError(f"{what}: {int(bad.sum())}/{bad.size} outside tolerance; worst at {i}: "
+                             f"y={y[i]!r} ref={ref[i]!r} err={err[i]:.3e} bound={bound[i]:.3e}")
+
+
+def run_stack(P, dev, gains, x, eps, act):
+    import torch
+
+    xd = Q.dev(np.ascontiguousarray(x, np.float32))
+    P.ffn_stack(dev, [Q.dev(g) for g in gains], xd, eps, act=act)
+    torch.cuda.synchronize()
+    return xd.cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("M,act", [(1, "f32"), (3, "f32"), (8, "f32"), (5, "bf16"), (70, "bf16")])
+def test_stack_small(P, orc, syn, M, act):
+    import torch
+
+    H, I, Lc, eps = 1024, 2048, 3, 1e-6
+    dev, host, gains = make_layers(P, orc, syn, 30 + M, Lc, H, I)
+    x = syn.ffn_input(30 + M, 0, M, H, "f32")
+    got = run_stack(P, dev, gains, x, eps, torch.float32 if act == "f32" else torch.bfloat16)
+    ref, bound = oracle_with_bound(orc, host, gains, x.astype(np.float64), eps, act == "bf16")
+    check_stack(got, ref, bound, f"stack L={Lc} M={M} {act}")
+
+
+def test_stack_one_layer_is_residual_plus_block(P, orc, syn):
+    # with one layer the stack is x + ffn(rmsnorm(x) g): compare the increment
+    # with the single-block tolerance directly
+    import torch
+
+    H, I, eps = 1024, 2048, 1e-5
+    dev, host, gains = make_layers(P, orc, syn, 40, 1, H, I)
+    x = syn.ffn_input(40, 0, 2, H, "f32")
+    got = run_stack(P, dev, gains, x, eps, torch.float32)
+    x64 = x.astype(np.float64)
+    ref = orc.ffn_stack(host, [g.astype(np.float64) for g in gains], x64, eps)
+    Q.check_f32(got - x64, ref - x64, "stack L=1 increment")
+
+
+def test_stack_eps_dominates_a_tiny_row(P, orc, syn):
+    # a row of mean square 1e-8 with eps = 1e-2: the norm is x / sqrt(eps)
+    # to within 1e-6, so eps must reach the kernel as given
+    import torch
+
+    H, I, eps = 1024, 2048, 1e-2
+    dev, host, gains = make_layers(P, orc, syn, 41, 2, H, I)
+    x = (1e-4 * syn.ffn_input(41, 0, 1, H, "f32")).astype(np.float32)
+    got = run_stack(P, dev, gains, x, eps, torch.float32)
+    ref, bound = oracle_with_bound(orc, host, gains, x.astype(np.float64), eps, False)
+    check_stack(got, ref, bound, "stack eps-dominated row")
+
+
+def test_stack_refused_layer_leaves_x_alone(P, syn):
+    import torch
+
+    H, I = 1024, 2048
+    F = syn.ffn_layer(42, 0, H, I)
+    lay = (Q.dev(P.pack(F.wgu_trits)), Q.dev(F.wgu_scales), Q.dev(P.pack(F.wd_trits)),
+           Q.dev(F.wd_scales), Q.dev(F.signs_in), Q.dev(F.signs_mid))
+    g = Q.dev(syn.norm_gain(42, 0, H))
+    x = Q.dev(syn.ffn_input(42, 0, 2, H, "f32"))
+    x0 = x.clone()
+    short = (lay[0], lay[1], lay[2], lay[3][:-8], lay[4], lay[5])  # fine for the ABI ...
+    bad = (lay[0], lay[1], lay[2], lay[3], lay[4], lay[5][1:])     # ... misaligned signs are not
+    with pytest.raises(P.PTQError, match="ALIGN"):
+        P.ffn_stack([lay, short, bad], [g, g, g], x, 1e-6)
+    torch.cuda.synchronize()
+    assert torch.equal(x, x0)
+
+
+def test_stack_decode_full_size_ring(P, orc, syn):
+    # the bench's decode shape: H = 5120, I = 17408, M = 1, fp32, over the 8
+    # distinct layers the 64-layer step cycles through
+    import torch
+
+    H, I, Lc, eps = 5120, 17408, 8, 1e-6
+    dev, host, gains = make_layers(P, orc, syn, 4, Lc, H, I)
+    x = syn.ffn_input(4, 0, 1, H, "f32")
+    got = run_stack(P, dev, gains, x, eps, torch.float32)
+    ref, bound = oracle_with_bound(orc, host, gains, x.astype(np.float64), eps, False)
+    check_stack(got, ref, bound, "stack decode H=5120 I=17408 L=8")
+
+
+def test_stack_prefill_full_size_sampled_tokens(P, orc, syn):
+    # the bench's prefill shape (M = 256, bf16 activations) over two layers;
+    # rows are independent in the stack, so the oracle runs sampled tokens
+    import torch
+
+    H, I, Lc, eps, M = 5120, 17408, 2, 1e-6, 256
+    dev, host, gains = make_layers(P, orc, syn, 4, Lc, H, I)
+    x = syn.ffn_input(4, 1, M, H, "f32")
+    got = run_stack(P, dev, gains, x, eps, torch.bfloat16)
+    tokens = [0, 1, 128, 255]
+    ref, bound = oracle_with_bound(orc, host, gains, x[tokens].astype(np.float64), eps, True)
+    check_stack(got[tokens], ref, bound, "stack prefill M=256 sampled tokens")
