@@ -92,6 +92,21 @@ def test_stack_small(P, orc, syn, M, act):
     check_stack(got, ref, bound, f"stack L={Lc} M={M} {act}")
 
 
+@pytest.mark.parametrize("H", [1024, 5120, 12288, 17408])
+@pytest.mark.parametrize("M,act", [(2, "f32"), (3, "bf16")])
+def test_stack_row_lengths(P, orc, syn, H, M, act):
+    # the add-and-norm kernel holds 1, 2 or 4 vectors of a row per thread
+    # (H = 1024, 5120, 12288) and loops over longer rows (H = 17408)
+    import torch
+
+    I, Lc, eps = 1024, 2, 1e-6
+    dev, host, gains = make_layers(P, orc, syn, 50 + H // 1024, Lc, H, I)
+    x = syn.ffn_input(50, 0, M, H, "f32")
+    got = run_stack(P, dev, gains, x, eps, torch.float32 if act == "f32" else torch.bfloat16)
+    ref, bound = oracle_with_bound(orc, host, gains, x.astype(np.float64), eps, act == "bf16")
+    check_stack(got, ref, bound, f"stack H={H} M={M} {act}")
+
+
 def test_stack_one_layer_is_residual_plus_block(P, orc, syn):
     # with one layer the stack is x + ffn(rmsnorm(x) g): compare the increment
     # with the single-block tolerance directly
