@@ -483,3 +483,19 @@ def test_stack_rmsnorm_worked_values(orc, syn):
     np.testing.assert_allclose(orc.ffn_stack([lay], [np.ones(H)], x, 0.0), expect, rtol=1e-12,
                                atol=1e-12)
 
+
+def test_stack_gain_and_eps_worked_values(orc, syn):
+    # rows of 3s and 4s (mean square 12.5).  Gains alternating 2 and 1/2 with
+    # eps = 0 give the block 6/sqrt(12.5) and 2/sqrt(12.5); eps = 3.5 with unit
+    # gains makes the divisor sqrt(16) = 4 exactly, so the block sees 0.75 and
+    # 1.0 (a divisor sqrt(12.5) + 3.5 would not)
+    H, I = 1024, 1024
+    x = np.tile([3.0, 4.0], (1, H // 2))
+    lay = _stack_layer(syn, 63, 0, H, I)
+    g = np.tile([2.0, 0.5], H // 2)
+    xn = np.tile([6.0 / np.sqrt(12.5), 2.0 / np.sqrt(12.5)], (1, H // 2))
+    np.testing.assert_allclose(orc.ffn_stack([lay], [g], x, 0.0), x + orc.ffn(*lay, xn),
+                               rtol=1e-12, atol=1e-12)
+    xn = np.tile([0.75, 1.0], (1, H // 2))
+    np.testing.assert_allclose(orc.ffn_stack([lay], [np.ones(H)], x, 3.5), x + orc.ffn(*lay, xn),
+                               rtol=1e-12, atol=1e-12)
