@@ -215,8 +215,9 @@ PTQ_API size_t ptq_ffn_stack_workspace_bytes(int64_t M, int64_t H, int64_t I,
  * RMSNorm's epsilon, finite and >= 0.  dtype selects the blocks' routing and
  * activation type as in ptq_ffn: PTQ_F32 (M <= 8) keeps xn and the block
  * output in fp32; PTQ_BF16 stores them in bf16 (the residual stream stays
- * fp32 either way).  Per layer the call launches one add-and-norm kernel
- * and the block's kernels; one final kernel adds the last block's output.
+ * fp32 either way).  ptq_ffn_stack_route names the implementation: one
+ * persistent launch per 24 layers for a single fp32 token, else per layer
+ * an add-and-norm kernel and the block's kernels, and a final add.
  * workspace: device scratch of ptq_ffn_stack_workspace_bytes(...) bytes,
  * 16-byte aligned, caller-owned, contents unspecified on return.  Every
  * layer is validated before the first launch, so a refused call leaves x
@@ -226,6 +227,19 @@ PTQ_API PTQ_NODISCARD ptq_status ptq_ffn_stack(
     const ptq_ffn_layer* layers, int64_t L, float* x, int64_t M, int64_t H,
     int64_t I, float eps, ptq_dtype dtype, void* workspace,
     size_t workspace_bytes, ptq_stream_t stream);
+
+/* ptq_ffn_stack_route -- which implementation ptq_ffn_stack uses for
+ * (M, H, I, dtype) on the current device: "stack_decode_persistent" (M = 1,
+ * PTQ_F32: the whole stack in one cooperative launch per 24 layers, one CTA
+ * per SM, the layers separated by grid-wide barriers whose waits are
+ * bounded -- a wait that runs out raises the status ptq_device_check
+ * reports) or "stack_per_layer" (an add-and-norm kernel, then ptq_ffn's
+ * kernels, per layer).  *name points to a static string.  Errors:
+ * PTQ_ERR_NULL, PTQ_ERR_VALUE (dtype), PTQ_ERR_SHAPE, PTQ_ERR_UNSUPPORTED
+ * (no kernel for M and dtype). */
+PTQ_API PTQ_NODISCARD ptq_status ptq_ffn_stack_route(int64_t M, int64_t H,
+                                                     int64_t I, ptq_dtype dtype,
+                                                     const char** name);
 
 /* ptq_ffn_noalloc -- ptq_ffn without a workspace argument; it allocates
  * nothing.  (The source pages have no counterpart: this exists for callers,

@@ -28,7 +28,8 @@ STATUS = {
 # Every symbol include/ptq.h declares.
 EXPORTS = ("ptq1_pack", "ptq1_unpack", "ptq_fwht", "ptq_matmul_workspace_bytes", "ptq_matmul",
            "ptq_rotate_matmul_workspace_bytes", "ptq_rotate_matmul", "ptq_ffn_workspace_bytes",
-           "ptq_ffn", "ptq_ffn_noalloc", "ptq_ffn_stack_workspace_bytes", "ptq_ffn_stack", "ptq2_pack", "ptq2_unpack",
+           "ptq_ffn", "ptq_ffn_noalloc", "ptq_ffn_stack_workspace_bytes", "ptq_ffn_stack",
+           "ptq_ffn_stack_route", "ptq2_pack", "ptq2_unpack",
            "ptq_matmul_pq2_workspace_bytes", "ptq_matmul_pq2", "ptq_embed", "ptq_embed_ptq1",
            "ptq_route", "ptq_selftest_timeout",
            "ptq_device_check", "ptq_status_str", "ptq_last_error")
@@ -77,6 +78,7 @@ def load(path: str | None = None):
     L.ptq_ffn_stack_workspace_bytes.restype = ctypes.c_size_t
     L.ptq_ffn_stack.argtypes = [_P, _I64, _P, _I64, _I64, _I64, ctypes.c_float, _I32, _P,
                                 ctypes.c_size_t, _P]
+    L.ptq_ffn_stack_route.argtypes = [_I64, _I64, _I64, _I32, ctypes.POINTER(ctypes.c_char_p)]
     L.ptq2_pack.argtypes = [_P, _P, _I64, _I64]
     L.ptq2_unpack.argtypes = [_P, _P, _I64, _I64, _P]
     L.ptq_matmul_pq2_workspace_bytes.argtypes = [_I64, _I64, _I64, _I32]
@@ -92,7 +94,8 @@ def load(path: str | None = None):
     L.ptq_last_error.argtypes = []
     L.ptq_last_error.restype = ctypes.c_char_p
     for name in ("ptq1_pack", "ptq1_unpack", "ptq_fwht", "ptq_matmul", "ptq_rotate_matmul", "ptq_ffn",
-                 "ptq_ffn_noalloc", "ptq_ffn_stack", "ptq2_pack", "ptq2_unpack", "ptq_matmul_pq2", "ptq_embed",
+                 "ptq_ffn_noalloc", "ptq_ffn_stack", "ptq_ffn_stack_route", "ptq2_pack",
+                 "ptq2_unpack", "ptq_matmul_pq2", "ptq_embed",
                  "ptq_embed_ptq1", "ptq_route", "ptq_device_check", "ptq_selftest_timeout"):
         getattr(L, name).restype = _I32
     _lib = L
@@ -300,6 +303,13 @@ class FfnLayer(ctypes.Structure):
 
 def ffn_stack_workspace_bytes(M: int, H: int, I: int, dtype: int) -> int:
     return int(load().ptq_ffn_stack_workspace_bytes(M, H, I, dtype))
+
+
+def ffn_stack_route(M: int, H: int, I: int, dtype: int) -> str:
+    """The implementation ptq_ffn_stack uses for (M, H, I, dtype) here."""
+    name = ctypes.c_char_p()
+    _check(load().ptq_ffn_stack_route(M, H, I, dtype, ctypes.byref(name)), "ptq_ffn_stack_route")
+    return name.value.decode()
 
 
 def ffn_stack(layers, norm_w, x, eps: float, act=None, workspace=None, stream=None):

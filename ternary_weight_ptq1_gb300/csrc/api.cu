@@ -642,6 +642,27 @@ PTQ_API size_t ptq_ffn_stack_workspace_bytes(int64_t M, int64_t H, int64_t I, pt
   return total;
 }
 
+// One decode token in fp32 runs the stack as one persistent launch per 24
+// layers when the device and the shapes allow it.
+static bool stack_persistent(int64_t M, int64_t H, int64_t I, ptq_dtype dt) {
+  return M == 1 && dt == PTQ_F32 && stack_decode_supported(H, I);
+}
+
+PTQ_API ptq_status ptq_ffn_stack_route(int64_t M, int64_t H, int64_t I, ptq_dtype dtype,
+                                       const char** name) {
+  t_msg[0] = 0;
+  if (!name) return fail(PTQ_ERR_NULL, "ptq_ffn_stack_route: name is NULL");
+  if (!dtype_ok(dtype))
+    return fail(PTQ_ERR_VALUE, "ptq_ffn_stack_route: unknown dtype %d", (int)dtype);
+  if (M < 1 || !ffn_shape_ok(M, H, I))
+    return fail(PTQ_ERR_SHAPE, "ptq_ffn_stack_route: need M >= 1, H and I multiples of 1024");
+  if (!find_route(M, dtype))
+    return fail(PTQ_ERR_UNSUPPORTED, "ptq_ffn_stack_route: no kernel for M=%lld dtype=%s",
+                (long long)M, dtype == PTQ_F32 ? "f32" : "bf16");
+  *name = stack_persistent(M, H, I, dtype) ? "stack_decode_persistent" : "stack_per_layer";
+  return PTQ_OK;
+}
+
 PTQ_API ptq_status ptq_ffn_stack(const ptq_ffn_layer* layers, int64_t L, float* x, int64_t M,
                                  int64_t H, int64_t I, float eps, ptq_dtype dtype, void* ws,
                                  size_t ws_bytes, ptq_stream_t stream) {
@@ -684,6 +705,19 @@ PTQ_API ptq_status ptq_ffn_stack(const ptq_ffn_layer* layers, int64_t L, float* 
     if (l == 0) r0 = r;
   }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (stack_persistent(M, H, I, dtype) && stack_decode_ss_bytes() <= off[1] - off[0] &&
+      stack_decode_bar_bytes(L) <= off[2] - off[1]) {
+    // one decode token: the whole stack as one persistent launch per 24
+    // layers; its scratch is carved from this workspace (the two gate/up
+    // buffers where the block's gate/up sums and row partials would go, the
+    // norm statistics where xn would, the barrier counters where y would)
+    const cudaError_t e = launch_stack_decode(
+        layers, L, x, reinterpret_cast<float*>(fbase + foff[1]),
+        reinterpret_cast<float*>(fbase + foff[4]), reinterpret_cast<float*>(base + off[0]),
+        reinterpret_cast<unsigned*>(base + off[1]), H, I, eps, st);
+    if (e != cudaErrorNotSupported)
+      return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq_ffn_stack launch");
+  }
   const Act t = act_of(dtype);
   cudaError_t e = cudaSuccess;
   for (int64_t l = 0; l < L && e == cudaSuccess; ++l) {

@@ -86,6 +86,10 @@ cudaError_t launch_gemv_lut(const uint8_t* wq, const uint16_t* scales, const flo
                             const int8_t* signs, float* y, float* part, int64_t N, int64_t K,
                             LutEpilogue ep, cudaStream_t st);
 size_t gemv_lut_workspace_bytes(int64_t N, int64_t K);
+// K-chunks of a row (0 when the table-lookup GEMV does not serve K), and the
+// CTAs that share one chunk's rows on a device of `sms` SMs.
+int64_t gemv_lut_chunks(int64_t K);
+int64_t gemv_lut_ctas_per_chunk(int64_t sms, int64_t nch, int64_t N);
 // The same decode for PQ2_0 weights (k_gemv_lut.cu): K % 1024 == 0 only.
 cudaError_t launch_gemv_lut_pq2(const uint8_t* wq, const uint16_t* scales, const float* x,
                                 const int8_t* signs, float* y, float* part, int64_t N, int64_t K,
@@ -103,6 +107,21 @@ cudaError_t launch_gemm(const uint8_t* wq, const uint16_t* scales, const void* x
 // gu: M x 2I fp32 (gate half first) -> h: M x I fp32.
 cudaError_t launch_swiglu(const float* gu, float* h, int64_t M, int64_t I,
                           cudaStream_t st);
+
+// The chained feed-forward stack at M = 1, fp32, as one persistent launch
+// per 24 layers (k_stack_decode.cu).  x: H fp32, updated in place.  gu0,
+// gu1: 2I fp32 scratch each; ss: 2 fp32; bars: one unsigned per launch (all
+// zeroed here).  Every layer's tensor maps are made before the first launch.
+// cudaErrorNotSupported when the shapes or the device do not fit it (nothing
+// was launched then).
+cudaError_t launch_stack_decode(const ptq_ffn_layer* layers, int64_t L, float* x, float* gu0,
+                                float* gu1, float* ss, unsigned* bars, int64_t H, int64_t I,
+                                float eps, cudaStream_t st);
+// Whether launch_stack_decode serves (H, I) on the current device.
+bool stack_decode_supported(int64_t H, int64_t I);
+// Workspace bytes launch_stack_decode needs in `ss` and `bars`.
+size_t stack_decode_ss_bytes();
+size_t stack_decode_bar_bytes(int64_t L);
 
 // Residual add and RMSNorm between chained blocks (k_norm.cu): per row of
 // x (M x H fp32, in place) x += y, then xn = x / sqrt(mean(x^2) + eps) * g.

@@ -170,6 +170,13 @@ def test_stack_refusals_before_launch(P):
     assert st([good, good, no_w], 3) == 1
     assert b"layer 2" in L.ptq_last_error()
     assert st([bad_w], 1) == 3
+    # the route query refuses before it looks at the device
+    name = ctypes.c_char_p()
+    assert L.ptq_ffn_stack_route(1, H, I, P.PTQ_F32, None) == 1
+    assert L.ptq_ffn_stack_route(1, H, I, 7, ctypes.byref(name)) == 4
+    assert L.ptq_ffn_stack_route(1, 1000, I, P.PTQ_F32, ctypes.byref(name)) == 2
+    assert L.ptq_ffn_stack_route(0, H, I, P.PTQ_F32, ctypes.byref(name)) == 2
+    assert L.ptq_ffn_stack_route(9, H, I, P.PTQ_F32, ctypes.byref(name)) == 5
     # no layers or no rows: nothing to do
     assert st([], 0, x=None, ws=None, wsb=0) == 0
     assert st([good], 1, M=0, x=None, ws=None, wsb=0) == 0

@@ -9,8 +9,13 @@ the next block's output scaled by at most 2 rho, with
 rho = max_l rms(y_l) / rms(x_l): the norm divides d by rms(x), and SwiGLU's
 product of two linear maps at most doubles a relative change.  So after L
 blocks
-    |x - x_ref| <= (1 + 2 rho)^(L-1) * sum_l tol(y_l),
-with every y_l and x_l taken from the oracle, layer by layer."""
+    |x - x_ref| <= (1 + 2 rho)^(L-1) * sum_l [tol(y_l) + k 2^-24 |x_(l+1)|],
+with every y_l and x_l taken from the oracle, layer by layer.  The last
+term is the fp32 storage of the residual stream itself: each addition into
+x rounds once, by at most 2^-24 |x|, and a layer makes k of them -- one per
+K-chunk of the down projection (ceil(13 I / 256 / 32) chunks of at most 32
+words) when the chunk sums are added into x one at a time, which bounds the
+single addition of the per-layer path too."""
 import numpy as np
 import pytest
 
@@ -45,16 +50,23 @@ def make_layers(P, orc, syn, seed, Lc, H, I):
     return dev, host, gains
 
 
+def down_chunks(I):
+    """K-chunks of a row of the down projection: 13 I / 256 words, <= 32 each."""
+    return -(-(13 * I // 256) // 32)
+
+
 def oracle_with_bound(orc, host, gains, x64, eps, bf16):
     """The oracle's stack output and the elementwise bound of the docstring."""
     x = x64.copy()
     tol = np.zeros_like(x)
     rho = 0.0
+    k = down_chunks(host[0][5].shape[0]) if host else 1
     for lay, g in zip(host, gains):
         nx = orc.ffn_stack([lay], [g.astype(np.float64)], x, eps)
         y = nx - x
         r = Q.rms(y)
         tol += (1e-2 * r + 2.0 ** -8 * np.abs(y)) if bf16 else 1e-4 * (np.abs(y) + r)
+        tol += k * 2.0 ** -24 * np.abs(nx)
         rho = max(rho, r / Q.rms(x))
         x = nx
     return x, tol * (1.0 + 2.0 * rho) ** (len(host) - 1)
@@ -105,6 +117,45 @@ def test_stack_row_lengths(P, orc, syn, H, M, act):
     got = run_stack(P, dev, gains, x, eps, torch.float32 if act == "f32" else torch.bfloat16)
     ref, bound = oracle_with_bound(orc, host, gains, x.astype(np.float64), eps, act == "bf16")
     check_stack(got, ref, bound, f"stack H={H} M={M} {act}")
+
+
+def test_stack_routes(P):
+    # one fp32 token runs the persistent kernel; everything else per layer
+    assert P.ffn_stack_route(1, 5120, 17408, P.PTQ_F32) == "stack_decode_persistent"
+    assert P.ffn_stack_route(1, 1024, 2048, P.PTQ_F32) == "stack_decode_persistent"
+    assert P.ffn_stack_route(2, 5120, 17408, P.PTQ_F32) == "stack_per_layer"
+    assert P.ffn_stack_route(1, 5120, 17408, P.PTQ_BF16) == "stack_per_layer"
+
+
+def quarter_scales(bits):
+    """fp16 scale patterns divided by 4 (exact for normal values)."""
+    return (bits.view(np.float16) / np.float16(4)).astype(np.float16).view(np.uint16)
+
+
+def test_stack_decode_spans_launches(P, orc, syn):
+    # 26 layers run as two persistent launches (24 + 2): the second starts by
+    # adding the first one's last block output.  Quarter scales keep each
+    # block's increment near 3% of the stream, so the bound stays tight
+    # enough that a dropped or repeated layer fails it.
+    import torch
+
+    H, I, Lc, eps = 1024, 2048, 26, 1e-6
+    dev, host, gains = [], [], []
+    for l in range(Lc):
+        F = syn.ffn_layer(70, l, H, I)
+        sg, sd = quarter_scales(F.wgu_scales), quarter_scales(F.wd_scales)
+        dev.append((Q.dev(P.pack(F.wgu_trits)), Q.dev(sg), Q.dev(P.pack(F.wd_trits)), Q.dev(sd),
+                    Q.dev(F.signs_in), Q.dev(F.signs_mid)))
+        host.append((orc.pack(F.wgu_trits), sg, orc.pack(F.wd_trits), sd, F.signs_in, F.signs_mid))
+        gains.append(syn.norm_gain(70, l, H))
+    x = syn.ffn_input(70, 0, 1, H, "f32")
+    got = run_stack(P, dev, gains, x, eps, torch.float32)
+    P.device_check()
+    ref, bound = oracle_with_bound(orc, host, gains, x.astype(np.float64), eps, False)
+    check_stack(got, ref, bound, "stack decode L=26")
+    # the bound is far below one layer's increment
+    one = orc.ffn_stack(host[-1:], [gains[-1].astype(np.float64)], ref, eps) - ref
+    assert bound.max() < 0.2 * np.abs(one).max()
 
 
 def test_stack_one_layer_is_residual_plus_block(P, orc, syn):
@@ -161,6 +212,7 @@ def test_stack_decode_full_size_ring(P, orc, syn):
     dev, host, gains = make_layers(P, orc, syn, 4, Lc, H, I)
     x = syn.ffn_input(4, 0, 1, H, "f32")
     got = run_stack(P, dev, gains, x, eps, torch.float32)
+    P.device_check()
     ref, bound = oracle_with_bound(orc, host, gains, x.astype(np.float64), eps, False)
     check_stack(got, ref, bound, "stack decode H=5120 I=17408 L=8")
 
