@@ -356,6 +356,15 @@ PTQ_API PTQ_NODISCARD ptq_status ptq_device_check(ptq_stream_t stream);
  * clears the word.  Errors: PTQ_ERR_CUDA. */
 PTQ_API PTQ_NODISCARD ptq_status ptq_selftest_timeout(ptq_stream_t stream);
 
+/* ptq_selftest_grid_timeout -- test export for the grid barrier of the
+ * persistent stack (ptq_ffn_stack_route "stack_decode_persistent").
+ * Launches 8 CTAs of which one never arrives at the barrier; the other
+ * seven poll, with the stack's bounded wait and a short poll limit, run
+ * out, raise the device status word and return (no fault, no hang).  The
+ * next ptq_device_check then returns PTQ_ERR_TIMEOUT.  Errors:
+ * PTQ_ERR_CUDA. */
+PTQ_API PTQ_NODISCARD ptq_status ptq_selftest_grid_timeout(ptq_stream_t stream);
+
 /* ptq_status_str -- static name of a status code. */
 PTQ_API const char* ptq_status_str(ptq_status status);
 

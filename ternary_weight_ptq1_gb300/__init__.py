@@ -31,7 +31,7 @@ EXPORTS = ("ptq1_pack", "ptq1_unpack", "ptq_fwht", "ptq_matmul_workspace_bytes",
            "ptq_ffn", "ptq_ffn_noalloc", "ptq_ffn_stack_workspace_bytes", "ptq_ffn_stack",
            "ptq_ffn_stack_route", "ptq2_pack", "ptq2_unpack",
            "ptq_matmul_pq2_workspace_bytes", "ptq_matmul_pq2", "ptq_embed", "ptq_embed_ptq1",
-           "ptq_route", "ptq_selftest_timeout",
+           "ptq_route", "ptq_selftest_timeout", "ptq_selftest_grid_timeout",
            "ptq_device_check", "ptq_status_str", "ptq_last_error")
 
 # Size of the built-in scratch array behind ptq_ffn_noalloc (include/ptq.h).
@@ -89,6 +89,7 @@ def load(path: str | None = None):
     L.ptq_route.argtypes = [_I64, _I32, ctypes.POINTER(ctypes.c_char_p)]
     L.ptq_device_check.argtypes = [_P]
     L.ptq_selftest_timeout.argtypes = [_P]
+    L.ptq_selftest_grid_timeout.argtypes = [_P]
     L.ptq_status_str.argtypes = [_I32]
     L.ptq_status_str.restype = ctypes.c_char_p
     L.ptq_last_error.argtypes = []
@@ -96,7 +97,8 @@ def load(path: str | None = None):
     for name in ("ptq1_pack", "ptq1_unpack", "ptq_fwht", "ptq_matmul", "ptq_rotate_matmul", "ptq_ffn",
                  "ptq_ffn_noalloc", "ptq_ffn_stack", "ptq_ffn_stack_route", "ptq2_pack",
                  "ptq2_unpack", "ptq_matmul_pq2", "ptq_embed",
-                 "ptq_embed_ptq1", "ptq_route", "ptq_device_check", "ptq_selftest_timeout"):
+                 "ptq_embed_ptq1", "ptq_route", "ptq_device_check", "ptq_selftest_timeout",
+                 "ptq_selftest_grid_timeout"):
         getattr(L, name).restype = _I32
     _lib = L
     return L
@@ -410,6 +412,13 @@ def selftest_timeout(stream=None) -> None:
     """Runs the bounded wait that is made to run out (ptq_selftest_timeout);
     the next device_check raises PTQ_ERR_TIMEOUT."""
     _check(load().ptq_selftest_timeout(_stream(stream)), "ptq_selftest_timeout")
+
+
+def selftest_grid_timeout(stream=None) -> None:
+    """Runs the persistent stack's grid barrier with one CTA that never
+    arrives (ptq_selftest_grid_timeout); the next device_check raises
+    PTQ_ERR_TIMEOUT."""
+    _check(load().ptq_selftest_grid_timeout(_stream(stream)), "ptq_selftest_grid_timeout")
 
 
 def device_check(stream=None) -> None:

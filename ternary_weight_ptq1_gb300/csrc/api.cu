@@ -738,6 +738,12 @@ PTQ_API ptq_status ptq_selftest_timeout(ptq_stream_t stream) {
   return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq_selftest_timeout launch");
 }
 
+PTQ_API ptq_status ptq_selftest_grid_timeout(ptq_stream_t stream) {
+  t_msg[0] = 0;
+  cudaError_t e = launch_selftest_grid_timeout(reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq_selftest_grid_timeout launch");
+}
+
 PTQ_API ptq_status ptq_device_check(ptq_stream_t stream) {
   t_msg[0] = 0;
   int v = 0;

@@ -103,7 +103,8 @@ __device__ __forceinline__ float4 ldcg4(const float* p) {
 // Grid-wide barrier number `n` (0, 1, ...): all CTAs have arrived once the
 // counter reaches (n + 1) * gridDim.x.  Returns false (in every thread of
 // the CTA) when the wait ran out or another CTA has raised the status word.
-__device__ __forceinline__ bool grid_sync(unsigned* ctr, unsigned n, int* status) {
+__device__ __forceinline__ bool grid_sync(unsigned* ctr, unsigned n, int* status,
+                                          uint32_t limit = kSpinLimit) {
   __syncthreads();
   int ok = 1;
   if (threadIdx.x == 0) {
@@ -115,7 +116,7 @@ __device__ __forceinline__ bool grid_sync(unsigned* ctr, unsigned n, int* status
       unsigned v;
       asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
       if (v >= target) break;
-      if (i >= kSpinLimit || *reinterpret_cast<volatile int*>(status) != 0) {
+      if (i >= limit || *reinterpret_cast<volatile int*>(status) != 0) {
         ok = 0;
         break;
       }
@@ -329,7 +330,29 @@ __global__ void __launch_bounds__(kThreads, 1) stack_decode_kernel(const __grid_
 
 int g_stack_ready[64];  // per device: kernel attributes set
 
+// The grid barrier made to run out, without a fault: CTA 0 never arrives,
+// so the others poll up to their (short) limit, raise the status word and
+// return.  Nothing else is in flight.
+__global__ void selftest_grid_kernel(unsigned* ctr, int* status) {
+  if (blockIdx.x == 0) return;
+  static_cast<void>(grid_sync(ctr, 0u, status, 4096u));
+}
+
+__device__ unsigned g_selftest_ctr;
+
 }  // namespace
+
+cudaError_t launch_selftest_grid_timeout(cudaStream_t st) {
+  int* status = device_status_ptr();
+  if (!status) return cudaErrorInvalidDevice;
+  void* ctr = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&ctr, g_selftest_ctr);
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(ctr, 0, sizeof(unsigned), st);
+  if (e != cudaSuccess) return e;
+  selftest_grid_kernel<<<8, 32, 0, st>>>(static_cast<unsigned*>(ctr), status);
+  return cudaGetLastError();
+}
 
 size_t stack_decode_ss_bytes() { return 2 * sizeof(float); }
 size_t stack_decode_bar_bytes(int64_t L) {

@@ -117,6 +117,9 @@ cudaError_t launch_swiglu(const float* gu, float* h, int64_t M, int64_t I,
 cudaError_t launch_stack_decode(const ptq_ffn_layer* layers, int64_t L, float* x, float* gu0,
                                 float* gu1, float* ss, unsigned* bars, int64_t H, int64_t I,
                                 float eps, cudaStream_t st);
+// A grid barrier of the persistent stack that one CTA never reaches: the
+// others' bounded waits run out and raise the status word.
+cudaError_t launch_selftest_grid_timeout(cudaStream_t st);
 // Whether launch_stack_decode serves (H, I) on the current device.
 bool stack_decode_supported(int64_t H, int64_t I);
 // Workspace bytes launch_stack_decode needs in `ss` and `bars`.

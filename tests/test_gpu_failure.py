@@ -1,6 +1,7 @@
 """The timeout path on a GPU, without a fault: a bounded mbarrier wait that
-nothing completes runs out, raises the device status word, and
-ptq_device_check reports PTQ_ERR_TIMEOUT once; the context stays usable."""
+nothing completes, and a grid barrier one CTA never reaches, run out, raise
+the device status word, and ptq_device_check reports PTQ_ERR_TIMEOUT once;
+the context stays usable."""
 import time
 
 import numpy as np
@@ -27,6 +28,36 @@ def test_wait_that_runs_out_is_reported_and_cleared(P, orc, syn):
     torch.cuda.synchronize()
     Q.check_f32(Q.host_f64(y), orc.matmul(orc.pack(mv.trits), mv.scales, Q.x_f64(mv.x)), "after")
     P.device_check()
+
+
+def test_grid_barrier_that_runs_out_is_reported(P, orc, syn):
+    # the persistent stack's grid barrier with one CTA that never arrives:
+    # the others give up, raise the status word and return
+    import torch
+
+    P.device_check()
+    t0 = time.time()
+    P.selftest_grid_timeout()
+    with pytest.raises(P.PTQError, match="TIMEOUT"):
+        P.device_check()
+    assert time.time() - t0 < 30.0
+    P.device_check()
+    # the persistent stack still runs and agrees with the oracle
+    H, I = 1024, 2048
+    F = syn.ffn_layer(80, 0, H, I)
+    lay = (Q.dev(P.pack(F.wgu_trits)), Q.dev(F.wgu_scales), Q.dev(P.pack(F.wd_trits)),
+           Q.dev(F.wd_scales), Q.dev(F.signs_in), Q.dev(F.signs_mid))
+    g = syn.norm_gain(80, 0, H)
+    x = syn.ffn_input(80, 0, 1, H, "f32")
+    xd = Q.dev(x.copy())
+    assert P.ffn_stack_route(1, H, I, P.PTQ_F32) == "stack_decode_persistent"
+    P.ffn_stack([lay], [Q.dev(g)], xd, 1e-6)
+    torch.cuda.synchronize()
+    P.device_check()
+    x64 = x.astype(np.float64)
+    ref = orc.ffn_stack([(orc.pack(F.wgu_trits), F.wgu_scales, orc.pack(F.wd_trits), F.wd_scales,
+                          F.signs_in, F.signs_mid)], [g.astype(np.float64)], x64, 1e-6)
+    Q.check_f32(Q.host_f64(xd) - x64, ref - x64, "stack after the grid timeout")
 
 
 @pytest.fixture(scope="module")
