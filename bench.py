@@ -531,26 +531,48 @@ def run_reference(args, world, rank):
 def run_profile_case(which: str):
     """A few launches of one kernel on a small case sized for an ncu capture:
     gemv -- decode GEMV, M=1, K=5120, N=8*17408 (156 MB of weights > L2);
-    gemm -- prefill GEMM, M=512, K=5120, N=17408, bf16.  Prints the event
-    time of the last launch (not a bench number)."""
+    gemm -- prefill GEMM, M=512, K=5120, N=17408, bf16;
+    stack -- the persistent decode stack, 4 layers of H=5120, I=17408.
+    Prints the event time of the last call (not a bench number)."""
     import torch
 
     import synth as syn
     import ternary_weight_ptq1_gb300 as P
 
-    if which == "gemv":
+    if which == "stack":
+        # the persistent decode stack over 4 layers (234 MB of weights > L2),
+        # H=5120, I=17408: one cooperative launch
+        H, I = 5120, 17408
+        lays, gains = [], []
+        for l in range(4):
+            F = syn.ffn_layer(4, l, H, I)
+            lays.append(tuple(torch.from_numpy(a).cuda() for a in (
+                P.pack(F.wgu_trits), F.wgu_scales.view(np.int16), P.pack(F.wd_trits),
+                F.wd_scales.view(np.int16), F.signs_in, F.signs_mid)))
+            gains.append(torch.from_numpy(syn.norm_gain(4, l, H)).cuda())
+        x = torch.from_numpy(syn.ffn_input(4, 0, 1, H, "f32")).cuda()
+        ws = torch.empty(P.ffn_stack_workspace_bytes(1, H, I, P.PTQ_F32), dtype=torch.uint8,
+                         device="cuda")
+        call = lambda: P.ffn_stack(lays, gains, x, 1e-6, workspace=ws)  # noqa: E731
+        M, N = 1, 3 * H * I // K_COLS
+    elif which == "gemv":
         M, N, dt = 1, 8 * N_ROWS, "f32"
     else:
         M, N, dt = PREFILL_M, N_ROWS, "bf16"
-    mv = syn.gaussian_matvec(7, M, N, K_COLS, dtype=dt)
-    wq = torch.from_numpy(P.pack(mv.trits)).cuda()
-    sc = torch.from_numpy(mv.scales.view(np.int16)).cuda()
-    if dt == "f32":  # the bench's decode call: rotation fused into the GEMV
+    if which == "stack":
+        pass
+    elif dt == "f32":  # the bench's decode call: rotation fused into the GEMV
+        mv = syn.gaussian_matvec(7, M, N, K_COLS, dtype=dt)
+        wq = torch.from_numpy(P.pack(mv.trits)).cuda()
+        sc = torch.from_numpy(mv.scales.view(np.int16)).cuda()
         x = torch.from_numpy(mv.x).cuda()
         y = torch.empty((M, N), device="cuda")
         signs = torch.from_numpy(syn.signs(7, 3, K_COLS)).cuda()
         call = lambda: P.rotate_matmul(wq, sc, x, signs, out=y)
     else:
+        mv = syn.gaussian_matvec(7, M, N, K_COLS, dtype=dt)
+        wq = torch.from_numpy(P.pack(mv.trits)).cuda()
+        sc = torch.from_numpy(mv.scales.view(np.int16)).cuda()
         x = torch.from_numpy(mv.x.view(np.int16)).cuda().view(torch.bfloat16)
         y = torch.empty((M, N), device="cuda", dtype=torch.bfloat16)
         call = lambda: P.matmul(wq, sc, x, out=y)
@@ -580,7 +602,7 @@ def main():
     ap.add_argument("--skip-embed", action="store_true")
     ap.add_argument("--skip-pq2", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
-    ap.add_argument("--profile", choices=["gemv", "gemm"],
+    ap.add_argument("--profile", choices=["gemv", "gemm", "stack"],
                     help="run a small case of one kernel for an ncu capture, then exit")
     args = ap.parse_args()
     if args.profile:
