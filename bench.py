@@ -3,7 +3,8 @@
 Headline workload (decode gate/up): M=1, K=5120, N=17408 PTQ1_0 weights
 (19,496,960 bytes).  One step = rotate the activation (5 signed 1024-blocks)
 + decode GEMV.  Metric: weight bytes per second.  A second line item times
-the prefill GEMM (M=512, K=5120, N=17408, bf16) in TFLOP/s.
+the prefill GEMM (M=512, K=5120, N=17408, bf16) in TFLOP/s, with M=128 and
+M=2048 beside it.
 
 Inputs are resident in HBM before the timed region.  Every step uses the next
 of R distinct weight sets (R * 19.5 MB > the 129 MB L2), so no step finds its
@@ -420,6 +421,26 @@ def run_ours(args, world, rank):
                "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": pk["bf16"],
                             "unit": "TFLOP/s", "frac": round(tf / pk["bf16"], 4),
                             "traffic": TRAFFIC_PREFILL, "peak_source": pk["source"] + " burst bf16"}}
+        # the other two prefill sizes of the workload, on the same weight ring
+        # with activations of their own
+        pre["other_M"] = {}
+        for Mo in (128, 2048):
+            oxs = [torch.from_numpy(syn.normal_bf16(1000 + r, 4, (Mo, K_COLS)).view(np.int16)).cuda()
+                   .view(torch.bfloat16) for r in range(pre_R)]
+            oys = [torch.empty((Mo, N_ROWS), device="cuda", dtype=torch.bfloat16)
+                   for _ in range(pre_R)]
+
+            def ostep(i, oxs=oxs, oys=oys):
+                wq, sc, _ = pring[i % pre_R]
+                P.matmul(wq, sc, oxs[i % pre_R], out=oys[i % pre_R])
+
+            oK = max(3, min(K, 100))
+            oms = timed_steps(torch, ostep, oK, 3, chunk=50) / oK
+            otf = 2.0 * Mo * N_ROWS * K_COLS / (oms * 1e-3) / 1e12
+            pre["other_M"][str(Mo)] = {"us_per_call": round(oms * 1e3, 2),
+                                       "TFLOP/s": round(world * otf, 1),
+                                       "frac_of_bf16_peak": round(otf / pk["bf16"], 4)}
+            del oxs, oys
 
     ffn = None if args.skip_ffn else ffn_lines(P, torch, syn, pk, world, args)
     emb = None if args.skip_embed else embed_lines(P, torch, syn, pk, world, args)
