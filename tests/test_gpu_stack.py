@@ -105,10 +105,12 @@ def test_stack_small(P, orc, syn, M, act):
 
 
 @pytest.mark.parametrize("H", [1024, 5120, 12288, 17408])
-@pytest.mark.parametrize("M,act", [(2, "f32"), (3, "bf16")])
+@pytest.mark.parametrize("M,act", [(1, "f32"), (2, "f32"), (3, "bf16")])
 def test_stack_row_lengths(P, orc, syn, H, M, act):
-    # the add-and-norm kernel holds 1, 2 or 4 vectors of a row per thread
-    # (H = 1024, 5120, 12288) and loops over longer rows (H = 17408)
+    # per layer: the add-and-norm kernel holds 1, 2 or 4 vectors of a row per
+    # thread (H = 1024, 5120, 12288) and loops over longer rows (H = 17408);
+    # M = 1 runs the persistent kernel, whose gate/up rows are then cut into
+    # 4 to 28 K-chunks and whose down rows into 2
     import torch
 
     I, Lc, eps = 1024, 2, 1e-6
@@ -156,6 +158,42 @@ def test_stack_decode_spans_launches(P, orc, syn):
     # the bound is far below one layer's increment
     one = orc.ffn_stack(host[-1:], [gains[-1].astype(np.float64)], ref, eps) - ref
     assert bound.max() < 0.2 * np.abs(one).max()
+
+
+def test_stack_persistent_in_a_graph(P, orc, syn):
+    # the bench replays the persistent launches from a CUDA graph: capture two
+    # calls of three layers (one cooperative launch each, with the memsets
+    # before it), replay them, and compare with the oracle's six layers
+    import torch
+
+    H, I, Lc, eps = 1024, 2048, 3, 1e-6
+    dev, host, gains = make_layers(P, orc, syn, 44, Lc, H, I)
+    x = syn.ffn_input(44, 0, 1, H, "f32")
+    xd = Q.dev(x.copy())
+    gd = [Q.dev(g) for g in gains]
+    ws = torch.empty(P.ffn_stack_workspace_bytes(1, H, I, P.PTQ_F32), dtype=torch.uint8,
+                     device="cuda")
+    P.ffn_stack(dev, gd, xd, eps, workspace=ws)  # warm-up outside the capture
+    torch.cuda.synchronize()
+    xd.copy_(Q.dev(x.copy()))
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            P.ffn_stack(dev, gd, xd, eps, workspace=ws)
+            P.ffn_stack(dev, gd, xd, eps, workspace=ws)
+    torch.cuda.synchronize()
+    xd.copy_(Q.dev(x.copy()))  # the capture did not run the kernels
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    P.device_check()
+    got = Q.host_f64(xd)
+    ref, bound = oracle_with_bound(orc, host + host, gains + gains, x.astype(np.float64), eps,
+                                   False)
+    check_stack(got, ref, bound, "persistent stack replayed from a graph")
 
 
 def test_stack_one_layer_is_residual_plus_block(P, orc, syn):
