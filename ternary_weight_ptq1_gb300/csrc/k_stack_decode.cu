@@ -476,8 +476,17 @@ cudaError_t launch_stack_decode(const ptq_ffn_layer* layers, int64_t L, float* x
   if (e == cudaSuccess) e = cudaMemsetAsync(gu0, 0, (size_t)(2 * I) * sizeof(float), st);
   if (e == cudaSuccess) e = cudaMemsetAsync(gu1, 0, (size_t)(2 * I) * sizeof(float), st);
   if (e == cudaSuccess) e = cudaMemsetAsync(ss, 0, 2 * sizeof(float), st);
-  for (int64_t j = 0; j < nl && e == cudaSuccess; ++j)
+  int64_t j = 0;
+  for (; j < nl && e == cudaSuccess; ++j)
     e = cudaLaunchKernelEx(&cfg, stack_decode_kernel, args[(size_t)j]);
+  // a device whose SMs are partly held elsewhere (MPS, a green context) cannot
+  // take the whole grid at once: when the first launch is refused nothing
+  // ran, and the caller takes the per-layer path (the memsets only cleared
+  // scratch)
+  if (e == cudaErrorCooperativeLaunchTooLarge && j == 1) {
+    static_cast<void>(cudaGetLastError());
+    return cudaErrorNotSupported;
+  }
   return e;
 }
 

@@ -112,8 +112,8 @@ cudaError_t launch_swiglu(const float* gu, float* h, int64_t M, int64_t I,
 // per 24 layers (k_stack_decode.cu).  x: H fp32, updated in place.  gu0,
 // gu1: 2I fp32 scratch each; ss: 2 fp32; bars: one unsigned per launch (all
 // zeroed here).  Every layer's tensor maps are made before the first launch.
-// cudaErrorNotSupported when the shapes or the device do not fit it (nothing
-// was launched then).
+// cudaErrorNotSupported when the shapes or the device do not fit it, or the
+// device cannot hold the cooperative grid at launch time (nothing ran then).
 cudaError_t launch_stack_decode(const ptq_ffn_layer* layers, int64_t L, float* x, float* gu0,
                                 float* gu1, float* ss, unsigned* bars, int64_t H, int64_t I,
                                 float eps, cudaStream_t st);
