@@ -480,6 +480,7 @@ def run_ours(args, world, rank):
         "embed": emb,
         "pq2": pq2,
         "cpu_baseline": cpu,
+        "host": host_receipt() if rank == 0 else None,
     }
     if rank == 0:
         print(json.dumps(line))
@@ -511,10 +512,44 @@ def cpu_baseline(args):
 
     reps = max(1, args.cpu_reps)
     secs, nbytes = _oracle_step(orc, syn, reps)
-    return {"value": round(nbytes / secs / 1e9, 3), "unit": "GB/s", "cores": orc.get_threads(),
-            "kind": "oracle",
-            "sample": f"{reps} full decode gate/up steps (rotation + 17408x5120 GEMV, fp64 C, "
-                      f"OpenMP over output rows), {secs:.2f} s"}
+    cores = orc.get_threads()
+    out = {"value": round(nbytes / secs / 1e9, 3), "unit": "GB/s", "cores": cores,
+           "kind": "oracle",
+           "sample": f"{reps} full decode gate/up steps (rotation + 17408x5120 GEMV, fp64 C, "
+                     f"OpenMP over output rows), {secs:.2f} s"}
+    # the same oracle on one core, on a sample of about the same CPU time
+    reps1 = max(1, reps // max(1, cores))
+    orc.set_threads(1)
+    try:
+        secs1, nbytes1 = _oracle_step(orc, syn, reps1)
+    finally:
+        orc.set_threads(cores)
+    out["single_thread"] = {"value": round(nbytes1 / secs1 / 1e9, 4), "unit": "GB/s",
+                            "sample": f"{reps1} steps on one core, {secs1:.2f} s"}
+    return out
+
+
+def host_receipt():
+    """Load, CPU and the other processes on the GPU, for the JSON line."""
+    rec = {"loadavg": [round(v, 2) for v in os.getloadavg()],
+           "cpus": len(os.sched_getaffinity(0))}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                key = ln.split(":", 1)[0].strip().lower()
+                if key in ("model name", "cpu part", "hardware"):
+                    rec["cpu"] = ln.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    try:
+        r = subprocess.run(["nvidia-smi", "--query-compute-apps=pid,used_memory",
+                            "--format=csv,noheader,nounits"], capture_output=True, text=True,
+                           timeout=20)
+        rec["gpu_processes"] = [ln.strip() for ln in r.stdout.splitlines() if ln.strip()]
+    except Exception:
+        rec["gpu_processes"] = None
+    return rec
 
 
 def run_reference(args, world, rank):
