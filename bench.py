@@ -530,7 +530,8 @@ def cpu_baseline(args):
 
 
 def host_receipt():
-    """Load, CPU and the other processes on the GPU, for the JSON line."""
+    """Load, CPU, the GPU (name, driver, SMs) and the other processes on it,
+    for the JSON line."""
     rec = {"loadavg": [round(v, 2) for v in os.getloadavg()],
            "cpus": len(os.sched_getaffinity(0))}
     try:
@@ -547,8 +548,19 @@ def host_receipt():
                             "--format=csv,noheader,nounits"], capture_output=True, text=True,
                            timeout=20)
         rec["gpu_processes"] = [ln.strip() for ln in r.stdout.splitlines() if ln.strip()]
+        r = subprocess.run(["nvidia-smi", "--query-gpu=name,driver_version", "--format=csv,noheader"],
+                           capture_output=True, text=True, timeout=20)
+        rec["gpu"] = r.stdout.strip().splitlines()[0] if r.stdout.strip() else None
     except Exception:
         rec["gpu_processes"] = None
+    try:
+        import torch
+
+        props = torch.cuda.get_device_properties(torch.cuda.current_device())
+        rec["sms"] = props.multi_processor_count
+        rec["torch"] = torch.__version__
+    except Exception:
+        pass
     return rec
 
 

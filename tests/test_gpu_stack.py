@@ -196,6 +196,33 @@ def test_stack_persistent_in_a_graph(P, orc, syn):
     check_stack(got, ref, bound, "persistent stack replayed from a graph")
 
 
+@pytest.mark.parametrize("M,act", [(1, "f32"), (3, "bf16")])
+def test_stack_writes_stay_in_bounds(P, orc, syn, M, act):
+    # the residual and the workspace sit between guard bands of a known byte
+    # pattern; after the call (persistent at M = 1, per layer at M = 3) the
+    # guards are untouched and the result still agrees with the oracle
+    import torch
+
+    H, I, Lc, eps, guard = 1024, 2048, 2, 1e-6, 4096
+    dev, host, gains = make_layers(P, orc, syn, 46, Lc, H, I)
+    x = syn.ffn_input(46, 0, M, H, "f32")
+    xbuf = torch.full((M * H + 2 * guard,), float("nan"), device="cuda")
+    xd = xbuf[guard:guard + M * H].view(M, H)
+    xd.copy_(Q.dev(x.copy()))
+    pdt = P.PTQ_F32 if act == "f32" else P.PTQ_BF16
+    need = P.ffn_stack_workspace_bytes(M, H, I, pdt)
+    wbuf = torch.full((need + 2 * guard,), 0xA5, dtype=torch.uint8, device="cuda")
+    ws = wbuf[guard:guard + need]
+    P.ffn_stack(dev, [Q.dev(g) for g in gains], xd, eps,
+                act=torch.float32 if act == "f32" else torch.bfloat16, workspace=ws)
+    torch.cuda.synchronize()
+    P.device_check()
+    assert torch.isnan(xbuf[:guard]).all() and torch.isnan(xbuf[-guard:]).all()
+    assert (wbuf[:guard] == 0xA5).all() and (wbuf[-guard:] == 0xA5).all()
+    ref, bound = oracle_with_bound(orc, host, gains, x.astype(np.float64), eps, act == "bf16")
+    check_stack(Q.host_f64(xd), ref, bound, f"stack between guard bands M={M}")
+
+
 def test_stack_one_layer_is_residual_plus_block(P, orc, syn):
     # with one layer the stack is x + ffn(rmsnorm(x) g): compare the increment
     # with the single-block tolerance directly
