@@ -269,10 +269,13 @@ def test_prefill_split_k(P, orc, syn, M, N, K):
     assert torch.equal(P.matmul(*args, workspace=ws), split)
 
 
-def test_prefill_in_bounds(P, syn):
+@pytest.mark.parametrize("M,N,K", [(130, 300, 1024), (100, 300, 1024), (128, 400, 2048),
+                                   (64, 520, 5120)])
+def test_prefill_in_bounds(P, syn, M, N, K):
+    # ragged tiles at M <= 128 (one 128-row half) and above; N = 520 at
+    # K = 5120 leaves few enough tiles to split K
     import torch
 
-    M, N, K = 130, 300, 1024
     mv = syn.gaussian_matvec(40, M, N, K, dtype="bf16")
     guard = 8192
     buf = torch.full((M * N + 2 * guard,), float("nan"), device="cuda", dtype=torch.bfloat16)
@@ -280,3 +283,4 @@ def test_prefill_in_bounds(P, syn):
     P.matmul(Q.dev(P.pack(mv.trits)), Q.dev(mv.scales), Q.dev_bf16(mv.x), out=out)
     assert torch.isnan(buf[:guard].float()).all() and torch.isnan(buf[-guard:].float()).all()
     assert torch.isfinite(out.float()).all()
+    P.device_check()
