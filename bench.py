@@ -599,7 +599,7 @@ def run_reference(args, world, rank):
 def run_profile_case(which: str):
     """A few launches of one kernel on a small case sized for an ncu capture:
     gemv -- decode GEMV, M=1, K=5120, N=8*17408 (156 MB of weights > L2);
-    gemm -- prefill GEMM, M=512, K=5120, N=17408, bf16;
+    gemm -- prefill GEMM, M=512, K=5120, N=17408, bf16 (gemm128: M=128);
     stack -- the persistent decode stack, 4 layers of H=5120, I=17408.
     Prints the event time of the last call (not a bench number)."""
     import torch
@@ -625,6 +625,8 @@ def run_profile_case(which: str):
         M, N = 1, 3 * H * I // K_COLS
     elif which == "gemv":
         M, N, dt = 1, 8 * N_ROWS, "f32"
+    elif which == "gemm128":
+        M, N, dt = 128, N_ROWS, "bf16"
     else:
         M, N, dt = PREFILL_M, N_ROWS, "bf16"
     if which == "stack":
@@ -670,7 +672,7 @@ def main():
     ap.add_argument("--skip-embed", action="store_true")
     ap.add_argument("--skip-pq2", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
-    ap.add_argument("--profile", choices=["gemv", "gemm", "stack"],
+    ap.add_argument("--profile", choices=["gemv", "gemm", "gemm128", "stack"],
                     help="run a small case of one kernel for an ncu capture, then exit")
     args = ap.parse_args()
     if args.profile:
