@@ -25,9 +25,10 @@
 // by phase B of layer l - 1, two barriers earlier).  The chunk sums arrive
 // in no fixed order, so results may differ between runs by fp32 rounding.
 //
-// The weights do not depend on the activations: before a warp enters a
-// barrier it requests the first two boxes of its next projection into its
-// weight ring, so HBM keeps streaming through the barrier.  The barrier is a
+// The weights do not depend on the activations: once its CTA has arrived at
+// a barrier, a warp requests the first two boxes of its next projection into
+// its weight ring before it waits, so HBM keeps streaming through the barrier
+// and the requests overlap the barrier's own latency.  The barrier is a
 // counter in global memory (release by a fence before the arrive, acquire
 // loads while polling); a barrier that does not complete within its poll
 // limit raises the device status word, and every CTA then leaves at its next
@@ -100,16 +101,24 @@ __device__ __forceinline__ float4 ldcg4(const float* p) {
   return __ldcg(reinterpret_cast<const float4*>(p));
 }
 
-// Grid-wide barrier number `n` (0, 1, ...): all CTAs have arrived once the
-// counter reaches (n + 1) * gridDim.x.  Returns false (in every thread of
-// the CTA) when the wait ran out or another CTA has raised the status word.
-__device__ __forceinline__ bool grid_sync(unsigned* ctr, unsigned n, int* status,
-                                          uint32_t limit = kSpinLimit) {
+// Grid-wide barrier number `n` (0, 1, ...), in two halves: grid_arrive
+// publishes this CTA's writes and counts it in; grid_wait returns once the
+// counter reaches (n + 1) * gridDim.x.  Work that reads nothing other CTAs
+// write (requesting weight boxes) may run between the two.  grid_wait
+// returns false (in every thread of the CTA) when the wait ran out or
+// another CTA has raised the status word.
+__device__ __forceinline__ void grid_arrive(unsigned* ctr) {
   __syncthreads();
-  int ok = 1;
   if (threadIdx.x == 0) {
     __threadfence();  // release: this CTA's writes before its arrival
     atomicAdd(ctr, 1u);
+  }
+}
+
+__device__ __forceinline__ bool grid_wait(unsigned* ctr, unsigned n, int* status,
+                                          uint32_t limit = kSpinLimit) {
+  int ok = 1;
+  if (threadIdx.x == 0) {
     const unsigned target = (n + 1u) * gridDim.x;
     uint32_t i = 0;
     for (;; ++i) {
@@ -125,6 +134,12 @@ __device__ __forceinline__ bool grid_sync(unsigned* ctr, unsigned n, int* status
     if (!ok) atomicOr(status, kDevTimeout);
   }
   return __syncthreads_and(ok) != 0;
+}
+
+__device__ __forceinline__ bool grid_sync(unsigned* ctr, unsigned n, int* status,
+                                          uint32_t limit = kSpinLimit) {
+  grid_arrive(ctr);
+  return grid_wait(ctr, n, status, limit);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) stack_decode_kernel(const __grid_constant__ StackArgs P) {
@@ -301,8 +316,10 @@ __global__ void __launch_bounds__(kThreads, 1) stack_decode_kernel(const __grid_
       if (threadIdx.x == 0) atomicOr(P.status, kDevTimeout);
       break;
     }
+    // arrive, request B's first boxes while the others arrive, then wait
+    grid_arrive(P.bar);
     prefetch(wb, &P.tw_d[l], &P.ts_d[l]);
-    ok = grid_sync(P.bar, nbar++, P.status);
+    ok = grid_wait(P.bar, nbar++, P.status);
     if (!ok) break;
     // ---- B: h from the gate/up sums, down projection into x ----
     const float r = 1.0f / sqrtf(__ldcg(P.ss[par]) / (float)P.H + P.eps);
@@ -321,8 +338,9 @@ __global__ void __launch_bounds__(kThreads, 1) stack_decode_kernel(const __grid_
       break;
     }
     if (l + 1 < P.L) {
+      grid_arrive(P.bar);
       prefetch(wa, &P.tw_gu[l + 1], &P.ts_gu[l + 1]);
-      ok = grid_sync(P.bar, nbar++, P.status);
+      ok = grid_wait(P.bar, nbar++, P.status);
     }
   }
   drain();
