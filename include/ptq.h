@@ -217,7 +217,11 @@ PTQ_API size_t ptq_ffn_stack_workspace_bytes(int64_t M, int64_t H, int64_t I,
  * output in fp32; PTQ_BF16 stores them in bf16 (the residual stream stays
  * fp32 either way).  ptq_ffn_stack_route names the implementation: one
  * persistent launch per 24 layers for a single fp32 token, else per layer
- * an add-and-norm kernel and the block's kernels, and a final add.
+ * an add-and-norm kernel and the block's kernels, and a final add.  The
+ * persistent path adds the row sums of its projections with atomics, so its
+ * results may differ between runs by fp32 rounding; the per-layer path is
+ * bitwise reproducible.  When the device cannot hold the persistent grid
+ * (its SMs partly held elsewhere) the call takes the per-layer path.
  * workspace: device scratch of ptq_ffn_stack_workspace_bytes(...) bytes,
  * 16-byte aligned, caller-owned, contents unspecified on return.  Every
  * layer is validated before the first launch, so a refused call leaves x
