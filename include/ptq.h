@@ -23,8 +23,10 @@
  *   x, y   activations: PTQ_F32 -> float, PTQ_BF16 -> bfloat16 bit patterns.
  *
  * Conventions:
- *   - Every call returns a ptq_status and never aborts.  A call that returns
- *     anything but PTQ_OK has launched nothing.  ptq_last_error() returns a
+ *   - Every call returns a ptq_status and never aborts.  A call refused by
+ *     its argument checks (any status but PTQ_OK and PTQ_ERR_CUDA) has
+ *     launched nothing.  PTQ_ERR_CUDA from a call that launches several
+ *     kernels may follow launches already made.  ptq_last_error() returns a
  *     message for the calling thread's most recent failure.
  *   - Device pointers must be 16-byte aligned (signs: 4-byte aligned).
  *   - Device calls are asynchronous on `stream` (NULL = the legacy default
