@@ -134,14 +134,16 @@ def quarter_scales(bits):
     return (bits.view(np.float16) / np.float16(4)).astype(np.float16).view(np.uint16)
 
 
-def test_stack_decode_spans_launches(P, orc, syn):
-    # 26 layers run as two persistent launches (24 + 2): the second starts by
-    # adding the first one's last block output.  Quarter scales keep each
-    # block's increment near 3% of the stream, so the bound stays tight
-    # enough that a dropped or repeated layer fails it.
+@pytest.mark.parametrize("Lc", [24, 25, 26])
+def test_stack_decode_spans_launches(P, orc, syn, Lc):
+    # 24 layers fill one persistent launch exactly; 25 and 26 run as two
+    # launches (24 + 1, 24 + 2), the second starting on the buffers the first
+    # zeroed.  Quarter scales keep each block's increment small against the
+    # stream, so the bound stays tight enough that a dropped or repeated layer
+    # fails it.
     import torch
 
-    H, I, Lc, eps = 1024, 2048, 26, 1e-6
+    H, I, eps = 1024, 2048, 1e-6
     dev, host, gains = [], [], []
     for l in range(Lc):
         F = syn.ffn_layer(70, l, H, I)
@@ -154,7 +156,7 @@ def test_stack_decode_spans_launches(P, orc, syn):
     got = run_stack(P, dev, gains, x, eps, torch.float32)
     P.device_check()
     ref, bound = oracle_with_bound(orc, host, gains, x.astype(np.float64), eps, False)
-    check_stack(got, ref, bound, "stack decode L=26")
+    check_stack(got, ref, bound, f"stack decode L={Lc}")
     # the bound is far below one layer's increment
     one = orc.ffn_stack(host[-1:], [gains[-1].astype(np.float64)], ref, eps) - ref
     assert bound.max() < 0.2 * np.abs(one).max()
