@@ -232,27 +232,34 @@ def ffn_lines(P, torch, syn, pk, world, args):
     # the chained stack: the same 64 blocks, each preceded by the residual add
     # and RMSNorm kernel, over an fp32 residual stream updated in place
     gains = [torch.from_numpy(syn.norm_gain(4, l, H)).cuda() for l in range(RING)]
-    for name, M, act in (("stack_decode", 1, torch.float32), ("stack_prefill", 256, torch.bfloat16)):
+    # M = 4 decode tokens: the persistent kernel, and beside it the
+    # bitwise-reproducible per-layer path the caller can ask for instead
+    for name, M, act, det in (("stack_decode", 1, torch.float32, False),
+                              ("stack_decode_m4", 4, torch.float32, False),
+                              ("stack_decode_m4_per_layer", 4, torch.float32, True),
+                              ("stack_prefill", 256, torch.bfloat16, False)):
         xs = torch.from_numpy(syn.ffn_input(4, 0, M, H, "f32")).cuda()
         pdt = P.PTQ_F32 if act == torch.float32 else P.PTQ_BF16
         ws = torch.empty(P.ffn_stack_workspace_bytes(M, H, I, pdt), dtype=torch.uint8, device="cuda")
         lays = [layers[l % RING] for l in range(LAYERS)]
         gs = [gains[l % RING] for l in range(LAYERS)]
 
-        def step(i, xs=xs, ws=ws, act=act, lays=lays, gs=gs):
-            P.ffn_stack(lays, gs, xs, 1e-6, act=act, workspace=ws)
+        def step(i, xs=xs, ws=ws, act=act, lays=lays, gs=gs, det=det):
+            P.ffn_stack(lays, gs, xs, 1e-6, act=act, workspace=ws, deterministic=det)
 
-        K = max(3, min(args.steps, 40 if M == 1 else 8))
+        K = max(3, min(args.steps, 40 if M <= 4 else 8))
         ms = timed_steps(torch, step, K, 3, chunk=2) / K
-        base = out["decode" if M == 1 else "prefill"]["ms_per_step"]
         line = {"workload": f"pre-norm residual stack of {LAYERS} feed-forward blocks, M={M}",
                 "M": M, "H": H, "I": I, "dtype": "f32 residual stream, "
-                + ("f32 activations" if M == 1 else "bf16 activations"),
+                + ("f32 activations" if act == torch.float32 else "bf16 activations"),
+                "path": P.ffn_stack_route(M, H, I, pdt) if not det else "stack_per_layer",
                 "ms_per_step": round(ms, 4),
-                "norm_and_residual_ms": round(ms - base, 4),
                 "weight_GB/s": round(world * wbytes / (ms * 1e-3) / 1e9, 1)}
-        if M == 1:
-            line["tokens_per_s"] = round(world * 1e3 / ms, 1)
+        if M in (1, 256):
+            base = out["decode" if M == 1 else "prefill"]["ms_per_step"]
+            line["norm_and_residual_ms"] = round(ms - base, 4)
+        if act == torch.float32:
+            line["tokens_per_s"] = round(world * M * 1e3 / ms, 1)
         else:
             line["TFLOP/s"] = round(world * 2.0 * M * LAYERS * 3 * H * I / (ms * 1e-3) / 1e12, 1)
         out[name] = line

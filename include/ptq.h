@@ -218,8 +218,8 @@ PTQ_API size_t ptq_ffn_stack_workspace_bytes(int64_t M, int64_t H, int64_t I,
  * activation type as in ptq_ffn: PTQ_F32 (M <= 8) keeps xn and the block
  * output in fp32; PTQ_BF16 stores them in bf16 (the residual stream stays
  * fp32 either way).  ptq_ffn_stack_route names the implementation: one
- * persistent launch per 24 layers for a single fp32 token, else per layer
- * an add-and-norm kernel and the block's kernels, and a final add.  The
+ * persistent launch per 24 layers for 1 to 8 fp32 tokens, else per layer an
+ * add-and-norm kernel and the block's kernels, and a final add.  The
  * persistent path adds the row sums of its projections with atomics, so its
  * results may differ between runs by fp32 rounding; the per-layer path is
  * bitwise reproducible.  When the device cannot hold the persistent grid
@@ -234,13 +234,24 @@ PTQ_API PTQ_NODISCARD ptq_status ptq_ffn_stack(
     int64_t I, float eps, ptq_dtype dtype, void* workspace,
     size_t workspace_bytes, ptq_stream_t stream);
 
-/* ptq_ffn_stack_route -- which implementation ptq_ffn_stack uses for
- * (M, H, I, dtype) on the current device: "stack_decode_persistent" (M = 1,
- * PTQ_F32: the whole stack in one cooperative launch per 24 layers, one CTA
- * per SM, the layers separated by grid-wide barriers whose waits are
- * bounded -- a wait that runs out raises the status ptq_device_check
- * reports) or "stack_per_layer" (an add-and-norm kernel, then ptq_ffn's
- * kernels, per layer).  *name points to a static string.  Errors:
+/* ptq_ffn_stack_ex -- ptq_ffn_stack with flags.  PTQ_STACK_DETERMINISTIC
+ * takes the per-layer path for every M and dtype, whose results are bitwise
+ * reproducible.  Other bits are refused with PTQ_ERR_VALUE.
+ * ptq_ffn_stack(...) is ptq_ffn_stack_ex(..., 0, stream). */
+#define PTQ_STACK_DETERMINISTIC 1u
+PTQ_API PTQ_NODISCARD ptq_status ptq_ffn_stack_ex(
+    const ptq_ffn_layer* layers, int64_t L, float* x, int64_t M, int64_t H,
+    int64_t I, float eps, ptq_dtype dtype, void* workspace,
+    size_t workspace_bytes, unsigned flags, ptq_stream_t stream);
+
+/* ptq_ffn_stack_route -- which implementation ptq_ffn_stack (no flags) uses
+ * for (M, H, I, dtype) on the current device: "stack_decode_persistent"
+ * (M = 1 to 8, PTQ_F32: the whole stack in one cooperative launch per 24
+ * layers, the tokens taken in turn inside each phase, one CTA per SM, the
+ * layers separated by grid-wide barriers whose waits are bounded -- a wait
+ * that runs out raises the status ptq_device_check reports) or
+ * "stack_per_layer" (an add-and-norm kernel, then ptq_ffn's kernels, per
+ * layer).  *name points to a static string.  Errors:
  * PTQ_ERR_NULL, PTQ_ERR_VALUE (dtype), PTQ_ERR_SHAPE, PTQ_ERR_UNSUPPORTED
  * (no kernel for M and dtype). */
 PTQ_API PTQ_NODISCARD ptq_status ptq_ffn_stack_route(int64_t M, int64_t H,

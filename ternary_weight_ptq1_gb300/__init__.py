@@ -29,7 +29,7 @@ STATUS = {
 EXPORTS = ("ptq1_pack", "ptq1_unpack", "ptq_fwht", "ptq_matmul_workspace_bytes", "ptq_matmul",
            "ptq_rotate_matmul_workspace_bytes", "ptq_rotate_matmul", "ptq_ffn_workspace_bytes",
            "ptq_ffn", "ptq_ffn_noalloc", "ptq_ffn_stack_workspace_bytes", "ptq_ffn_stack",
-           "ptq_ffn_stack_route", "ptq2_pack", "ptq2_unpack",
+           "ptq_ffn_stack_ex", "ptq_ffn_stack_route", "ptq2_pack", "ptq2_unpack",
            "ptq_matmul_pq2_workspace_bytes", "ptq_matmul_pq2", "ptq_embed", "ptq_embed_ptq1",
            "ptq_route", "ptq_selftest_timeout", "ptq_selftest_grid_timeout",
            "ptq_device_check", "ptq_status_str", "ptq_last_error")
@@ -78,6 +78,8 @@ def load(path: str | None = None):
     L.ptq_ffn_stack_workspace_bytes.restype = ctypes.c_size_t
     L.ptq_ffn_stack.argtypes = [_P, _I64, _P, _I64, _I64, _I64, ctypes.c_float, _I32, _P,
                                 ctypes.c_size_t, _P]
+    L.ptq_ffn_stack_ex.argtypes = [_P, _I64, _P, _I64, _I64, _I64, ctypes.c_float, _I32, _P,
+                                   ctypes.c_size_t, ctypes.c_uint, _P]
     L.ptq_ffn_stack_route.argtypes = [_I64, _I64, _I64, _I32, ctypes.POINTER(ctypes.c_char_p)]
     L.ptq2_pack.argtypes = [_P, _P, _I64, _I64]
     L.ptq2_unpack.argtypes = [_P, _P, _I64, _I64, _P]
@@ -95,7 +97,7 @@ def load(path: str | None = None):
     L.ptq_last_error.argtypes = []
     L.ptq_last_error.restype = ctypes.c_char_p
     for name in ("ptq1_pack", "ptq1_unpack", "ptq_fwht", "ptq_matmul", "ptq_rotate_matmul", "ptq_ffn",
-                 "ptq_ffn_noalloc", "ptq_ffn_stack", "ptq_ffn_stack_route", "ptq2_pack",
+                 "ptq_ffn_noalloc", "ptq_ffn_stack", "ptq_ffn_stack_ex", "ptq_ffn_stack_route", "ptq2_pack",
                  "ptq2_unpack", "ptq_matmul_pq2", "ptq_embed",
                  "ptq_embed_ptq1", "ptq_route", "ptq_device_check", "ptq_selftest_timeout",
                  "ptq_selftest_grid_timeout"):
@@ -314,12 +316,17 @@ def ffn_stack_route(M: int, H: int, I: int, dtype: int) -> str:
     return name.value.decode()
 
 
-def ffn_stack(layers, norm_w, x, eps: float, act=None, workspace=None, stream=None):
+PTQ_STACK_DETERMINISTIC = 1
+
+
+def ffn_stack(layers, norm_w, x, eps: float, act=None, workspace=None, stream=None,
+              deterministic: bool = False):
     """L chained pre-norm feed-forward blocks over the fp32 residual stream x
     (M x H, updated in place and returned): x += ffn_l(rmsnorm(x) * g_l).
     `layers`: per layer (wgu_q, wgu_s, wd_q, wd_s, signs_in, signs_mid) as for
     ffn(); `norm_w`: per layer an H-vector of fp32 gains.  `act` is the
-    blocks' activation dtype, torch.float32 (default) or torch.bfloat16."""
+    blocks' activation dtype, torch.float32 (default) or torch.bfloat16.
+    `deterministic` takes the bitwise-reproducible per-layer path."""
     import torch
 
     if len(layers) != len(norm_w):
@@ -338,9 +345,11 @@ def ffn_stack(layers, norm_w, x, eps: float, act=None, workspace=None, stream=No
         ptrs = [_dev(t, ty, f"layers[{l}].{n}") for t, ty, n in zip(lay, types, names)]
         ptrs.append(_dev(g, torch.float32, f"norm_w[{l}]"))
         arr[l] = FfnLayer(*[p.value for p in ptrs])
-    _check(load().ptq_ffn_stack(ctypes.cast(arr, ctypes.c_void_p), L, _dev(x, torch.float32, "x"),
-                                M, H, I, float(eps), dt, _dev(workspace, None, "workspace"),
-                                workspace.numel() * workspace.element_size(), _stream(stream)),
+    _check(load().ptq_ffn_stack_ex(ctypes.cast(arr, ctypes.c_void_p), L,
+                                   _dev(x, torch.float32, "x"), M, H, I, float(eps), dt,
+                                   _dev(workspace, None, "workspace"),
+                                   workspace.numel() * workspace.element_size(),
+                                   PTQ_STACK_DETERMINISTIC if deterministic else 0, _stream(stream)),
            "ptq_ffn_stack")
     return x
 

@@ -619,33 +619,39 @@ PTQ_API ptq_status ptq_ffn(const uint8_t* wgu_q, const uint16_t* wgu_s, const ui
 
 // Workspace of ptq_ffn_stack, each region rounded up to 256 bytes:
 //   xn (M x H, dtype: the block input) | y (M x H, dtype: the block output)
-//   | ptq_ffn's workspace
-static bool stack_layout(int64_t M, int64_t H, int64_t I, ptq_dtype dt, size_t off[3],
+//   | ptq_ffn's workspace | [fp32, M <= 8: a second M x 2I fp32 gate/up buffer
+//   for the persistent path]
+static bool stack_layout(int64_t M, int64_t H, int64_t I, ptq_dtype dt, size_t off[4],
                          size_t ffn_off[5], size_t* ffn_need, size_t* total) {
-  int64_t a;
+  int64_t a, b = 0;
   if (!mul_ok(M, H, &a) || !mul_ok(a, (int64_t)dsize(dt), &a) || a > INT64_MAX / 4) return false;
+  if (dt == PTQ_F32 && M <= kStackMaxTokens && (!mul_ok(M, 2 * I, &b) || !mul_ok(b, 4, &b)))
+    return false;
   if (!ffn_layout(M, H, I, dt, ffn_off, ffn_need)) return false;
   const size_t r = (size_t)((a + 255) / 256 * 256);
   off[0] = 0;
   off[1] = r;
   off[2] = 2 * r;
-  if (*ffn_need > SIZE_MAX - off[2]) return false;
-  *total = off[2] + *ffn_need;
+  if (*ffn_need > SIZE_MAX / 2 - off[2]) return false;
+  off[3] = off[2] + (*ffn_need + 255) / 256 * 256;
+  *total = off[3] + (size_t)b;
   return true;
 }
 
 PTQ_API size_t ptq_ffn_stack_workspace_bytes(int64_t M, int64_t H, int64_t I, ptq_dtype dtype) {
-  size_t off[3], foff[5], fneed, total;
+  size_t off[4], foff[5], fneed, total;
   if (!dtype_ok(dtype) || !ffn_shape_ok(M, H, I) ||
       !stack_layout(M, H, I, dtype, off, foff, &fneed, &total))
     return 0;
   return total;
 }
 
-// One decode token in fp32 runs the stack as one persistent launch per 24
-// layers when the device and the shapes allow it.
-static bool stack_persistent(int64_t M, int64_t H, int64_t I, ptq_dtype dt) {
-  return M == 1 && dt == PTQ_F32 && stack_decode_supported(H, I);
+// Up to 8 decode tokens in fp32 run the stack as one persistent launch per
+// 24 layers when the device and the shapes allow it, unless the caller asks
+// for the bitwise-reproducible per-layer path.
+static bool stack_persistent(int64_t M, int64_t H, int64_t I, ptq_dtype dt, unsigned flags) {
+  return M >= 1 && M <= kStackMaxTokens && dt == PTQ_F32 &&
+         !(flags & PTQ_STACK_DETERMINISTIC) && stack_decode_supported(H, I);
 }
 
 PTQ_API ptq_status ptq_ffn_stack_route(int64_t M, int64_t H, int64_t I, ptq_dtype dtype,
@@ -659,22 +665,30 @@ PTQ_API ptq_status ptq_ffn_stack_route(int64_t M, int64_t H, int64_t I, ptq_dtyp
   if (!find_route(M, dtype))
     return fail(PTQ_ERR_UNSUPPORTED, "ptq_ffn_stack_route: no kernel for M=%lld dtype=%s",
                 (long long)M, dtype == PTQ_F32 ? "f32" : "bf16");
-  *name = stack_persistent(M, H, I, dtype) ? "stack_decode_persistent" : "stack_per_layer";
+  *name = stack_persistent(M, H, I, dtype, 0u) ? "stack_decode_persistent" : "stack_per_layer";
   return PTQ_OK;
 }
 
 PTQ_API ptq_status ptq_ffn_stack(const ptq_ffn_layer* layers, int64_t L, float* x, int64_t M,
                                  int64_t H, int64_t I, float eps, ptq_dtype dtype, void* ws,
                                  size_t ws_bytes, ptq_stream_t stream) {
+  return ptq_ffn_stack_ex(layers, L, x, M, H, I, eps, dtype, ws, ws_bytes, 0u, stream);
+}
+
+PTQ_API ptq_status ptq_ffn_stack_ex(const ptq_ffn_layer* layers, int64_t L, float* x, int64_t M,
+                                    int64_t H, int64_t I, float eps, ptq_dtype dtype, void* ws,
+                                    size_t ws_bytes, unsigned flags, ptq_stream_t stream) {
   t_msg[0] = 0;
   const char* who = "ptq_ffn_stack";
   if (!dtype_ok(dtype)) return fail(PTQ_ERR_VALUE, "%s: unknown dtype %d", who, (int)dtype);
+  if (flags & ~(unsigned)PTQ_STACK_DETERMINISTIC)
+    return fail(PTQ_ERR_VALUE, "%s: unknown flags 0x%x", who, flags);
   if (L < 0 || !ffn_shape_ok(M, H, I))
     return fail(PTQ_ERR_SHAPE, "%s: need L >= 0, M >= 0, H and I positive multiples of 1024",
                 who);
   if (!(eps >= 0.0f) || !(eps < INFINITY))
     return fail(PTQ_ERR_VALUE, "%s: eps must be finite and >= 0", who);
-  size_t off[3], foff[5], fneed, need;
+  size_t off[4], foff[5], fneed, need;
   if (!stack_layout(M, H, I, dtype, off, foff, &fneed, &need))
     return fail(PTQ_ERR_SHAPE, "%s: size overflow", who);
   if (M == 0 || L == 0) return PTQ_OK;
@@ -705,15 +719,15 @@ PTQ_API ptq_status ptq_ffn_stack(const ptq_ffn_layer* layers, int64_t L, float* 
     if (l == 0) r0 = r;
   }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (stack_persistent(M, H, I, dtype) && stack_decode_ss_bytes() <= off[1] - off[0] &&
+  if (stack_persistent(M, H, I, dtype, flags) && stack_decode_ss_bytes(M) <= off[1] - off[0] &&
       stack_decode_bar_bytes(L) <= off[2] - off[1]) {
-    // one decode token: the whole stack as one persistent launch per 24
-    // layers; its scratch is carved from this workspace (the two gate/up
-    // buffers where the block's gate/up sums and row partials would go, the
-    // norm statistics where xn would, the barrier counters where y would)
+    // decode tokens: the whole stack as one persistent launch per 24 layers;
+    // its scratch comes from this workspace (one gate/up buffer where the
+    // block's gate/up sums would go, the other in the last region, the norm
+    // statistics where xn would go, the barrier counters where y would)
     const cudaError_t e = launch_stack_decode(
-        layers, L, x, reinterpret_cast<float*>(fbase + foff[1]),
-        reinterpret_cast<float*>(fbase + foff[4]), reinterpret_cast<float*>(base + off[0]),
+        layers, L, x, M, reinterpret_cast<float*>(fbase + foff[1]),
+        reinterpret_cast<float*>(base + off[3]), reinterpret_cast<float*>(base + off[0]),
         reinterpret_cast<unsigned*>(base + off[1]), H, I, eps, st);
     if (e != cudaErrorNotSupported)
       return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq_ffn_stack launch");

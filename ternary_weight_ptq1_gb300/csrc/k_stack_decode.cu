@@ -1,5 +1,5 @@
-// k_stack_decode.cu -- the chained pre-norm feed-forward stack at M = 1 (one
-// decode token) as one persistent, cooperative launch.
+// k_stack_decode.cu -- the chained pre-norm feed-forward stack for 1 to 8
+// decode tokens as one persistent, cooperative launch.
 //
 // "A 27B model in 5.5 GB: Bonsai ternary on Ferrox, locally", section "Speed,
 // and where it goes", names running a whole layer without leaving the device
@@ -8,7 +8,8 @@
 // FFN_l = rotate, gate+up, SwiGLU, rotate, down, with x the fp32 residual.
 //
 // Every CTA of the grid (one per SM) runs every layer, as two phases
-// separated by grid-wide barriers:
+// separated by grid-wide barriers, each over the tokens in turn (a token
+// after the first streams the same weight boxes again, from L2):
 //   A  gate/up by table lookup: each CTA rotates the one or two 1024-blocks
 //      of x * g_l its K-chunk touches, builds the lane tables and streams its
 //      rows (as the stand-alone GEMV, k_gemv_lut.cu), adding each row's chunk
@@ -61,12 +62,12 @@ struct StackArgs {
   const int8_t* signs_mid[kStackLayers];
   const float* norm_w[kStackLayers];
   float* x;         // H: the residual stream (phase B adds into it)
-  float* gu[2];     // 2I each: gate/up row sums of even / odd layers
-  float* ss[2];     // sum of squares of x at even / odd layers
+  float* gu[2];     // M x 2I each: gate/up row sums of even / odd layers
+  float* ss[2];     // M each: sums of squares of the x rows at even / odd layers
   unsigned* bar;    // this launch's barrier counter, zero at launch
   int* status;
   Proj pgu, pd;
-  int L, l0, H, I;  // l0: stack index of this launch's first layer
+  int L, l0, M, H, I;  // l0: stack index of this launch's first layer; M tokens
   float eps;
 };
 
@@ -142,6 +143,8 @@ __device__ __forceinline__ bool grid_sync(unsigned* ctr, unsigned n, int* status
   return grid_wait(ctr, n, status, limit);
 }
 
+// kOne: a single token, known at compile time (the token loops fold away)
+template <bool kOne>
 __global__ void __launch_bounds__(kThreads, 1) stack_decode_kernel(const __grid_constant__ StackArgs P) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int L = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -278,41 +281,50 @@ __global__ void __launch_bounds__(kThreads, 1) stack_decode_kernel(const __grid_
   unsigned nbar = 0;
   bool ok = true;
   const Work wa = work_of(P.pgu, cta, warp), wb = work_of(P.pd, cta, warp);
-  const int I = P.I;
+  const int I = P.I, M = kOne ? 1 : P.M;
   prefetch(wa, &P.tw_gu[0], &P.ts_gu[0]);
   for (int l = 0; l < P.L && ok; ++l) {
     const int par = (P.l0 + l) & 1;
-    float* gu = P.gu[par];
-    // ---- A: gate/up, and the sum of squares of x ----
+    float* gu = P.gu[par];   // M x 2I
+    float* ssl = P.ss[par];  // M
+    // ---- A: gate/up of every token, and the sums of squares of x ----
     {
       // zero the buffers the next layer adds into (a contiguous slice per CTA)
       float* gn = P.gu[par ^ 1];
-      const int per = (2 * I + 4 * G - 1) / (4 * G) * 4;
-      const int z1 = min(2 * I, (cta + 1) * per);
+      const int tot = M * 2 * I;
+      const int per = (tot + 4 * G - 1) / (4 * G) * 4;
+      const int z1 = min(tot, (cta + 1) * per);
       for (int i = cta * per + 4 * threadIdx.x; i < z1; i += 4 * kThreads)
         *reinterpret_cast<float4*>(gn + i) = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (cta == 0 && threadIdx.x == 0) *P.ss[par ^ 1] = 0.0f;
+      if (cta == 0 && threadIdx.x < M) P.ss[par ^ 1][threadIdx.x] = 0.0f;
     }
     const float* g = P.norm_w[l];
-    float sq = 0.0f;  // this thread's share of one rotation block's sum of squares
-    ok = gemv(P.pgu, wa, &P.tw_gu[l], &P.ts_gu[l], P.signs_in[l], gu, [&](int f, int i) {
-      const float4 a = ldcg4(P.x + (size_t)f * kRot + 4 * i);
-      const float4 s = __ldg(reinterpret_cast<const float4*>(g + (size_t)f * kRot) + i);
-      sq = fmaf(a.x, a.x, fmaf(a.y, a.y, fmaf(a.z, a.z, a.w * a.w)));
-      return make_float4(a.x * s.x, a.y * s.y, a.z * s.z, a.w * s.w);
-    });
-    if (cta < P.pgu.nch * P.pgu.cpc) {
-      int f0, f1;
-      chunk_rot_blocks<false>(wa.ws, wa.we, &f0, &f1);
-      const int f = f0 + (warp >> 3);
-      if (f <= f1 && owns_block(P.pgu, wa, f)) {
+    for (int m = 0; m < M && ok; ++m) {
+      // token m > 0 streams the same boxes again (from L2)
+      if (m > 0) prefetch(wa, &P.tw_gu[l], &P.ts_gu[l]);
+      const float* xm = P.x + (size_t)m * P.H;
+      float sq = 0.0f;  // this thread's share of one rotation block's sum of squares
+      bool okm = gemv(P.pgu, wa, &P.tw_gu[l], &P.ts_gu[l], P.signs_in[l], gu + (size_t)m * 2 * I,
+                      [&](int f, int i) {
+                        const float4 a = ldcg4(xm + (size_t)f * kRot + 4 * i);
+                        const float4 s = __ldg(reinterpret_cast<const float4*>(g + (size_t)f * kRot) + i);
+                        sq = fmaf(a.x, a.x, fmaf(a.y, a.y, fmaf(a.z, a.z, a.w * a.w)));
+                        return make_float4(a.x * s.x, a.y * s.y, a.z * s.z, a.w * s.w);
+                      });
+      if (cta < P.pgu.nch * P.pgu.cpc) {
+        int f0, f1;
+        chunk_rot_blocks<false>(wa.ws, wa.we, &f0, &f1);
+        const int f = f0 + (warp >> 3);
+        if (f <= f1 && owns_block(P.pgu, wa, f)) {
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-        if (L == 0) atomicAdd(P.ss[par], sq);
+          for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+          if (L == 0) atomicAdd(ssl + m, sq);
+        }
       }
+      // every warp of the CTA leaves the token loop together
+      ok = __syncthreads_and(okm) != 0;
     }
-    if (!__syncthreads_and(ok)) {
-      ok = false;
+    if (!ok) {
       if (threadIdx.x == 0) atomicOr(P.status, kDevTimeout);
       break;
     }
@@ -321,19 +333,24 @@ __global__ void __launch_bounds__(kThreads, 1) stack_decode_kernel(const __grid_
     prefetch(wb, &P.tw_d[l], &P.ts_d[l]);
     ok = grid_wait(P.bar, nbar++, P.status);
     if (!ok) break;
-    // ---- B: h from the gate/up sums, down projection into x ----
-    const float r = 1.0f / sqrtf(__ldcg(P.ss[par]) / (float)P.H + P.eps);
-    ok = gemv(P.pd, wb, &P.tw_d[l], &P.ts_d[l], P.signs_mid[l], P.x, [&](int f, int i) {
-      const float4 a = ldcg4(gu + (size_t)f * kRot + 4 * i);
-      const float4 b = ldcg4(gu + I + (size_t)f * kRot + 4 * i);
-      auto hv = [r](float gg, float uu) {
-        gg *= r;
-        return gg / (1.0f + expf(-gg)) * (uu * r);
-      };
-      return make_float4(hv(a.x, b.x), hv(a.y, b.y), hv(a.z, b.z), hv(a.w, b.w));
-    });
-    if (!__syncthreads_and(ok)) {
-      ok = false;
+    // ---- B: h from the gate/up sums, the down projection into each x row ----
+    for (int m = 0; m < M && ok; ++m) {
+      if (m > 0) prefetch(wb, &P.tw_d[l], &P.ts_d[l]);
+      const float* gum = gu + (size_t)m * 2 * I;
+      const float r = 1.0f / sqrtf(__ldcg(ssl + m) / (float)P.H + P.eps);
+      bool okm = gemv(P.pd, wb, &P.tw_d[l], &P.ts_d[l], P.signs_mid[l], P.x + (size_t)m * P.H,
+                      [&](int f, int i) {
+                        const float4 a = ldcg4(gum + (size_t)f * kRot + 4 * i);
+                        const float4 b = ldcg4(gum + I + (size_t)f * kRot + 4 * i);
+                        auto hv = [r](float gg, float uu) {
+                          gg *= r;
+                          return gg / (1.0f + expf(-gg)) * (uu * r);
+                        };
+                        return make_float4(hv(a.x, b.x), hv(a.y, b.y), hv(a.z, b.z), hv(a.w, b.w));
+                      });
+      ok = __syncthreads_and(okm) != 0;
+    }
+    if (!ok) {
       if (threadIdx.x == 0) atomicOr(P.status, kDevTimeout);
       break;
     }
@@ -372,7 +389,7 @@ cudaError_t launch_selftest_grid_timeout(cudaStream_t st) {
   return cudaGetLastError();
 }
 
-size_t stack_decode_ss_bytes() { return 2 * sizeof(float); }
+size_t stack_decode_ss_bytes(int64_t M) { return (size_t)(2 * M) * sizeof(float); }
 size_t stack_decode_bar_bytes(int64_t L) {
   return (size_t)((L + kStackLayers - 1) / kStackLayers) * sizeof(unsigned);
 }
@@ -389,14 +406,14 @@ static cudaError_t stack_device(int* sms_out) {
   if (e != cudaSuccess) return e;
   if (sms > 1024) return cudaErrorNotSupported;
   if (!g_stack_ready[dev]) {
-    e = cudaFuncSetAttribute(stack_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemTma);
-    if (e != cudaSuccess) return e;
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stack_decode_kernel, kThreads,
-                                                      kSmemTma);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) return cudaErrorNotSupported;
+    for (auto kern : {stack_decode_kernel<true>, stack_decode_kernel<false>}) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemTma);
+      if (e != cudaSuccess) return e;
+      int per_sm = 0;
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, kSmemTma);
+      if (e != cudaSuccess) return e;
+      if (per_sm < 1) return cudaErrorNotSupported;
+    }
     g_stack_ready[dev] = 1;
   }
   *sms_out = sms;
@@ -414,10 +431,11 @@ bool stack_decode_supported(int64_t H, int64_t I) {
 
 // Runs layers [0, L) of the stack as ceil(L / 24) cooperative launches of
 // one CTA per SM.
-cudaError_t launch_stack_decode(const ptq_ffn_layer* layers, int64_t L, float* x, float* gu0,
-                                float* gu1, float* ss, unsigned* bars, int64_t H, int64_t I,
-                                float eps, cudaStream_t st) {
-  if (L <= 0) return cudaSuccess;
+cudaError_t launch_stack_decode(const ptq_ffn_layer* layers, int64_t L, float* x, int64_t M,
+                                float* gu0, float* gu1, float* ss, unsigned* bars, int64_t H,
+                                int64_t I, float eps, cudaStream_t st) {
+  if (L <= 0 || M <= 0) return cudaSuccess;
+  if (M > kStackMaxTokens) return cudaErrorNotSupported;
   if (!stack_decode_supported(H, I)) return cudaErrorNotSupported;
   int* status = device_status_ptr();
   int sms = 0;
@@ -467,7 +485,8 @@ cudaError_t launch_stack_decode(const ptq_ffn_layer* layers, int64_t L, float* x
     A.gu[0] = gu0;
     A.gu[1] = gu1;
     A.ss[0] = ss;
-    A.ss[1] = ss + 1;
+    A.ss[1] = ss + M;
+    A.M = (int)M;
     A.bar = bars + j;
     A.status = status;
     A.pgu = pg;
@@ -491,12 +510,13 @@ cudaError_t launch_stack_decode(const ptq_ffn_layer* layers, int64_t L, float* x
   // the first layer adds into zeroed buffers (each later layer's are zeroed
   // inside the kernel, by the layer before it)
   e = cudaMemsetAsync(bars, 0, stack_decode_bar_bytes(L), st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(gu0, 0, (size_t)(2 * I) * sizeof(float), st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(gu1, 0, (size_t)(2 * I) * sizeof(float), st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(ss, 0, 2 * sizeof(float), st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(gu0, 0, (size_t)(M * 2 * I) * sizeof(float), st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(gu1, 0, (size_t)(M * 2 * I) * sizeof(float), st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ss, 0, stack_decode_ss_bytes(M), st);
   int64_t j = 0;
   for (; j < nl && e == cudaSuccess; ++j)
-    e = cudaLaunchKernelEx(&cfg, stack_decode_kernel, args[(size_t)j]);
+    e = M == 1 ? cudaLaunchKernelEx(&cfg, stack_decode_kernel<true>, args[(size_t)j])
+               : cudaLaunchKernelEx(&cfg, stack_decode_kernel<false>, args[(size_t)j]);
   // a device whose SMs are partly held elsewhere (MPS, a green context) cannot
   // take the whole grid at once: when the first launch is refused nothing
   // ran, and the caller takes the per-layer path (the memsets only cleared

@@ -108,22 +108,26 @@ cudaError_t launch_gemm(const uint8_t* wq, const uint16_t* scales, const void* x
 cudaError_t launch_swiglu(const float* gu, float* h, int64_t M, int64_t I,
                           cudaStream_t st);
 
-// The chained feed-forward stack at M = 1, fp32, as one persistent launch
-// per 24 layers (k_stack_decode.cu).  x: H fp32, updated in place.  gu0,
-// gu1: 2I fp32 scratch each; ss: 2 fp32; bars: one unsigned per launch (all
-// zeroed here).  Every layer's tensor maps are made before the first launch.
-// cudaErrorNotSupported when the shapes or the device do not fit it, or the
-// device cannot hold the cooperative grid at launch time (nothing ran then).
-cudaError_t launch_stack_decode(const ptq_ffn_layer* layers, int64_t L, float* x, float* gu0,
-                                float* gu1, float* ss, unsigned* bars, int64_t H, int64_t I,
-                                float eps, cudaStream_t st);
+// Decode tokens (fp32) the persistent stack serves at once.
+constexpr int kStackMaxTokens = 8;
+
+// The chained feed-forward stack for M = 1..8 fp32 decode tokens, as one
+// persistent launch per 24 layers (k_stack_decode.cu).  x: M x H fp32,
+// updated in place.  gu0, gu1: M x 2I fp32 scratch each; ss: 2M fp32; bars:
+// one unsigned per launch (all zeroed here).  Every layer's tensor maps are
+// made before the first launch.  cudaErrorNotSupported when the shapes or
+// the device do not fit it, or the device cannot hold the cooperative grid
+// at launch time (nothing ran then).
+cudaError_t launch_stack_decode(const ptq_ffn_layer* layers, int64_t L, float* x, int64_t M,
+                                float* gu0, float* gu1, float* ss, unsigned* bars, int64_t H,
+                                int64_t I, float eps, cudaStream_t st);
 // A grid barrier of the persistent stack that one CTA never reaches: the
 // others' bounded waits run out and raise the status word.
 cudaError_t launch_selftest_grid_timeout(cudaStream_t st);
 // Whether launch_stack_decode serves (H, I) on the current device.
 bool stack_decode_supported(int64_t H, int64_t I);
 // Workspace bytes launch_stack_decode needs in `ss` and `bars`.
-size_t stack_decode_ss_bytes();
+size_t stack_decode_ss_bytes(int64_t M);
 size_t stack_decode_bar_bytes(int64_t L);
 
 // Residual add and RMSNorm between chained blocks (k_norm.cu): per row of

@@ -135,10 +135,12 @@ def test_stack_refusals_before_launch(P):
     odd = ctypes.c_void_p(16 * 1024 + 4)
     H, I = 1024, 2048
     need = P.ffn_stack_workspace_bytes(1, H, I, P.PTQ_F32)
-    # xn and y regions (256-byte rounded) ahead of the block's own scratch
-    assert need == 2 * H * 4 + P.ffn_workspace_bytes(1, H, I, P.PTQ_F32)
+    # xn and y regions (256-byte rounded) ahead of the block's own scratch,
+    # and for fp32 at M <= 8 a second gate/up buffer of the persistent path
+    up = lambda v: (v + 255) // 256 * 256  # noqa: E731
+    assert need == 2 * H * 4 + up(P.ffn_workspace_bytes(1, H, I, P.PTQ_F32)) + 2 * I * 4
     assert P.ffn_stack_workspace_bytes(3, H, I, P.PTQ_BF16) == (
-        2 * ((3 * H * 2 + 255) // 256 * 256) + P.ffn_workspace_bytes(3, H, I, P.PTQ_BF16))
+        2 * up(3 * H * 2) + up(P.ffn_workspace_bytes(3, H, I, P.PTQ_BF16)))
     assert P.ffn_stack_workspace_bytes(1, 1000, I, P.PTQ_F32) == 0
     assert P.ffn_stack_workspace_bytes(1, H, I, 9) == 0
     good = P.FfnLayer(*([16 * 1024] * 7))
@@ -163,6 +165,9 @@ def test_stack_refusals_before_launch(P):
     assert st([good], 1, wsb=need - 1) == 6
     assert st([good], 1, ws=odd) == 3
     assert st([good], 1, M=9, wsb=10 ** 9) == 5         # fp32 serves M <= 8
+    arr1 = (P.FfnLayer * 1)(good)
+    assert L.ptq_ffn_stack_ex(ctypes.cast(arr1, ctypes.c_void_p), 1, p16, 1, H, I, 1e-6,
+                              P.PTQ_F32, p16, need, 2, None) == 4  # unknown flag
     assert L.ptq_ffn_stack(None, 1, p16, 1, H, I, 1e-6, P.PTQ_F32, p16, need, None) == 1
     # every layer is checked before the first launch; the message names it
     assert st([good, no_q], 2) == 1

@@ -107,10 +107,10 @@ def test_stack_small(P, orc, syn, M, act):
 @pytest.mark.parametrize("H", [1024, 5120, 12288, 17408])
 @pytest.mark.parametrize("M,act", [(1, "f32"), (2, "f32"), (3, "bf16")])
 def test_stack_row_lengths(P, orc, syn, H, M, act):
-    # per layer: the add-and-norm kernel holds 1, 2 or 4 vectors of a row per
-    # thread (H = 1024, 5120, 12288) and loops over longer rows (H = 17408);
-    # M = 1 runs the persistent kernel, whose gate/up rows are then cut into
-    # 4 to 28 K-chunks and whose down rows into 2
+    # fp32 runs the persistent kernel, whose gate/up rows are cut into 4 to
+    # 28 K-chunks and whose down rows into 2; bf16 runs per layer, where the
+    # add-and-norm kernel holds 1, 2 or 4 vectors of a row per thread (H =
+    # 1024, 5120, 12288) and loops over longer rows (H = 17408)
     import torch
 
     I, Lc, eps = 1024, 2, 1e-6
@@ -122,11 +122,33 @@ def test_stack_row_lengths(P, orc, syn, H, M, act):
 
 
 def test_stack_routes(P):
-    # one fp32 token runs the persistent kernel; everything else per layer
-    assert P.ffn_stack_route(1, 5120, 17408, P.PTQ_F32) == "stack_decode_persistent"
+    # 1 to 8 fp32 tokens run the persistent kernel; bf16 runs per layer
+    for M in (1, 2, 8):
+        assert P.ffn_stack_route(M, 5120, 17408, P.PTQ_F32) == "stack_decode_persistent"
     assert P.ffn_stack_route(1, 1024, 2048, P.PTQ_F32) == "stack_decode_persistent"
-    assert P.ffn_stack_route(2, 5120, 17408, P.PTQ_F32) == "stack_per_layer"
     assert P.ffn_stack_route(1, 5120, 17408, P.PTQ_BF16) == "stack_per_layer"
+    assert P.ffn_stack_route(256, 5120, 17408, P.PTQ_BF16) == "stack_per_layer"
+
+
+@pytest.mark.parametrize("M", [1, 3, 8])
+def test_stack_deterministic_path(P, orc, syn, M):
+    # the per-layer path on request: within the bound, and bitwise the same
+    # on a second run
+    import torch
+
+    H, I, Lc, eps = 1024, 2048, 3, 1e-6
+    dev, host, gains = make_layers(P, orc, syn, 90 + M, Lc, H, I)
+    x = syn.ffn_input(90 + M, 0, M, H, "f32")
+    gd = [Q.dev(g) for g in gains]
+    runs = []
+    for _ in range(2):
+        xd = Q.dev(x.copy())
+        P.ffn_stack(dev, gd, xd, eps, deterministic=True)
+        torch.cuda.synchronize()
+        runs.append(xd)
+    assert torch.equal(runs[0], runs[1])
+    ref, bound = oracle_with_bound(orc, host, gains, x.astype(np.float64), eps, False)
+    check_stack(Q.host_f64(runs[0]), ref, bound, f"deterministic stack M={M}")
 
 
 def quarter_scales(bits):
@@ -198,10 +220,10 @@ def test_stack_persistent_in_a_graph(P, orc, syn):
     check_stack(got, ref, bound, "persistent stack replayed from a graph")
 
 
-@pytest.mark.parametrize("M,act", [(1, "f32"), (3, "bf16")])
+@pytest.mark.parametrize("M,act", [(1, "f32"), (4, "f32"), (3, "bf16")])
 def test_stack_writes_stay_in_bounds(P, orc, syn, M, act):
     # the residual and the workspace sit between guard bands of a known byte
-    # pattern; after the call (persistent at M = 1, per layer at M = 3) the
+    # pattern; after the call (persistent for fp32, per layer for bf16) the
     # guards are untouched and the result still agrees with the oracle
     import torch
 
