@@ -607,17 +607,18 @@ def run_profile_case(which: str):
     """A few launches of one kernel on a small case sized for an ncu capture:
     gemv -- decode GEMV, M=1, K=5120, N=8*17408 (156 MB of weights > L2);
     gemm -- prefill GEMM, M=512, K=5120, N=17408, bf16 (gemm128: M=128);
-    stack -- the persistent decode stack, 4 layers of H=5120, I=17408.
+    stack -- the persistent decode stack, 4 layers of H=5120, I=17408, one
+    token (stack4: four tokens).
     Prints the event time of the last call (not a bench number)."""
     import torch
 
     import synth as syn
     import ternary_weight_ptq1_gb300 as P
 
-    if which == "stack":
+    if which in ("stack", "stack4"):
         # the persistent decode stack over 4 layers (234 MB of weights > L2),
         # H=5120, I=17408: one cooperative launch
-        H, I = 5120, 17408
+        H, I, T = 5120, 17408, 1 if which == "stack" else 4
         lays, gains = [], []
         for l in range(4):
             F = syn.ffn_layer(4, l, H, I)
@@ -625,18 +626,18 @@ def run_profile_case(which: str):
                 P.pack(F.wgu_trits), F.wgu_scales.view(np.int16), P.pack(F.wd_trits),
                 F.wd_scales.view(np.int16), F.signs_in, F.signs_mid)))
             gains.append(torch.from_numpy(syn.norm_gain(4, l, H)).cuda())
-        x = torch.from_numpy(syn.ffn_input(4, 0, 1, H, "f32")).cuda()
-        ws = torch.empty(P.ffn_stack_workspace_bytes(1, H, I, P.PTQ_F32), dtype=torch.uint8,
+        x = torch.from_numpy(syn.ffn_input(4, 0, T, H, "f32")).cuda()
+        ws = torch.empty(P.ffn_stack_workspace_bytes(T, H, I, P.PTQ_F32), dtype=torch.uint8,
                          device="cuda")
         call = lambda: P.ffn_stack(lays, gains, x, 1e-6, workspace=ws)  # noqa: E731
-        M, N = 1, 3 * H * I // K_COLS
+        M, N = T, 3 * H * I // K_COLS
     elif which == "gemv":
         M, N, dt = 1, 8 * N_ROWS, "f32"
     elif which == "gemm128":
         M, N, dt = 128, N_ROWS, "bf16"
     else:
         M, N, dt = PREFILL_M, N_ROWS, "bf16"
-    if which == "stack":
+    if which in ("stack", "stack4"):
         pass
     elif dt == "f32":  # the bench's decode call: rotation fused into the GEMV
         mv = syn.gaussian_matvec(7, M, N, K_COLS, dtype=dt)
@@ -679,7 +680,7 @@ def main():
     ap.add_argument("--skip-embed", action="store_true")
     ap.add_argument("--skip-pq2", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
-    ap.add_argument("--profile", choices=["gemv", "gemm", "gemm128", "stack"],
+    ap.add_argument("--profile", choices=["gemv", "gemm", "gemm128", "stack", "stack4"],
                     help="run a small case of one kernel for an ncu capture, then exit")
     args = ap.parse_args()
     if args.profile:
