@@ -25,7 +25,7 @@
  *   byte = ceil(256 v / 243), last byte of a block holds 3 trits padded with
  *   digit 1) is the workload definition of the tiny PTQ1_0 matvec case.
  *
- * Readings where the pages are silent (each is stated again in the design doc):
+ * Readings where the pages are silent:
  *   - trit order inside a block is contiguous: byte j, digit n <-> weight
  *     5j+n, n = 0 is the most significant base-3 digit;
  *   - the rotation flips signs first, then applies the Sylvester-ordered
