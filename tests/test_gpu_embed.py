@@ -134,12 +134,17 @@ def test_dispatch_paths(P, orc, syn):
     t, sc = syn.weights(38, V, H)
     wq = P.pack(t)
     ids = syn.token_ids(38, 3, 16000, V)          # 80000 pairs
-    ids[-1] = V                                   # a bad id in the last pass
+    # bad ids: in the last pass, and next to good ones mid-way
+    bad = [15999, 3000, 3001, 7000]
+    ids[bad] = [V, -1, V + 5, -2 ** 31]
     y = P.embed_ptq1(Q.dev(wq), Q.dev(sc), _ids_dev(ids), Q.dev(s))
-    rows = np.array([0, 1, 7777, 15197, 15198, 15998])
+    rows = np.array([0, 1, 2999, 3002, 6999, 7001, 7777, 15197, 15198, 15998])
     Q.check_fwht(Q.host_f64(y[torch.from_numpy(rows).cuda()]), orc.embed_ptq1(wq, sc, ids[rows], s),
                  what="several pairs per CTA")
-    assert torch.isnan(y[-1]).all() and torch.isfinite(y[:-1]).all()
+    isbad = np.zeros(len(ids), bool)
+    isbad[bad] = True
+    mask = torch.from_numpy(isbad).cuda()
+    assert torch.isnan(y[mask]).all() and torch.isfinite(y[~mask]).all()
 
 
 def test_full_size_sampled(P, orc, syn):
