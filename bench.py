@@ -2,9 +2,10 @@
 
 Headline workload (decode gate/up): M=1, K=5120, N=17408 PTQ1_0 weights
 (19,496,960 bytes).  One step = rotate the activation (5 signed 1024-blocks)
-+ decode GEMV.  Metric: weight bytes per second.  A second line item times
-the prefill GEMM (M=512, K=5120, N=17408, bf16) in TFLOP/s, with M=128 and
-M=2048 beside it.
++ decode GEMV.  Metric: weight bytes per second.  Line items beside it: the
+decode at 4 tokens (the same shape) and at 8 tokens (K=17408, N=5120); the
+prefill GEMM (M=512, K=5120, N=17408, bf16) in TFLOP/s, with M=128 and
+M=2048.
 
 Inputs are resident in HBM before the timed region.  Every step uses the next
 of R distinct weight sets (R * 19.5 MB > the 129 MB L2), so no step finds its
@@ -404,6 +405,37 @@ def run_ours(args, world, rank):
     ms_e2e = max_over_ranks(e0.elapsed_time(e1)) / E
     e2e = world * WEIGHT_BYTES / (ms_e2e * 1e-3) / 1e9
 
+    # the other decode sizes of the workload, rotation fused, in CUDA graphs:
+    # 4 tokens on the gate/up shape (this ring's weights) and 8 tokens on the
+    # down shape (K = 17408, N = 5120, a ring of its own, 156 MB)
+    dec = {}
+    if not args.skip_decode_m:
+        for Mo, No, Ko in ((4, N_ROWS, K_COLS), (8, K_COLS, N_ROWS)):
+            dring = ring if No == N_ROWS else make_ring(P, torch, syn, 8, 1, No, Ko, "f32")
+            Rd = len(dring)
+            dxs = [torch.from_numpy(syn.normal_f32(2000 + r, 5, (Mo, Ko))).cuda() for r in range(8)]
+            dys = [torch.empty((Mo, No), device="cuda") for _ in range(8)]
+            dsg = torch.from_numpy(syn.signs(1, 3, Ko)).cuda()
+            dws = torch.empty(max(1, P.rotate_matmul_workspace_bytes(Mo, No, Ko, P.PTQ_F32)),
+                              dtype=torch.uint8, device="cuda")
+
+            def dstep(i, dring=dring, Rd=Rd, dxs=dxs, dys=dys, dsg=dsg, dws=dws):
+                wq, sc, _ = dring[i % Rd]
+                P.rotate_matmul(wq, sc, dxs[i % 8], dsg, out=dys[i % 8], workspace=dws)
+
+            dK = max(3, min(K, 200))
+            dms = timed_steps(torch, dstep, dK, 3, chunk=100) / dK
+            wb = No * Ko * 7 / 32
+            dec[f"M{Mo}"] = {"workload": f"decode rotate+GEMV, M={Mo}, K={Ko}, N={No}, fp32",
+                             "us_per_call": round(dms * 1e3, 2),
+                             "weight_GB/s_per_pass": round(world * wb / (dms * 1e-3) / 1e9, 1),
+                             "tokens_per_s_equiv": round(world * Mo * wb / (dms * 1e-3) / 5.906e9, 1),
+                             "kernels": "one gemv_lut_tma_kernel over the M tokens + one reduction"}
+            if dring is not ring:
+                del dring
+            del dxs, dys, dws
+        P.device_check()
+
     # prefill GEMM line item (M=512, bf16)
     pre = None
     if not args.skip_prefill:
@@ -482,6 +514,7 @@ def run_ours(args, world, rank):
                 "path": "python ctypes binding, eager launches, pinned host buffers"},
         "gpu_launches": 2 * K,   # fused rotation + table-lookup GEMV, chunk reduction
         "clocks": clocks,
+        "decode_other_M": dec or None,
         "prefill": pre,
         "ffn": ffn,
         "embed": emb,
@@ -676,6 +709,7 @@ def main():
     ap.add_argument("--cpu-reps", type=int, default=1000)       # about 10 s of oracle work
     ap.add_argument("--reference-max-steps", type=int, default=1000)
     ap.add_argument("--skip-prefill", action="store_true")
+    ap.add_argument("--skip-decode-m", action="store_true")
     ap.add_argument("--skip-ffn", action="store_true")
     ap.add_argument("--skip-embed", action="store_true")
     ap.add_argument("--skip-pq2", action="store_true")

@@ -109,8 +109,8 @@ PTQ_API PTQ_NODISCARD ptq_status ptq_fwht(const void* x, void* y,
 
 /* ptq_matmul_workspace_bytes -- scratch size ptq_matmul needs for
  * (M, N, K, dtype); 0 when it needs none or the arguments are invalid.
- * fp32 decode (M <= 8, K/128 even): one fp32 partial row sum per (K-chunk of
- * at most 640 weights, output row), reused by the tokens in turn; required.
+ * fp32 decode (M <= 8, K/128 even): one fp32 partial row sum per (token,
+ * K-chunk of at most 640 weights, output row); required.
  * bf16 GEMM: fp32 partial sums for shapes with too few output tiles to fill
  * the GPU, whose K is then split in up to 6 parts; optional (with less, the
  * product runs with fewer splits). */
@@ -122,8 +122,9 @@ PTQ_API size_t ptq_matmul_workspace_bytes(int64_t M, int64_t N, int64_t K,
  * x is M x K and must already be rotated (ptq_fwht) when W carries the fold.
  * Routing (one table, queryable with ptq_route):
  *   PTQ_F32,  1 <= M <= 8 : decode GEMV by per-position lookup tables of the
- *                           five-trit sums, one token after the other, fp32
- *                           throughout (K/128 odd: a GEMV with the fp32 peel)
+ *                           five-trit sums, the tokens one after the other in
+ *                           one launch, fp32 throughout (K/128 odd: a GEMV
+ *                           with the fp32 peel)
  *   PTQ_BF16, M >= 1      : prefill GEMM, bf16 in / fp32 accumulate / bf16 out
  *   PTQ_F32,  M > 8       : refused with PTQ_ERR_UNSUPPORTED
  * M == 0 or N == 0 is a no-op.  Requires K % 128 == 0 (fastest at

@@ -262,15 +262,12 @@ static ptq_status check_matmul(const uint8_t* wq, const uint16_t* scales, const 
 // x_t / y_t: the GEMV is fp32 in and out; the GEMM reads bf16 (public call)
 // or fp16 (inside the feed-forward block) and writes bf16 (public call) or
 // fp32 (the feed-forward block keeps gate/up in fp32).
-// The table-lookup GEMV for each of the M tokens in turn (its tables hold one
-// token's activations); the calls share the scratch, in stream order.
+// The table-lookup GEMV of the M tokens (one launch takes them in turn: its
+// tables hold one token's activations at a time), then one reduction.
 static cudaError_t gemv_lut_tokens(const uint8_t* wq, const uint16_t* scales, const float* x,
                                    const int8_t* signs, float* y, float* part, int64_t M,
                                    int64_t N, int64_t K, cudaStream_t st) {
-  cudaError_t e = cudaSuccess;
-  for (int64_t m = 0; m < M && e == cudaSuccess; ++m)
-    e = launch_gemv_lut(wq, scales, x + m * K, signs, y + m * N, part, N, K, LutEpilogue::Plain, st);
-  return e;
+  return launch_gemv_lut(wq, scales, x, signs, y, part, M, N, K, LutEpilogue::Plain, st);
 }
 
 // ws: ws_bytes of scratch, matmul_ws_bytes(M, N, K, dtype) for full speed
@@ -280,7 +277,7 @@ static cudaError_t run_matmul(const Route* r, const uint8_t* wq, const uint16_t*
                               int64_t K, void* ws, size_t ws_bytes, cudaStream_t st) {
   switch (r->kernel) {
     case Kernel::GemvF32:
-      if (gemv_lut_supported(N, K, false))  // table-lookup decode, one token at a time
+      if (gemv_lut_supported(N, K, false))  // table-lookup decode, the tokens in turn
         return gemv_lut_tokens(wq, scales, static_cast<const float*>(x), nullptr,
                                static_cast<float*>(y), static_cast<float*>(ws), M, N, K, st);
       return launch_gemv(wq, scales, static_cast<const float*>(x), static_cast<float*>(y), M, N,
@@ -293,7 +290,7 @@ static cudaError_t run_matmul(const Route* r, const uint8_t* wq, const uint16_t*
 
 // Scratch of ptq_matmul for valid arguments: the GEMV's per-chunk row sums.
 static size_t matmul_ws_bytes(int64_t M, int64_t N, int64_t K, ptq_dtype dt) {
-  if (dt == PTQ_F32) return (M >= 1 && M <= 8) ? gemv_lut_workspace_bytes(N, K) : 0;
+  if (dt == PTQ_F32) return (M >= 1 && M <= 8) ? gemv_lut_workspace_bytes(N, K, M) : 0;
   return gemm_tc_workspace_bytes(M, N, K);  // split-K partial sums
 }
 
@@ -370,7 +367,7 @@ PTQ_API ptq_status ptq2_unpack(const uint8_t* wq, int8_t* trits, int64_t N, int6
 }
 
 static size_t matmul_pq2_ws_bytes(int64_t M, int64_t N, int64_t K, ptq_dtype dt) {
-  if (dt == PTQ_F32) return (M >= 1 && M <= 8) ? gemv_lut_pq2_workspace_bytes(N, K) : 0;
+  if (dt == PTQ_F32) return (M >= 1 && M <= 8) ? gemv_lut_pq2_workspace_bytes(N, K, M) : 0;
   return gemm_tc_workspace_bytes(M, N, K);
 }
 
@@ -403,10 +400,9 @@ PTQ_API ptq_status ptq_matmul_pq2(const uint8_t* wq, const uint16_t* scales, con
     return fail(PTQ_ERR_ALIGN, "%s: workspace needs 16-byte alignment", who);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
-  if (r->kernel == Kernel::GemvF32) {  // one token at a time, as for PTQ1_0
-    for (int64_t m = 0; m < M && e == cudaSuccess; ++m)
-      e = launch_gemv_lut_pq2(wq, scales, static_cast<const float*>(x) + m * K, nullptr,
-                              static_cast<float*>(y) + m * N, static_cast<float*>(ws), N, K, st);
+  if (r->kernel == Kernel::GemvF32) {  // the tokens in turn in one launch, as for PTQ1_0
+    e = launch_gemv_lut_pq2(wq, scales, static_cast<const float*>(x), nullptr,
+                            static_cast<float*>(y), static_cast<float*>(ws), M, N, K, st);
   } else {
     e = launch_gemm_tc_pq2(wq, scales, x, y, M, N, K, ws, ws ? ws_bytes : 0, st);
   }
@@ -559,10 +555,10 @@ static cudaError_t run_ffn_block(const FfnRoutes& r, const uint8_t* wgu_q, const
     for (int64_t m = 0; m < M && e == cudaSuccess; ++m) {
       float* hm = h + m * I;
       e = launch_gemv_lut(wgu_q, wgu_s, static_cast<const float*>(x) + m * H, signs_in, hm,
-                          static_cast<float*>(part), 2 * I, H, LutEpilogue::SwiGLU, st);
+                          static_cast<float*>(part), 1, 2 * I, H, LutEpilogue::SwiGLU, st);
       if (e == cudaSuccess)
         e = launch_gemv_lut(wd_q, wd_s, hm, signs_mid, static_cast<float*>(y) + m * H,
-                            static_cast<float*>(part), H, I, LutEpilogue::Plain, st);
+                            static_cast<float*>(part), 1, H, I, LutEpilogue::Plain, st);
     }
     return e;
   }

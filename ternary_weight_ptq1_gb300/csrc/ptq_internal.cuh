@@ -75,27 +75,29 @@ cudaError_t launch_embed(const void* table, Act table_t, const int32_t* ids, con
 cudaError_t launch_embed_ptq1(const uint8_t* wq, const uint16_t* scales, const int32_t* ids,
                               const int8_t* signs, void* out, Act out_t, int64_t M, int64_t V,
                               int64_t H, cudaStream_t st);
-// M = 1 decode by lookup tables (k_gemv_lut.cu).  part: scratch of
-// gemv_lut_workspace_bytes(N, K) bytes.  cudaErrorNotSupported when the
-// shape does not fit it (K/128 odd, more K-chunks than SMs); the caller then
-// runs launch_gemv.
+// Decode by lookup tables (k_gemv_lut.cu) of M tokens: x is M x K, y M x N.
+// part: scratch of gemv_lut_workspace_bytes(N, K, M) bytes (the row sums of
+// every K-chunk of every token).  cudaErrorNotSupported when the shape does
+// not fit it (K/128 odd, more K-chunks than SMs); the caller then runs
+// launch_gemv.
 // signs != NULL: x is not rotated yet and the kernel rotates it (K % 1024).
-// SwiGLU: the weight is the fused gate+up (N = 2I) and y receives h (I).
+// SwiGLU (M = 1 only): the weight is the fused gate+up (N = 2I) and y
+// receives h (I).
 enum class LutEpilogue { Plain, SwiGLU };
 cudaError_t launch_gemv_lut(const uint8_t* wq, const uint16_t* scales, const float* x,
-                            const int8_t* signs, float* y, float* part, int64_t N, int64_t K,
-                            LutEpilogue ep, cudaStream_t st);
-size_t gemv_lut_workspace_bytes(int64_t N, int64_t K);
+                            const int8_t* signs, float* y, float* part, int64_t M, int64_t N,
+                            int64_t K, LutEpilogue ep, cudaStream_t st);
+size_t gemv_lut_workspace_bytes(int64_t N, int64_t K, int64_t M);
 // K-chunks of a row (0 when the table-lookup GEMV does not serve K), and the
 // CTAs that share one chunk's rows on a device of `sms` SMs.
 int64_t gemv_lut_chunks(int64_t K);
 int64_t gemv_lut_ctas_per_chunk(int64_t sms, int64_t nch, int64_t N);
 // The same decode for PQ2_0 weights (k_gemv_lut.cu): K % 1024 == 0 only.
 cudaError_t launch_gemv_lut_pq2(const uint8_t* wq, const uint16_t* scales, const float* x,
-                                const int8_t* signs, float* y, float* part, int64_t N, int64_t K,
-                                cudaStream_t st);
+                                const int8_t* signs, float* y, float* part, int64_t M, int64_t N,
+                                int64_t K, cudaStream_t st);
 int64_t gemv_lut_pq2_chunks(int64_t K);
-size_t gemv_lut_pq2_workspace_bytes(int64_t N, int64_t K);
+size_t gemv_lut_pq2_workspace_bytes(int64_t N, int64_t K, int64_t M);
 // Whether launch_gemv_lut serves (N, K) on the current device (with the
 // rotation when `rotate`).
 bool gemv_lut_supported(int64_t N, int64_t K, bool rotate);

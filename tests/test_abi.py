@@ -91,7 +91,7 @@ def test_refusals_before_launch(P):
     assert L.ptq_matmul(*args, None, need, None) == 6
     assert L.ptq_matmul(*args, p16, need - 1, None) == 6
     assert L.ptq_matmul(*args, odd, need, None) == 3
-    assert P.matmul_workspace_bytes(4, 17408, 5120, P.PTQ_F32) == need  # reused per token
+    assert P.matmul_workspace_bytes(4, 17408, 5120, P.PTQ_F32) == 4 * need  # per token
     assert P.matmul_workspace_bytes(9, 17408, 5120, P.PTQ_F32) == 0
     assert P.matmul_workspace_bytes(512, 17408, 5120, P.PTQ_BF16) == 0
     assert P.matmul_workspace_bytes(1, 17408, 5120 + 128, P.PTQ_F32) == 0  # K/128 odd
