@@ -91,7 +91,13 @@ def test_refusals_before_launch(P):
     assert L.ptq_matmul(*args, None, need, None) == 6
     assert L.ptq_matmul(*args, p16, need - 1, None) == 6
     assert L.ptq_matmul(*args, odd, need, None) == 3
-    assert P.matmul_workspace_bytes(4, 17408, 5120, P.PTQ_F32) == 4 * need  # per token
+    # one scratch row sum per (token, chunk, row): M = 4 needs four times as much
+    need4 = P.matmul_workspace_bytes(4, 17408, 5120, P.PTQ_F32)
+    assert need4 == 4 * need
+    args4 = (p16, p16, p16, p16, 4, 17408, 5120, P.PTQ_F32)
+    assert L.ptq_matmul(*args4, p16, need, None) == 6
+    assert L.ptq_matmul(*args4, p16, need4 - 1, None) == 6
+    assert P.rotate_matmul_workspace_bytes(4, 17408, 5120, P.PTQ_F32) >= need4
     assert P.matmul_workspace_bytes(9, 17408, 5120, P.PTQ_F32) == 0
     assert P.matmul_workspace_bytes(512, 17408, 5120, P.PTQ_BF16) == 0
     assert P.matmul_workspace_bytes(1, 17408, 5120 + 128, P.PTQ_F32) == 0  # K/128 odd
@@ -239,6 +245,7 @@ def test_pq2_host_side(P, orc, syn):
     assert mm(None, p16, p16, p16, 1, 8, 1024, P.PTQ_BF16) == 1
     need = P.matmul_pq2_workspace_bytes(1, 17408, 5120, P.PTQ_F32)
     assert need == 10 * 17408 * 4                                  # 320 words a row: 10 chunks
+    assert P.matmul_pq2_workspace_bytes(8, 17408, 5120, P.PTQ_F32) == 8 * need  # per token
     assert mm(p16, p16, p16, p16, 1, 17408, 5120, P.PTQ_F32) == 6  # no workspace
     assert P.matmul_pq2_workspace_bytes(1, 100, 1152, P.PTQ_F32) == 0
 
