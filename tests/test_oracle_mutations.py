@@ -43,6 +43,10 @@ MUTATIONS = [
     ("sum of squares for the mean", "const double inv = 1.0 / sqrt(ss / (double)H + eps);",
      "const double inv = 1.0 / sqrt(ss + eps);"),
     ("no residual add", "x[i] += y[i];", "x[i] = y[i];"),
+    ("activations of the next token", "const double* xm = x + m * K;",
+     "const double* xm = x + ((m + 1) % M) * K;"),
+    ("norm of the next token's row", "const double* xm = x + m * H;",
+     "const double* xm = x + ((m + 1) % M) * H;"),
     ("PQ2_0 code taken as the trit", "(2 * (i % ORC_PQ2_PER_BYTE))) & 3) - 1);",
      "(2 * (i % ORC_PQ2_PER_BYTE))) & 3));"),
     ("embedding row of the next id", "orc_unrotate_def(table + (int64_t)ids[m] * H, signs, om, 1, H);",

@@ -472,6 +472,19 @@ def test_stack_composes_and_is_scale_free(orc, syn):
     np.testing.assert_allclose(inc_c, inc, rtol=1e-12, atol=1e-12)
 
 
+def test_stack_rows_are_independent(orc, syn):
+    # every token row goes through the stack on its own (the norm is per row):
+    # a 3-row call equals three 1-row calls, for rows of different scales
+    H, I = 1024, 1024
+    x = syn.normal_f64(64, 2, (3, H)) * np.array([[1.0], [5.0], [0.2]])
+    lay = _stack_layer(syn, 64, 0, H, I)
+    g = 1.0 + 0.1 * syn.normal_f64(64, 7, (H,))
+    all3 = orc.ffn_stack([lay], [g], x, 1e-5)
+    for m in range(3):
+        np.testing.assert_allclose(all3[m:m + 1], orc.ffn_stack([lay], [g], x[m:m + 1], 1e-5),
+                                   rtol=0, atol=1e-12)
+
+
 def test_stack_rmsnorm_worked_values(orc, syn):
     # rows of 3s and 4s have mean square 12.5: with eps = 0 and unit gains
     # the block's input is x / sqrt(12.5), i.e. 0.8485... and 1.1313...
