@@ -15,7 +15,16 @@ ROOT = os.path.dirname(HERE)
 
 # (name, text in oracle/ptq_oracle.c, the planted replacement)
 MUTATIONS = [
+    ("fp16 exponent bias off by one", "v = ldexp((double)(m + 1024), e - 25);",
+     "v = ldexp((double)(m + 1024), e - 24);"),
+    ("fp16 subnormals scaled by 2^-23", "v = ldexp((double)m, -24);", "v = ldexp((double)m, -23);"),
+    ("bf16 exponent bias off by one", "v = ldexp((double)(m + 128), e - 134);",
+     "v = ldexp((double)(m + 128), e - 133);"),
     ("encode rounds down", "(256 * v + 242) / 243", "(256 * v) / 243"),
+    ("padding digit 0 past the block", "int d = pos < ORC_WEIGHTS_PER_BLOCK ? t[pos] + 1 : 1;",
+     "int d = pos < ORC_WEIGHTS_PER_BLOCK ? t[pos] + 1 : 0;"),
+    ("definition rotation without the signs", "acc += h * (double)sb[i] * xb[i];",
+     "acc += h * (double)(sb[i] * 0 + 1) * xb[i];"),
     ("digits of a byte reversed", "int pos = ORC_TRITS_PER_BYTE * j + i;",
      "int pos = ORC_TRITS_PER_BYTE * j + (ORC_TRITS_PER_BYTE - 1 - i);"),
     ("trit decoded as the digit", "t[pos] = (int8_t)(orc_peel_digit(in[j], i) - 1);",
