@@ -38,6 +38,9 @@ MUTATIONS = [
      "xb[i] = (double)(sb[i] * 0 + 1) * acc / 32.0;"),
     ("scale index shifted", "double s = orc_half_to_double(scales[n * nb + b]);",
      "double s = orc_half_to_double(scales[n * nb + (b + 1) % nb]);"),
+    ("second rotation skipped", "orc_fwht_fast(h, signs_mid, h, M, I);", "(void)signs_mid;"),
+    ("first rotation with the second's signs", "orc_fwht_fast(x, signs_in, xr, M, H);",
+     "orc_fwht_fast(x, signs_mid, xr, M, H); (void)signs_in;"),
     ("silu with the wrong sign", "g[i] / (1.0 + exp(-g[i])) * u[i]", "g[i] / (1.0 + exp(g[i])) * u[i]"),
     ("gate and up swapped", "orc_swiglu(gu + m * 2 * I, gu + m * 2 * I + I, h + m * I, I);",
      "orc_swiglu(gu + m * 2 * I + I, gu + m * 2 * I, h + m * I, I);"),
