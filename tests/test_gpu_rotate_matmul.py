@@ -1,7 +1,7 @@
 """GPU parity of ptq_rotate_matmul, y = (R x) W^T, against the oracle's
-rotation followed by its matmul: the fp32 M = 1 route rotates inside the
-table-lookup GEMV (one or two 1024-blocks per chunk), every other route runs
-the rotation kernel first."""
+rotation followed by its matmul: the fp32 decode route (M <= 8) rotates
+inside the table-lookup GEMV (one or two 1024-blocks per chunk, each token in
+turn), the bf16 route runs the rotation kernel first."""
 import numpy as np
 import pytest
 
@@ -44,6 +44,21 @@ def test_rotate_gemv_down_shape(P, orc, syn):
     Q.check_f32(Q.host_f64(y), rot_ref(orc, t, s, Q.x_f64(h), signs), "rotate+gemv down")
 
 
+def test_rotate_gemv_several_tokens_full_size(P, orc, syn):
+    # the bench's multi-token decode calls: 4 tokens on the gate/up shape and
+    # 8 on the down shape, one launch taking the tokens in turn
+    mv = syn.gaussian_matvec(330, 4, 17408, 5120)
+    signs = syn.signs(330, 9, 5120)
+    y = P.rotate_matmul(Q.dev(P.pack(mv.trits)), Q.dev(mv.scales), Q.dev(mv.x), Q.dev(signs))
+    Q.check_f32(Q.host_f64(y), rot_ref(orc, mv.trits, mv.scales, Q.x_f64(mv.x), signs),
+                "rotate+gemv M=4 17408x5120")
+    t, s = syn.weights(331, 5120, 17408, p_zero=0.4)
+    h = Q.swiglu_like(331, 8, 17408)
+    signs = syn.signs(331, 9, 17408)
+    y = P.rotate_matmul(Q.dev(P.pack(t)), Q.dev(s), Q.dev(h), Q.dev(signs))
+    Q.check_f32(Q.host_f64(y), rot_ref(orc, t, s, Q.x_f64(h), signs), "rotate+gemv M=8 down")
+
+
 def test_rotate_matches_separate_calls(P, syn):
     import torch
 
@@ -60,7 +75,7 @@ def test_rotate_matches_separate_calls(P, syn):
 
 
 @pytest.mark.parametrize("M,dtype", [(4, "f32"), (8, "f32"), (64, "bf16"), (3, "bf16")])
-def test_rotate_matmul_unfused_routes(P, orc, syn, M, dtype):
+def test_rotate_matmul_other_sizes(P, orc, syn, M, dtype):
     N, K = 600, 2048
     mv = syn.gaussian_matvec(320 + M, M, N, K, dtype=dtype)
     signs = syn.signs(320 + M, 9, K)
