@@ -267,6 +267,40 @@ def ffn_lines(P, torch, syn, pk, world, args):
     return out
 
 
+def fwht_lines(P, torch, syn, pk, world, args):
+    """The stand-alone signed rotation (ptq_fwht) where it is bandwidth-bound:
+    the prefill activations (M=2048 x K=5120, bf16 in and out) and the
+    feed-forward prefill's intermediate (M=256 x I=17408, fp32 in and out;
+    inside ptq_ffn the same kernel writes fp16).  Each step rotates the next
+    of 8 distinct inputs into its own output (336 MB and 285 MB in all, more
+    than the L2).  Algorithmic bytes: the input and the output once each,
+    plus the K sign bytes."""
+    out = {}
+    R = 8
+    for name, M, K, dt in (("prefill_x_bf16", 2048, 5120, torch.bfloat16),
+                           ("ffn_prefill_h_f32", 256, 17408, torch.float32)):
+        sg = torch.from_numpy(syn.signs(11, 3, K)).cuda()
+        if dt == torch.bfloat16:
+            xs = [torch.from_numpy(syn.normal_bf16(1100 + r, 2, (M, K)).view(np.int16)).cuda()
+                  .view(torch.bfloat16) for r in range(R)]
+        else:
+            xs = [torch.from_numpy(syn.normal_f32(1100 + r, 2, (M, K))).cuda() for r in range(R)]
+        ys = [torch.empty_like(xs[0]) for _ in range(R)]
+        esz = 2 if dt == torch.bfloat16 else 4
+        nbytes = 2 * M * K * esz + K
+        Kf = max(3, min(args.steps, 400))
+        us = timed_steps(torch, lambda i: P.fwht(xs[i % R], sg, out=ys[i % R]), Kf, 3,
+                         chunk=100) / Kf * 1e3
+        gbs = nbytes / (us * 1e-6) / 1e9
+        out[name] = {"workload": f"signed FWHT-1024, M={M}, K={K}, "
+                                 f"{'bf16' if esz == 2 else 'f32'} in and out",
+                     "us_per_call": round(us, 3), "bytes_per_call": nbytes,
+                     "GB/s": round(world * gbs, 1), "frac_of_hbm": round(gbs / pk["hbm"], 4),
+                     "kernel": "fwht1024_kernel"}
+        del xs, ys
+    return out
+
+
 def embed_lines(P, torch, syn, pk, world, args):
     """The token-embedding lookup on a rotated table (gather + inverse signed
     rotation), V=131,072 x H=5,120: one token (decode) and 2,048 (prefill),
@@ -481,6 +515,7 @@ def run_ours(args, world, rank):
                                        "frac_of_bf16_peak": round(otf / pk["bf16"], 4)}
             del oxs, oys
 
+    fwht = None if args.skip_fwht else fwht_lines(P, torch, syn, pk, world, args)
     ffn = None if args.skip_ffn else ffn_lines(P, torch, syn, pk, world, args)
     emb = None if args.skip_embed else embed_lines(P, torch, syn, pk, world, args)
     pq2 = None if args.skip_pq2 else pq2_lines(P, torch, syn, pk, world, args)
@@ -516,6 +551,7 @@ def run_ours(args, world, rank):
         "clocks": clocks,
         "decode_other_M": dec or None,
         "prefill": pre,
+        "fwht": fwht,
         "ffn": ffn,
         "embed": emb,
         "pq2": pq2,
@@ -641,14 +677,24 @@ def run_profile_case(which: str):
     gemv -- decode GEMV, M=1, K=5120, N=8*17408 (156 MB of weights > L2);
     gemm -- prefill GEMM, M=512, K=5120, N=17408, bf16 (gemm128: M=128);
     stack -- the persistent decode stack, 4 layers of H=5120, I=17408, one
-    token (stack4: four tokens).
+    token (stack4: four tokens);
+    fwht -- the stand-alone rotation, M=16384 x K=5120, bf16 in and out.
     Prints the event time of the last call (not a bench number)."""
     import torch
 
     import synth as syn
     import ternary_weight_ptq1_gb300 as P
 
-    if which in ("stack", "stack4"):
+    if which == "fwht":
+        # the stand-alone rotation of bf16 prefill activations, M=16384 x
+        # K=5120 (168 MB in and 168 MB out, more than the L2)
+        M, K = 16384, K_COLS
+        x = torch.from_numpy(syn.normal_bf16(11, 2, (M, K)).view(np.int16)).cuda().view(torch.bfloat16)
+        y = torch.empty_like(x)
+        sg = torch.from_numpy(syn.signs(11, 3, K)).cuda()
+        call = lambda: P.fwht(x, sg, out=y)  # noqa: E731
+        N = 0
+    elif which in ("stack", "stack4"):
         # the persistent decode stack over 4 layers (234 MB of weights > L2),
         # H=5120, I=17408: one cooperative launch
         H, I, T = 5120, 17408, 1 if which == "stack" else 4
@@ -670,7 +716,7 @@ def run_profile_case(which: str):
         M, N, dt = 128, N_ROWS, "bf16"
     else:
         M, N, dt = PREFILL_M, N_ROWS, "bf16"
-    if which in ("stack", "stack4"):
+    if which in ("stack", "stack4", "fwht"):
         pass
     elif dt == "f32":  # the bench's decode call: rotation fused into the GEMV
         mv = syn.gaussian_matvec(7, M, N, K_COLS, dtype=dt)
@@ -711,10 +757,11 @@ def main():
     ap.add_argument("--skip-prefill", action="store_true")
     ap.add_argument("--skip-decode-m", action="store_true")
     ap.add_argument("--skip-ffn", action="store_true")
+    ap.add_argument("--skip-fwht", action="store_true")
     ap.add_argument("--skip-embed", action="store_true")
     ap.add_argument("--skip-pq2", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
-    ap.add_argument("--profile", choices=["gemv", "gemm", "gemm128", "stack", "stack4"],
+    ap.add_argument("--profile", choices=["gemv", "gemm", "gemm128", "stack", "stack4", "fwht"],
                     help="run a small case of one kernel for an ncu capture, then exit")
     args = ap.parse_args()
     if args.profile:

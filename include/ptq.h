@@ -68,7 +68,12 @@ typedef enum ptq_status {
   PTQ_ERR_UNSUPPORTED = 5, /* a valid but unsupported (M, dtype) combination */
   PTQ_ERR_WORKSPACE = 6,   /* workspace missing or too small */
   PTQ_ERR_CUDA = 7,        /* a CUDA runtime call or launch failed */
-  PTQ_ERR_TIMEOUT = 8      /* a bounded device-side wait ran out */
+  PTQ_ERR_TIMEOUT = 8,     /* a bounded device-side wait ran out */
+  PTQ_ERR_RANGE = 9        /* reported by ptq_device_check: a value the bf16
+                              route keeps in fp16 (the rotated operands of
+                              ptq_rotate_matmul, ptq_ffn, ptq_ffn_stack and
+                              ptq_ffn_noalloc) exceeded the fp16 range
+                              (|v| >= 65520) and was stored as infinity */
 } ptq_status;
 
 typedef enum ptq_dtype { PTQ_F32 = 0, PTQ_BF16 = 1 } ptq_dtype;
@@ -158,7 +163,14 @@ PTQ_API size_t ptq_rotate_matmul_workspace_bytes(int64_t M, int64_t N,
  * signs: K int8 (device, 4-byte aligned).  Requires K % 1024 == 0.
  * workspace: at least ptq_rotate_matmul_workspace_bytes(...) bytes, 16-byte
  * aligned, any initial contents.  Other arguments, routing and errors as
- * ptq_matmul. */
+ * ptq_matmul.
+ * fp16 operand range (PTQ_BF16): the rotated activation R x is held in
+ * fp16 between the rotation and the tensor-core GEMM (11 significant bits,
+ * so the block scale times a trit is exact), so |R x| must stay below 65520.
+ * Beyond that the value is stored as infinity and the output is not finite;
+ * the rotation then raises the device status word and the next
+ * ptq_device_check returns PTQ_ERR_RANGE.  The fp32 route has no such
+ * limit. */
 PTQ_API PTQ_NODISCARD ptq_status ptq_rotate_matmul(
     const uint8_t* wq, const uint16_t* scales, const void* x,
     const int8_t* signs, void* y, int64_t M, int64_t N, int64_t K,
@@ -179,7 +191,13 @@ PTQ_API size_t ptq_ffn_workspace_bytes(int64_t M, int64_t H, int64_t I,
  * H % 1024 == 0 and I % 1024 == 0; dtype routing as in ptq_matmul.
  * workspace: device scratch of at least ptq_ffn_workspace_bytes(...) bytes,
  * 16-byte aligned, owned by the caller; its contents on return are
- * unspecified.  Errors as ptq_matmul, plus PTQ_ERR_WORKSPACE. */
+ * unspecified.  Errors as ptq_matmul, plus PTQ_ERR_WORKSPACE.
+ * fp16 operand range (PTQ_BF16): the rotated operands xr = R_in x and
+ * hr = R_mid h are held in fp16 (the block scale times a trit is exact in
+ * fp16); gate/up and h stay fp32 and y is bf16.  |xr| and |hr| must stay
+ * below 65520: beyond it the value is stored as infinity, y is not finite,
+ * and the next ptq_device_check returns PTQ_ERR_RANGE.  The fp32 route has
+ * no such limit. */
 PTQ_API PTQ_NODISCARD ptq_status ptq_ffn(
     const uint8_t* wgu_q, const uint16_t* wgu_s, const uint8_t* wd_q,
     const uint16_t* wd_s, const int8_t* signs_in, const int8_t* signs_mid,
@@ -229,7 +247,9 @@ PTQ_API size_t ptq_ffn_stack_workspace_bytes(int64_t M, int64_t H, int64_t I,
  * 16-byte aligned, caller-owned, contents unspecified on return.  Every
  * layer is validated before the first launch, so a refused call leaves x
  * unchanged.  L == 0 or M == 0 is a no-op.  Errors as ptq_ffn (the message
- * names the layer), plus PTQ_ERR_VALUE for a bad eps. */
+ * names the layer), plus PTQ_ERR_VALUE for a bad eps.  On PTQ_BF16 each
+ * block has ptq_ffn's fp16 operand range (PTQ_ERR_RANGE from
+ * ptq_device_check when it is exceeded). */
 PTQ_API PTQ_NODISCARD ptq_status ptq_ffn_stack(
     const ptq_ffn_layer* layers, int64_t L, float* x, int64_t M, int64_t H,
     int64_t I, float eps, ptq_dtype dtype, void* workspace,
@@ -262,17 +282,19 @@ PTQ_API PTQ_NODISCARD ptq_status ptq_ffn_stack_route(int64_t M, int64_t H,
 /* ptq_ffn_noalloc -- ptq_ffn without a workspace argument; it allocates
  * nothing.  (The source pages have no counterpart: this exists for callers,
  * not for the method.)
- * Some callers cannot allocate device memory: code running while its stream
- * is captured into a CUDA graph, real-time decode loops that may not take the
- * synchronisation and latency of cudaMalloc, and hosts whose device memory is
+ * Some callers cannot allocate device memory: real-time decode loops that
+ * may not take the synchronisation and latency of cudaMalloc, plug-ins that
+ * are handed a stream but no allocator, and hosts whose device memory is
  * held by another allocator that a C caller cannot reach.  This entry point
  * takes the block's scratch from one file-scope device array of
  * PTQ_FFN_NOALLOC_SCRATCH_BYTES bytes that every device loading the library
  * holds until the process exits; inputs and output are still the caller's.
- * Arguments, layouts and errors are those of ptq_ffn; a shape whose scratch
+ * Arguments, layouts, errors and the bf16 route's fp16 operand range are
+ * those of ptq_ffn; a shape whose scratch
  * (ptq_ffn_workspace_bytes) exceeds the array is refused with
  * PTQ_ERR_WORKSPACE.  At the default shapes (H = 5120, I = 17408) that admits
- * the fp32 decode path up to M = 8 and the bf16 path up to M = 16.
+ * the fp32 decode path up to M = 2 (1.48 MB of scratch a token, most of it
+ * the decode GEMV's per-chunk row sums) and the bf16 path up to M = 16.
  * The first call on a device looks the array's device address up
  * (cudaGetSymbolAddress) and caches it; make that first call before any
  * stream capture.  All calls share the one array and it keeps the last
@@ -363,8 +385,23 @@ PTQ_API PTQ_NODISCARD ptq_status ptq_route(int64_t M, ptq_dtype dtype,
 /* ptq_device_check -- synchronises `stream`, then reads and clears the
  * library's device status word.  Returns PTQ_ERR_TIMEOUT if a bounded
  * device-side wait in an earlier kernel ran out (that kernel's outputs are
- * then invalid), PTQ_ERR_CUDA if the stream reports an error, else PTQ_OK. */
+ * then invalid), else PTQ_ERR_RANGE if a bf16-route call stored an operand
+ * beyond the fp16 range as infinity (its outputs are then not finite),
+ * PTQ_ERR_CUDA if the stream reports an error, else PTQ_OK. */
 PTQ_API PTQ_NODISCARD ptq_status ptq_device_check(ptq_stream_t stream);
+
+/* ptq_matmul_bf16_accumulator -- test export: ptq_matmul's bf16 route (the
+ * prefill GEMM: same kernel, expanded t * bf16(s) weight tiles and split-K
+ * choice) writing the fp32 accumulator y (M x N fp32, device, 16-byte
+ * aligned) instead of rounding it to bf16.  It lets tests hold the route's
+ * arithmetic to the bare 1e-2 rms(y) bound of the workload text, which the
+ * bf16 output's own rounding (up to 2^-8 |y|) would otherwise hide.
+ * workspace: as ptq_matmul with PTQ_BF16 (may be NULL: fewer K splits).
+ * Errors as ptq_matmul. */
+PTQ_API PTQ_NODISCARD ptq_status ptq_matmul_bf16_accumulator(
+    const uint8_t* wq, const uint16_t* scales, const void* x, float* y,
+    int64_t M, int64_t N, int64_t K, void* workspace, size_t workspace_bytes,
+    ptq_stream_t stream);
 
 /* ptq_selftest_timeout -- test export for the timeout path.  Launches one
  * CTA that waits, with the library's bounded mbarrier wait and a short poll

@@ -23,6 +23,7 @@ PTQ_BF16 = 1
 STATUS = {
     0: "PTQ_OK", 1: "PTQ_ERR_NULL", 2: "PTQ_ERR_SHAPE", 3: "PTQ_ERR_ALIGN", 4: "PTQ_ERR_VALUE",
     5: "PTQ_ERR_UNSUPPORTED", 6: "PTQ_ERR_WORKSPACE", 7: "PTQ_ERR_CUDA", 8: "PTQ_ERR_TIMEOUT",
+    9: "PTQ_ERR_RANGE",
 }
 
 # Every symbol include/ptq.h declares.
@@ -31,7 +32,8 @@ EXPORTS = ("ptq1_pack", "ptq1_unpack", "ptq_fwht", "ptq_matmul_workspace_bytes",
            "ptq_ffn", "ptq_ffn_noalloc", "ptq_ffn_stack_workspace_bytes", "ptq_ffn_stack",
            "ptq_ffn_stack_ex", "ptq_ffn_stack_route", "ptq2_pack", "ptq2_unpack",
            "ptq_matmul_pq2_workspace_bytes", "ptq_matmul_pq2", "ptq_embed", "ptq_embed_ptq1",
-           "ptq_route", "ptq_selftest_timeout", "ptq_selftest_grid_timeout",
+           "ptq_route", "ptq_matmul_bf16_accumulator", "ptq_selftest_timeout",
+           "ptq_selftest_grid_timeout",
            "ptq_device_check", "ptq_status_str", "ptq_last_error")
 
 # Size of the built-in scratch array behind ptq_ffn_noalloc (include/ptq.h).
@@ -89,6 +91,8 @@ def load(path: str | None = None):
     L.ptq_embed.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _P]
     L.ptq_embed_ptq1.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _P]
     L.ptq_route.argtypes = [_I64, _I32, ctypes.POINTER(ctypes.c_char_p)]
+    L.ptq_matmul_bf16_accumulator.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _P,
+                                              ctypes.c_size_t, _P]
     L.ptq_device_check.argtypes = [_P]
     L.ptq_selftest_timeout.argtypes = [_P]
     L.ptq_selftest_grid_timeout.argtypes = [_P]
@@ -200,6 +204,25 @@ def matmul(wq, scales, x, out=None, workspace=None, stream=None):
     _check(load().ptq_matmul(_dev(wq, torch.uint8, "wq"), _dev(scales, torch.int16, "scales"),
                              _dev(x, None, "x"), _dev(y, x.dtype, "out"), M, N, K, dt, ws,
                              ws_bytes, _stream(stream)), "ptq_matmul")
+    return y
+
+
+def matmul_bf16_accumulator(wq, scales, x, stream=None):
+    """Test export: the bf16 prefill GEMM's fp32 accumulator (y = x W^T with
+    x bfloat16, y float32), the same kernel as matmul() on bfloat16 input
+    without the output's bf16 rounding."""
+    import torch
+
+    M, K = x.shape
+    N = wq.shape[0]
+    y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    need = matmul_workspace_bytes(M, N, K, PTQ_BF16)
+    ws = torch.empty(need, dtype=torch.uint8, device=x.device) if need > 0 else None
+    _check(load().ptq_matmul_bf16_accumulator(
+        _dev(wq, torch.uint8, "wq"), _dev(scales, torch.int16, "scales"),
+        _dev(x, torch.bfloat16, "x"), _dev(y, torch.float32, "out"), M, N, K,
+        _dev(ws, None, "workspace") if ws is not None else None, need, _stream(stream)),
+        "ptq_matmul_bf16_accumulator")
     return y
 
 

@@ -6,7 +6,7 @@
 #include <stdio.h>
 #include <string.h>
 
-#include <mutex>
+#include <atomic>
 
 #include "ptq_internal.cuh"
 
@@ -30,19 +30,21 @@ ptq_status cuda_fail(cudaError_t e, const char* what) {
 // ---- device status word ----------------------------------------------------
 static __device__ int g_device_status;
 static constexpr int kMaxDevices = 64;
-static int* g_status_ptr[kMaxDevices];
-static std::once_flag g_status_once[kMaxDevices];
+static std::atomic<int*> g_status_ptr[kMaxDevices];
 
+// The status word's device address on the current device.  Only a lookup
+// that succeeded is cached: a failed one (a sticky error left by an earlier
+// call, a lookup attempted during stream capture) is retried by the next call.
 int* device_status_ptr() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
     return nullptr;
-  std::call_once(g_status_once[dev], [dev] {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_device_status) == cudaSuccess)
-      g_status_ptr[dev] = static_cast<int*>(p);
-  });
-  return g_status_ptr[dev];
+  int* p = g_status_ptr[dev].load(std::memory_order_acquire);
+  if (p) return p;
+  void* q = nullptr;
+  if (cudaGetSymbolAddress(&q, g_device_status) != cudaSuccess || q == nullptr) return nullptr;
+  g_status_ptr[dev].store(static_cast<int*>(q), std::memory_order_release);
+  return static_cast<int*>(q);
 }
 
 cudaError_t read_and_clear_device_status(int* out, cudaStream_t st) {
@@ -109,6 +111,7 @@ PTQ_API const char* ptq_status_str(ptq_status s) {
     case PTQ_ERR_WORKSPACE: return "PTQ_ERR_WORKSPACE";
     case PTQ_ERR_CUDA: return "PTQ_ERR_CUDA";
     case PTQ_ERR_TIMEOUT: return "PTQ_ERR_TIMEOUT";
+    case PTQ_ERR_RANGE: return "PTQ_ERR_RANGE";
   }
   return "PTQ_ERR_UNKNOWN";
 }
@@ -323,6 +326,26 @@ PTQ_API ptq_status ptq_matmul(const uint8_t* wq, const uint16_t* scales, const v
   cudaError_t e = run_matmul(r, wq, scales, x, act_of(dtype), y, act_of(dtype), M, N, K,
                              ws, ws ? ws_bytes : 0, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq_matmul launch");
+}
+
+// Test export: the bf16 route's prefill GEMM writing its fp32 accumulator.
+// Same kernel, tiles and split-K choice as ptq_matmul with PTQ_BF16; only the
+// output's own bf16 rounding is left out, so the arithmetic error of the
+// route can be checked against the bare 1e-2 rms(y) bound.
+PTQ_API ptq_status ptq_matmul_bf16_accumulator(const uint8_t* wq, const uint16_t* scales,
+                                               const void* x, float* y, int64_t M, int64_t N,
+                                               int64_t K, void* ws, size_t ws_bytes,
+                                               ptq_stream_t stream) {
+  t_msg[0] = 0;
+  const char* who = "ptq_matmul_bf16_accumulator";
+  const Route* r = nullptr;
+  ptq_status s = check_matmul(wq, scales, x, y, M, N, K, PTQ_BF16, who, &r);
+  if (s != PTQ_OK || M == 0 || N == 0) return s;
+  if (ws && !aligned(ws, 16))
+    return fail(PTQ_ERR_ALIGN, "%s: workspace needs 16-byte alignment", who);
+  cudaError_t e = launch_gemm(wq, scales, x, Act::BF16, y, Act::F32, M, N, K, ws,
+                              ws ? ws_bytes : 0, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq_matmul_bf16_accumulator launch");
 }
 
 // ---- PQ2_0 ----------------------------------------------------------------
@@ -761,6 +784,10 @@ PTQ_API ptq_status ptq_device_check(ptq_stream_t stream) {
   if (e != cudaSuccess) return cuda_fail(e, "ptq_device_check");
   if (v & kDevTimeout)
     return fail(PTQ_ERR_TIMEOUT, "a bounded device-side wait ran out (status word 0x%x)", v);
+  if (v & kDevRange)
+    return fail(PTQ_ERR_RANGE,
+                "a rotated bf16-route operand exceeded the fp16 range (|v| >= 65520) and was "
+                "stored as infinity (status word 0x%x)", v);
   return PTQ_OK;
 }
 

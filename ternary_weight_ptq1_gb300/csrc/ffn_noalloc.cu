@@ -1,21 +1,20 @@
 // ffn_noalloc.cu -- ptq_ffn for callers that cannot allocate device memory.
 //
-// Some callers of this library cannot call cudaMalloc at all: code that runs
-// while its stream is being captured into a CUDA graph (an allocation there
-// would not be part of the graph), real-time decode loops that may not take
-// the device-wide synchronisation and unbounded latency of an allocation,
-// and hosts whose device memory is entirely reserved by another allocator
-// (a framework's caching allocator) that a C-ABI caller cannot reach.  For
-// them this file holds the feed-forward block's scratch in a file-scope
-// device array, so the call allocates nothing.  The caller still passes the
-// inputs and the output.
+// Some callers of this library cannot call cudaMalloc: real-time decode loops
+// that may not take the device-wide synchronisation and unbounded latency of
+// an allocation, plug-ins and embedded hosts that are handed a stream but no
+// allocator, and processes whose device memory is entirely reserved by
+// another allocator (a framework's caching allocator) that a C-ABI caller
+// cannot reach.  For them this file holds the feed-forward block's scratch in
+// a file-scope device array, so the call allocates nothing.  The caller
+// still passes the inputs and the output.
 //
 // The array lives in every device that loads this library, for as long as
 // the process lives.  All calls share it: two calls whose kernels overlap on
 // the GPU (different streams without ordering) race on it.  Nothing in it
 // has to start at zero: every region the block reads is written earlier in
 // the same call.
-#include <mutex>
+#include <atomic>
 
 #include "ptq_internal.cuh"
 
@@ -25,25 +24,27 @@ namespace {
 static __device__ __align__(256) unsigned char g_ffn_scratch[PTQ_FFN_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDev = 64;
-static void* g_scratch_addr[kMaxDev];
-static cudaError_t g_scratch_err[kMaxDev];
-static std::once_flag g_scratch_once[kMaxDev];
+static std::atomic<void*> g_scratch_addr[kMaxDev];
 
 // Device address of the scratch array on the current device.  In host code
 // the array's name is only a host-side stand-in, so the address is asked of
-// the runtime, once per device, with that device current.
+// the runtime with that device current.  Only a successful lookup is cached;
+// after a failed one (for instance a sticky error from an earlier call) the
+// next call asks again.
 static cudaError_t scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
-  std::call_once(g_scratch_once[dev], [dev] {
-    void* p = nullptr;
-    g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_ffn_scratch);
-    g_scratch_addr[dev] = p;
-  });
-  *out = g_scratch_addr[dev];
-  return g_scratch_err[dev];
+  void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
+    e = cudaGetSymbolAddress(&p, g_ffn_scratch);
+    if (e != cudaSuccess) return e;
+    if (p == nullptr) return cudaErrorInvalidSymbol;
+    g_scratch_addr[dev].store(p, std::memory_order_release);
+  }
+  *out = p;
+  return cudaSuccess;
 }
 
 }  // namespace

@@ -36,11 +36,20 @@ __device__ __forceinline__ uint32_t to16(float f) {
   else return __half_as_ushort(__float2half_rn(f));
 }
 
+// fp16 rounds |v| >= 65520 (the largest finite value 65504 plus half its
+// last-place step) to infinity.
+__device__ __forceinline__ bool beyond_f16(float v) {
+  const float a = fabsf(v);
+  return a >= 65520.0f && a <= 3.402823466e38f;
+}
+
 template <Act kIn, Act kOut>
 __global__ void __launch_bounds__(256) fwht1024_kernel(const void* x, void* y,
                                                        const int8_t* __restrict__ signs,
-                                                       int64_t total_blocks, int64_t blocks_per_row) {
+                                                       int64_t total_blocks, int64_t blocks_per_row,
+                                                       int* status) {
   const int lane = threadIdx.x & 31;
+  bool over = false;  // kOut == F16: a finite value stored as infinity
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
   pdl_release();  // the consumer's prologue (its weight prefetch) may start now
   pdl_wait();     // x may come from the previous kernel
@@ -75,6 +84,10 @@ __global__ void __launch_bounds__(256) fwht1024_kernel(const void* x, void* y,
     for (int j = 0; j < 8; ++j) {
       const int64_t e = base + 128 * j + 4 * lane;
       const float s = 1.0f / 32.0f;
+      if constexpr (kOut == Act::F16) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) over |= beyond_f16(v[j][c] * s);
+      }
       if constexpr (kOut != Act::F32) {
         uint2 out;
         out.x = to16<kOut>(v[j][0] * s) | (to16<kOut>(v[j][1] * s) << 16);
@@ -85,6 +98,9 @@ __global__ void __launch_bounds__(256) fwht1024_kernel(const void* x, void* y,
             make_float4(v[j][0] * s, v[j][1] * s, v[j][2] * s, v[j][3] * s);
       }
     }
+  }
+  if constexpr (kOut == Act::F16) {
+    if (__any_sync(0xffffffffu, over) && lane == 0) atomicOr(status, kDevRange);
   }
 }
 
@@ -98,14 +114,20 @@ cudaError_t launch_fwht(const void* x, Act in, void* y, Act out, const int8_t* s
   int64_t grid = (total + warps - 1) / warps;
   if (grid > 152 * 64) grid = 152 * 64;
   const dim3 g((unsigned)grid), b(32 * warps);
+  int* status = nullptr;
+  if (out == Act::F16 && (status = device_status_ptr()) == nullptr) return cudaErrorInvalidDevice;
   if (in == Act::F32 && out == Act::F32)
-    return launch_pdl(fwht1024_kernel<Act::F32, Act::F32>, g, b, 0, st, x, y, signs, total, bpr);
+    return launch_pdl(fwht1024_kernel<Act::F32, Act::F32>, g, b, 0, st, x, y, signs, total, bpr,
+                      status);
   if (in == Act::BF16 && out == Act::BF16)
-    return launch_pdl(fwht1024_kernel<Act::BF16, Act::BF16>, g, b, 0, st, x, y, signs, total, bpr);
+    return launch_pdl(fwht1024_kernel<Act::BF16, Act::BF16>, g, b, 0, st, x, y, signs, total, bpr,
+                      status);
   if (in == Act::BF16 && out == Act::F16)
-    return launch_pdl(fwht1024_kernel<Act::BF16, Act::F16>, g, b, 0, st, x, y, signs, total, bpr);
+    return launch_pdl(fwht1024_kernel<Act::BF16, Act::F16>, g, b, 0, st, x, y, signs, total, bpr,
+                      status);
   if (in == Act::F32 && out == Act::F16)
-    return launch_pdl(fwht1024_kernel<Act::F32, Act::F16>, g, b, 0, st, x, y, signs, total, bpr);
+    return launch_pdl(fwht1024_kernel<Act::F32, Act::F16>, g, b, 0, st, x, y, signs, total, bpr,
+                      status);
   return cudaErrorInvalidValue;
 }
 

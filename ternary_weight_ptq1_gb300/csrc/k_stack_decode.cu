@@ -438,6 +438,7 @@ cudaError_t launch_stack_decode(const ptq_ffn_layer* layers, int64_t L, float* x
   if (M > kStackMaxTokens) return cudaErrorNotSupported;
   if (!stack_decode_supported(H, I)) return cudaErrorNotSupported;
   int* status = device_status_ptr();
+  if (!status) return cudaErrorInvalidDevice;
   int sms = 0;
   cudaError_t e = stack_device(&sms);
   if (e != cudaSuccess) return e;

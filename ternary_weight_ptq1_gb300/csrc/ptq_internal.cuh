@@ -24,8 +24,12 @@ constexpr int kGroupBytes = kGroupBlocks * kBlockBytes;  // 208 = 13 * 16
 enum class Act { F32, BF16, F16 };
 inline Act act_of(ptq_dtype d) { return d == PTQ_BF16 ? Act::BF16 : Act::F32; }
 
-// Device status word: bounded waits that run out OR in a code here.
+// Device status word: bounded waits that run out OR in kDevTimeout; a
+// finite value that overflows the fp16 range where the bf16 route stores its
+// rotated tensor-core operands (|v| >= 65520 rounds to infinity) ORs in
+// kDevRange.
 constexpr int kDevTimeout = 1;
+constexpr int kDevRange = 2;
 
 // Launch with programmatic dependent launch allowed: the kernel may start
 // while the previous kernel in the stream is still running, and must run
@@ -63,6 +67,8 @@ cudaError_t launch_unpack(const uint8_t* wq, int8_t* trits, int64_t N,
 cudaError_t launch_unpack_pq2(const uint8_t* wq, int8_t* trits, int64_t N, int64_t K,
                               cudaStream_t st);
 // Supported (in, out): (F32, F32), (BF16, BF16), (BF16, F16), (F32, F16).
+// An F16 output raises kDevRange in the device status word when a finite
+// rotated value lies beyond the fp16 range (it is stored as infinity).
 cudaError_t launch_fwht(const void* x, Act in, void* y, Act out,
                         const int8_t* signs, int64_t M, int64_t K, cudaStream_t st);
 cudaError_t launch_gemv(const uint8_t* wq, const uint16_t* scales,

@@ -220,6 +220,12 @@ def test_workspace_sizes(P):
     assert gu_part > 28 * H * 4
     assert f >= H * 4 + 2 * I * 4 + I * 4 + gu_part
     assert f <= P.FFN_NOALLOC_SCRATCH_BYTES
+    # the allocation-free entry point's stated limits at these shapes: fp32
+    # decode up to 2 tokens, bf16 up to 16
+    assert P.ffn_workspace_bytes(2, H, I, P.PTQ_F32) <= P.FFN_NOALLOC_SCRATCH_BYTES
+    assert P.ffn_workspace_bytes(3, H, I, P.PTQ_F32) > P.FFN_NOALLOC_SCRATCH_BYTES
+    assert P.ffn_workspace_bytes(16, H, I, P.PTQ_BF16) <= P.FFN_NOALLOC_SCRATCH_BYTES
+    assert P.ffn_workspace_bytes(17, H, I, P.PTQ_BF16) > P.FFN_NOALLOC_SCRATCH_BYTES
     # chunk count: 13 K/256 words per row, at most 32 per chunk
     for K in (256, 512, 1024, 2048, 5120, 17408):
         words = 13 * K // 256

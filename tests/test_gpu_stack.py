@@ -292,23 +292,61 @@ def test_stack_refused_layer_leaves_x_alone(P, syn):
     assert torch.equal(x, x0)
 
 
+def assert_bound_discriminates(orc, host, gains, x64, eps, ref, bound, drop):
+    """The bound must be able to fail: far below one layer's increment, and
+    exceeded somewhere by the oracle's own stack with layer `drop` left out
+    (the mistake a chained kernel that skipped or repeated a layer would
+    make)."""
+    g64 = [g.astype(np.float64) for g in gains]
+    one = orc.ffn_stack(host[-1:], g64[-1:], ref, eps) - ref
+    assert bound.max() < 0.2 * np.abs(one).max(), (bound.max(), np.abs(one).max())
+    dropped = orc.ffn_stack(host[:drop] + host[drop + 1:], g64[:drop] + g64[drop + 1:], x64, eps)
+    assert (np.abs(dropped - ref) > bound).any(), "a dropped layer would pass this bound"
+
+
+def quarter_scale_layers(P, orc, syn, seed, Lc, H, I):
+    """As make_layers, with every block scale divided by 4: each block's
+    increment stays small against the residual stream, so the chained bound
+    (1 + 2 rho)^(L-1) stays tight enough to catch a dropped or repeated layer."""
+    dev, host, gains = [], [], []
+    for l in range(Lc):
+        F = syn.ffn_layer(seed, l, H, I)
+        sg, sd = quarter_scales(F.wgu_scales), quarter_scales(F.wd_scales)
+        gq, dq = P.pack(F.wgu_trits), P.pack(F.wd_trits)
+        dev.append((Q.dev(gq), Q.dev(sg), Q.dev(dq), Q.dev(sd), Q.dev(F.signs_in),
+                    Q.dev(F.signs_mid)))
+        host.append((orc.pack(F.wgu_trits), sg, orc.pack(F.wd_trits), sd, F.signs_in,
+                     F.signs_mid))
+        del F
+        gains.append(syn.norm_gain(seed, l, H))
+    return dev, host, gains
+
+
 def test_stack_decode_full_size_ring(P, orc, syn):
     # the bench's decode shape: H = 5120, I = 17408, M = 1, fp32, over the 8
-    # distinct layers the 64-layer step cycles through
+    # distinct layers the 64-layer step cycles through.  At the workload's
+    # own scales one layer multiplies rms(x) by about 1.8, and the chained
+    # bound grows to 25 times the last layer's increment -- a dropped layer
+    # would pass; with quarter scales the bound is 1e-3 of an increment and a
+    # dropped layer exceeds it about 1500-fold.
     import torch
 
     H, I, Lc, eps = 5120, 17408, 8, 1e-6
-    dev, host, gains = make_layers(P, orc, syn, 4, Lc, H, I)
+    dev, host, gains = quarter_scale_layers(P, orc, syn, 4, Lc, H, I)
     x = syn.ffn_input(4, 0, 1, H, "f32")
     got = run_stack(P, dev, gains, x, eps, torch.float32)
     P.device_check()
-    ref, bound = oracle_with_bound(orc, host, gains, x.astype(np.float64), eps, False)
+    x64 = x.astype(np.float64)
+    ref, bound = oracle_with_bound(orc, host, gains, x64, eps, False)
     check_stack(got, ref, bound, "stack decode H=5120 I=17408 L=8")
+    assert_bound_discriminates(orc, host, gains, x64, eps, ref, bound, drop=3)
 
 
 def test_stack_prefill_full_size_sampled_tokens(P, orc, syn):
     # the bench's prefill shape (M = 256, bf16 activations) over two layers;
-    # rows are independent in the stack, so the oracle runs sampled tokens
+    # rows are independent in the stack, so the oracle runs sampled tokens.
+    # Two layers keep the bound at 0.05 of the last increment, and the stack
+    # without its first layer exceeds it about 40-fold.
     import torch
 
     H, I, Lc, eps, M = 5120, 17408, 2, 1e-6, 256
@@ -316,5 +354,7 @@ def test_stack_prefill_full_size_sampled_tokens(P, orc, syn):
     x = syn.ffn_input(4, 1, M, H, "f32")
     got = run_stack(P, dev, gains, x, eps, torch.bfloat16)
     tokens = [0, 1, 128, 255]
-    ref, bound = oracle_with_bound(orc, host, gains, x[tokens].astype(np.float64), eps, True)
+    x64 = x[tokens].astype(np.float64)
+    ref, bound = oracle_with_bound(orc, host, gains, x64, eps, True)
     check_stack(got[tokens], ref, bound, "stack prefill M=256 sampled tokens")
+    assert_bound_discriminates(orc, host, gains, x64, eps, ref, bound, drop=0)

@@ -1,9 +1,10 @@
 """ptq_ffn_noalloc: the feed-forward block for callers that cannot allocate
-device memory (code inside a CUDA-graph capture, real-time decode loops that
-may not pay for cudaMalloc, hosts whose memory another allocator owns).  Its
-scratch is a built-in device array, so its results must match ptq_ffn (which
-takes a caller-allocated workspace) within the parity tolerance, call after
-call -- the array keeps the previous call's contents.
+device memory (real-time decode loops that may not pay for cudaMalloc,
+plug-ins handed a stream but no allocator, hosts whose memory another
+allocator owns).  Its scratch is a built-in device array, so its results must
+match ptq_ffn (which takes a caller-allocated workspace) within the parity
+tolerance, call after call -- the array keeps the previous call's contents --
+and both must match the oracle's block.
 
 This file is collected last so that a run stopping at the first failure has
 already run every other test; it also passes on its own in a fresh process.
@@ -33,20 +34,27 @@ def _layer(P, syn, seed, H, I):
             Q.dev(L.wd_scales), Q.dev(L.signs_in), Q.dev(L.signs_mid)]
 
 
-@pytest.mark.parametrize("M,dtype,H,I", [(1, "f32", 5120, 17408), (8, "f32", 1024, 2048),
-                                         (16, "bf16", 5120, 17408)])
-def test_noalloc_matches_ffn_twice(P, syn, M, dtype, H, I):
+@pytest.mark.parametrize("M,dtype,H,I", [(1, "f32", 5120, 17408), (2, "f32", 5120, 17408),
+                                         (8, "f32", 1024, 2048), (16, "bf16", 5120, 17408)])
+def test_noalloc_matches_ffn_twice(P, orc, syn, M, dtype, H, I):
     import torch
 
     check = Q.check_f32 if dtype == "f32" else Q.check_bf16
+    # the oracle checks every token of small calls and two tokens of large ones
+    tokens = np.arange(M) if M * H * I <= 8 * 1024 * 2048 or M == 1 else np.array([0, M - 1])
     for call, seed in enumerate((41, 42)):   # two calls in a row, different data
+        L = syn.ffn_layer(seed, 0, H, I)
         w = _layer(P, syn, seed, H, I)
         x = syn.ffn_input(seed, 0, M, H, dtype)
         xd = Q.dev(x) if dtype == "f32" else Q.dev_bf16(x)
         y_ref = P.ffn(*w, xd)
         y = P.ffn_noalloc(*w, xd)
         torch.cuda.synchronize()
-        check(Q.host_f64(y), Q.host_f64(y_ref), f"noalloc call {call} M={M} {dtype}")
+        yh = Q.host_f64(y)
+        check(yh, Q.host_f64(y_ref), f"noalloc call {call} M={M} {dtype} against ptq_ffn")
+        ref = orc.ffn(orc.pack(L.wgu_trits), L.wgu_scales, orc.pack(L.wd_trits), L.wd_scales,
+                      L.signs_in, L.signs_mid, Q.x_f64(x)[tokens])
+        check(yh[tokens], ref, f"noalloc call {call} M={M} {dtype} against the oracle")
 
 
 def test_noalloc_refuses_shapes_beyond_its_array(P, syn):
