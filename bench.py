@@ -183,9 +183,8 @@ def max_over_ranks(v: float) -> float:
 # case; None when the kernel has changed since those counters were taken.
 # Prefill: the capture is this exact launch (M=512, N=17408, K=5120).
 TRAFFIC_PREFILL = 24_840_448 + 7_168
-# Decode: the capture runs eight stacked gate/up matrices; the per-launch
-# figure is that capture's bytes / 8 (traffic grows with the rows streamed).
-TRAFFIC_DECODE = (156_060_416 + 5_802_496) // 8
+# Decode: the capture of the bench's own call (`--profile gemv1`).
+TRAFFIC_DECODE = 19_558_912 + 0
 
 
 def ffn_lines(P, torch, syn, pk, world, args):
@@ -338,6 +337,14 @@ def embed_lines(P, torch, syn, pk, world, args):
     return out
 
 
+def plan_text(plan, gemv):
+    """The decode launch ptq_gemv_plan reports, in words."""
+    if plan["cluster"]:
+        return (f"{gemv}: {plan['ctas']} CTAs in clusters of {plan['cluster']} (one per K-chunk), "
+                "row sums added in distributed shared memory; no second kernel")
+    return f"{gemv} ({plan['ctas']} CTAs) + gemv_lut_reduce_kernel"
+
+
 def pq2_lines(P, torch, syn, pk, world, args):
     """The same hot path over PQ2_0 weights (2 bits a weight + a 16-bit scale
     per 128: 34 bytes a block): the decode GEMV at the gate/up shape (M=1,
@@ -358,9 +365,10 @@ def pq2_lines(P, torch, syn, pk, world, args):
     us = timed_steps(torch, lambda i: P.matmul_pq2(ring[i % R][0], ring[i % R][1], x, out=ys[i % R],
                                                     workspace=ws), K1, 3) / K1 * 1e3
     gbs = (wbytes + 4 * K + 4 * N) / (us * 1e-6) / 1e9
+    plan = P.gemv_plan(1, N, K, pq2=True)
     dec = {"workload": "PQ2_0 decode GEMV, M=1, K=5120, N=17408 (x rotated)", "us_per_call": round(us, 3),
            "weight_bytes": wbytes, "GB/s": round(world * gbs, 1), "frac_of_hbm": round(gbs / pk["hbm"], 4),
-           "kernels": "gemv_lut_tma_kernel<PQ2_0> + gemv_lut_reduce_kernel"}
+           "kernels": plan_text(plan, "gemv_lut_tma_kernel<PQ2_0>")}
     M = PREFILL_M
     xb = torch.from_numpy(syn.normal_bf16(2000, 2, (M, K)).view(np.int16)).cuda().view(torch.bfloat16)
     yb = [torch.empty((M, N), device="cuda", dtype=torch.bfloat16) for _ in range(8)]
@@ -411,6 +419,7 @@ def run_ours(args, world, rank):
     ms_per_step = ms / K
     value = world * WEIGHT_BYTES / (ms_per_step * 1e-3) / 1e9       # GB/s, all ranks
     gemv_bytes = WEIGHT_BYTES + K_COLS * 4 + N_ROWS * 4
+    plan1 = P.gemv_plan(1, N_ROWS, K_COLS)
     gemv_us = ms_gemv / K * 1e3
     step_us = ms_per_step * 1e3
     achieved = gemv_bytes / (step_us * 1e-6) / 1e9
@@ -538,7 +547,7 @@ def run_ours(args, world, rank):
                      "traffic": TRAFFIC_DECODE,
                      "kernel": P.route(1, P.PTQ_F32), "kernel_us": round(step_us, 3),
                      "timed": "one ptq_rotate_matmul call: the table-lookup GEMV with the "
-                              "rotation fused in, and its chunk-reduction kernel",
+                              "rotation fused in (" + plan_text(plan1, "gemv_lut_tma_kernel") + ")",
                      "bytes_per_launch": gemv_bytes, "peak_source": pk["source"] + " copy bandwidth"},
         "stage_us": {"step_rotate_gemv_fused": round(step_us, 3),
                      "unfused_fwht": round(ms_fwht / K * 1e3, 3),
@@ -547,7 +556,7 @@ def run_ours(args, world, rank):
         "e2e": {"value": round(e2e, 2), "unit": "GB/s", "h2d_bytes_per_step": K_COLS * 4,
                 "d2h_bytes_per_step": N_ROWS * 4, "ms_per_step": round(ms_e2e, 5),
                 "path": "python ctypes binding, eager launches, pinned host buffers"},
-        "gpu_launches": 2 * K,   # fused rotation + table-lookup GEMV, chunk reduction
+        "gpu_launches": plan1["kernels"] * K,   # per call, as ptq_gemv_plan reports
         "clocks": clocks,
         "decode_other_M": dec or None,
         "prefill": pre,
@@ -675,6 +684,9 @@ def run_reference(args, world, rank):
 def run_profile_case(which: str):
     """A few launches of one kernel on a small case sized for an ncu capture:
     gemv -- decode GEMV, M=1, K=5120, N=8*17408 (156 MB of weights > L2);
+    gemv1 -- the bench's decode call itself, M=1, K=5120, N=17408 (ncu
+    flushes the caches before each pass, so its DRAM counters are cold, as
+    in the bench's ring of weight sets);
     gemm -- prefill GEMM, M=512, K=5120, N=17408, bf16 (gemm128: M=128);
     stack -- the persistent decode stack, 4 layers of H=5120, I=17408, one
     token (stack4: four tokens);
@@ -712,6 +724,8 @@ def run_profile_case(which: str):
         M, N = T, 3 * H * I // K_COLS
     elif which == "gemv":
         M, N, dt = 1, 8 * N_ROWS, "f32"
+    elif which == "gemv1":
+        M, N, dt = 1, N_ROWS, "f32"
     elif which == "gemm128":
         M, N, dt = 128, N_ROWS, "bf16"
     else:
@@ -761,7 +775,8 @@ def main():
     ap.add_argument("--skip-embed", action="store_true")
     ap.add_argument("--skip-pq2", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
-    ap.add_argument("--profile", choices=["gemv", "gemm", "gemm128", "stack", "stack4", "fwht"],
+    ap.add_argument("--profile", choices=["gemv", "gemv1", "gemm", "gemm128", "stack", "stack4",
+                                          "fwht"],
                     help="run a small case of one kernel for an ncu capture, then exit")
     args = ap.parse_args()
     if args.profile:

@@ -403,6 +403,20 @@ PTQ_API PTQ_NODISCARD ptq_status ptq_matmul_bf16_accumulator(
     int64_t M, int64_t N, int64_t K, void* workspace, size_t workspace_bytes,
     ptq_stream_t stream);
 
+/* ptq_gemv_plan -- introspection: the launch ptq_matmul's fp32 decode route
+ * (pq2 != 0: ptq_matmul_pq2's) makes for (M, N, K) on the current device,
+ * K % 1024 == 0, plain output (ptq_ffn's gate/up projection always adds the
+ * reduction kernel).  plan (host, 4 int32): CTAs, thread-block cluster size
+ * (0: no clusters), K-chunks a row is cut into, kernels launched.  At one
+ * token, when the device holds enough clusters of one CTA per K-chunk, the
+ * chunks of a row group form a cluster that adds its row sums in distributed
+ * shared memory and writes y (one kernel); otherwise a second kernel adds the
+ * chunk sums from the workspace.  Both give the same bits.  Host only (it
+ * asks the current device).  Errors: PTQ_ERR_NULL, PTQ_ERR_UNSUPPORTED,
+ * PTQ_ERR_CUDA. */
+PTQ_API PTQ_NODISCARD ptq_status ptq_gemv_plan(int64_t M, int64_t N, int64_t K,
+                                               int pq2, int32_t plan[4]);
+
 /* ptq_selftest_timeout -- test export for the timeout path.  Launches one
  * CTA that waits, with the library's bounded mbarrier wait and a short poll
  * limit, on a barrier that nothing arrives on; the wait runs out and the

@@ -32,7 +32,7 @@ EXPORTS = ("ptq1_pack", "ptq1_unpack", "ptq_fwht", "ptq_matmul_workspace_bytes",
            "ptq_ffn", "ptq_ffn_noalloc", "ptq_ffn_stack_workspace_bytes", "ptq_ffn_stack",
            "ptq_ffn_stack_ex", "ptq_ffn_stack_route", "ptq2_pack", "ptq2_unpack",
            "ptq_matmul_pq2_workspace_bytes", "ptq_matmul_pq2", "ptq_embed", "ptq_embed_ptq1",
-           "ptq_route", "ptq_matmul_bf16_accumulator", "ptq_selftest_timeout",
+           "ptq_route", "ptq_gemv_plan", "ptq_matmul_bf16_accumulator", "ptq_selftest_timeout",
            "ptq_selftest_grid_timeout",
            "ptq_device_check", "ptq_status_str", "ptq_last_error")
 
@@ -91,6 +91,7 @@ def load(path: str | None = None):
     L.ptq_embed.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _P]
     L.ptq_embed_ptq1.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _P]
     L.ptq_route.argtypes = [_I64, _I32, ctypes.POINTER(ctypes.c_char_p)]
+    L.ptq_gemv_plan.argtypes = [_I64, _I64, _I64, _I32, ctypes.POINTER(ctypes.c_int32)]
     L.ptq_matmul_bf16_accumulator.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _P,
                                               ctypes.c_size_t, _P]
     L.ptq_device_check.argtypes = [_P]
@@ -103,8 +104,8 @@ def load(path: str | None = None):
     for name in ("ptq1_pack", "ptq1_unpack", "ptq_fwht", "ptq_matmul", "ptq_rotate_matmul", "ptq_ffn",
                  "ptq_ffn_noalloc", "ptq_ffn_stack", "ptq_ffn_stack_ex", "ptq_ffn_stack_route", "ptq2_pack",
                  "ptq2_unpack", "ptq_matmul_pq2", "ptq_embed",
-                 "ptq_embed_ptq1", "ptq_route", "ptq_device_check", "ptq_selftest_timeout",
-                 "ptq_selftest_grid_timeout"):
+                 "ptq_embed_ptq1", "ptq_route", "ptq_gemv_plan", "ptq_device_check",
+                 "ptq_selftest_timeout", "ptq_selftest_grid_timeout"):
         getattr(L, name).restype = _I32
     _lib = L
     return L
@@ -438,6 +439,14 @@ def route(M: int, dtype: int) -> str:
     name = ctypes.c_char_p()
     _check(load().ptq_route(M, dtype, ctypes.byref(name)), "ptq_route")
     return name.value.decode()
+
+
+def gemv_plan(M: int, N: int, K: int, pq2: bool = False) -> dict:
+    """The launch of the fp32 decode GEMV for (M, N, K) on the current device
+    (ptq_gemv_plan): CTAs, cluster size (0: none), K-chunks, kernels."""
+    out = (ctypes.c_int32 * 4)()
+    _check(load().ptq_gemv_plan(M, N, K, int(pq2), out), "ptq_gemv_plan")
+    return {"ctas": out[0], "cluster": out[1], "chunks": out[2], "kernels": out[3]}
 
 
 def selftest_timeout(stream=None) -> None:

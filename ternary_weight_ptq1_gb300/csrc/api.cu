@@ -348,6 +348,23 @@ PTQ_API ptq_status ptq_matmul_bf16_accumulator(const uint8_t* wq, const uint16_t
   return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq_matmul_bf16_accumulator launch");
 }
 
+PTQ_API ptq_status ptq_gemv_plan(int64_t M, int64_t N, int64_t K, int pq2, int32_t plan[4]) {
+  t_msg[0] = 0;
+  if (!plan) return fail(PTQ_ERR_NULL, "ptq_gemv_plan: plan is NULL");
+  LutPlan p{};
+  const cudaError_t e = gemv_lut_plan(M, N, K, pq2 != 0, &p);
+  if (e == cudaErrorNotSupported)
+    return fail(PTQ_ERR_UNSUPPORTED,
+                "ptq_gemv_plan: the TMA-fed decode GEMV does not serve M=%lld N=%lld K=%lld",
+                (long long)M, (long long)N, (long long)K);
+  if (e != cudaSuccess) return cuda_fail(e, "ptq_gemv_plan");
+  plan[0] = p.ctas;
+  plan[1] = p.cluster;
+  plan[2] = p.chunks;
+  plan[3] = p.kernels;
+  return PTQ_OK;
+}
+
 // ---- PQ2_0 ----------------------------------------------------------------
 // "Why I Am Building Another Inference Engine", section "Level 2: The short
 // answer": two bits per ternary weight plus one 16-bit scale per 128

@@ -39,6 +39,8 @@
 // bitwise reproducible.  No kernel here waits on another CTA.
 #include <cuda_fp16.h>
 
+#include <atomic>
+
 #include "async_util.cuh"
 #include "lut_core.cuh"
 #include "ptq_internal.cuh"
@@ -132,9 +134,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_lut_kernel(const LutArgs P) 
   extern __shared__ __align__(16) unsigned char smem[];
   const int L = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t base = (smem_u32(smem) + 15u) & ~15u;
-  // The table addresses are absolute; the layout needs the dynamic window
-  // to start low enough.  (It starts after the 1 KB the driver reserves.)
-  if (base + (uint32_t)kLowBytes > kTab) return;
+  // The tables sit at a fixed offset of the shared window; the layout needs
+  // the dynamic window to start low enough.  (It starts after the 1 KB the
+  // driver reserves.)
+  const uint32_t tab = table_base(smem_u32(smem));
+  if (base + (uint32_t)kLowBytes > tab) return;
   const uint32_t red = base + (uint32_t)(warp * kRedBytes);
   const uint32_t xs = base + (uint32_t)(kWarps * kRedBytes);
 
@@ -179,14 +183,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_lut_kernel(const LutArgs P) 
 
   // ---- activations of the chunk, then its tables ---------------------------------
   pdl_wait();
-  stage_tables(P.x, P.signs, ws, we, live, base, xs);
+  stage_tables(P.x, P.signs, ws, we, live, base, xs, tab);
   __syncthreads();
   pdl_release();  // the reduction kernel may start its prologue
 
   // ---- main loop: 16 rows per batch ----------------------------------------------
   // address of entry e of position j: byte 0 = lane column (+128 for odd j),
   // byte 1 = e, byte 2 = region 1 + j / 2
-  const uint32_t lb0 = kTab + 4u * L, lb1 = lb0 + 128u, lb2 = lb0 + 0x10000u, lb3 = lb2 + 128u;
+  const uint32_t lb0 = tab + 4u * L, lb1 = lb0 + 128u, lb2 = lb0 + 0x10000u, lb3 = lb2 + 128u;
   const Lanes ln{lb0, lb1, lb2, lb3, ssel, red, (uint32_t)P.words, (uint32_t)(P.nblk / 2)};
   const uint32_t* pw0 = reinterpret_cast<const uint32_t*>(P.wq) + (size_t)ra * wrow + wl;
   const uint32_t* qw0 = reinterpret_cast<const uint32_t*>(P.sc) + (size_t)ra * srow + pw;
@@ -233,8 +237,37 @@ struct LutTmaArgs {
 };
 
 
+// ---- one token, a row group's chunks as one thread-block cluster ------------------
+// The nch CTAs that share a row group's nr rows (one K-chunk each) can run as
+// one cluster.  Each keeps its chunk's row sums in its own shared memory
+// while it runs.  The rows are cut into slices of S = ceil(nr / nch), slice o
+// owned by the CTA of rank o; at the end every CTA stores its sums of each
+// slice into the owner's shared memory (entry [chunk][row in slice]), and
+// after one cluster barrier each owner adds the nch sums of its rows in chunk
+// order (the order of the reduction kernel, so the bits are the same) and
+// writes y.  No workspace, no second kernel.  Both the own sums (nr floats)
+// and the entries (nch S floats) take the rotation scratch and the staged
+// activations, free once a CTA's tables are built (a CTA announces that with
+// a barrier arrival and waits for its peers' before its first remote store):
+// 16 KB, kClusterRows floats.
+constexpr int kClusterRows = kBarOff / 4;
+constexpr int kMaxClusterCtas = 16;  // non-portable cluster size limit
+
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t a, uint32_t rank, float v) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(ra), "f"(v) : "memory");
+}
+
 // kOne: a single token, known at compile time (the token loop folds away).
-template <bool kPQ2, bool kOne>
+// kCl (with kOne): the CTAs of a row group are a cluster and write y (P.part).
+template <bool kPQ2, bool kOne, bool kCl = false>
 __global__ void __launch_bounds__(kThreads, 1) gemv_lut_tma_kernel(const __grid_constant__ LutTmaArgs P) {
   constexpr int kBB = kPQ2 ? 32 : kBlockBytes;  // bytes per 128-weight block
   extern __shared__ __align__(16) unsigned char smem[];
@@ -244,15 +277,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_lut_tma_kernel(const __grid_
   const uint32_t exch = base, xs = base + (uint32_t)kExchBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (base - raw) + kBarOff);
   const uint32_t ring_lo = base + (uint32_t)kRingOff;
-  // The tables and the upper slots sit at fixed addresses: the window must
-  // start low enough for the lower slots to end below the tables (it starts
-  // after the 1 KB the driver reserves); otherwise nothing runs.
-  if (ring_lo + (uint32_t)(kLowSlots * kSlotBytes) > kTab ||
-      kTabEnd + (uint32_t)((kSlots - kLowSlots) * kSlotBytes) > raw + (uint32_t)kSmemTma)
+  // The tables and the upper slots sit at fixed offsets of the shared window
+  // (the same in every CTA of a cluster): the dynamic memory must start low
+  // enough for the lower slots to end below the tables (it starts after the
+  // 1 KB the driver reserves); otherwise nothing runs, in any CTA.
+  const uint32_t tab = table_base(raw), tab_end = tab + (kTabEnd - kTab);
+  if (ring_lo + (uint32_t)(kLowSlots * kSlotBytes) > tab ||
+      tab_end + (uint32_t)((kSlots - kLowSlots) * kSlotBytes) > raw + (uint32_t)kSmemTma)
     return;
 
   // ---- this CTA's chunk and rows ------------------------------------------------
-  const int c = blockIdx.x / P.cpc, k = blockIdx.x % P.cpc;
+  // a cluster is nch consecutive CTAs: rank = chunk
+  const int c = kCl ? (int)blockIdx.x % P.nch : (int)blockIdx.x / P.cpc;
+  const int k = kCl ? (int)blockIdx.x / P.nch : (int)blockIdx.x % P.cpc;
   const int R0 = (int)((long long)k * P.N / P.cpc);
   const int R1 = (int)((long long)(k + 1) * P.N / P.cpc);
   const int Q = P.words / 4;                   // 4-word quads per row
@@ -285,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_lut_tma_kernel(const __grid_
   auto slot_of = [&](int s) -> uint32_t {
     const int g = kSlotsPerWarp * warp + s;
     return g < kLowSlots ? ring_lo + (uint32_t)(g * kSlotBytes)
-                         : kTabEnd + (uint32_t)((g - kLowSlots) * kSlotBytes);
+                         : tab_end + (uint32_t)((g - kLowSlots) * kSlotBytes);
   };
   auto request = [&](int g) {  // lane 0: batch g into slot g % 2
     const int s = g & 1, r = ra + kBoxRows * (kOne ? g : g % nbat);
@@ -309,12 +346,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_lut_tma_kernel(const __grid_
     // (10.93 against 10.67 us at N = 17408, K = 5120).
     // ---- activations of the chunk, then its tables ---------------------------------
     pdl_wait();
-    stage_tables<kPQ2>(P.x, P.signs, ws, we, live, exch, xs);
+    stage_tables<kPQ2>(P.x, P.signs, ws, we, live, exch, xs, tab);
     __syncthreads();
     pdl_release();  // the reduction kernel may start its prologue
+    // clustered: this CTA's staging space may now take its peers' row sums
+    if constexpr (kCl) cluster_arrive();
 
     // ---- main loop: one box of 16 rows per batch -------------------------------------
-    const uint32_t lb0 = kTab + 4u * L, lb1 = lb0 + 128u, lb2 = lb0 + 0x10000u, lb3 = lb2 + 128u;
+    const uint32_t lb0 = tab + 4u * L, lb1 = lb0 + 128u, lb2 = lb0 + 0x10000u, lb3 = lb2 + 128u;
     const Lanes ln{lb0, lb1, lb2, lb3, ssel, 0u, 0u, 0u};
     float* out = P.part + (size_t)c * P.N;
     int b = 0;
@@ -352,7 +391,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_lut_tma_kernel(const __grid_
       float v = fold(k3a, k3b, L & 2, 2);
       v += __shfl_xor_sync(0xffffffffu, v, 1);
       const int row = ra + kBoxRows * b + (L >> 1);
-      if (!(L & 1) && row < rb) out[row] = v;
+      if (!(L & 1) && row < rb) {
+        if constexpr (kCl)
+          sts_f32(base + 4u * (uint32_t)(row - R0), v);
+        else
+          out[row] = v;
+      }
     }
     if (!ok) {
       if (L == 0) atomicOr(P.status, kDevTimeout);
@@ -360,10 +404,33 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_lut_tma_kernel(const __grid_
       for (int bb = b; bb < nbat && bb < b + 2; ++bb)
         static_cast<void>(mbar_wait(&full[bb & 1], (uint32_t)((bb >> 1) & 1), nullptr));
     }
+    if constexpr (kCl) {
+      // Every thread of the cluster takes both barrier phases.  After the
+      // first every peer's staging space is free; after the second every
+      // entry of this CTA's slice is in its shared memory, and no CTA touches
+      // another's afterwards.
+      const int S = (nr + P.nch - 1) / P.nch;
+      const uint32_t ent = base + 4u * (uint32_t)nr;  // entries [chunk][row in slice]
+      __syncthreads();                                // this CTA's row sums are written
+      cluster_wait();
+      for (int i = (int)threadIdx.x; i < nr; i += kThreads) {
+        const int o = i / S;
+        st_cluster_f32(ent + 4u * (uint32_t)(c * S + i - o * S), (uint32_t)o,
+                       lds_f32(base + 4u * (uint32_t)i));
+      }
+      cluster_arrive();
+      cluster_wait();
+      const int q0 = c * S, q1 = q0 + S < nr ? q0 + S : nr;
+      for (int j = (int)threadIdx.x; j < q1 - q0; j += kThreads) {
+        float acc = 0.0f;
+        for (int cc = 0; cc < P.nch; ++cc) acc += lds_f32(ent + 4u * (uint32_t)(cc * S + j));
+        P.part[R0 + q0 + j] = acc;
+      }
+    }
   } else {
     // ---- per token: its activations and tables, then its rows -----------------------
     pdl_wait();
-    const uint32_t lb0 = kTab + 4u * L, lb1 = lb0 + 128u, lb2 = lb0 + 0x10000u, lb3 = lb2 + 128u;
+    const uint32_t lb0 = tab + 4u * L, lb1 = lb0 + 128u, lb2 = lb0 + 0x10000u, lb3 = lb2 + 128u;
     const Lanes ln{lb0, lb1, lb2, lb3, ssel, 0u, 0u, 0u};
     const size_t K = (size_t)P.nblk * kBlockWeights;
     int g = 0;  // the warp's next batch: the one its ring waits on
@@ -375,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_lut_tma_kernel(const __grid_
         ok = false;
         break;
       }
-      stage_tables<kPQ2>(P.x + (size_t)m * K, P.signs, ws, we, live, exch, xs);
+      stage_tables<kPQ2>(P.x + (size_t)m * K, P.signs, ws, we, live, exch, xs, tab);
       __syncthreads();
       if (m == 0) pdl_release();  // the reduction kernel may start its prologue
 
@@ -460,6 +527,9 @@ __global__ void __launch_bounds__(256) gemv_lut_reduce_swiglu_kernel(
 }
 
 int g_sms[64];
+// Clusters of n CTAs of the one-token kernel (PTQ1_0, PQ2_0) that the device
+// holds at once, by device and n: 0 not asked yet, -1 none.
+std::atomic<int> g_clusters[64][2][kMaxClusterCtas + 1];
 
 }  // namespace
 
@@ -489,8 +559,13 @@ static cudaError_t device_sms(int* out) {
                              (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     for (auto kern : {gemv_lut_tma_kernel<false, true>, gemv_lut_tma_kernel<false, false>,
-                      gemv_lut_tma_kernel<true, true>, gemv_lut_tma_kernel<true, false>}) {
+                      gemv_lut_tma_kernel<true, true>, gemv_lut_tma_kernel<true, false>,
+                      gemv_lut_tma_kernel<false, true, true>, gemv_lut_tma_kernel<true, true, true>}) {
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemTma);
+      if (e != cudaSuccess) return e;
+    }
+    for (auto kern : {gemv_lut_tma_kernel<false, true, true>, gemv_lut_tma_kernel<true, true, true>}) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
       if (e != cudaSuccess) return e;
     }
     g_sms[dev] = sms;
@@ -519,13 +594,81 @@ int64_t gemv_lut_ctas_per_chunk(int64_t sms, int64_t nch, int64_t N) {
   return ctas_per_chunk(sms, nch, N);
 }
 
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), unsigned ctas, unsigned cl,
+                                      size_t smem, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cl;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// How many clusters of nch one-token CTAs the device runs at once (0: none;
+// asked once per device, format and nch).
+template <bool kPQ2>
+static int resident_clusters(int64_t nch) {
+  if (nch < 2 || nch > kMaxClusterCtas) return 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::atomic<int>& slot = g_clusters[dev][kPQ2 ? 1 : 0][nch];
+  int n = slot.load(std::memory_order_relaxed);
+  if (n == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)nch);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemTma;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)nch;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int got = 0;
+    if (cudaOccupancyMaxActiveClusters(&got, gemv_lut_tma_kernel<kPQ2, true, true>, &cfg) !=
+        cudaSuccess) {
+      static_cast<void>(cudaGetLastError());  // the query's own error, not sticky
+      got = 0;
+    }
+    n = got > 0 ? got : -1;
+    slot.store(n, std::memory_order_relaxed);
+  }
+  return n > 0 ? n : 0;
+}
+
+// Row groups for the clustered one-token kernel: as many as ctas_per_chunk
+// gives when that many clusters fit at once (fewer, down to 7/8 of them, when
+// not); 0 when the clustered kernel does not serve the shape.
+template <bool kPQ2>
+static int64_t cluster_row_groups(int64_t nch, int64_t cpc, int64_t N) {
+  const int64_t fit = resident_clusters<kPQ2>(nch);
+  const int64_t g = fit < cpc ? fit : cpc;
+  if (g < 1 || 8 * g < 7 * cpc) return 0;
+  const int64_t rows = (N + g - 1) / g;  // the most rows a group has
+  return rows + nch * ((rows + nch - 1) / nch) <= kClusterRows ? g : 0;
+}
+
 // The TMA-fed kernel for `words` 32-bit words of codes per row (both planes
 // need 16-byte aligned rows: K % 1024 == 0).  cudaErrorNotSupported when a
 // tensor map cannot be made.
+// clustered (one token, nch > 1): cpc row groups of nch CTAs, each group a
+// cluster that writes y itself; `part` is then not used.
 template <bool kPQ2>
 static cudaError_t launch_lut_tma(const void* wq, const uint16_t* scales, const float* x,
                                   const int8_t* signs, float* y, float* part, int64_t M, int64_t N,
-                                  int nblk, int words, int64_t nch, int64_t cpc, cudaStream_t st) {
+                                  int nblk, int words, int64_t nch, int64_t cpc, bool clustered,
+                                  cudaStream_t st) {
   int* status = device_status_ptr();
   if (status == nullptr) return cudaErrorNotSupported;
   LutTmaArgs T;
@@ -538,7 +681,7 @@ static cudaError_t launch_lut_tma(const void* wq, const uint16_t* scales, const 
     return cudaErrorNotSupported;
   T.x = x;
   T.signs = signs;
-  T.part = nch == 1 ? y : part;
+  T.part = (nch == 1 || clustered) ? y : part;
   T.status = status;
   T.N = (int)N;
   T.nblk = nblk;
@@ -546,6 +689,9 @@ static cudaError_t launch_lut_tma(const void* wq, const uint16_t* scales, const 
   T.nch = (int)nch;
   T.cpc = (int)cpc;
   T.M = (int)M;
+  if (clustered)
+    return launch_pdl_cluster(gemv_lut_tma_kernel<kPQ2, true, true>, (unsigned)(nch * cpc),
+                              (unsigned)nch, kSmemTma, st, T);
   if (M == 1)
     return launch_pdl(gemv_lut_tma_kernel<kPQ2, true>, dim3((unsigned)(nch * cpc)),
                       dim3(kThreads), kSmemTma, st, T);
@@ -591,9 +737,14 @@ cudaError_t launch_gemv_lut(const uint8_t* wq, const uint16_t* scales, const flo
   // TMA-fed kernel (its 4-word aligned chunks number the same nch) takes all
   // M tokens in one launch, and one reduction sums all M x N rows.
   if (K % kRot == 0) {
-    e = launch_lut_tma<false>(wq, scales, x, signs, y, part, M, N, nblk, words, nch, cpc, st);
+    // one token: the row groups as clusters when the device holds them
+    const int64_t g = (M == 1 && ep == LutEpilogue::Plain) ? cluster_row_groups<false>(nch, cpc, N)
+                                                             : 0;
+    e = launch_lut_tma<false>(wq, scales, x, signs, y, part, M, N, nblk, words, nch,
+                              g > 0 ? g : cpc, g > 0, st);
     if (e != cudaErrorNotSupported)
-      return (e != cudaSuccess || nch == 1) ? e : launch_chunk_sums(part, y, M, N, nch, ep, st);
+      return (e != cudaSuccess || nch == 1 || g > 0) ? e
+                                                     : launch_chunk_sums(part, y, M, N, nch, ep, st);
   }
   // the register-ring kernel: one token per launch, the scratch reused
   for (int64_t m = 0; m < M; ++m) {
@@ -613,6 +764,26 @@ cudaError_t launch_gemv_lut(const uint8_t* wq, const uint16_t* scales, const flo
     if (e == cudaSuccess && nch > 1) e = launch_chunk_sums(part, y + m * N, 1, N, nch, ep, st);
     if (e != cudaSuccess) return e;
   }
+  return cudaSuccess;
+}
+
+cudaError_t gemv_lut_plan(int64_t M, int64_t N, int64_t K, bool pq2, LutPlan* plan) {
+  const int64_t nch = pq2 ? gemv_lut_pq2_chunks(K) : gemv_lut_chunks(K);
+  if (nch == 0 || K % kRot != 0 || N < 1 || N > INT32_MAX / 2 || K > (1 << 24) || M < 1 ||
+      M > INT32_MAX / N)
+    return cudaErrorNotSupported;
+  int sms = 0;
+  cudaError_t e = device_sms(&sms);
+  if (e != cudaSuccess) return e;
+  if (nch > sms) return cudaErrorNotSupported;
+  const int64_t cpc = ctas_per_chunk(sms, nch, N);
+  const int64_t g =
+      M == 1 ? (pq2 ? cluster_row_groups<true>(nch, cpc, N) : cluster_row_groups<false>(nch, cpc, N))
+             : 0;
+  plan->ctas = (int)(nch * (g > 0 ? g : cpc));
+  plan->cluster = g > 0 ? (int)nch : 0;
+  plan->chunks = (int)nch;
+  plan->kernels = (g > 0 || nch == 1) ? 1 : 2;
   return cudaSuccess;
 }
 
@@ -642,9 +813,11 @@ cudaError_t launch_gemv_lut_pq2(const uint8_t* wq, const uint16_t* scales, const
   if (nch > sms) return cudaErrorNotSupported;
   if (nch > 1 && part == nullptr) return cudaErrorInvalidValue;
   const int nblk = (int)(K / kBlockWeights);
+  const int64_t cpc = ctas_per_chunk(sms, nch, N);
+  const int64_t g = M == 1 ? cluster_row_groups<true>(nch, cpc, N) : 0;
   e = launch_lut_tma<true>(wq, scales, x, signs, y, part, M, N, nblk, 8 * nblk, nch,
-                           ctas_per_chunk(sms, nch, N), st);
-  if (e != cudaSuccess || nch == 1) return e;
+                           g > 0 ? g : cpc, g > 0, st);
+  if (e != cudaSuccess || nch == 1 || g > 0) return e;
   return launch_chunk_sums(part, y, M, N, nch, LutEpilogue::Plain, st);
 }
 

@@ -153,10 +153,11 @@ __global__ void __launch_bounds__(kThreads, 1) stack_decode_kernel(const __grid_
   const uint32_t exch = base, xs = base + (uint32_t)kExchBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (base - raw) + kBarOff);
   const uint32_t ring_lo = base + (uint32_t)kRingOff;
-  // the same fixed-address layout as the stand-alone GEMV (the same for every
-  // CTA, so either all run or none does)
-  if (ring_lo + (uint32_t)(kLowSlots * kSlotBytes) > kTab ||
-      kTabEnd + (uint32_t)((kSlots - kLowSlots) * kSlotBytes) > raw + (uint32_t)kSmemTma) {
+  // the same layout as the stand-alone GEMV, at fixed offsets of the shared
+  // window (the same for every CTA, so either all run or none does)
+  const uint32_t tab = table_base(raw), tab_end = tab + (kTabEnd - kTab);
+  if (ring_lo + (uint32_t)(kLowSlots * kSlotBytes) > tab ||
+      tab_end + (uint32_t)((kSlots - kLowSlots) * kSlotBytes) > raw + (uint32_t)kSmemTma) {
     if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(P.status, kDevTimeout);
     return;
   }
@@ -166,10 +167,10 @@ __global__ void __launch_bounds__(kThreads, 1) stack_decode_kernel(const __grid_
   // to slot g % 2 and completes phase (g / 2) % 2 of that slot's barrier -----
   uint64_t* full = bars + kSlotsPerWarp * warp;
   const uint32_t slot0 = 2 * warp < kLowSlots ? ring_lo + (uint32_t)(2 * warp * kSlotBytes)
-                                               : kTabEnd + (uint32_t)((2 * warp - kLowSlots) * kSlotBytes);
+                                               : tab_end + (uint32_t)((2 * warp - kLowSlots) * kSlotBytes);
   const uint32_t slot1 = 2 * warp + 1 < kLowSlots
                              ? ring_lo + (uint32_t)((2 * warp + 1) * kSlotBytes)
-                             : kTabEnd + (uint32_t)((2 * warp + 1 - kLowSlots) * kSlotBytes);
+                             : tab_end + (uint32_t)((2 * warp + 1 - kLowSlots) * kSlotBytes);
   int issued = 0, done = 0;  // batches requested / consumed by this warp
   auto request = [&](const Work& w, const CUtensorMap* tw, const CUtensorMap* ts, int b) {
     const int s = issued & 1;
@@ -222,10 +223,10 @@ __global__ void __launch_bounds__(kThreads, 1) stack_decode_kernel(const __grid_
                    exch + (uint32_t)(half * kRot * 4), xs + (uint32_t)(half * kRot * 4), g8, bar);
     }
     __syncthreads();
-    build_tables<false>(w.ws, live, xs, f0 * kRot);
+    build_tables<false>(w.ws, live, xs, f0 * kRot, tab);
     __syncthreads();
 
-    const uint32_t lb0 = kTab + 4u * L, lb1 = lb0 + 128u, lb2 = lb0 + 0x10000u, lb3 = lb2 + 128u;
+    const uint32_t lb0 = tab + 4u * L, lb1 = lb0 + 128u, lb2 = lb0 + 0x10000u, lb3 = lb2 + 128u;
     const Lanes ln{lb0, lb1, lb2, lb3, ssel, 0u, 0u, 0u};
     bool ok = true;
     for (int b = 0; b < w.nbat; ++b, ++done) {

@@ -23,12 +23,18 @@ constexpr int kThreads = 32 * kWarps;
 constexpr int kChunkWords = 32;            // one word per lane
 constexpr int kXFloats = 2 * kRot;         // a chunk touches at most 6 blocks = 768
                                            // weights, inside at most two 1024-blocks
-constexpr uint32_t kTab = 0x10000u;        // shared address of the tables
+constexpr uint32_t kTab = 0x10000u;        // the tables' offset in the shared window
 constexpr uint32_t kTabEnd = 0x30000u;     // 4 positions x 32 lanes x 256 x 4 B
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+// The tables' shared address for a CTA whose dynamic shared memory starts at
+// `raw`: kTab into its shared window.  The window starts at 0, or, for the
+// CTA of rank r in a cluster, at r x 16 MB; either way the low 16 bits of the
+// table addresses are free for the byte a lookup puts in bits 8-15.
+__device__ __forceinline__ uint32_t table_base(uint32_t raw) { return (raw & 0xFFFF0000u) + kTab; }
+
 __device__ __forceinline__ float lds_f32(uint32_t a) {
   float v;
   asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
@@ -139,7 +145,8 @@ __device__ __forceinline__ void rotate_block(Load load, const int8_t* __restrict
 // chunk (`live` false) get all-zero tables.  All threads of the CTA take part.
 // kPQ2: the weights are PQ2_0 (32 bytes per block, four 2-bit codes a byte).
 template <bool kPQ2 = false>
-__device__ __forceinline__ void build_tables(int ws, bool live, uint32_t xs, int xbase) {
+__device__ __forceinline__ void build_tables(int ws, bool live, uint32_t xs, int xbase,
+                                             uint32_t tab) {
   constexpr int kBB = kPQ2 ? 32 : kBlockBytes;  // bytes per block
   const int L = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if constexpr (kPQ2) {
@@ -158,7 +165,7 @@ __device__ __forceinline__ void build_tables(int ws, bool live, uint32_t xs, int
       Lo[n] = fmaf(c1, xv[1], c0 * xv[0]);
       Hi[n] = fmaf(c1, xv[3], c0 * xv[2]);
     }
-    const uint32_t dst = kTab + 0x10000u * (uint32_t)(j >> 1) + 128u * (uint32_t)(j & 1) + 4u * L;
+    const uint32_t dst = tab + 0x10000u * (uint32_t)(j >> 1) + 128u * (uint32_t)(j & 1) + 4u * L;
     switch (warp >> 2) {
       case 0: build_entries_pq2<0>(Lo, Hi, dst); break;
       case 1: build_entries_pq2<1>(Lo, Hi, dst); break;
@@ -191,7 +198,7 @@ __device__ __forceinline__ void build_tables(int ws, bool live, uint32_t xs, int
       t = d3 > 0 ? t + xv[3] : (d3 < 0 ? t - xv[3] : t);
       B[bb] = d4 > 0 ? t + xv[4] : (d4 < 0 ? t - xv[4] : t);
     }
-    const uint32_t dst = kTab + 0x10000u * (uint32_t)(j >> 1) + 128u * (uint32_t)(j & 1) + 4u * L;
+    const uint32_t dst = tab + 0x10000u * (uint32_t)(j >> 1) + 128u * (uint32_t)(j & 1) + 4u * L;
     switch (warp >> 2) {
       case 0: build_entries<0>(A, B, dst); break;
       case 1: build_entries<1>(A, B, dst); break;
@@ -217,7 +224,8 @@ __device__ __forceinline__ void chunk_rot_blocks(int ws, int we, int* f0, int* f
 template <bool kPQ2 = false>
 __device__ __forceinline__ void stage_tables(const float* __restrict__ x,
                                              const int8_t* __restrict__ signs, int ws, int we,
-                                             bool live, uint32_t exch, uint32_t xs) {
+                                             bool live, uint32_t exch, uint32_t xs,
+                                             uint32_t tab) {
   constexpr int kBB = kPQ2 ? 32 : kBlockBytes;  // bytes per block
   const int warp = threadIdx.x >> 5;
   int xbase;  // weight index of xs[0]
@@ -245,7 +253,7 @@ __device__ __forceinline__ void stage_tables(const float* __restrict__ x,
     }
   }
   __syncthreads();
-  build_tables<kPQ2>(ws, live, xs, xbase);
+  build_tables<kPQ2>(ws, live, xs, xbase, tab);
 }
 
 constexpr int kBoxRows = 16;                          // rows per box = per batch

@@ -104,6 +104,15 @@ cudaError_t launch_gemv_lut_pq2(const uint8_t* wq, const uint16_t* scales, const
                                 int64_t K, cudaStream_t st);
 int64_t gemv_lut_pq2_chunks(int64_t K);
 size_t gemv_lut_pq2_workspace_bytes(int64_t N, int64_t K, int64_t M);
+// The launch launch_gemv_lut (pq2: launch_gemv_lut_pq2) makes for M tokens,
+// plain epilogue, on the current device: CTAs, cluster size (0: none), K
+// chunks and kernels (the GEMV and, unless its clusters write y or a row has
+// one chunk, the chunk reduction).  cudaErrorNotSupported when the TMA-fed
+// kernel does not serve the shape.
+struct LutPlan {
+  int ctas, cluster, chunks, kernels;
+};
+cudaError_t gemv_lut_plan(int64_t M, int64_t N, int64_t K, bool pq2, LutPlan* plan);
 // Whether launch_gemv_lut serves (N, K) on the current device (with the
 // rotation when `rotate`).
 bool gemv_lut_supported(int64_t N, int64_t K, bool rotate);

@@ -111,8 +111,11 @@ def test_gemv_deterministic_and_in_bounds(P, syn):
 
 
 # ---- the M = 1 table-lookup decode ----------------------------------------------
-# A row has 13 K/256 words of trits, cut into chunks of at most 32 words; each
-# chunk's row sums are added by a second kernel.
+# A row has 13 K/256 words of trits, cut into chunks of at most 32 words.  At
+# one token the chunks of a row group run as one thread-block cluster that
+# adds its row sums in distributed shared memory, when the device holds
+# enough such clusters (K % 1024 == 0); otherwise, and for several tokens, a
+# second kernel adds the chunk sums.
 
 @pytest.mark.parametrize("N,K", [(1, 256), (7, 512), (300, 768), (64, 1024), (513, 2560),
                                  (40, 12800), (3, 17408), (2000, 4096)])
@@ -124,6 +127,48 @@ def test_lut_chunking(P, orc, syn, N, K):
     y, _ = run(P, mv.trits, mv.scales, mv.x)
     Q.check_f32(Q.host_f64(y), orc.matmul(orc.pack(mv.trits), mv.scales, Q.x_f64(mv.x)),
                 f"lut N={N} K={K}")
+
+
+LUT_PLAN_SHAPES = [(17408, 5120), (5120, 17408), (3000, 5120), (1024, 1024), (257, 2048),
+                   (1, 3072), (40000, 4096), (6000, 12288)]
+
+
+@pytest.mark.parametrize("N,K", LUT_PLAN_SHAPES)
+def test_lut_one_token_matches_token_loop(P, orc, syn, N, K):
+    """The one-token launch (clustered or not) and the token loop with its
+    reduction kernel add the same chunk sums in the same order: token 0 of a
+    two-token call has the bits of the one-token call."""
+    import torch
+
+    plan = P.gemv_plan(1, N, K)
+    nch = (13 * K // 256 + 31) // 32
+    assert plan["chunks"] == nch
+    if plan["cluster"]:
+        assert plan["cluster"] == nch and plan["ctas"] % nch == 0 and plan["kernels"] == 1
+    else:
+        assert plan["kernels"] == 2
+    assert P.gemv_plan(2, N, K)["cluster"] == 0
+    mv = syn.gaussian_matvec(300 + K // 1024, 2, N, K)
+    wq, s, x = Q.dev(P.pack(mv.trits)), Q.dev(mv.scales), Q.dev(mv.x)
+    y1 = P.matmul(wq, s, x[:1])
+    y2 = P.matmul(wq, s, x)
+    assert torch.equal(y1[0], y2[0]), plan
+    rows = np.unique(np.linspace(0, N - 1, 64).astype(np.int64))
+    Q.check_f32(Q.host_f64(y1)[:, rows],
+                orc.matmul(orc.pack(mv.trits[rows]), mv.scales[rows], Q.x_f64(mv.x[:1])),
+                f"one token N={N} K={K}")
+
+
+def test_lut_cluster_route_is_taken(P):
+    """On a device that holds them (a GB300 does), the decode shapes of the
+    feed-forward block's gate/up weight run as clusters, so the parity tests
+    above cover the distributed-shared-memory reduction; a row group too large
+    for the 16 KB of row sums falls back to the reduction kernel."""
+    plan = P.gemv_plan(1, 17408, 5120)
+    assert plan["cluster"] == 9 and plan["kernels"] == 1, plan
+    assert P.gemv_plan(1, 5120, 17408)["cluster"] == 0  # 28 chunks: more than 16 CTAs
+    big = P.gemv_plan(1, 200000, 5120)                    # > 4096 rows a group
+    assert big["cluster"] == 0 and big["kernels"] == 2
 
 
 @pytest.mark.parametrize("K", [128, 384, 640])
