@@ -49,21 +49,34 @@ namespace ptq {
 namespace {
 
 constexpr int BM = 256, BN = 128, BK = 64, UM = 128;   // UM: rows per MMA
-constexpr int kStages = 2;
-constexpr int kASlice = BM * BK * 2;                        // 32 KB
 constexpr int kBSlice = BN * BK * 2;                        // 16 KB
-constexpr int kThreads = 10 * 32;
-constexpr int kExpWarp0 = 2, kExpThreads = 256;
+constexpr int kExpWarp0 = 2;  // warps 0, 1: A producer, MMA issuer; then the expansion
 
-// shared memory layout (offsets from a 1024-aligned base)
-constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kStages * kASlice;
-constexpr int kOffBar = kOffB + kStages * kBSlice;
-// barriers: a_full[S], b_full[S], empty[S], acc
-constexpr int kNumBars = 3 * kStages + 1;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;            // tmem base, abort flag
-constexpr int kSmemBytes = kOffMisc + 16;
-static_assert(2 * (kSmemBytes + 1024) <= 228 * 1024, "two CTAs per SM");
+// Shared memory layout (offsets from a 1024-aligned base) and warps of the
+// two variants.  Large M: 256-row A slices, a 2-deep ring, 98 KB, 8
+// expansion warps (two CTAs per SM).  Small M (M <= 128, one accumulator,
+// for shapes that run unsplit in one wave): 128-row A slices, a 6-deep ring,
+// 193 KB, 16 expansion warps (one CTA per SM).  A slice then holds only
+// 128 x 128 x 64 of MMA work, so the expansion must run further ahead of the
+// MMAs and have more warps to hide its latencies: each of four groups of 128
+// threads takes one half of every other block.
+template <bool kSmall>
+struct Lay {
+  static constexpr int kExpThreads = kSmall ? 512 : 256;
+  static constexpr int kThreads = 32 * kExpWarp0 + kExpThreads;
+  static constexpr int kStages = kSmall ? 6 : 2;
+  static constexpr int kASlice = (kSmall ? UM : BM) * BK * 2;  // 16 or 32 KB
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kOffA + kStages * kASlice;
+  static constexpr int kOffBar = kOffB + kStages * kBSlice;
+  // barriers: a_full[S], b_full[S], empty[S], acc
+  static constexpr int kNumBars = 3 * kStages + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
+  static constexpr int kSmemBytes = kOffMisc + 16;
+  static constexpr int kCtasPerSm = kSmall ? 1 : 2;
+};
+static_assert(2 * (Lay<false>::kSmemBytes + 1024) <= 228 * 1024, "two CTAs per SM");
+static_assert(Lay<true>::kSmemBytes + 1024 <= 227 * 1024, "one CTA per SM");
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return smem_addr(p); }
 
@@ -271,45 +284,67 @@ __device__ __forceinline__ void expand_half_pq2(const uint32_t (&win)[4], uint32
 struct ExpCtx {
   const uint8_t* row;     // this thread's packed row
   const uint16_t* srow;   // its scales
-  int g_lo, nblk;         // first group, and the end of this split's blocks
-  uint32_t bbase;         // shared address of B slice h
-  uint64_t* empty;        // empty[h]
-  uint64_t* b_full;       // b_full[h]
+  int g_lo, ng;           // the split's first 1024-wide group and its group count
+  uint32_t bbase;         // shared address of B slice 0 (slice s at + s kBSlice)
+  uint64_t* empty;        // empty[0 .. S)
+  uint64_t* b_full;       // b_full[0 .. S)
   int r;
   volatile int* abort_flag;
 };
 
-// One block kb = 8 g + q of the expansion: prefetch block kb + 2 into ring
-// slot (q + 2) % 4, wait for B slice h to be free, expand, publish.
-template <bool kBf16, int h, int q>
-__device__ __forceinline__ bool expand_step(const ExpCtx& c, int g, uint32_t (&win)[4][12],
+// The split's j-th 1024-wide group (j < ng).
+__device__ __forceinline__ int group_at(const ExpCtx& c, int j) { return c.g_lo + j; }
+
+// Slice 2 lb + h (block lb of the split, half h) takes ring stage
+// (2 lb + h) % S for the ((2 lb + h) / S)-th time: wait until the MMAs of its
+// previous use have read it (bounded), and return the stage.
+template <int kS, int h>
+__device__ __forceinline__ int claim_stage(const ExpCtx& c, int lb, bool* ok) {
+  const int i = 2 * lb + h, st = i % kS, n = i / kS;
+  *ok = n == 0 || mbar_wait(c.empty + st, (uint32_t)((n - 1) & 1), c.abort_flag);
+  return st;
+}
+
+// Block q of the split's j-th group (block lb = 8 j + q in the split's order):
+// prefetch block lb + 3 into ring slot (q + 3) % 4 (the slot block lb - 1
+// has left), wait for its B slice to be free, expand, publish.
+template <bool kBf16, int kS, int h, int q>
+__device__ __forceinline__ bool expand_step(const ExpCtx& c, int j, uint32_t (&win)[4][12],
                                             uint32_t (&sc)[4]) {
-  const int kb = 8 * g + q;           // block index within the row
-  const int lb = kb - 8 * c.g_lo;      // block index within this split
-  if (kb + 2 < c.nblk)
-    load_block<(q + 2) % 8>(c.row, c.srow, kb + 2, win[(q + 2) % 4], sc[(q + 2) % 4]);
+  const int lb = 8 * j + q;  // block index in the split's order
+  if (lb + 3 < 8 * c.ng) {
+    const int gn = q + 3 < 8 ? group_at(c, j) : group_at(c, j + 1);
+    load_block<(q + 3) % 8>(c.row, c.srow, 8 * gn + (q + 3) % 8, win[(q + 3) % 4],
+                            sc[(q + 3) % 4]);
+  }
   uint32_t s16 = sc[q % 4];
   if constexpr (kBf16)  // the fp16 scale rounded to nearest-even bf16
     s16 = __bfloat16_as_ushort(
         __float2bfloat16_rn(__half2float(__ushort_as_half((unsigned short)s16))));
   // PRMT sources: bytes 0-1 = -s, 2-3 = 0, 4-5 = +s
   const uint32_t ta = (s16 ^ 0x8000u), tb = s16;
-  if (lb > 0 && !mbar_wait(c.empty, (lb - 1) & 1, c.abort_flag)) return false;
-  expand_half<h, (kBlockBytes * q) & 15>(win[q % 4], ta, tb, c.bbase, c.r);
+  bool ok;
+  const int st = claim_stage<kS, h>(c, lb, &ok);
+  if (!ok) return false;
+  expand_half<h, (kBlockBytes * q) & 15>(win[q % 4], ta, tb, c.bbase + (uint32_t)(st * kBSlice),
+                                         c.r);
   // every writer makes its stores visible to the tensor core's (async) proxy
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  mbar_arrive(c.b_full);
+  mbar_arrive(c.b_full + st);
   return true;
 }
 
-// PQ2_0: block kb of this thread's half, with half-blocks kb + 1, kb + 2
-// prefetched into ring slots (q + 1) % 4, (q + 2) % 4.
-template <bool kBf16, int h, int q>
-__device__ __forceinline__ bool expand_step_pq2(const ExpCtx& c, int g, uint32_t (&win)[4][4],
+// PQ2_0: block lb = 8 j + q of this thread's half (in the split's order),
+// with the half-blocks of blocks lb + 1, lb + 2 prefetched into ring slots
+// (q + 1) % 4, (q + 2) % 4.
+template <bool kBf16, int kS, int h, int q>
+__device__ __forceinline__ bool expand_step_pq2(const ExpCtx& c, int j, uint32_t (&win)[4][4],
                                                 uint32_t (&sc)[4]) {
-  const int kb = 8 * g + q;
-  const int lb = kb - 8 * c.g_lo;
-  if (kb + 2 < c.nblk) load_half_pq2(c.row, c.srow, kb + 2, h, win[(q + 2) % 4], sc[(q + 2) % 4]);
+  const int lb = 8 * j + q;
+  if (lb + 2 < 8 * c.ng) {
+    const int gn = q + 2 < 8 ? group_at(c, j) : group_at(c, j + 1);
+    load_half_pq2(c.row, c.srow, 8 * gn + (q + 2) % 8, h, win[(q + 2) % 4], sc[(q + 2) % 4]);
+  }
   uint32_t s16 = sc[q % 4];
   float sf = __half2float(__ushort_as_half((unsigned short)s16));
   if constexpr (kBf16) {  // the fp16 scale rounded to nearest-even bf16
@@ -319,45 +354,92 @@ __device__ __forceinline__ bool expand_step_pq2(const ExpCtx& c, int g, uint32_t
   const uint32_t s2 = kBf16 ? (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(2.0f * sf))
                             : (uint32_t)__half_as_ushort(__float2half_rn(2.0f * sf));
   const uint32_t ta = (s16 ^ 0x8000u), tb = s16 | (s2 << 16);
-  if (lb > 0 && !mbar_wait(c.empty, (lb - 1) & 1, c.abort_flag)) return false;
-  expand_half_pq2(win[q % 4], ta, tb, c.bbase, c.r);
+  bool ok;
+  const int st = claim_stage<kS, h>(c, lb, &ok);
+  if (!ok) return false;
+  expand_half_pq2(win[q % 4], ta, tb, c.bbase + (uint32_t)(st * kBSlice), c.r);
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  mbar_arrive(c.b_full);
+  mbar_arrive(c.b_full + st);
   return true;
 }
 
-template <bool kBf16, int h>
+template <bool kBf16, int kS, int h>
 __device__ bool expand_all_pq2(const ExpCtx& c) {
   uint32_t win[4][4], sc[4];
-  load_half_pq2(c.row, c.srow, 8 * c.g_lo, h, win[0], sc[0]);
-  load_half_pq2(c.row, c.srow, 8 * c.g_lo + 1, h, win[1], sc[1]);
-  for (int g = c.g_lo; 8 * g < c.nblk; ++g) {
-    if (!expand_step_pq2<kBf16, h, 0>(c, g, win, sc)) return false;
-    if (!expand_step_pq2<kBf16, h, 1>(c, g, win, sc)) return false;
-    if (!expand_step_pq2<kBf16, h, 2>(c, g, win, sc)) return false;
-    if (!expand_step_pq2<kBf16, h, 3>(c, g, win, sc)) return false;
-    if (!expand_step_pq2<kBf16, h, 4>(c, g, win, sc)) return false;
-    if (!expand_step_pq2<kBf16, h, 5>(c, g, win, sc)) return false;
-    if (!expand_step_pq2<kBf16, h, 6>(c, g, win, sc)) return false;
-    if (!expand_step_pq2<kBf16, h, 7>(c, g, win, sc)) return false;
+  const int g0 = group_at(c, 0);
+  load_half_pq2(c.row, c.srow, 8 * g0, h, win[0], sc[0]);
+  load_half_pq2(c.row, c.srow, 8 * g0 + 1, h, win[1], sc[1]);
+  for (int g = 0; g < c.ng; ++g) {
+    if (!expand_step_pq2<kBf16, kS, h, 0>(c, g, win, sc)) return false;
+    if (!expand_step_pq2<kBf16, kS, h, 1>(c, g, win, sc)) return false;
+    if (!expand_step_pq2<kBf16, kS, h, 2>(c, g, win, sc)) return false;
+    if (!expand_step_pq2<kBf16, kS, h, 3>(c, g, win, sc)) return false;
+    if (!expand_step_pq2<kBf16, kS, h, 4>(c, g, win, sc)) return false;
+    if (!expand_step_pq2<kBf16, kS, h, 5>(c, g, win, sc)) return false;
+    if (!expand_step_pq2<kBf16, kS, h, 6>(c, g, win, sc)) return false;
+    if (!expand_step_pq2<kBf16, kS, h, 7>(c, g, win, sc)) return false;
   }
   return true;
 }
 
-template <bool kBf16, int h>
+// The small variant's expansion: half h of the blocks of parity p (blocks
+// 8 g + q, q = p, p + 2, p + 4, p + 6), each thread two of its own blocks
+// ahead in a 4-slot register ring (own block kb in slot q / 2).
+template <bool kBf16, int kS, int h, int q>
+__device__ __forceinline__ bool expand_step_par(const ExpCtx& c, int j, uint32_t (&win)[4][12],
+                                                uint32_t (&sc)[4]) {
+  const int lb = 8 * j + q;
+  if (lb + 4 < 8 * c.ng) {
+    const int gn = q + 4 < 8 ? group_at(c, j) : group_at(c, j + 1);
+    load_block<(q + 4) % 8>(c.row, c.srow, 8 * gn + (q + 4) % 8, win[((q >> 1) + 2) % 4],
+                            sc[((q >> 1) + 2) % 4]);
+  }
+  uint32_t s16 = sc[q >> 1];
+  if constexpr (kBf16)  // the fp16 scale rounded to nearest-even bf16
+    s16 = __bfloat16_as_ushort(
+        __float2bfloat16_rn(__half2float(__ushort_as_half((unsigned short)s16))));
+  const uint32_t ta = (s16 ^ 0x8000u), tb = s16;
+  bool ok;
+  const int st = claim_stage<kS, h>(c, lb, &ok);
+  if (!ok) return false;
+  expand_half<h, (kBlockBytes * q) & 15>(win[q >> 1], ta, tb, c.bbase + (uint32_t)(st * kBSlice),
+                                         c.r);
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  mbar_arrive(c.b_full + st);
+  return true;
+}
+
+template <bool kBf16, int kS, int h, int p>
+__device__ bool expand_par(const ExpCtx& c) {
+  uint32_t win[4][12], sc[4];
+  const int g0 = group_at(c, 0);
+  load_block<p>(c.row, c.srow, 8 * g0 + p, win[0], sc[0]);  // a split holds >= 8 blocks
+  load_block<p + 2>(c.row, c.srow, 8 * g0 + p + 2, win[1], sc[1]);
+  for (int g = 0; g < c.ng; ++g) {
+    if (!expand_step_par<kBf16, kS, h, p>(c, g, win, sc)) return false;
+    if (!expand_step_par<kBf16, kS, h, p + 2>(c, g, win, sc)) return false;
+    if (!expand_step_par<kBf16, kS, h, p + 4>(c, g, win, sc)) return false;
+    if (!expand_step_par<kBf16, kS, h, p + 6>(c, g, win, sc)) return false;
+  }
+  return true;
+}
+
+template <bool kBf16, int kS, int h>
 __device__ bool expand_all(const ExpCtx& c) {
   uint32_t win[4][12], sc[4];
-  load_block<0>(c.row, c.srow, 8 * c.g_lo, win[0], sc[0]);
-  load_block<1>(c.row, c.srow, 8 * c.g_lo + 1, win[1], sc[1]);  // a split holds >= 8 blocks
-  for (int g = c.g_lo; 8 * g < c.nblk; ++g) {
-    if (!expand_step<kBf16, h, 0>(c, g, win, sc)) return false;
-    if (!expand_step<kBf16, h, 1>(c, g, win, sc)) return false;
-    if (!expand_step<kBf16, h, 2>(c, g, win, sc)) return false;
-    if (!expand_step<kBf16, h, 3>(c, g, win, sc)) return false;
-    if (!expand_step<kBf16, h, 4>(c, g, win, sc)) return false;
-    if (!expand_step<kBf16, h, 5>(c, g, win, sc)) return false;
-    if (!expand_step<kBf16, h, 6>(c, g, win, sc)) return false;
-    if (!expand_step<kBf16, h, 7>(c, g, win, sc)) return false;
+  const int g0 = group_at(c, 0);
+  load_block<0>(c.row, c.srow, 8 * g0, win[0], sc[0]);
+  load_block<1>(c.row, c.srow, 8 * g0 + 1, win[1], sc[1]);  // a split holds >= 8 blocks
+  load_block<2>(c.row, c.srow, 8 * g0 + 2, win[2], sc[2]);
+  for (int g = 0; g < c.ng; ++g) {
+    if (!expand_step<kBf16, kS, h, 0>(c, g, win, sc)) return false;
+    if (!expand_step<kBf16, kS, h, 1>(c, g, win, sc)) return false;
+    if (!expand_step<kBf16, kS, h, 2>(c, g, win, sc)) return false;
+    if (!expand_step<kBf16, kS, h, 3>(c, g, win, sc)) return false;
+    if (!expand_step<kBf16, kS, h, 4>(c, g, win, sc)) return false;
+    if (!expand_step<kBf16, kS, h, 5>(c, g, win, sc)) return false;
+    if (!expand_step<kBf16, kS, h, 6>(c, g, win, sc)) return false;
+    if (!expand_step<kBf16, kS, h, 7>(c, g, win, sc)) return false;
   }
   return true;
 }
@@ -383,8 +465,9 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
 // columns and the matching up rows in the other 64, so the epilogue holds
 // both factors of each output; no split.
 // kPQ2: the weights are PQ2_0 (2-bit codes, 32 bytes a block).
-template <bool kBf16, bool kOutF32, bool kSwiGLU = false, bool kPQ2 = false>
-__global__ void __launch_bounds__(kThreads, 2)
+// kSmall: M <= 128 (one 128-row accumulator), the deep ring of Lay<true>.
+template <bool kBf16, bool kOutF32, bool kSwiGLU = false, bool kPQ2 = false, bool kSmall = false>
+__global__ void __launch_bounds__(Lay<kSmall>::kThreads, Lay<kSmall>::kCtasPerSm)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const uint8_t* __restrict__ wq,
                    const uint16_t* __restrict__ scales, void* __restrict__ y, int M, int N, int K,
                    int splits, int* status) {
@@ -394,7 +477,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   // shared-memory instruction (an address laundered through an integer
   // would turn them into generic ones).
   extern __shared__ __align__(1024) unsigned char smem[];
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  using Y = Lay<kSmall>;
+  constexpr int kStages = Y::kStages, kASlice = Y::kASlice;
+  constexpr int kOffA = Y::kOffA, kOffB = Y::kOffB, kOffMisc = Y::kOffMisc;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Y::kOffBar);
   uint64_t* a_full = bars;
   uint64_t* b_full = bars + kStages;
   uint64_t* empty = bars + 2 * kStages;
@@ -410,13 +496,14 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int g_lo = (int)((long long)z * G / splits), g_hi = (int)((long long)(z + 1) * G / splits);
   const int kb0 = g_lo * (kRot / BK), kb1 = g_hi * (kRot / BK);  // this split's 64-wide slices
   const int nk = kb1 - kb0;
-  const int nmh = M - m0 > UM ? 2 : 1;  // the second 128-row half only when it holds rows
+  // the second 128-row half only when it holds rows (never in the small variant)
+  const int nmh = !kSmall && M - m0 > UM ? 2 : 1;
   if (kOutF32 && splits > 1) y = static_cast<float*>(y) + (size_t)z * M * N;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&a_full[s], 1);
-      mbar_init(&b_full[s], kExpThreads / 2);
+      mbar_init(&b_full[s], BN);  // the 128 threads (one per row) that expand a slice
       mbar_init(&empty[s], 1);
     }
     mbar_init(acc_full, 1);
@@ -446,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (round > 0) ok = mbar_wait(&empty[s], (round - 1) & 1, abort_flag);
         if (!ok) break;
         // M <= 128: the A box is 128 rows (no zero fill for the empty half)
-        mbar_expect_tx(&a_full[s], M <= UM ? kASlice / 2 : kASlice);
+        mbar_expect_tx(&a_full[s], (kSmall || M <= UM) ? UM * BK * 2 : kASlice);
         tma_2d(smem_u32(smem + kOffA + s * kASlice), &map_a, (kb0 + kb) * BK, m0, &a_full[s]);
         ++a_issued;
       }
@@ -472,8 +559,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       umma_commit(acc_full);     // all MMAs issued by this thread
     }
   } else {
-    // ---- B expansion: thread (row r, half h); slice 2 kb + h uses stage h ----------
-    const int t = threadIdx.x - 32 * kExpWarp0, r = t & (BN - 1), h = t >> 7;  // h: warp-uniform
+    // ---- B expansion: thread (row r, half h); slice 2 kb + h uses stage (2 kb + h) % S
+    // h, p: warp-uniform; p (small variant) picks the blocks of one parity
+    const int t = threadIdx.x - 32 * kExpWarp0, r = t & (BN - 1), h = (t >> 7) & 1, p = t >> 8;
     int n;
     if constexpr (kSwiGLU) {  // columns 0-63: gate rows n0.., 64-127: up rows I + n0..
       const int i = n0 + (r & (BN / 2 - 1));
@@ -485,16 +573,20 @@ __global__ void __launch_bounds__(kThreads, 2)
     c.row = wq + (size_t)n * nblk * (kPQ2 ? 32 : kBlockBytes);
     c.srow = scales + (size_t)n * nblk;
     c.g_lo = g_lo;
-    c.nblk = g_hi * kGroupBlocks;
-    c.bbase = smem_u32(smem + kOffB + h * kBSlice);
-    c.empty = &empty[h];
-    c.b_full = &b_full[h];
+    c.ng = g_hi - g_lo;
+    c.bbase = smem_u32(smem + kOffB);
+    c.empty = empty;
+    c.b_full = b_full;
     c.r = r;
     c.abort_flag = abort_flag;
+    static_assert(!(kPQ2 && kSmall), "the small variant expands PTQ1_0 blocks");
     if constexpr (kPQ2)
-      ok = h == 0 ? expand_all_pq2<kBf16, 0>(c) : expand_all_pq2<kBf16, 1>(c);
+      ok = h == 0 ? expand_all_pq2<kBf16, kStages, 0>(c) : expand_all_pq2<kBf16, kStages, 1>(c);
+    else if constexpr (kSmall)
+      ok = h == 0 ? (p == 0 ? expand_par<kBf16, kStages, 0, 0>(c) : expand_par<kBf16, kStages, 0, 1>(c))
+                  : (p == 0 ? expand_par<kBf16, kStages, 1, 0>(c) : expand_par<kBf16, kStages, 1, 1>(c));
     else
-      ok = h == 0 ? expand_all<kBf16, 0>(c) : expand_all<kBf16, 1>(c);
+      ok = h == 0 ? expand_all<kBf16, kStages, 0>(c) : expand_all<kBf16, kStages, 1>(c);
   }
   if (!ok) {
     *abort_flag = 1;
@@ -503,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   // ---- epilogue: warps 2-9; warp w reads TMEM lanes 32 (w % 4) .. + 31 of
   // accumulator (w - 2) / 4 -------------------------------------------------------------
-  if (warp >= kExpWarp0) {
+  if (warp >= kExpWarp0 && warp < kExpWarp0 + 8) {  // small variant: the other warps idle
     const bool done = !*abort_flag && mbar_wait(acc_full, 0, abort_flag);
     if (done) {
       pdl_wait();  // the previous kernel may still read y
@@ -638,10 +730,11 @@ static cudaError_t encode_a(CUtensorMap* ma, const void* x, int64_t M, int64_t K
                        CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <bool kBf16, bool kOutF32, bool kSwiGLU = false, bool kPQ2 = false>
-cudaError_t launch_t(const CUtensorMap& ma, const uint8_t* wq, const uint16_t* scales, void* y,
+template <bool kBf16, bool kOutF32, bool kSwiGLU, bool kPQ2, bool kSmall>
+cudaError_t launch_v(const CUtensorMap& ma, const uint8_t* wq, const uint16_t* scales, void* y,
                      int M, int N, int K, int splits, int* status, cudaStream_t st) {
-  auto kern = gemm_tc_kernel<kBf16, kOutF32, kSwiGLU, kPQ2>;
+  auto kern = gemm_tc_kernel<kBf16, kOutF32, kSwiGLU, kPQ2, kSmall>;
+  constexpr int kSmemBytes = Lay<kSmall>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -649,8 +742,31 @@ cudaError_t launch_t(const CUtensorMap& ma, const uint8_t* wq, const uint16_t* s
   const int ncols = kSwiGLU ? N / 2 : N;
   const dim3 grid((unsigned)((ncols + cols - 1) / cols), (unsigned)((M + BM - 1) / BM),
                   (unsigned)splits);
-  return launch_pdl(kern, grid, dim3(kThreads), (size_t)kSmemBytes, st, ma, wq, scales, y, M, N,
+  return launch_pdl(kern, grid, dim3(Lay<kSmall>::kThreads), (size_t)kSmemBytes, st, ma, wq,
+                    scales, y, M, N,
                     K, splits, status);
+}
+
+constexpr int64_t kGpuSms = 152;
+
+// The small-M variant (one accumulator, deep ring, one CTA per SM) serves
+// M <= 128 when the tiles fill between half and all of the SMs: unsplit, in
+// one wave.  Fewer tiles are split along K over two CTAs per SM, more run
+// two per SM in the large variant.
+static bool small_variant(int64_t M, int64_t N) {
+  const int64_t tiles = (N + BN - 1) / BN;
+  return M <= UM && 2 * tiles > kGpuSms && tiles <= kGpuSms;
+}
+
+template <bool kBf16, bool kOutF32, bool kSwiGLU = false, bool kPQ2 = false>
+cudaError_t launch_t(const CUtensorMap& ma, const uint8_t* wq, const uint16_t* scales, void* y,
+                     int M, int N, int K, int splits, int* status, cudaStream_t st) {
+  if constexpr (!kPQ2)  // (the PQ2_0 expansion has no parity-strided form)
+    if (splits == 1 && small_variant(M, N))
+      return launch_v<kBf16, kOutF32, kSwiGLU, kPQ2, true>(ma, wq, scales, y, M, N, K, splits,
+                                                           status, st);
+  return launch_v<kBf16, kOutF32, kSwiGLU, kPQ2, false>(ma, wq, scales, y, M, N, K, splits,
+                                                        status, st);
 }
 
 }  // namespace
@@ -662,7 +778,7 @@ cudaError_t launch_t(const CUtensorMap& ma, const uint8_t* wq, const uint16_t* s
 // and at most kMaxSplits.  A function of the shape alone, so the workspace
 // query and the launch agree.
 int gemm_tc_splits(int64_t M, int64_t N, int64_t K) {
-  constexpr int64_t kSms = 152, kMaxSplits = 6;
+  constexpr int64_t kSms = kGpuSms, kMaxSplits = 6;
   if (K % kRot != 0 || M <= 0 || N <= 0) return 1;
   const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   if (2 * tiles > kSms) return 1;

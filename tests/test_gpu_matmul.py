@@ -323,6 +323,24 @@ def test_prefill_small_shapes(P, orc, syn, M, N, K):
     Q.check_bf16(Q.host_f64(y), orc.matmul(wq, mv.scales, Q.x_f64(mv.x)), f"bf16 {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("M,N,K", [(128, 17408, 5120), (1, 9800, 1024), (77, 12000, 2048),
+                                   (128, 19456, 3072), (100, 19457, 1024)])
+def test_prefill_small_m(P, orc, syn, M, N, K):
+    # M <= 128 with 77 to 152 column tiles: the GEMM's small-M form (one
+    # 128-row accumulator, a 6-deep ring, 16 expansion warps that take every
+    # other block, one CTA per SM); 19457 columns (153 tiles) is the first
+    # shape past it.  Sampled columns include both tile edges and the ragged
+    # end; a second call gives the same bits.
+    import torch
+
+    mv = syn.gaussian_matvec(40 + M, M, N, K, dtype="bf16")
+    rng = np.random.default_rng(N)
+    cols = np.unique(np.concatenate([rng.integers(0, N, 160), [0, 1, 127, 128, 255, N - 2, N - 1]]))
+    y = _sampled(P, orc, mv, cols, f"small-M prefill {M}x{N}x{K}")
+    y2, _ = run(P, mv.trits, mv.scales, mv.x)
+    assert torch.equal(y, y2)
+
+
 @pytest.mark.parametrize("M,N,K", [(64, 1000, 6144), (256, 5120, 17408), (300, 640, 3072)])
 def test_prefill_split_k(P, orc, syn, M, N, K):
     # few output tiles: K is split over several CTAs whose fp32 partial sums
