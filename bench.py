@@ -410,11 +410,16 @@ def run_ours(args, world, rank):
     def fwht_only(i):
         P.fwht(ring[i % R][2], signs, out=xr[i % R])
 
+    def peel_only(i):  # the pages' decode design: the trits peeled on the float pipe
+        wq, sc, _ = ring[i % R]
+        P.matmul_f32_peel(wq, sc, xr[i % R], out=ys[i % R])
+
     K, W = args.steps, args.warmup
     with ClockSampler(dev_index) as clk:
         ms = max_over_ranks(timed_steps(torch, step, K, W))
         ms_gemv = timed_steps(torch, gemv_only, K, W)
         ms_fwht = timed_steps(torch, fwht_only, K, W)
+        ms_peel = timed_steps(torch, peel_only, K, W)
     P.device_check()
     ms_per_step = ms / K
     value = world * WEIGHT_BYTES / (ms_per_step * 1e-3) / 1e9       # GB/s, all ranks
@@ -552,6 +557,12 @@ def run_ours(args, world, rank):
         "stage_us": {"step_rotate_gemv_fused": round(step_us, 3),
                      "unfused_fwht": round(ms_fwht / K * 1e3, 3),
                      "unfused_gemv_on_rotated_x": round(gemv_us, 3)},
+        "decode_peel": {"workload": "the same GEMV (rotated x, the same ring) by the SIMT kernel "
+                                    "that peels the trits on the float pipe with 16-byte loads",
+                        "us_per_call": round(ms_peel / K * 1e3, 3),
+                        "GB/s": round(world * gemv_bytes / (ms_peel / K * 1e-3) / 1e9, 1),
+                        "frac_of_hbm": round(gemv_bytes / (ms_peel / K * 1e-3) / 1e9 / pk["hbm"], 4),
+                        "kernel": "gemv_ptq1_f32_kernel (ptq_matmul_f32_peel)"},
         "tokens_per_s_equiv": round(value * 1e9 / 5.906e9, 1),
         "e2e": {"value": round(e2e, 2), "unit": "GB/s", "h2d_bytes_per_step": K_COLS * 4,
                 "d2h_bytes_per_step": N_ROWS * 4, "ms_per_step": round(ms_e2e, 5),

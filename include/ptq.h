@@ -403,6 +403,17 @@ PTQ_API PTQ_NODISCARD ptq_status ptq_matmul_bf16_accumulator(
     int64_t M, int64_t N, int64_t K, void* workspace, size_t workspace_bytes,
     ptq_stream_t stream);
 
+/* ptq_matmul_f32_peel -- test export: ptq_matmul's fp32 route (1 <= M <= 8)
+ * computed by its other kernel, the SIMT GEMV that peels the trits on the
+ * float pipe with 16-byte loads (the route's kernel when K/128 is odd), on
+ * any shape.  It lets the peel design of "What Ferrox does with it" be timed
+ * against the table-lookup kernel on the same weights.  No workspace.
+ * x must already be rotated.  Arguments and errors as ptq_matmul with
+ * PTQ_F32. */
+PTQ_API PTQ_NODISCARD ptq_status ptq_matmul_f32_peel(
+    const uint8_t* wq, const uint16_t* scales, const float* x, float* y,
+    int64_t M, int64_t N, int64_t K, ptq_stream_t stream);
+
 /* ptq_gemv_plan -- introspection: the launch ptq_matmul's fp32 decode route
  * (pq2 != 0: ptq_matmul_pq2's) makes for (M, N, K) on the current device,
  * K % 1024 == 0, plain output (ptq_ffn's gate/up projection always adds the

@@ -32,7 +32,8 @@ EXPORTS = ("ptq1_pack", "ptq1_unpack", "ptq_fwht", "ptq_matmul_workspace_bytes",
            "ptq_ffn", "ptq_ffn_noalloc", "ptq_ffn_stack_workspace_bytes", "ptq_ffn_stack",
            "ptq_ffn_stack_ex", "ptq_ffn_stack_route", "ptq2_pack", "ptq2_unpack",
            "ptq_matmul_pq2_workspace_bytes", "ptq_matmul_pq2", "ptq_embed", "ptq_embed_ptq1",
-           "ptq_route", "ptq_gemv_plan", "ptq_matmul_bf16_accumulator", "ptq_selftest_timeout",
+           "ptq_route", "ptq_gemv_plan", "ptq_matmul_bf16_accumulator", "ptq_matmul_f32_peel",
+           "ptq_selftest_timeout",
            "ptq_selftest_grid_timeout",
            "ptq_device_check", "ptq_status_str", "ptq_last_error")
 
@@ -92,6 +93,8 @@ def load(path: str | None = None):
     L.ptq_embed_ptq1.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _P]
     L.ptq_route.argtypes = [_I64, _I32, ctypes.POINTER(ctypes.c_char_p)]
     L.ptq_gemv_plan.argtypes = [_I64, _I64, _I64, _I32, ctypes.POINTER(ctypes.c_int32)]
+    L.ptq_matmul_f32_peel.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _P]
+    L.ptq_matmul_f32_peel.restype = _I32
     L.ptq_matmul_bf16_accumulator.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _P,
                                               ctypes.c_size_t, _P]
     L.ptq_device_check.argtypes = [_P]
@@ -439,6 +442,21 @@ def route(M: int, dtype: int) -> str:
     name = ctypes.c_char_p()
     _check(load().ptq_route(M, dtype, ctypes.byref(name)), "ptq_route")
     return name.value.decode()
+
+
+def matmul_f32_peel(wq, scales, x, out=None, stream=None):
+    """Test export: the fp32 route's SIMT peel GEMV (ptq_matmul_f32_peel),
+    y = x W^T with x float32 (already rotated), on any shape."""
+    import torch
+
+    M, K = x.shape
+    N = wq.shape[0]
+    y = torch.empty((M, N), dtype=torch.float32, device=x.device) if out is None else out
+    _check(load().ptq_matmul_f32_peel(
+        _dev(wq, torch.uint8, "wq"), _dev(scales, torch.int16, "scales"),
+        _dev(x, torch.float32, "x"), _dev(y, torch.float32, "out"), M, N, K, _stream(stream)),
+        "ptq_matmul_f32_peel")
+    return y
 
 
 def gemv_plan(M: int, N: int, K: int, pq2: bool = False) -> dict:

@@ -348,6 +348,21 @@ PTQ_API ptq_status ptq_matmul_bf16_accumulator(const uint8_t* wq, const uint16_t
   return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq_matmul_bf16_accumulator launch");
 }
 
+// The fp32 route's other kernel, forced: the SIMT peel GEMV that the route
+// runs when K/128 is odd, here on any shape, so that the two decode designs
+// can be timed on the same weights.
+PTQ_API ptq_status ptq_matmul_f32_peel(const uint8_t* wq, const uint16_t* scales, const float* x,
+                                       float* y, int64_t M, int64_t N, int64_t K,
+                                       ptq_stream_t stream) {
+  t_msg[0] = 0;
+  const char* who = "ptq_matmul_f32_peel";
+  const Route* r = nullptr;
+  ptq_status s = check_matmul(wq, scales, x, y, M, N, K, PTQ_F32, who, &r);
+  if (s != PTQ_OK || M == 0 || N == 0) return s;
+  const cudaError_t e = launch_gemv(wq, scales, x, y, M, N, K, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq_matmul_f32_peel launch");
+}
+
 PTQ_API ptq_status ptq_gemv_plan(int64_t M, int64_t N, int64_t K, int pq2, int32_t plan[4]) {
   t_msg[0] = 0;
   if (!plan) return fail(PTQ_ERR_NULL, "ptq_gemv_plan: plan is NULL");

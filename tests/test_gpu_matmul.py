@@ -171,6 +171,20 @@ def test_lut_cluster_route_is_taken(P):
     assert big["cluster"] == 0 and big["kernels"] == 2
 
 
+@pytest.mark.parametrize("M,N,K", [(1, 17408, 5120), (4, 17408, 5120), (8, 5120, 17408),
+                                   (1, 300, 1024), (3, 777, 2560)])
+def test_peel_gemv_export(P, orc, syn, M, N, K):
+    # the fp32 route's peel kernel forced on shapes the table-lookup kernel
+    # serves (the bench times both on the decode shape): sampled rows at full
+    # size, every row on the small shapes
+    mv = syn.gaussian_matvec(500 + M, M, N, K)
+    wq = P.pack(mv.trits)
+    y = P.matmul_f32_peel(Q.dev(wq), Q.dev(mv.scales), Q.dev(mv.x))
+    rows = np.unique(np.linspace(0, N - 1, min(N, 96)).astype(np.int64))
+    ref = orc.matmul_rows(wq, mv.scales, Q.x_f64(mv.x), rows)
+    Q.check_f32(Q.host_f64(y)[:, rows], ref, f"peel {M}x{N}x{K}")
+
+
 @pytest.mark.parametrize("K", [128, 384, 640])
 def test_lut_odd_block_count_uses_general_gemv(P, orc, syn, K):
     # K/128 odd leaves rows that are not whole 32-bit words apart
