@@ -177,6 +177,34 @@ PTQ_API PTQ_NODISCARD ptq_status ptq_rotate_matmul(
     ptq_dtype dtype, void* workspace, size_t workspace_bytes,
     ptq_stream_t stream);
 
+/* ptq_rotate_matmul_host_workspace_bytes -- device scratch of
+ * ptq_rotate_matmul_host: room for x and y, then ptq_rotate_matmul's own
+ * workspace (each rounded up to 256 bytes); 0 when the arguments are
+ * invalid. */
+PTQ_API size_t ptq_rotate_matmul_host_workspace_bytes(int64_t M, int64_t N,
+                                                      int64_t K, ptq_dtype dtype);
+
+/* ptq_rotate_matmul_host -- ptq_rotate_matmul on host buffers, for callers
+ * whose activations live on the host: copies x_host (M x K, host) into the
+ * workspace, runs ptq_rotate_matmul there, and copies y (M x N) back to
+ * y_host, all queued on `stream` (one cudaMemcpyAsync each way).  The call
+ * returns once the work is queued: y_host is valid after the stream is
+ * synchronised, and x_host must stay unchanged until then.  Page-locked host
+ * memory gives asynchronous copies; other host memory works but the copies
+ * then synchronise.  When the runtime maps both host buffers into the
+ * device's address space (page-locked memory on a system with unified
+ * addressing), the kernels read x and write y there directly instead, with
+ * no copies.  wq, scales and signs are device pointers as in
+ * ptq_rotate_matmul.  workspace: at least
+ * ptq_rotate_matmul_host_workspace_bytes(...) bytes, 256-byte aligned.
+ * Errors as ptq_rotate_matmul, plus PTQ_ERR_NULL for a NULL host buffer and
+ * PTQ_ERR_CUDA if a copy cannot be queued. */
+PTQ_API PTQ_NODISCARD ptq_status ptq_rotate_matmul_host(
+    const uint8_t* wq, const uint16_t* scales, const void* x_host,
+    const int8_t* signs, void* y_host, int64_t M, int64_t N, int64_t K,
+    ptq_dtype dtype, void* workspace, size_t workspace_bytes,
+    ptq_stream_t stream);
+
 /* ptq_ffn_workspace_bytes -- scratch size ptq_ffn needs for (M, H, I, dtype);
  * 0 when the arguments are invalid. */
 PTQ_API size_t ptq_ffn_workspace_bytes(int64_t M, int64_t H, int64_t I,

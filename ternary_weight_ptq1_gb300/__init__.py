@@ -28,7 +28,8 @@ STATUS = {
 
 # Every symbol include/ptq.h declares.
 EXPORTS = ("ptq1_pack", "ptq1_unpack", "ptq_fwht", "ptq_matmul_workspace_bytes", "ptq_matmul",
-           "ptq_rotate_matmul_workspace_bytes", "ptq_rotate_matmul", "ptq_ffn_workspace_bytes",
+           "ptq_rotate_matmul_workspace_bytes", "ptq_rotate_matmul",
+           "ptq_rotate_matmul_host_workspace_bytes", "ptq_rotate_matmul_host", "ptq_ffn_workspace_bytes",
            "ptq_ffn", "ptq_ffn_noalloc", "ptq_ffn_stack_workspace_bytes", "ptq_ffn_stack",
            "ptq_ffn_stack_ex", "ptq_ffn_stack_route", "ptq2_pack", "ptq2_unpack",
            "ptq_matmul_pq2_workspace_bytes", "ptq_matmul_pq2", "ptq_embed", "ptq_embed_ptq1",
@@ -71,6 +72,11 @@ def load(path: str | None = None):
     L.ptq_matmul.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, ctypes.c_size_t, _P]
     L.ptq_rotate_matmul_workspace_bytes.argtypes = [_I64, _I64, _I64, _I32]
     L.ptq_rotate_matmul_workspace_bytes.restype = ctypes.c_size_t
+    L.ptq_rotate_matmul_host_workspace_bytes.argtypes = [_I64, _I64, _I64, _I32]
+    L.ptq_rotate_matmul_host_workspace_bytes.restype = ctypes.c_size_t
+    L.ptq_rotate_matmul_host.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _P,
+                                         ctypes.c_size_t, _P]
+    L.ptq_rotate_matmul_host.restype = _I32
     L.ptq_rotate_matmul.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, ctypes.c_size_t,
                                     _P]
     L.ptq_ffn_workspace_bytes.argtypes = [_I64, _I64, _I64, _I32]
@@ -120,11 +126,17 @@ def _check(status: int, call: str) -> None:
         raise PTQError(status, call, msg)
 
 
-def _stream(stream=None) -> ctypes.c_void_p:
+def _stream(stream=None, device=None) -> int:
+    """The raw handle of `stream`, else of PyTorch's current stream on
+    `device` (an index; the current device when None)."""
     import torch
 
-    s = torch.cuda.current_stream() if stream is None else stream
-    return ctypes.c_void_p(s.cuda_stream)
+    if stream is not None:
+        return stream.cuda_stream
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None:  # no Stream object per call
+        return raw(torch.cuda.current_device() if device is None else device)
+    return torch.cuda.current_stream(device).cuda_stream
 
 
 def _dev(t, dtype=None, name="tensor"):
@@ -136,7 +148,7 @@ def _dev(t, dtype=None, name="tensor"):
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()
 
 
 def _act_dtype(t):
@@ -277,6 +289,33 @@ def matmul_pq2(wq, scales, x, out=None, workspace=None, stream=None):
 
 def rotate_matmul_workspace_bytes(M: int, N: int, K: int, dtype: int) -> int:
     return int(load().ptq_rotate_matmul_workspace_bytes(M, N, K, dtype))
+
+
+def rotate_matmul_host_workspace_bytes(M: int, N: int, K: int, dtype: int) -> int:
+    return int(load().ptq_rotate_matmul_host_workspace_bytes(M, N, K, dtype))
+
+
+def rotate_matmul_host(wq, scales, x_host, signs, y_host, workspace, stream=None):
+    """ptq_rotate_matmul_host: x_host (M x K) and y_host (M x N) are CPU
+    tensors (page-locked for asynchronous copies) of one dtype, float32 or
+    bfloat16; the copies and the product are queued on the stream, and
+    y_host is valid once it is synchronised."""
+    import torch
+
+    M, K = x_host.shape
+    N = wq.shape[0]
+    dt = _act_dtype(x_host)
+    for t, name in ((x_host, "x_host"), (y_host, "y_host")):
+        if t.is_cuda or not t.is_contiguous() or t.dtype != x_host.dtype:
+            raise TypeError(f"{name} must be a contiguous CPU tensor of the activations' dtype")
+    if tuple(y_host.shape) != (M, N):
+        raise ValueError(f"y_host must be {M} x {N}")
+    _check(load().ptq_rotate_matmul_host(
+        _dev(wq, torch.uint8, "wq"), _dev(scales, torch.int16, "scales"), x_host.data_ptr(),
+        _dev(signs, torch.int8, "signs"), y_host.data_ptr(), M, N, K, dt,
+        _dev(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream, wq.device.index)), "ptq_rotate_matmul_host")
+    return y_host
 
 
 def rotate_matmul(wq, scales, x, signs, out=None, workspace=None, stream=None):

@@ -528,6 +528,76 @@ PTQ_API ptq_status ptq_rotate_matmul(const uint8_t* wq, const uint16_t* scales, 
   return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq_rotate_matmul launch");
 }
 
+// ptq_rotate_matmul on host buffers: the workspace holds x (M x K), y (M x
+// N) and then ptq_rotate_matmul's own workspace, each rounded up to 256 bytes.
+static bool rotmm_host_layout(int64_t M, int64_t N, int64_t K, ptq_dtype dt, size_t* y_off,
+                              size_t* ws_off, size_t* total) {
+  int64_t xb, yb;
+  if (!mul_ok(M, K, &xb) || !mul_ok(xb, (int64_t)dsize(dt), &xb) || !mul_ok(M, N, &yb) ||
+      !mul_ok(yb, (int64_t)dsize(dt), &yb))
+    return false;
+  const size_t inner = ptq_rotate_matmul_workspace_bytes(M, N, K, dt);
+  auto up = [](int64_t v) { return (size_t)((v + 255) / 256 * 256); };
+  *y_off = up(xb);
+  *ws_off = *y_off + up(yb);
+  *total = *ws_off + inner;
+  return true;
+}
+
+PTQ_API size_t ptq_rotate_matmul_host_workspace_bytes(int64_t M, int64_t N, int64_t K,
+                                                      ptq_dtype dtype) {
+  size_t y_off, ws_off, total;
+  if (ptq_rotate_matmul_workspace_bytes(M, N, K, dtype) == 0 ||
+      !rotmm_host_layout(M, N, K, dtype, &y_off, &ws_off, &total))
+    return 0;
+  return total;
+}
+
+PTQ_API ptq_status ptq_rotate_matmul_host(const uint8_t* wq, const uint16_t* scales,
+                                          const void* x_host, const int8_t* signs, void* y_host,
+                                          int64_t M, int64_t N, int64_t K, ptq_dtype dtype,
+                                          void* ws, size_t ws_bytes, ptq_stream_t stream) {
+  t_msg[0] = 0;
+  const char* who = "ptq_rotate_matmul_host";
+  if (!dtype_ok(dtype)) return fail(PTQ_ERR_VALUE, "%s: unknown dtype %d", who, (int)dtype);
+  if (M < 0 || N < 0 || K <= 0 || K % kRot != 0)
+    return fail(PTQ_ERR_SHAPE, "%s: need M, N >= 0 and K %% 1024 == 0 (M=%lld N=%lld K=%lld)", who,
+                (long long)M, (long long)N, (long long)K);
+  if (M == 0 || N == 0) return PTQ_OK;
+  if (!x_host || !y_host) return fail(PTQ_ERR_NULL, "%s: NULL host buffer", who);
+  size_t y_off, ws_off, need;
+  if (ptq_rotate_matmul_workspace_bytes(M, N, K, dtype) == 0 ||
+      !rotmm_host_layout(M, N, K, dtype, &y_off, &ws_off, &need))
+    return fail(PTQ_ERR_SHAPE, "%s: size overflow", who);
+  if (!ws) return fail(PTQ_ERR_WORKSPACE, "%s: workspace is NULL (%zu bytes needed)", who, need);
+  if (ws_bytes < need)
+    return fail(PTQ_ERR_WORKSPACE, "%s: workspace has %zu bytes, %zu needed", who, ws_bytes, need);
+  if (!aligned(ws, 256)) return fail(PTQ_ERR_ALIGN, "%s: workspace needs 256-byte alignment", who);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char* base = static_cast<char*>(ws);
+  const size_t es = dsize(dtype);
+  // Page-locked memory that the runtime maps into the device's address space
+  // (a device address for both buffers): the kernels read x and write y there
+  // directly, over the host link, with no copy engine in between.
+  cudaPointerAttributes ax, ay;
+  const cudaError_t qx = cudaPointerGetAttributes(&ax, x_host);
+  const cudaError_t qy = cudaPointerGetAttributes(&ay, y_host);
+  if (qx != cudaSuccess || qy != cudaSuccess)
+    static_cast<void>(cudaGetLastError());  // the query's own error: use the copies
+  else if (ax.type == cudaMemoryTypeHost && ay.type == cudaMemoryTypeHost &&
+           ax.devicePointer != nullptr && ay.devicePointer != nullptr &&
+           aligned(ax.devicePointer, 16) && aligned(ay.devicePointer, 16))
+    return ptq_rotate_matmul(wq, scales, ax.devicePointer, signs, ay.devicePointer, M, N, K,
+                             dtype, base + ws_off, need - ws_off, stream);
+  cudaError_t e = cudaMemcpyAsync(base, x_host, (size_t)(M * K) * es, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return cuda_fail(e, "ptq_rotate_matmul_host: copy of x");
+  const ptq_status s = ptq_rotate_matmul(wq, scales, base, signs, base + y_off, M, N, K, dtype,
+                                         base + ws_off, need - ws_off, stream);
+  if (s != PTQ_OK) return s;
+  e = cudaMemcpyAsync(y_host, base + y_off, (size_t)(M * N) * es, cudaMemcpyDeviceToHost, st);
+  return e == cudaSuccess ? PTQ_OK : cuda_fail(e, "ptq_rotate_matmul_host: copy of y");
+}
+
 // Workspace of ptq_ffn, each region rounded up to 256 bytes:
 //   xr (M x H) | gu (M x 2I, fp32) | h (M x I, fp32) [| hr (M x I, fp16)]
 //   | part (the decode GEMV's row sums, shared by the two projections, which

@@ -192,6 +192,32 @@ def test_stack_refusals_before_launch(P):
     assert st([], 0, x=None, ws=None, wsb=0) == 0
     assert st([good], 1, M=0, x=None, ws=None, wsb=0) == 0
 
+def test_rotate_matmul_host_refusals(P):
+    # host-buffer entry: the workspace holds x and y (256-byte rounded) before
+    # ptq_rotate_matmul's own; refusals come before any copy or launch
+    L = P.load()
+    p16 = ctypes.c_void_p(16 * 1024)
+    up = lambda v: (v + 255) // 256 * 256  # noqa: E731
+    inner = P.rotate_matmul_workspace_bytes(1, 17408, 5120, P.PTQ_F32)
+    need = P.rotate_matmul_host_workspace_bytes(1, 17408, 5120, P.PTQ_F32)
+    assert need == up(5120 * 4) + up(17408 * 4) + inner
+    assert P.rotate_matmul_host_workspace_bytes(2, 300, 2048, P.PTQ_BF16) == (
+        up(2 * 2048 * 2) + up(2 * 300 * 2) + P.rotate_matmul_workspace_bytes(2, 300, 2048,
+                                                                             P.PTQ_BF16))
+    assert P.rotate_matmul_host_workspace_bytes(1, 100, 1000, P.PTQ_F32) == 0
+    host = lambda x, y, ws, nb: L.ptq_rotate_matmul_host(  # noqa: E731
+        p16, p16, x, p16, y, 1, 17408, 5120, P.PTQ_F32, ws, nb, None)
+    assert host(None, p16, p16, need) == 1                 # NULL host x
+    assert host(p16, None, p16, need) == 1                 # NULL host y
+    assert host(p16, p16, None, need) == 6                 # no workspace
+    assert host(p16, p16, p16, need - 1) == 6
+    assert host(p16, p16, ctypes.c_void_p(16 * 1024 + 16), need) == 3  # not 256-aligned
+    assert L.ptq_rotate_matmul_host(p16, p16, p16, p16, p16, 1, 8, 1000, P.PTQ_F32, p16, need,
+                                    None) == 2             # K % 1024
+    assert L.ptq_rotate_matmul_host(p16, p16, p16, p16, p16, 0, 8, 1024, P.PTQ_F32, None, 0,
+                                    None) == 0             # nothing to do
+
+
 def test_routing_table(P):
     for M in range(1, 9):
         assert P.route(M, P.PTQ_F32) == "gemv_ptq1_f32_lut"

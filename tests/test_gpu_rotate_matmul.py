@@ -74,6 +74,38 @@ def test_rotate_matches_separate_calls(P, syn):
     assert rel < 1e-5, float(rel)
 
 
+@pytest.mark.parametrize("M,N,K,dtype", [(1, 17408, 5120, "f32"), (4, 1000, 2048, "f32"),
+                                         (3, 700, 3072, "bf16")])
+def test_rotate_matmul_host_buffers(P, orc, syn, M, N, K, dtype):
+    # ptq_rotate_matmul_host: x from page-locked host memory, y back to it,
+    # around the same product; the result has the bits of the device call
+    import torch
+
+    mv = syn.gaussian_matvec(330 + M, M, N, K, dtype=dtype)
+    signs = Q.dev(syn.signs(330 + M, 9, K))
+    wq, s = Q.dev(P.pack(mv.trits)), Q.dev(mv.scales)
+    xd = Q.dev(mv.x) if dtype == "f32" else Q.dev_bf16(mv.x)
+    ref = P.rotate_matmul(wq, s, xd, signs)
+    xh = xd.cpu().pin_memory()
+    yh = torch.full((M, N), float("nan"), dtype=xd.dtype).pin_memory()
+    ws = torch.empty(P.rotate_matmul_host_workspace_bytes(M, N, K, P._act_dtype(xd)),
+                     dtype=torch.uint8, device="cuda")
+    # page-locked buffers (mapped: the kernels read x and write y in place),
+    # then ordinary pageable ones (the copy path)
+    P.rotate_matmul_host(wq, s, xh, signs, yh, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(yh, ref.cpu())
+    xp, yp = xd.cpu(), torch.full((M, N), float("nan"), dtype=xd.dtype)
+    P.rotate_matmul_host(wq, s, xp, signs, yp, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(yp, ref.cpu())
+    rows = np.unique(np.linspace(0, N - 1, 64).astype(np.int64))
+    want = orc.matmul(orc.pack(mv.trits[rows]), mv.scales[rows],
+                      orc.fwht(Q.x_f64(mv.x), syn.signs(330 + M, 9, K)))
+    got = yh.float().numpy().astype(np.float64)[:, rows]
+    (Q.check_f32 if dtype == "f32" else Q.check_bf16)(got, want, f"host buffers {M}x{N}x{K}")
+
+
 @pytest.mark.parametrize("M,dtype", [(4, "f32"), (8, "f32"), (64, "bf16"), (3, "bf16")])
 def test_rotate_matmul_other_sizes(P, orc, syn, M, dtype):
     N, K = 600, 2048
