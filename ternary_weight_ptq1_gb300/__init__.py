@@ -410,7 +410,7 @@ def ffn_stack(layers, norm_w, x, eps: float, act=None, workspace=None, stream=No
     for l, (lay, g) in enumerate(zip(layers, norm_w)):
         ptrs = [_dev(t, ty, f"layers[{l}].{n}") for t, ty, n in zip(lay, types, names)]
         ptrs.append(_dev(g, torch.float32, f"norm_w[{l}]"))
-        arr[l] = FfnLayer(*[p.value for p in ptrs])
+        arr[l] = FfnLayer(*ptrs)
     _check(load().ptq_ffn_stack_ex(ctypes.cast(arr, ctypes.c_void_p), L,
                                    _dev(x, torch.float32, "x"), M, H, I, float(eps), dt,
                                    _dev(workspace, None, "workspace"),
