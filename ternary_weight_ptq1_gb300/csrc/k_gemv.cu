@@ -279,15 +279,22 @@ cudaError_t launch_gemv(const uint8_t* wq, const uint16_t* scales, const float* 
                         int64_t M, int64_t N, int64_t K, cudaStream_t st) {
   if (N > INT32_MAX || K > INT32_MAX) return cudaErrorInvalidValue;
   const int n = (int)N, k = (int)K;
+  // At most three tokens per launch: a kernel instance for more tokens no
+  // longer unrolls its loop over the 52 words of a group, indexes them in
+  // local memory and ran 15-30x slower (measured at M = 4 and 8).  More
+  // tokens take several launches, the weights read again (mostly from L2).
+  if (M > 3) {
+    for (int64_t m0 = 0; m0 < M; m0 += 3) {
+      const int64_t c = M - m0 < 3 ? M - m0 : 3;
+      const cudaError_t e = launch_gemv(wq, scales, x + m0 * K, y + m0 * N, c, N, K, st);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
   switch (M) {
     case 1: return launch_m<1>(wq, scales, x, y, n, k, st);
     case 2: return launch_m<2>(wq, scales, x, y, n, k, st);
     case 3: return launch_m<3>(wq, scales, x, y, n, k, st);
-    case 4: return launch_m<4>(wq, scales, x, y, n, k, st);
-    case 5: return launch_m<5>(wq, scales, x, y, n, k, st);
-    case 6: return launch_m<6>(wq, scales, x, y, n, k, st);
-    case 7: return launch_m<7>(wq, scales, x, y, n, k, st);
-    case 8: return launch_m<8>(wq, scales, x, y, n, k, st);
   }
   return cudaErrorInvalidValue;
 }
