@@ -24,19 +24,24 @@
 // a range of rows, and lane L of every warp owns word L of the chunk, i.e.
 // byte positions 4L..4L+3.  The four tables of lane L live in shared-memory
 // bank L only (entry e of position j at 0x10000 * (1 + j/2) + 256 e +
-// 128 (j%2) + 4L), so the 32 lookups of a warp never conflict, whatever the
-// bytes are.  The table region starts at shared address 0x10000, so one
-// byte permute builds the whole address: byte 1 is the weight byte, byte 0
-// the lane's column, byte 2 the region.
+// 128 (j%2) + 4L from the start of the CTA's shared window), so the 32
+// lookups of a warp never conflict, whatever the bytes are.  The table
+// region starts 0x10000 into the window, so one byte permute builds the
+// whole address: byte 1 is the weight byte, byte 0 the lane's column, bytes
+// 2-3 the region (and, in a cluster, the CTA's rank).
 //
-// A warp streams its rows with 4-byte coalesced loads kept 16 rows ahead in
-// registers (the weights do not depend on the previous kernel, so the first
-// loads are issued before griddepcontrol.wait), turns every row into one
-// fp32 value per lane (the block scales of the lane's two half-words applied),
-// and sums the 32 lanes of 16 rows at a time through a padded shared-memory
-// transpose.  Each CTA writes its chunk's row sums to part[c][n]; a second
-// kernel adds the nch chunks of every row in a fixed order, so the result is
-// bitwise reproducible.  No kernel here waits on another CTA.
+// Two kernels stream the rows.  The register-ring kernel (any K/128 even)
+// keeps 16 rows of 4-byte coalesced loads in flight in registers and sums
+// the 32 lanes of 16 rows through a padded shared-memory transpose.  The
+// TMA-fed kernel (K % 1024 == 0) is described before LutTmaArgs.  In both the
+// first weight loads are issued before griddepcontrol.wait (the weights do
+// not depend on the previous kernel), and every row becomes one fp32 value
+// per lane, the block scales of the lane's two half-words applied.  The nch
+// chunk sums of a row are added in a fixed chunk order, so the result is
+// bitwise reproducible: by a second kernel from part[c][n], or, at one token,
+// by the row group's own cluster in distributed shared memory.  Only the
+// cluster waits on other CTAs: its hardware barriers, which every CTA of
+// the cluster reaches.
 #include <cuda_fp16.h>
 
 #include <atomic>
