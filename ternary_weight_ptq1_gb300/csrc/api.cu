@@ -622,7 +622,8 @@ static bool ffn_layout(int64_t M, int64_t H, int64_t I, ptq_dtype dt, size_t off
   off[3] = off[2] + (size_t)up(c);
   off[4] = off[3] + (size_t)up(d);
   // decode: the larger of the two projections' row sums; prefill: gate/up's
-  // split-K sums (the down projection's use the gate/up region, dead by then)
+  // split-K sums (the down projection's use the gate/up region, dead by
+  // then, and on the bf16 path the h region after it)
   const size_t p1 = matmul_ws_bytes(M, 2 * I, H, dt), p2 = matmul_ws_bytes(M, H, I, dt);
   *total = off[4] + (dt == PTQ_BF16 ? p1 : (p1 > p2 ? p1 : p2));
   return true;
@@ -702,9 +703,10 @@ static cudaError_t run_ffn_block(const FfnRoutes& r, const uint8_t* wgu_q, const
   }
   if (e == cudaSuccess) e = launch_fwht(h, Act::F32, hr, op, signs_mid, M, I, st);
   // the down projection's split-K partials go where gate/up was (dead after
-  // SwiGLU)
+  // SwiGLU) and, on the bf16 path, where h was (dead once rotated into hr)
   if (e == cudaSuccess)
-    e = run_matmul(r.d, wd_q, wd_s, hr, op, y, act_of(dtype), M, H, I, gu, off[2] - off[1], st);
+    e = run_matmul(r.d, wd_q, wd_s, hr, op, y, act_of(dtype), M, H, I, gu,
+                   (bf ? off[3] : off[2]) - off[1], st);
   return e;
 }
 
