@@ -34,6 +34,18 @@ __device__ __forceinline__ uint32_t to16(float f) {
   else return __half_as_ushort(__float2half_rn(f));
 }
 
+// Two values rounded to nearest-even into one 16-bit pair (x low, y high).
+template <Act T>
+__device__ __forceinline__ uint32_t pack16(float2 f) {
+  if constexpr (T == Act::BF16) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(f.x, f.y);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  } else {
+    const __half2 h = __floats2half2_rn(f.x, f.y);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
+}
+
 // fp16 rounds |v| >= 65520 (the largest finite value 65504 plus half its
 // last-place step) to infinity.
 __device__ __forceinline__ bool beyond_f16(float v) {
@@ -41,29 +53,37 @@ __device__ __forceinline__ bool beyond_f16(float v) {
   return a >= 65520.0f && a <= 3.402823466e38f;
 }
 
-// Butterflies over the register index bits of v[8][4] (index 4 j + c): the
-// pairs that differ in bit `bit` of that index, unnormalised.
-template <int kBit>
-__device__ __forceinline__ void reg_stage(float (&v)[32]) {
+// Butterflies over the register index bits of 32 values held as 16 pairs:
+// value 2 k + e is v[k].x (e = 0) or v[k].y (e = 1).  Index bit 0 pairs the
+// halves of each v[k] (scalar adds); bits 1-4 pair whole v[k] and v[k | m],
+// two butterflies per packed fp32x2 add and one packed fused multiply-add
+// (d * -1 + a is a - d, rounded once, as a subtraction is).  Unnormalised.
+__device__ __forceinline__ void reg_hadamard_32(float2 (&v)[16]) {
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    if (i & (1 << kBit)) continue;
-    const float a = v[i], d = v[i | (1 << kBit)];
-    v[i] = a + d;
-    v[i | (1 << kBit)] = a - d;
+  for (int k = 0; k < 16; ++k) {
+    const float a = v[k].x, d = v[k].y;
+    v[k] = make_float2(a + d, a - d);
   }
+  const float2 neg1 = make_float2(-1.0f, -1.0f);
+#pragma unroll
+  for (int m = 1; m < 16; m <<= 1)
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      if (k & m) continue;
+      const float2 a = v[k], d = v[k | m];
+      v[k] = __fadd2_rn(a, d);
+      v[k | m] = __ffma2_rn(d, neg1, a);
+    }
 }
 
-__device__ __forceinline__ void reg_hadamard_32(float (&v)[32]) {
-  reg_stage<0>(v);
-  reg_stage<1>(v);
-  reg_stage<2>(v);
-  reg_stage<3>(v);
-  reg_stage<4>(v);
+// The sign bits of sign bytes c = 2 h and 2 h + 1 of `sg` at bits 15 and 31,
+// the sign positions of a 16-bit pair.
+__device__ __forceinline__ uint32_t pair_sign_mask(uint32_t sg, int h) {
+  return __byte_perm(sg, 0u, h ? 0x3424u : 0x1404u) & 0x80008000u;
 }
 
 // One warp owns one 1024-element block at a time.  Lane l first holds the
-// elements 128 j + 4 l + c (j = 0..7, c = 0..3) in u[4 j + c]: index bits 0-1
+// elements 128 j + 4 l + c (j = 0..7, c = 0..3) as value 4 j + c: index bits 0-1
 // (c) and 7-9 (j) are in registers, bits 2-6 are the lane.  H is a tensor
 // product over the index bits, so the stages can run in any order: the five
 // register bits first; then a transpose through shared memory (row R = 8 c +
@@ -71,8 +91,10 @@ __device__ __forceinline__ void reg_hadamard_32(float (&v)[32]) {
 // conflicts) gives lane l the 32 elements 128 j' + 4 t + c' (t = 0..31) with
 // (c', j') = (l / 8, l % 8), whose index bits 2-6 are now in registers; their
 // five stages follow, and the transpose back gives the natural layout for
-// 16-byte (8-byte) global stores.  No shuffles: each element costs 10 FADDs,
-// 2.5 shared-memory instructions, its load, its store and the conversions.
+// 16-byte (8-byte) global stores.  No shuffles: of each element's ten
+// butterfly adds, eight are halves of packed fp32x2 instructions; then come
+// 2.5 shared-memory instructions, its load, its store and the conversions
+// (16-bit values are sign-flipped and rounded two at a time).
 constexpr int kRowPad = 36;
 constexpr int kWarpBuf = 32 * kRowPad;  // floats per warp
 
@@ -92,67 +114,74 @@ __global__ void __launch_bounds__(256) fwht1024_kernel(const void* x, void* y,
        wb += nwarps) {
     const int64_t b = wb % blocks_per_row;
     const int64_t base = wb * kRot;  // rows are contiguous: row m, block b -> wb * 1024
-    float u[32];
+    float2 v[16];  // value 4 j + c in v[2 j + c / 2], half c % 2
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int64_t e = base + 128 * j + 4 * lane;
       const uint32_t sg = *reinterpret_cast<const uint32_t*>(signs + b * kRot + 128 * j + 4 * lane);
-      float a[4];
       if constexpr (kIn != Act::F32) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(x) + e);
-        a[0] = from16<kIn>(raw.x & 0xffffu);
-        a[1] = from16<kIn>(raw.x >> 16);
-        a[2] = from16<kIn>(raw.y & 0xffffu);
-        a[3] = from16<kIn>(raw.y >> 16);
+        // the sign bits flip the 16-bit values before they widen
+        uint2 raw = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(x) + e);
+        raw.x ^= pair_sign_mask(sg, 0);
+        raw.y ^= pair_sign_mask(sg, 1);
+        v[2 * j] = make_float2(from16<kIn>(raw.x & 0xffffu), from16<kIn>(raw.x >> 16));
+        v[2 * j + 1] = make_float2(from16<kIn>(raw.y & 0xffffu), from16<kIn>(raw.y >> 16));
       } else {
         const float4 raw = *reinterpret_cast<const float4*>(static_cast<const float*>(x) + e);
-        a[0] = raw.x; a[1] = raw.y; a[2] = raw.z; a[3] = raw.w;
-      }
+        float a[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-      for (int c = 0; c < 4; ++c)  // the sign bit of sign byte c flips the element
-        u[4 * j + c] = __uint_as_float(__float_as_uint(a[c]) ^ ((sg << (24 - 8 * c)) & 0x80000000u));
+        for (int c = 0; c < 4; ++c)  // the sign bit of sign byte c flips the element
+          a[c] = __uint_as_float(__float_as_uint(a[c]) ^ ((sg << (24 - 8 * c)) & 0x80000000u));
+        v[2 * j] = make_float2(a[0], a[1]);
+        v[2 * j + 1] = make_float2(a[2], a[3]);
+      }
     }
     // index bits 0, 1 (c) and 7, 8, 9 (j)
-    reg_hadamard_32(u);
+    reg_hadamard_32(v);
     // transpose: element (j, c, lane) to row 8 c + j, column lane
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) buf[(8 * c + j) * kRowPad + lane] = u[4 * j + c];
+    for (int j = 0; j < 8; ++j) {
+      buf[(8 * 0 + j) * kRowPad + lane] = v[2 * j].x;
+      buf[(8 * 1 + j) * kRowPad + lane] = v[2 * j].y;
+      buf[(8 * 2 + j) * kRowPad + lane] = v[2 * j + 1].x;
+      buf[(8 * 3 + j) * kRowPad + lane] = v[2 * j + 1].y;
+    }
     __syncwarp();
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const float4 q = *reinterpret_cast<const float4*>(buf + lane * kRowPad + 4 * k);
-      u[4 * k] = q.x; u[4 * k + 1] = q.y; u[4 * k + 2] = q.z; u[4 * k + 3] = q.w;
+      v[2 * k] = make_float2(q.x, q.y);
+      v[2 * k + 1] = make_float2(q.z, q.w);
     }
     // index bits 2..6 (t, now the register index)
-    reg_hadamard_32(u);
+    reg_hadamard_32(v);
     __syncwarp();  // every lane has read its row before any is overwritten
 #pragma unroll
     for (int k = 0; k < 8; ++k)
       *reinterpret_cast<float4*>(buf + lane * kRowPad + 4 * k) =
-          make_float4(u[4 * k], u[4 * k + 1], u[4 * k + 2], u[4 * k + 3]);
+          make_float4(v[2 * k].x, v[2 * k].y, v[2 * k + 1].x, v[2 * k + 1].y);
     __syncwarp();
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) u[4 * j + c] = buf[(8 * c + j) * kRowPad + lane];
+    for (int j = 0; j < 8; ++j) {
+      v[2 * j] = make_float2(buf[(8 * 0 + j) * kRowPad + lane], buf[(8 * 1 + j) * kRowPad + lane]);
+      v[2 * j + 1] =
+          make_float2(buf[(8 * 2 + j) * kRowPad + lane], buf[(8 * 3 + j) * kRowPad + lane]);
+    }
     __syncwarp();  // the buffer is free for the warp's next block
-    const float s = 1.0f / 32.0f;
+    const float2 s = make_float2(1.0f / 32.0f, 1.0f / 32.0f);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int64_t e = base + 128 * j + 4 * lane;
-      const float o0 = u[4 * j] * s, o1 = u[4 * j + 1] * s, o2 = u[4 * j + 2] * s,
-                  o3 = u[4 * j + 3] * s;
+      const float2 o01 = __fmul2_rn(v[2 * j], s), o23 = __fmul2_rn(v[2 * j + 1], s);
       if constexpr (kOut == Act::F16)
-        over |= beyond_f16(o0) | beyond_f16(o1) | beyond_f16(o2) | beyond_f16(o3);
+        over |= beyond_f16(o01.x) | beyond_f16(o01.y) | beyond_f16(o23.x) | beyond_f16(o23.y);
       if constexpr (kOut != Act::F32) {
         uint2 out;
-        out.x = to16<kOut>(o0) | (to16<kOut>(o1) << 16);
-        out.y = to16<kOut>(o2) | (to16<kOut>(o3) << 16);
+        out.x = pack16<kOut>(o01);
+        out.y = pack16<kOut>(o23);
         *reinterpret_cast<uint2*>(static_cast<uint16_t*>(y) + e) = out;
       } else {
-        *reinterpret_cast<float4*>(static_cast<float*>(y) + e) = make_float4(o0, o1, o2, o3);
+        *reinterpret_cast<float4*>(static_cast<float*>(y) + e) = make_float4(o01.x, o01.y, o23.x, o23.y);
       }
     }
   }

@@ -242,10 +242,10 @@ __global__ void __launch_bounds__(kThreads, 1) stack_decode_kernel(const __grid_
         sw[r] = lds_u32(slot + (uint32_t)kSlotTrits + (uint32_t)(r * kBoxScaleWords * 4) + soff);
         seen ^= wv[r] ^ sw[r];
       }
-      // the slot is read; the proxy fence orders these reads before the
-      // asynchronous writes of the batch two ahead
+      // the slot is read: `seen` consumes every load, so the data is in
+      // registers before the warp synchronises and the slot goes to the TMA
+      // for the batch two ahead (completed reads need no proxy fence)
       asm volatile("" ::"r"(seen));
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       if (b + 2 < w.nbat) request(w, tw, ts, b + 2);
       float k1[8];
