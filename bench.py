@@ -184,7 +184,7 @@ def max_over_ranks(v: float) -> float:
 # Prefill: the capture is this exact launch (M=512, N=17408, K=5120).
 TRAFFIC_PREFILL = 24_840_448 + 7_168
 # Decode: the capture of the bench's own call (`--profile gemv1`).
-TRAFFIC_DECODE = 19_558_912 + 0
+TRAFFIC_DECODE = 19_558_400 + 0
 
 
 def ffn_lines(P, torch, syn, pk, world, args):
