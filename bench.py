@@ -182,7 +182,7 @@ def max_over_ranks(v: float) -> float:
 # dominant kernel, from the ncu capture of the matching `bench.py --profile`
 # case; None when the kernel has changed since those counters were taken.
 # Prefill: the capture is this exact launch (M=512, N=17408, K=5120).
-TRAFFIC_PREFILL = 24_840_448 + 7_168
+TRAFFIC_PREFILL = 24_838_144 + 2_816
 # Decode: the capture of the bench's own call (`--profile gemv1`).
 TRAFFIC_DECODE = 19_558_400 + 0
 

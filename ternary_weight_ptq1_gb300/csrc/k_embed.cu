@@ -10,8 +10,8 @@
 //
 // A (token m, 1024-block b) pair goes to one CTA of 256 threads, 4 values
 // each, which keeps the dependent chain short (a decode step has only
-// H / 1024 pairs); for dense tables and many pairs, to one warp instead, laid
-// out over the lanes as warp_hadamard_1024 (fwht_warp.cuh) wants it.  The
+// H / 1024 pairs); with many pairs, to one warp instead, laid out over the
+// lanes as warp_hadamard_1024 (fwht_warp.cuh) wants it.  The
 // table is dense (fp32 or bf16 rows, read with 16- or 8-byte vector loads) or
 // PTQ1_0: a thread's four weights 4l..4l+3 of a 128-weight block sit in one
 // or two of its 26 bytes, and each is the pages' peel (section "What Ferrox
@@ -97,41 +97,125 @@ __device__ __forceinline__ void store1(void* out, int64_t e, float o) {
 
 constexpr float kQNaN = __builtin_nanf("");
 
-// Many (token, block) pairs: one warp each, 32 values a lane.
+// Many (token, block) pairs: one warp each, 32 values a lane in the layout
+// of warp_hadamard_1024, which does the butterfly around two transposes
+// through the warp's kWarpBuf floats of shared memory.
+//
+// A PTQ1_0 group (208 bytes and 8 scales, 16 bytes) is read by lanes 0..13
+// with one 16-byte load each and staged in shared memory; each lane then
+// takes its two bytes per block from there.  A byte's five digits come from
+// a 256-entry table of codes (digit n in bits 2n, 2n + 1) that the CTA
+// builds once with the pages' peel, so a weight costs a shift-and-mask, a
+// conversion and d * s - s.
+constexpr int kEmbedWarps = 8;
+constexpr int kStageBytes = kGroupBytes + 16;  // a group's trits and its 8 scales
+constexpr size_t kEmbedSmem =
+    (size_t)kEmbedWarps * kWarpBuf * 4 + 256 * 4 + (size_t)kEmbedWarps * kStageBytes;
+
+template <Act kOut>
+__device__ __forceinline__ void store_pair4(void* out, int64_t e, float2 a, float2 b,
+                                            uint32_t sg) {
+  const float2 s = make_float2(1.0f / 32.0f, 1.0f / 32.0f);
+  a = __fmul2_rn(a, s);
+  b = __fmul2_rn(b, s);
+  if constexpr (kOut == Act::BF16) {  // rounding is symmetric: flip after it
+    const __nv_bfloat162 ha = __floats2bfloat162_rn(a.x, a.y), hb = __floats2bfloat162_rn(b.x, b.y);
+    uint2 r;
+    r.x = *reinterpret_cast<const uint32_t*>(&ha) ^ pair_sign_mask(sg, 0);
+    r.y = *reinterpret_cast<const uint32_t*>(&hb) ^ pair_sign_mask(sg, 1);
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + e) = r;
+  } else {
+    float4 r;
+    r.x = __uint_as_float(__float_as_uint(a.x) ^ f32_sign_mask(sg, 0));
+    r.y = __uint_as_float(__float_as_uint(a.y) ^ f32_sign_mask(sg, 1));
+    r.z = __uint_as_float(__float_as_uint(b.x) ^ f32_sign_mask(sg, 2));
+    r.w = __uint_as_float(__float_as_uint(b.y) ^ f32_sign_mask(sg, 3));
+    *reinterpret_cast<float4*>(static_cast<float*>(out) + e) = r;
+  }
+}
+
 template <Tab kT, Act kOut>
-__global__ void __launch_bounds__(256) embed_warp_kernel(const void* __restrict__ table,
-                                                         const uint16_t* __restrict__ scales,
-                                                         const int32_t* ids,
-                                                         const int8_t* __restrict__ signs,
-                                                         void* out, int64_t total_blocks,
-                                                         int64_t blocks_per_row, int64_t V) {
-  const int lane = threadIdx.x & 31;
+__global__ void __launch_bounds__(32 * kEmbedWarps) embed_warp_kernel(
+    const void* __restrict__ table, const uint16_t* __restrict__ scales, const int32_t* ids,
+    const int8_t* __restrict__ signs, void* out, int64_t total_blocks, int64_t blocks_per_row,
+    int64_t V) {
+  extern __shared__ __align__(16) unsigned char esmem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float* buf = reinterpret_cast<float*>(esmem) + warp * kWarpBuf;
+  uint32_t* code = reinterpret_cast<uint32_t*>(esmem + kEmbedWarps * kWarpBuf * 4);
+  unsigned char* stage = esmem + kEmbedWarps * kWarpBuf * 4 + 256 * 4 + warp * kStageBytes;
   const int64_t H = blocks_per_row * kRot;
-  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int64_t nwarps = (int64_t)gridDim.x * kEmbedWarps;
   pdl_release();
+  if constexpr (kT == Tab::PTQ1) {
+    for (int e = threadIdx.x; e < 256; e += blockDim.x) {
+      uint32_t c = 0;
+#pragma unroll
+      for (int n = 0; n < 5; ++n) c |= (uint32_t)peel((uint32_t)e, pow3(n)) << (2 * n);
+      code[e] = c;
+    }
+    __syncthreads();
+  }
+  // PTQ1_0: this lane's weights 4 l .. 4 l + 3 of each block sit in bytes
+  // q0 and q1 (q1 = q0 or q0 + 1); weight c is digit dn[c] of byte q0 or q1
+  const int q0 = (4 * lane) / 5, q1 = (4 * lane + 3) / 5;
   pdl_wait();  // the ids may come from the previous kernel (a sampler)
-  for (int64_t wb = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); wb < total_blocks;
-       wb += nwarps) {
+  for (int64_t wb = (int64_t)blockIdx.x * kEmbedWarps + warp; wb < total_blocks; wb += nwarps) {
     const int64_t m = wb / blocks_per_row, b = wb % blocks_per_row;
     const int32_t id = ids[m];
     const bool ok = id >= 0 && (int64_t)id < V;  // the same for the whole warp
-    float v[8][4] = {};
-    if (ok) {
+    if (!ok) {
+      const float4 nan4 = make_float4(kQNaN, kQNaN, kQNaN, kQNaN);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) load4<kT>(table, scales, (int64_t)id * blocks_per_row + b, j, lane, v[j]);
-      warp_hadamard_1024(v, lane);
+      for (int j = 0; j < 8; ++j) {
+        const int64_t e = m * H + b * kRot + 128 * j + 4 * lane;
+        const float o[4] = {nan4.x, nan4.y, nan4.z, nan4.w};
+        store4<kOut>(out, e, o);
+      }
+      continue;
     }
+    const int64_t rg = (int64_t)id * blocks_per_row + b;  // the table row's group
+    float2 v[16];
+    if constexpr (kT == Tab::PTQ1) {
+      if (lane < 14) {  // 13 x 16 bytes of trits, then the 8 scales
+        const uint4 q = lane < 13 ? reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(table) +
+                                                                   rg * kGroupBytes)[lane]
+                                  : *reinterpret_cast<const uint4*>(scales + rg * kGroupBlocks);
+        *reinterpret_cast<uint4*>(stage + 16 * lane) = q;
+      }
+      __syncwarp();
+      const uint4 sraw = *reinterpret_cast<const uint4*>(stage + kGroupBytes);
+      const uint32_t sw[4] = {sraw.x, sraw.y, sraw.z, sraw.w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float s = __half2float(__ushort_as_half((unsigned short)(sw[j / 2] >> (16 * (j & 1)))));
+        const uint32_t c0 = code[stage[kBlockBytes * j + q0]];
+        const uint32_t c1 = code[stage[kBlockBytes * j + q1]];
+        float t[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int w = 4 * lane + c;
+          const uint32_t d = ((w / 5 == q0 ? c0 : c1) >> (2 * (w % 5))) & 3u;
+          t[c] = fmaf((float)d, s, -s);  // (d - 1) s, exact
+        }
+        v[2 * j] = make_float2(t[0], t[1]);
+        v[2 * j + 1] = make_float2(t[2], t[3]);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        float t[4];
+        load4<kT>(table, scales, rg, j, lane, t);
+        v[2 * j] = make_float2(t[0], t[1]);
+        v[2 * j + 1] = make_float2(t[2], t[3]);
+      }
+    }
+    warp_hadamard_1024(v, buf, lane);  // its barriers also free the stage
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int64_t k = b * kRot + 128 * j + 4 * lane;  // index within the row
       const uint32_t sg = *reinterpret_cast<const uint32_t*>(signs + k);
-      float o[4];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const float f = v[j][c] * (1.0f / 32.0f);
-        o[c] = ok ? ((int8_t)(sg >> (8 * c)) < 0 ? -f : f) : kQNaN;
-      }
-      store4<kOut>(out, m * H + k, o);
+      store_pair4<kOut>(out, m * H + k, v[2 * j], v[2 * j + 1], sg);
     }
   }
 }
@@ -140,10 +224,9 @@ __global__ void __launch_bounds__(256) embed_warp_kernel(const void* __restrict_
 // Thread (warp j, lane l) holds elements 128 j + 4 l + c: index bits 0-1 in
 // registers, bits 2-6 across the lanes; bits 7-9 (the warp) are done after a
 // transpose through shared memory, by 128 threads holding elements t + 128 k.
-// kEarlySigns: the output signs are requested before the id (a short chain
-// for a decode step's few pairs); with many pairs, after the butterfly
-// (measured faster there: 30.6 against 32.3 us for 10,240 PTQ1_0 pairs).
-template <Tab kT, Act kOut, bool kEarlySigns>
+// The output signs are requested before the id: they do not depend on it,
+// and a decode step's chain of few pairs is short.
+template <Tab kT, Act kOut>
 __global__ void __launch_bounds__(256) embed_cta_kernel(const void* __restrict__ table,
                                                         const uint16_t* __restrict__ scales,
                                                         const int32_t* ids,
@@ -159,7 +242,7 @@ __global__ void __launch_bounds__(256) embed_cta_kernel(const void* __restrict__
     const int64_t m = wb / blocks_per_row, b = wb % blocks_per_row;
     // the output signs do not depend on the id
     int8_t sg[8];
-    if (kEarlySigns && t < 128) {
+    if (t < 128) {
 #pragma unroll
       for (int k = 0; k < 8; ++k) sg[k] = signs[b * kRot + t + 128 * k];
     }
@@ -202,7 +285,7 @@ __global__ void __launch_bounds__(256) embed_cta_kernel(const void* __restrict__
       for (int k = 0; k < 8; ++k) {
         const int64_t i = b * kRot + t + 128 * k;
         const float f = w[k] * (1.0f / 32.0f);
-        const int8_t sk = kEarlySigns ? sg[k] : signs[i];
+        const int8_t sk = sg[k];
         store1<kOut>(out, m * H + i, sk < 0 ? -f : f);
       }
     }
@@ -215,23 +298,18 @@ cudaError_t launch_embed_t(const void* table, const uint16_t* scales, const int3
                            cudaStream_t st) {
   const int64_t bpr = H / kRot, total = M * bpr;
   constexpr int64_t kSms = 152;
-  // Measured on a GB300 (V = 131072, H = 5120): a CTA per pair is faster for
-  // PTQ1_0 tables at every M (2.5 against 7.5 us at M = 1, 31 against 42 us
-  // at M = 2048) and for dense tables up to M = 256 (1280 pairs); a warp per
-  // pair is faster for dense tables at M = 2048 (12 against 18 us).
-  if (kT == Tab::PTQ1 || total < 16 * kSms) {
-    const int64_t grid = total < kSms * 512 ? total : kSms * 512;
-    if (total < 16 * kSms)
-      return launch_pdl(embed_cta_kernel<kT, kOut, true>, dim3((unsigned)grid), dim3(256), 0, st,
-                        table, scales, ids, signs, out, total, bpr, V);
-    return launch_pdl(embed_cta_kernel<kT, kOut, false>, dim3((unsigned)grid), dim3(256), 0, st,
+  // Measured on a GB300 (V = 131072, H = 5120) with the earlier shuffle
+  // butterfly: a CTA per pair was faster up to M = 256 (1280 pairs) for
+  // dense tables and at every M for PTQ1_0 ones.
+  if (total < 16 * kSms) {
+    const int64_t grid = total;
+    return launch_pdl(embed_cta_kernel<kT, kOut>, dim3((unsigned)grid), dim3(256), 0, st,
                       table, scales, ids, signs, out, total, bpr, V);
   }
-  const int warps = 8;
-  int64_t grid = (total + warps - 1) / warps;
+  int64_t grid = (total + kEmbedWarps - 1) / kEmbedWarps;
   if (grid > kSms * 64) grid = kSms * 64;
-  return launch_pdl(embed_warp_kernel<kT, kOut>, dim3((unsigned)grid), dim3(32 * warps), 0, st,
-                    table, scales, ids, signs, out, total, bpr, V);
+  return launch_pdl(embed_warp_kernel<kT, kOut>, dim3((unsigned)grid), dim3(32 * kEmbedWarps),
+                    kEmbedSmem, st, table, scales, ids, signs, out, total, bpr, V);
 }
 
 }  // namespace
