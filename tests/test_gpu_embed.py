@@ -76,6 +76,24 @@ def test_ptq1_every_byte_value(P, orc, syn):
     Q.check_fwht(Q.host_f64(y), orc.embed_ptq1(wq, sc, ids, s), what="all bytes")
 
 
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_ptq1_every_byte_value_many_pairs(P, orc, syn, out):
+    # the same table looked up 10 times over (2,560 pairs): the warp-per-pair
+    # kernel, whose digits come from its code table and whose bf16 output
+    # takes its signs after rounding
+    import torch
+
+    V, H = 256, 1024
+    wq = ((np.arange(V)[:, None] * 7 + np.arange(8 * 26)[None, :] * 3) % 256).astype(np.uint8)
+    sc = syn.scales_f16(39, 1, (V, H // 128))
+    ids = np.tile(np.arange(V, dtype=np.int32), 10)
+    s = syn.signs(39, 2, H)
+    od = torch.float32 if out == "f32" else torch.bfloat16
+    y = P.embed_ptq1(Q.dev(wq), Q.dev(sc), _ids_dev(ids), Q.dev(s), out_dtype=od)
+    Q.check_fwht(Q.host_f64(y), orc.embed_ptq1(wq, sc, ids, s), bf16_out=out == "bf16",
+                 what=f"all bytes, many pairs, {out}")
+
+
 def test_ids_outside_the_table_give_nan_rows(P, orc, syn):
     import torch
 
@@ -122,7 +140,7 @@ def test_empty_and_in_bounds(P, syn):
 
 def test_dispatch_paths(P, orc, syn):
     # a dense table with many (token, block) pairs runs a warp per pair; a
-    # PTQ1_0 table past 152 x 512 pairs makes each CTA take several pairs
+    # PTQ1_0 table past 152 x 64 CTAs x 8 warps makes a warp take several
     import torch
 
     V, H = 97, 5120
@@ -140,7 +158,7 @@ def test_dispatch_paths(P, orc, syn):
     y = P.embed_ptq1(Q.dev(wq), Q.dev(sc), _ids_dev(ids), Q.dev(s))
     rows = np.array([0, 1, 2999, 3002, 6999, 7001, 7777, 15197, 15198, 15998])
     Q.check_fwht(Q.host_f64(y[torch.from_numpy(rows).cuda()]), orc.embed_ptq1(wq, sc, ids[rows], s),
-                 what="several pairs per CTA")
+                 what="several pairs per warp")
     isbad = np.zeros(len(ids), bool)
     isbad[bad] = True
     mask = torch.from_numpy(isbad).cuda()
