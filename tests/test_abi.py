@@ -102,6 +102,13 @@ def test_refusals_before_launch(P):
     assert P.matmul_workspace_bytes(512, 17408, 5120, P.PTQ_BF16) == 0
     assert P.matmul_workspace_bytes(1, 17408, 5120 + 128, P.PTQ_F32) == 0  # K/128 odd
     assert P.matmul_workspace_bytes(1, 17408, 100, P.PTQ_F32) == 0
+    # prefill split-K scratch, a function of the shape alone: fewer output
+    # tiles than half of 152 SMs split K over up to 6 CTAs (at most one per
+    # 1024-wide group), one fp32 M x N partial sum each
+    assert P.matmul_workspace_bytes(256, 5120, 17408, P.PTQ_BF16) == 6 * 256 * 5120 * 4
+    assert P.matmul_workspace_bytes(64, 1000, 6144, P.PTQ_BF16) == 6 * 64 * 1000 * 4
+    assert P.matmul_workspace_bytes(300, 640, 3072, P.PTQ_BF16) == 3 * 300 * 640 * 4
+    assert P.matmul_workspace_bytes(128, 17408, 5120, P.PTQ_BF16) == 0  # 136 tiles
     # rotation
     assert L.ptq_fwht(p16, p16, p16, 1, 1000, P.PTQ_F32, None) == 2
     assert L.ptq_fwht(p16, odd, p16, 1, 1024, P.PTQ_F32, None) == 3
